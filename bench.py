@@ -1,0 +1,482 @@
+"""Benchmark of the fused preprocess + exact Top-K hot path on GB300.
+
+One step = one replay of a lane's CUDA Graph: preprocess a batch of RGB8
+frames into the FP32 NCHW tensor, then the row-wise exact Top-K of the
+logits (the network between them is out of scope; its output slot is a
+fixed logits buffer).  Default workload: 64 independent 1920x1080 RGB8
+frames -> 224x224 mean/std, Top-32 of [64, 1000] logits, the batched
+HBM-throughput configuration.  Also measured on every run:
+
+* batch-1 graph-replay latency (p50 / p99 / max, GPU events and host steady
+  clock, graph and no-graph) on one 1920x1080 frame -> 224x224, Top-5 of 1000;
+* end-to-end throughput through the lane API with host buffers: the graph
+  copies the frames from pinned host memory and the result back;
+* the roofline of the dominant kernel (the preprocess) from in-graph event
+  nodes around it, against the measured HBM copy bandwidth;
+* the CPU oracle on the host cores (a bounded sample), as a reported baseline.
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+       [--workload NAME] [--latency-samples S] [--no-cpu-baseline]
+Multi-GPU (replicas, no collective on the data path) runs under torchrun.
+Rank 0 prints one JSON line on stdout; everything else goes to stderr.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+METRIC = "frames/s + HBM GB/s (% of roofline); p50/p99 batch-1 graph-replay latency"
+DEFAULT_WORKLOAD = "b64_1080p_to_224"
+LATENCY_WORKLOAD = "b1_1080p_to_224"
+FALLBACK_HBM_GBS = 6800.0
+LANES = 3
+
+# DRAM traffic of the staged preprocess kernel per launch from one ncu
+# capture (dram__bytes_read.sum + dram__bytes_write.sum), keyed by the SHA-256
+# of the kernel source it was taken on; reported only while that source is
+# unchanged.  Filled from the committed ncu summary under profiles/.
+NCU_TRAFFIC = {
+    "b64_1080p_to_224": {
+        "bytes": 165_189_632 + 22_113_024,
+        "source_sha": "fc82e5cd0da2fca242797cc4127f42558d70faef4c9e06d1eabe9ace5c57a5a9",
+    },
+}
+
+
+def log(*a):
+    print(*a, file=sys.stderr, flush=True)
+
+
+# ----------------------------------------------------------------- geometry
+# Bytes the path must move at minimum (the algorithmic bytes): the 32-byte
+# sectors of the source that taps with a non-zero weight touch, the FP32
+# tensor written once, the logits read once and the K pairs written.
+
+def _axis(S: int, D: int):
+    x = np.arange(D, dtype=np.int64)
+    num = (2 * x + 1) * S - D
+    den = 2 * D
+    q = np.floor_divide(num, den)
+    rem = num - q * den
+    lo = np.clip(q, 0, S - 1)
+    hi = np.clip(q + 1, 0, S - 1)
+    return lo, hi, rem != 0
+
+
+def _box(sw, sh, dw, dh, letterbox):
+    if not letterbox:
+        return dw, dh
+    if dw * sh <= dh * sw:
+        return dw, max(1, (2 * sh * dw + sw) // (2 * sw))
+    return max(1, (2 * sw * dh + sh) // (2 * sh)), dh
+
+
+def algorithmic_bytes(w: dict) -> dict:
+    nw, nh = _box(w["src_w"], w["src_h"], w["dst_w"], w["dst_h"], w["resize"] == "letterbox")
+    lo, hi, nz = _axis(w["src_h"], nh)
+    rows = np.unique(np.concatenate([lo, hi[nz]]))
+    lo, hi, nz = _axis(w["src_w"], nw)
+    cols = np.unique(np.concatenate([lo, hi[nz]]))
+    row_bytes = 3 * w["src_w"]
+    col_bytes = (3 * cols[:, None] + np.arange(3)[None, :]).reshape(-1)
+    src_sectors = 0
+    for j in rows:                                   # rows start at j * row_bytes in a packed frame
+        src_sectors += np.unique((j * row_bytes + col_bytes) // 32).size
+    src = src_sectors * 32 * w["batch"]
+    dst = w["batch"] * 3 * w["dst_w"] * w["dst_h"] * 4
+    topk = w["rows"] * w["cols"] * 4 + w["rows"] * w["k"] * 8
+    return {"preprocess": int(src + dst), "source": int(src), "tensor": int(dst), "topk": int(topk),
+            "total": int(src + dst + topk)}
+
+
+# ----------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled during timed regions."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str | None):
+        self.gpu_id = gpu_id
+        self.proc = None
+        self.lines: list[str] = []
+        self.thread = None
+
+    def start(self):
+        cmd = ["nvidia-smi", "--query-gpu=" + self.FIELDS, "--format=csv,noheader,nounits", "-lms", "100"]
+        if self.gpu_id:
+            cmd += ["--id=" + self.gpu_id]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+
+        def pump():
+            for line in self.proc.stdout:
+                self.lines.append(line.strip())
+        self.thread = threading.Thread(target=pump, daemon=True)
+        self.thread.start()
+        time.sleep(0.3)
+
+    def stop(self) -> dict | None:
+        if self.proc is None:
+            return None
+        time.sleep(0.15)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=2)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ----------------------------------------------------------------- distributed
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def max_over_ranks(value: float, world: int, device=None) -> float:
+    """Maximum of a per-rank number over the job (identity on one process)."""
+    if world == 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(units_per_rank: float, seconds_per_rank: float, world: int, device=None) -> tuple[float, float]:
+    """Units of all ranks divided by the slowest rank's time."""
+    t = max_over_ranks(seconds_per_rank, world, device)
+    return units_per_rank * world / t, t
+
+
+# ----------------------------------------------------------------- oracle baseline
+
+def cpu_baseline(w: dict, frames: np.ndarray, logits: np.ndarray, budget_s: float = 10.0) -> dict:
+    """The oracle as it stands, single-threaded, repeated over a bounded sample."""
+    import oracle as oracle_pkg
+    o = oracle_pkg.Oracle()
+    n_frames = 2
+    lb = w["resize"] == "letterbox"
+    done, t0 = 0, time.perf_counter()
+    while True:
+        for b in range(0, frames.shape[0], n_frames):
+            o.preprocess(frames[b:b + n_frames], w["src_w"], w["src_h"], w["dst_w"], w["dst_h"],
+                         letterbox=lb, norm=w["norm"])
+            o.topk(logits[b:b + n_frames], w["k"])
+            done += n_frames
+            if time.perf_counter() - t0 >= budget_s:
+                break
+        if time.perf_counter() - t0 >= budget_s:
+            break
+    dt = time.perf_counter() - t0
+    return {"value": done / dt, "unit": "frames/s", "cores": 1, "kind": "oracle",
+            "sample": f"{done} frames of the workload (preprocess of the frame + Top-{w['k']} of its "
+                      f"{w['cols']}-logit row), single-threaded C++ oracle, {dt:.1f} s"}
+
+
+def run_reference(args, w: dict) -> None:
+    """--impl reference: the oracle timed on the host cores, one frame per step."""
+    world, rank, _ = dist_setup()
+    if rank != 0:
+        return
+    import oracle as oracle_pkg
+    o = oracle_pkg.Oracle()
+    frames = synth.make_frames(args.workload, batch=1)
+    logits = synth.make_logits(args.workload, rows=1)
+    lb = w["resize"] == "letterbox"
+
+    def step():
+        o.preprocess(frames, w["src_w"], w["src_h"], w["dst_w"], w["dst_h"], letterbox=lb, norm=w["norm"])
+        o.topk(logits, w["k"])
+
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    dt = time.perf_counter() - t0
+    value = args.steps / dt
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "frames/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000 * dt / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic", "config": workload_config(args.workload, w),
+        "cpu_baseline": {"value": value, "unit": "frames/s", "cores": 1, "kind": "oracle",
+                         "sample": "one frame of the workload per step (its preprocess + the Top-K of its "
+                                   "logit row), single-threaded C++ oracle"},
+        "e2e": {"value": value, "unit": "frames/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def workload_config(name: str, w: dict) -> dict:
+    return {"workload": f"{w['batch']}x {w['src_w']}x{w['src_h']} RGB8 -> "
+                        f"{'letterbox ' if w['resize'] == 'letterbox' else ''}{w['dst_w']}x{w['dst_h']} "
+                        f"{'mean/std' if w['norm'] == 'mean_std' else '1/255'} FP32 NCHW + exact Top-{w['k']} "
+                        f"of [{w['rows']},{w['cols']}] FP32 logits",
+            "name": name, "batch": w["batch"], "k": w["k"], "rows": w["rows"], "cols": w["cols"]}
+
+
+# ----------------------------------------------------------------- GPU arm
+
+def percentiles(xs):
+    a = np.sort(np.asarray(xs, dtype=np.float64))
+    return {"p50": float(np.percentile(a, 50)), "p99": float(np.percentile(a, 99)), "max": float(a[-1]),
+            "mean": float(a.mean())}
+
+
+def source_sha(path: str) -> str:
+    return hashlib.sha256(open(path, "rb").read()).hexdigest()
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20000)
+    ap.add_argument("--warmup", type=int, default=200)
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=list(synth.WORKLOADS))
+    ap.add_argument("--latency-samples", type=int, default=10000)
+    ap.add_argument("--e2e-steps", type=int, default=60)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    w = synth.WORKLOADS[args.workload]
+
+    if args.impl == "reference":
+        run_reference(args, w)
+        return
+
+    import torch
+    world, rank, local = dist_setup()
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=device)
+    import __graft_entry__
+    if rank == 0:
+        __graft_entry__.build()
+    if world > 1:
+        torch.distributed.barrier()
+    __graft_entry__.build()
+    from post_processing_gb300 import Lane
+    from post_processing_gb300 import binding as B
+
+    props = torch.cuda.get_device_properties(device)
+    l2 = getattr(props, "L2_cache_size", 126 * 2 ** 20)
+    try:
+        gpu_id = "GPU-" + str(props.uuid)
+    except Exception:
+        gpu_id = None
+    clocks = ClockSampler(gpu_id)
+
+    # inputs: one seeded batch, copied into every lane's fixed buffers
+    t0 = time.perf_counter()
+    frames = synth.make_frames(args.workload)
+    logits = synth.make_logits(args.workload)
+    log(f"[bench] inputs generated in {time.perf_counter() - t0:.1f} s")
+    frames_dev = torch.from_numpy(frames).to(device)
+    logits_dev = torch.from_numpy(logits).to(device)
+
+    stream = torch.cuda.Stream(device)
+    pre = B.preprocess_desc(w["src_w"], w["src_h"], w["dst_w"], w["dst_h"],
+                            letterbox=w["resize"] == "letterbox", norm=w["norm"])
+    lanes, keep = [], []
+    for _ in range(LANES):
+        src = frames_dev.clone()
+        lg = logits_dev.clone()
+        keep += [src, lg]
+        d = B.lane_desc(pre, w["batch"], w["rows"], w["cols"], w["k"], input=src.data_ptr(), logits=lg.data_ptr(),
+                        stream=stream.cuda_stream, flags=B.WS_LANE_FLAG_STAGE_TIMING)
+        lanes.append(Lane(d))
+    torch.cuda.synchronize()
+    alg = algorithmic_bytes(w)
+    touched_per_rotation = LANES * alg["total"]
+
+    def run_steps(n, record):
+        inflight = []
+        for s in range(n):
+            lane = lanes[s % LANES]
+            if lane.state == B.WS_LANE_IN_FLIGHT:
+                t = lane.wait()
+                inflight.remove(lane)
+                if record is not None:
+                    record.append((t.preprocess_us, t.topk_us))
+            lane.acquire()
+            lane.submit()
+            inflight.append(lane)
+        for lane in inflight:
+            t = lane.wait()
+            if record is not None:
+                record.append((t.preprocess_us, t.topk_us))
+
+    run_steps(args.warmup, None)
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    clocks.start()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    stage = []
+    torch.cuda.synchronize()
+    ev0.record(stream)
+    run_steps(args.steps, stage)
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    elapsed_s = ev0.elapsed_time(ev1) / 1000.0
+    if world > 1:
+        torch.distributed.barrier()
+
+    # batch-1 latency: one lane, submit -> wait, graph and direct launches
+    lw = synth.WORKLOADS[LATENCY_WORKLOAD]
+    lframes = torch.from_numpy(synth.make_frames(LATENCY_WORKLOAD)).to(device)
+    llogits = torch.from_numpy(synth.make_logits(LATENCY_WORKLOAD)).to(device)
+    lpre = B.preprocess_desc(lw["src_w"], lw["src_h"], lw["dst_w"], lw["dst_h"], norm=lw["norm"])
+    latency = {"workload": workload_config(LATENCY_WORKLOAD, lw)["workload"], "samples": args.latency_samples,
+               "warmup": min(1000, args.latency_samples), "input": "device-resident"}
+    for label, flags in (("graph", 0), ("no_graph", B.WS_LANE_FLAG_NO_GRAPH)):
+        d = B.lane_desc(lpre, 1, 1, lw["cols"], lw["k"], input=lframes.data_ptr(), logits=llogits.data_ptr(),
+                        flags=flags)
+        with Lane(d) as lane:
+            gpu, host = [], []
+            for i in range(latency["warmup"] + args.latency_samples):
+                lane.acquire()
+                lane.submit()
+                t = lane.wait()
+                if i >= latency["warmup"]:
+                    gpu.append(t.gpu_us)
+                    host.append(t.host_us)
+            latency[label] = {"gpu_us": percentiles(gpu), "host_us": percentiles(host)}
+    clk = clocks.stop()
+
+    # end to end through the lane API with host buffers: pinned frames in, result out
+    e2e = None
+    if args.e2e_steps > 0:
+        e_lanes = []
+        for _ in range(2):
+            d = B.lane_desc(pre, w["batch"], w["rows"], w["cols"], w["k"], input_mode=B.WS_INPUT_COPY,
+                            result_mode=B.WS_RESULT_COPY, logits=logits_dev.data_ptr())
+            lane = Lane(d)
+            import ctypes
+            buf = (ctypes.c_char * frames.nbytes).from_address(lane.buffers.input_host)
+            np.frombuffer(buf, dtype=np.uint8)[:] = frames.reshape(-1)
+            e_lanes.append(lane)
+        for lane in e_lanes:
+            lane.acquire(); lane.submit(); lane.wait()
+        torch.cuda.synchronize()
+        if world > 1:
+            torch.distributed.barrier()
+        t0 = time.perf_counter()
+        pending = []
+        for s in range(args.e2e_steps):
+            lane = e_lanes[s % 2]
+            if lane.state == B.WS_LANE_IN_FLIGHT:
+                lane.wait()
+            lane.acquire()
+            lane.submit()
+        for lane in e_lanes:
+            if lane.state == B.WS_LANE_IN_FLIGHT:
+                lane.wait()
+        e_dt = time.perf_counter() - t0
+        e_rate, _ = whole_job_rate(w["batch"] * args.e2e_steps, e_dt, world, device)
+        e2e = {"value": e_rate, "unit": "frames/s", "h2d_bytes_per_step": int(frames.nbytes),
+               "d2h_bytes_per_step": int(w["rows"] * w["k"] * 8),
+               "path": "ws_lane_submit/wait, input_mode=COPY (pinned host frames, H2D inside the graph), "
+                       "result_mode=COPY (D2H of the K pairs inside the graph), 2 lanes on their own streams"}
+        for lane in e_lanes:
+            lane.close()
+
+    for lane in lanes:
+        lane.close()
+
+    value, t_max = whole_job_rate(w["batch"] * args.steps, elapsed_s, world, device)
+    pre_us = np.array([s[0] for s in stage], dtype=np.float64)
+    topk_us = np.array([s[1] for s in stage], dtype=np.float64)
+    peaks_path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(peaks_path):
+        peak, peak_src = float(json.load(open(peaks_path))["hbm_gbs"]), "measured"
+    else:
+        peak, peak_src = FALLBACK_HBM_GBS, "fallback"
+    achieved = alg["preprocess"] / (pre_us.mean() * 1e-6) / 1e9
+    sha = source_sha(os.path.join(ROOT, "post_processing_gb300", "csrc", "preprocess.cu"))
+    traffic = NCU_TRAFFIC.get(args.workload)
+    traffic = traffic["bytes"] if traffic and traffic.get("source_sha") == sha else None
+
+    if rank == 0:
+        cpu = None
+        if not args.no_cpu_baseline:
+            cpu = cpu_baseline(w, frames, logits)
+        line = {
+            "metric": METRIC, "value": value, "unit": "frames/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": 1000.0 * t_max / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": dict(workload_config(args.workload, w),
+                           l2=f"{LANES} lanes rotate, {touched_per_rotation / 1e6:.0f} MB touched per rotation "
+                              f"(> {touched_per_rotation / l2:.1f}x the {l2 / 2 ** 20:.0f} MiB L2): inputs larger "
+                                "than L2",
+                           parallelism=f"replicas x{world}", graph=True,
+                           algorithmic_bytes_per_step=alg["total"]),
+            "hbm_gbs_step": alg["total"] * args.steps * world / t_max / 1e9,
+            "roofline": {"bound": "hbm", "kernel": "pre_staged_kernel", "achieved": achieved, "peak": peak,
+                         "unit": "GB/s", "frac": achieved / peak, "peak_source": peak_src,
+                         "traffic": traffic, "algorithmic_bytes_per_launch": alg["preprocess"],
+                         "avg_launch_us": float(pre_us.mean()), "p50_launch_us": float(np.median(pre_us)),
+                         "topk_avg_launch_us": float(topk_us.mean())},
+            "latency_b1": latency,
+            "e2e": e2e,
+            "gpu_launches": 2 * args.steps,
+            "clocks": clk,
+            "cpu_baseline": cpu,
+        }
+        line["roofline"]["frac_note"] = "of measured" if peak_src == "measured" else "of fallback"
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

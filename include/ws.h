@@ -1,0 +1,277 @@
+/* ws.h -- C ABI of the GB300 fused RGB8 -> FP32 NCHW preprocess and the
+ * exact Top-K, plus the fixed-shape lanes that replay both as one CUDA Graph.
+ *
+ * Sources of the operations (page title, then section):
+ *  - "Inside WarpStream TRT", problem-statement table: interleaved RGB8
+ *    producer, fixed-shape FP32 NCHW network input, fixed-size FP32 logits,
+ *    exact Top-K with K <= 32, fixed preallocated lanes, no allocation in
+ *    the submit/wait path.
+ *  - "Inside WarpStream TRT", fused-preprocessing section and its data-flow
+ *    figure: per destination pixel a centre-aligned bilinear sample, scaling
+ *    to [0,1], (value - mean) * inverse_std per channel, stored straight into
+ *    the channel plane of the NCHW tensor; no intermediate image exists.
+ *  - yolo.cu README, "Two ways to use it": the same preprocess as a letterbox
+ *    into the network input, and a small handle-based C API.
+ *  - "Inside WarpStream TRT", Top-K section: exact selection, ties to the
+ *    lower class index, NaN treated as negative infinity, only K score/index
+ *    pairs written back.
+ *  - "Inside WarpStream TRT", lane and CUDA Graph sections: each lane owns
+ *    fixed buffers, events, a non-blocking stream and one instantiated graph
+ *    (preprocess, network, Top-K captured once); submit records an event,
+ *    launches the graph and records completion; a lane cannot be submitted
+ *    unless acquired nor reused while busy, so backpressure is part of the API.
+ *  - "Streams, concurrency and CUDA Graphs" (CUDA handbook), CUDA Graphs
+ *    section: capture once, instantiate once, one launch per replay; fixed
+ *    addresses and shapes; nothing synchronising inside the graph.
+ *
+ * Conventions (apply to every call):
+ *  - Every call returns a ws_status; no exception crosses the ABI.  Outputs
+ *    are defined only when the call returns WS_OK.  On an error,
+ *    ws_last_error() returns a message for the calling thread.
+ *  - Arguments are validated on the host before anything is enqueued; a
+ *    rejected call enqueues nothing.
+ *  - ws_preprocess and ws_topk are asynchronous and stream-ordered; they
+ *    allocate nothing and never synchronise, so they may be captured into a
+ *    CUDA Graph.  A device fault shows up later, at a stream or event
+ *    synchronisation, as WS_ERR_CUDA.
+ *  - Pointers are plain addresses: "device" means memory the GPU reads or
+ *    writes (cudaMalloc, or the device view of mapped pinned memory), "host"
+ *    means CPU memory.  The caller owns every pointer it passes; the library
+ *    only keeps borrowed pointers inside a lane, and those must stay valid,
+ *    at the same address, until the lane is destroyed.
+ *  - Calls on one lane are not thread-safe; different lanes are independent.
+ *  - The library computes everything on the GPU.  There is no CPU fallback:
+ *    without a usable CUDA device the compute calls return WS_ERR_CUDA.
+ */
+#ifndef WS_H
+#define WS_H
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ------------------------------------------------------------------ status */
+
+typedef int32_t ws_status;
+#define WS_OK                   0
+#define WS_ERR_INVALID_ARGUMENT 1  /* a size, pointer, mode or stride was rejected          */
+#define WS_ERR_UNSUPPORTED      2  /* valid request this build or device cannot serve        */
+#define WS_ERR_CUDA             3  /* a CUDA runtime call failed (message names the error)   */
+#define WS_ERR_OUT_OF_MEMORY    4  /* a lane could not allocate its buffers                  */
+#define WS_ERR_LANE_STATE       5  /* lane call made in the wrong state (e.g. submit unacquired) */
+#define WS_ERR_LANE_BUSY        6  /* lane is acquired or in flight and cannot be taken      */
+#define WS_ERR_TIMEOUT          7  /* ws_lane_wait deadline passed; the lane stays in flight */
+#define WS_ERR_CAPTURE          8  /* graph capture or instantiation failed                  */
+#define WS_ERR_DEVICE           9  /* a kernel's bounded wait gave up (see ws_device_error)  */
+
+/* Static name of a status ("WS_OK", ...); never NULL. */
+const char* ws_status_string(ws_status status);
+
+/* Message of the last failed call made by this thread ("" if none).  The
+ * pointer stays valid until this thread's next ws_* call. */
+const char* ws_last_error(void);
+
+/* Library version: major * 10000 + minor * 100 + patch. */
+int32_t ws_version(void);
+
+/* Error bits that kernels set on the current device when a bounded wait
+ * (an mbarrier wait on a bulk copy) runs out, instead of hanging.  Reads the
+ * flags synchronously; clears them when clear != 0.  *flags == 0 means none. */
+ws_status ws_device_error(uint32_t* flags, int32_t clear);
+
+/* -------------------------------------------------------------- preprocess */
+
+#define WS_RESIZE_STRETCH   0  /* bilinear resize of the whole frame to dst_w x dst_h   */
+#define WS_RESIZE_LETTERBOX 1  /* aspect-preserving resize, centred, rest = pad_value  */
+
+#define WS_NORM_MEAN_STD 0     /* out = (v - 255 mean_c) / (255 std_c)                  */
+#define WS_NORM_SCALE    1     /* out = v * scale                                       */
+
+#define WS_ORDER_RGB 0         /* source bytes are R, G, B; planes are written R, G, B  */
+
+/* Geometry and normalisation of the fused preprocess.
+ *
+ * Resize convention (the pages say only "centre-aligned"; this is the
+ * reading taken): destination pixel x of a box of D pixels samples source
+ * coordinate (x + 1/2) * S / D - 1/2 (half-pixel centres), held as the exact
+ * rational ((2x+1) S - D) / (2 D); the lower neighbour is its floor, the
+ * weight is the remainder divided by 2D in one correctly rounded float
+ * division, and both neighbours are clamped to [0, S-1] (clamp to edge).
+ * Four neighbours, no antialias prefilter.  Interpolation and normalisation
+ * are FP32.  Letterbox: scale min(dst_w/src_w, dst_h/src_h); the short side of
+ * the inner box is the scaled length rounded half up (at least 1 pixel); the
+ * box is centred with the odd padding pixel at the bottom / right; pixels
+ * outside it take pad_value, normalised like a source byte. */
+typedef struct ws_preprocess_desc {
+    int32_t src_w, src_h;         /* source frame size in pixels, 1 .. 65535          */
+    int64_t src_row_stride;       /* bytes between source rows, >= 3 * src_w         */
+    int64_t src_frame_stride;     /* bytes between frames, >= row_stride * src_h    */
+    int32_t dst_w, dst_h;         /* destination size, 1 .. 65535                    */
+    int32_t resize;               /* WS_RESIZE_*                                     */
+    int32_t pad_value;            /* 0 .. 255, letterbox padding byte (e.g. 114)     */
+    int32_t norm;                 /* WS_NORM_*                                       */
+    float   mean[3];              /* WS_NORM_MEAN_STD, in [0,1] units, per channel   */
+    float   std[3];               /* WS_NORM_MEAN_STD, > 0, in [0,1] units           */
+    float   scale;                /* WS_NORM_SCALE (e.g. 1/255)                      */
+    int32_t channel_order;        /* WS_ORDER_RGB                                    */
+} ws_preprocess_desc;
+
+/* Host-only check of a descriptor for a batch; enqueues nothing. */
+ws_status ws_preprocess_validate(const ws_preprocess_desc* desc, int32_t batch);
+
+/* Fused preprocess of `batch` frames.
+ *   src: device, uint8; byte (b, row j, column i, channel c) is at
+ *        src[b * src_frame_stride + j * src_row_stride + 3 * i + c].
+ *   dst: device, float32 [batch][3][dst_h][dst_w] (NCHW, contiguous).
+ * One kernel launch on `stream`.  Any alignment is accepted; a 16-byte
+ * aligned src, row stride and frame stride select the staged bulk-copy
+ * kernel, anything else a per-pixel kernel with the same results.
+ * Errors: WS_ERR_INVALID_ARGUMENT (NULL pointer, batch < 1, bad descriptor),
+ * WS_ERR_CUDA (launch failed). */
+ws_status ws_preprocess(const ws_preprocess_desc* desc, const uint8_t* src, int32_t batch,
+                        float* dst, cudaStream_t stream);
+
+/* ------------------------------------------------------------------- top-k */
+
+/* Host-only check: rows >= 1, 1 <= cols < 2^31, 1 <= k <= min(32, cols). */
+ws_status ws_topk_validate(int64_t rows, int64_t cols, int32_t k);
+
+/* Bytes of device workspace ws_topk needs for this shape (0 when every row
+ * fits one block).  Depends only on (rows, cols, k). */
+ws_status ws_topk_workspace_bytes(int64_t rows, int64_t cols, int32_t k, size_t* bytes);
+
+/* Zero a workspace before its first use (one cudaMemsetAsync on `stream`).
+ * Every completed ws_topk leaves it ready for the next call, so this is not
+ * needed between calls or graph replays. */
+ws_status ws_topk_workspace_init(void* workspace, size_t bytes, cudaStream_t stream);
+
+/* Exact Top-K of each row.
+ *   x:       device, float32 [rows][cols], read only.
+ *   out_val: device (or device view of mapped memory), float32 [rows][k].
+ *   out_idx: same, int32 [rows][k].
+ * Per row the k entries with the largest values in rank order; equal
+ * values (+0 equals -0) go to the lower index; NaN ranks as -inf.  out_val
+ * holds the input's own bits (-0.0 stays -0.0) except that NaN is written as
+ * -inf.  The result is unique, so it is bit-exact.
+ * workspace: device, at least ws_topk_workspace_bytes(), zeroed once by
+ * ws_topk_workspace_init() (or cudaMemset) before first use; calls that share
+ * a workspace must not overlap on the GPU.  May be NULL when the size is 0.
+ * One kernel launch on `stream`.
+ * Errors: WS_ERR_INVALID_ARGUMENT (shape, K, NULL pointer, workspace too
+ * small), WS_ERR_CUDA (launch failed). */
+ws_status ws_topk(const float* x, int64_t rows, int64_t cols, int32_t k,
+                  float* out_val, int32_t* out_idx,
+                  void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/* ------------------------------------------------------------------- lanes */
+
+#define WS_INPUT_DEVICE 0   /* producer writes a device buffer                       */
+#define WS_INPUT_MAPPED 1   /* producer writes mapped pinned host memory; the kernel reads it in place */
+#define WS_INPUT_COPY   2   /* producer writes pinned host memory; the graph copies it to the device first */
+
+#define WS_RESULT_DEVICE 0  /* Top-K result stays in device memory                   */
+#define WS_RESULT_MAPPED 1  /* Top-K kernel writes straight into mapped pinned host memory */
+#define WS_RESULT_COPY   2  /* result is copied into pinned host memory at the end of the graph */
+
+#define WS_LANE_FLAG_NO_GRAPH     1u  /* replay by direct launches instead of the CUDA Graph   */
+#define WS_LANE_FLAG_STAGE_TIMING 2u  /* event nodes around each stage for per-stage times   */
+#define WS_LANE_FLAG_NO_DEVICE    8u  /* host-only lane: no CUDA resource is made; submit marks
+                                         it in flight and the "GPU" finishes after fake_polls
+                                         completion queries.  Exercises the state machine on
+                                         machines without a GPU. */
+
+#define WS_LANE_FREE      0
+#define WS_LANE_ACQUIRED  1
+#define WS_LANE_IN_FLIGHT 2
+
+/* Everything a lane is built from.  Shapes are fixed for the lane's life.
+ * Each buffer pointer is optional: NULL makes the lane allocate (and own) it,
+ * non-NULL borrows the caller's buffer, which must outlive the lane. */
+typedef struct ws_lane_desc {
+    ws_preprocess_desc pre;       /* preprocess geometry                            */
+    int32_t  batch;               /* frames per submit                              */
+    int64_t  rows, cols;          /* logits shape                                   */
+    int32_t  k;                   /* Top-K per row, 1 .. 32                         */
+    int32_t  input_mode;          /* WS_INPUT_*                                     */
+    int32_t  result_mode;         /* WS_RESULT_*                                    */
+    uint32_t flags;               /* WS_LANE_FLAG_*                                 */
+    void*    input;               /* DEVICE: device buffer; MAPPED: host pointer of a
+                                     cudaHostAllocMapped allocation; COPY: pinned host
+                                     buffer.  batch * src_frame_stride bytes.       */
+    float*   tensor;              /* device, [batch][3][dst_h][dst_w]               */
+    float*   logits;              /* device, [rows][cols]; the network's output slot */
+    float*   result_val;          /* DEVICE: device; MAPPED: mapped host; COPY: pinned host; [rows][k] */
+    int32_t* result_idx;          /* same, int32 [rows][k]                          */
+    cudaStream_t stream;          /* NULL: the lane creates a non-blocking stream   */
+    int32_t  fake_polls;          /* WS_LANE_FLAG_NO_DEVICE only                    */
+} ws_lane_desc;
+
+typedef struct ws_lane ws_lane;
+
+/* Stable addresses of a lane's buffers (valid until ws_lane_destroy). */
+typedef struct ws_lane_buffers {
+    void*    input_host;          /* host view of the producer slot (MAPPED, COPY) or NULL */
+    void*    input_device;        /* device buffer the preprocess reads             */
+    float*   tensor;              /* device NCHW tensor                             */
+    float*   logits;              /* device logits                                  */
+    float*   result_val_host;     /* host view of the result (MAPPED, COPY) or NULL */
+    int32_t* result_idx_host;
+    float*   result_val_device;   /* where the Top-K kernel writes                  */
+    int32_t* result_idx_device;
+    size_t   input_bytes, tensor_bytes, logits_bytes, result_bytes;
+    cudaStream_t stream;
+} ws_lane_buffers;
+
+/* Times of one completed submit. */
+typedef struct ws_lane_timing {
+    float  gpu_us;         /* event before the graph launch -> event after the last stage */
+    float  preprocess_us;  /* STAGE_TIMING lanes: preprocess kernel alone, else -1   */
+    float  topk_us;        /* STAGE_TIMING lanes: Top-K kernel alone, else -1        */
+    double host_us;        /* steady clock, entry of submit -> return of wait       */
+} ws_lane_timing;
+
+/* Validate, allocate or borrow every buffer, run both kernels once directly
+ * (which settles any lazy set-up), capture copy-in -> preprocess -> Top-K ->
+ * copy-out into one graph on the lane's stream and instantiate it.  All
+ * allocation of the lane's life happens here.  Must not be called while the
+ * stream is being captured.  On failure everything made so far is released.
+ * Errors: WS_ERR_INVALID_ARGUMENT, WS_ERR_OUT_OF_MEMORY, WS_ERR_CUDA,
+ * WS_ERR_CAPTURE. */
+ws_status ws_lane_create(const ws_lane_desc* desc, ws_lane** lane);
+
+ws_status ws_lane_get_buffers(const ws_lane* lane, ws_lane_buffers* buffers);
+
+/* FREE -> ACQUIRED; WS_ERR_LANE_BUSY if the lane is acquired or in flight. */
+ws_status ws_lane_acquire(ws_lane* lane);
+
+/* ACQUIRED -> IN_FLIGHT: record the start event, launch the graph (or the
+ * direct launches), record the end event.  No allocation, no synchronisation.
+ * WS_ERR_LANE_STATE unless acquired; WS_ERR_CUDA if a launch fails (the lane
+ * then returns to ACQUIRED). */
+ws_status ws_lane_submit(ws_lane* lane);
+
+/* IN_FLIGHT -> FREE once the end event has completed.  timeout_us < 0 waits
+ * without limit; otherwise WS_ERR_TIMEOUT after timeout_us microseconds, with
+ * the lane still IN_FLIGHT (call again).  timing may be NULL.
+ * WS_ERR_LANE_STATE unless in flight; WS_ERR_CUDA if the GPU work failed
+ * (the lane is then FREE, its results undefined). */
+ws_status ws_lane_wait(ws_lane* lane, int64_t timeout_us, ws_lane_timing* timing);
+
+/* ACQUIRED -> FREE without a submit; WS_ERR_LANE_STATE otherwise. */
+ws_status ws_lane_release(ws_lane* lane);
+
+/* Free what the lane owns.  WS_ERR_LANE_BUSY while IN_FLIGHT (wait first). */
+ws_status ws_lane_destroy(ws_lane* lane);
+
+/* WS_LANE_FREE / ACQUIRED / IN_FLIGHT, or -1 for NULL. */
+int32_t ws_lane_state(const ws_lane* lane);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* WS_H */

@@ -1,0 +1,100 @@
+"""PyTorch-tensor front end of the C ABI (marshalling only).
+
+Tensors supply device memory, pinned host memory and streams; every result
+is computed by ``libws.so`` on the GPU.
+"""
+from __future__ import annotations
+
+import torch
+
+from . import binding as B
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def preprocess(frames: torch.Tensor, desc: B.ws_preprocess_desc, batch: int | None = None,
+               out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """ws_preprocess on a uint8 CUDA tensor holding `batch` frames."""
+    if frames.dtype != torch.uint8 or not frames.is_cuda:
+        raise TypeError("frames must be a uint8 CUDA tensor")
+    if batch is None:
+        batch = frames.shape[0]
+    if out is None:
+        out = torch.empty((batch, 3, desc.dst_h, desc.dst_w), dtype=torch.float32, device=frames.device)
+    B.check(B.ws_preprocess(desc, frames.data_ptr(), batch, out.data_ptr(), _stream(stream)))
+    return out
+
+
+def topk_workspace(rows: int, cols: int, k: int, device="cuda", stream=None) -> torch.Tensor | None:
+    """A zeroed workspace for ws_topk of this shape (None when none is needed)."""
+    st, n = B.ws_topk_workspace_bytes(rows, cols, k)
+    B.check(st)
+    if n == 0:
+        return None
+    ws = torch.empty(n + 256, dtype=torch.uint8, device=device)
+    off = (-ws.data_ptr()) % 256
+    ws = ws[off:off + n]
+    B.check(B.ws_topk_workspace_init(ws.data_ptr(), n, _stream(stream)))
+    return ws
+
+
+def topk(x: torch.Tensor, k: int, out_val: torch.Tensor | None = None, out_idx: torch.Tensor | None = None,
+         workspace: torch.Tensor | None = None, stream=None):
+    """ws_topk on a float32 CUDA tensor [rows, cols] (or [cols])."""
+    if x.dtype != torch.float32 or not x.is_cuda or not x.is_contiguous():
+        raise TypeError("x must be a contiguous float32 CUDA tensor")
+    rows, cols = (1, x.shape[0]) if x.dim() == 1 else x.shape
+    if out_val is None:
+        out_val = torch.empty((rows, k), dtype=torch.float32, device=x.device)
+    if out_idx is None:
+        out_idx = torch.empty((rows, k), dtype=torch.int32, device=x.device)
+    if workspace is None:
+        workspace = topk_workspace(rows, cols, k, x.device, stream)
+    wptr, wbytes = (workspace.data_ptr(), workspace.numel()) if workspace is not None else (None, 0)
+    B.check(B.ws_topk(x.data_ptr(), rows, cols, k, out_val.data_ptr(), out_idx.data_ptr(), wptr, wbytes,
+                      _stream(stream)))
+    return out_val, out_idx
+
+
+class Lane:
+    """One fixed-shape lane (ws_lane_*); destroyed by close() or `with`."""
+
+    def __init__(self, desc: B.ws_lane_desc):
+        st, h = B.ws_lane_create(desc)
+        B.check(st)
+        self.handle = h
+        st, self.buffers = B.ws_lane_get_buffers(h)
+        B.check(st)
+
+    def acquire(self):
+        B.check(B.ws_lane_acquire(self.handle))
+
+    def submit(self):
+        B.check(B.ws_lane_submit(self.handle))
+
+    def wait(self, timeout_us: int = -1) -> B.ws_lane_timing:
+        st, t = B.ws_lane_wait(self.handle, timeout_us)
+        B.check(st)
+        return t
+
+    def release(self):
+        B.check(B.ws_lane_release(self.handle))
+
+    @property
+    def state(self) -> int:
+        return B.ws_lane_state(self.handle)
+
+    def close(self):
+        if self.handle is not None:
+            B.check(B.ws_lane_destroy(self.handle))
+            self.handle = None
+
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *exc):
+        self.close()

@@ -1,0 +1,238 @@
+"""ctypes binding of ``include/ws.h`` (argument marshalling only).
+
+Every function of the header is exposed under its own name and returns the
+raw ``ws_status``; ``check()`` turns a non-zero status into ``WsError`` with
+the library's message.  All computation happens in ``libws.so`` on the GPU:
+this module never computes a result itself, and importing it fails loudly
+when the library has not been built.
+
+Pointers are plain integers (``tensor.data_ptr()``, ``stream.cuda_stream``),
+so PyTorch only supplies device memory, pinned host memory and streams.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+from . import build as _build
+
+WS_OK = 0
+WS_ERR_INVALID_ARGUMENT = 1
+WS_ERR_UNSUPPORTED = 2
+WS_ERR_CUDA = 3
+WS_ERR_OUT_OF_MEMORY = 4
+WS_ERR_LANE_STATE = 5
+WS_ERR_LANE_BUSY = 6
+WS_ERR_TIMEOUT = 7
+WS_ERR_CAPTURE = 8
+WS_ERR_DEVICE = 9
+
+WS_RESIZE_STRETCH, WS_RESIZE_LETTERBOX = 0, 1
+WS_NORM_MEAN_STD, WS_NORM_SCALE = 0, 1
+WS_ORDER_RGB = 0
+WS_INPUT_DEVICE, WS_INPUT_MAPPED, WS_INPUT_COPY = 0, 1, 2
+WS_RESULT_DEVICE, WS_RESULT_MAPPED, WS_RESULT_COPY = 0, 1, 2
+WS_LANE_FLAG_NO_GRAPH = 1
+WS_LANE_FLAG_STAGE_TIMING = 2
+WS_LANE_FLAG_NO_DEVICE = 8
+WS_LANE_FREE, WS_LANE_ACQUIRED, WS_LANE_IN_FLIGHT = 0, 1, 2
+
+_i32, _i64, _u32, _f32 = ctypes.c_int32, ctypes.c_int64, ctypes.c_uint32, ctypes.c_float
+_vp, _sz = ctypes.c_void_p, ctypes.c_size_t
+
+
+class ws_preprocess_desc(ctypes.Structure):
+    _fields_ = [("src_w", _i32), ("src_h", _i32), ("src_row_stride", _i64), ("src_frame_stride", _i64),
+                ("dst_w", _i32), ("dst_h", _i32), ("resize", _i32), ("pad_value", _i32), ("norm", _i32),
+                ("mean", _f32 * 3), ("std", _f32 * 3), ("scale", _f32), ("channel_order", _i32)]
+
+
+class ws_lane_desc(ctypes.Structure):
+    _fields_ = [("pre", ws_preprocess_desc), ("batch", _i32), ("rows", _i64), ("cols", _i64), ("k", _i32),
+                ("input_mode", _i32), ("result_mode", _i32), ("flags", _u32), ("input", _vp),
+                ("tensor", _vp), ("logits", _vp), ("result_val", _vp), ("result_idx", _vp),
+                ("stream", _vp), ("fake_polls", _i32)]
+
+
+class ws_lane_buffers(ctypes.Structure):
+    _fields_ = [("input_host", _vp), ("input_device", _vp), ("tensor", _vp), ("logits", _vp),
+                ("result_val_host", _vp), ("result_idx_host", _vp), ("result_val_device", _vp),
+                ("result_idx_device", _vp), ("input_bytes", _sz), ("tensor_bytes", _sz),
+                ("logits_bytes", _sz), ("result_bytes", _sz), ("stream", _vp)]
+
+
+class ws_lane_timing(ctypes.Structure):
+    _fields_ = [("gpu_us", _f32), ("preprocess_us", _f32), ("topk_us", _f32), ("host_us", ctypes.c_double)]
+
+
+# name: (restype, argtypes) -- one entry per declaration in include/ws.h
+SIGNATURES = {
+    "ws_status_string": (ctypes.c_char_p, [_i32]),
+    "ws_last_error": (ctypes.c_char_p, []),
+    "ws_version": (_i32, []),
+    "ws_device_error": (_i32, [ctypes.POINTER(_u32), _i32]),
+    "ws_preprocess_validate": (_i32, [ctypes.POINTER(ws_preprocess_desc), _i32]),
+    "ws_preprocess": (_i32, [ctypes.POINTER(ws_preprocess_desc), _vp, _i32, _vp, _vp]),
+    "ws_topk_validate": (_i32, [_i64, _i64, _i32]),
+    "ws_topk_workspace_bytes": (_i32, [_i64, _i64, _i32, ctypes.POINTER(_sz)]),
+    "ws_topk_workspace_init": (_i32, [_vp, _sz, _vp]),
+    "ws_topk": (_i32, [_vp, _i64, _i64, _i32, _vp, _vp, _vp, _sz, _vp]),
+    "ws_lane_create": (_i32, [ctypes.POINTER(ws_lane_desc), ctypes.POINTER(_vp)]),
+    "ws_lane_get_buffers": (_i32, [_vp, ctypes.POINTER(ws_lane_buffers)]),
+    "ws_lane_acquire": (_i32, [_vp]),
+    "ws_lane_submit": (_i32, [_vp]),
+    "ws_lane_wait": (_i32, [_vp, _i64, ctypes.POINTER(ws_lane_timing)]),
+    "ws_lane_release": (_i32, [_vp]),
+    "ws_lane_destroy": (_i32, [_vp]),
+    "ws_lane_state": (_i32, [_vp]),
+}
+
+
+def _load():
+    path = _build.LIBRARY
+    if not os.path.exists(path):
+        raise ImportError(
+            f"{path} is missing: build it first (python -m post_processing_gb300.build or "
+            "__graft_entry__.build()); there is no fallback implementation")
+    lib = ctypes.CDLL(path)
+    for name, (res, args) in SIGNATURES.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    return lib
+
+
+lib = _load()
+LIBRARY_PATH = _build.LIBRARY
+
+
+class WsError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"{ws_status_string(status)}: {message}")
+        self.status = status
+
+
+def check(status: int) -> int:
+    if status != WS_OK:
+        raise WsError(status, ws_last_error())
+    return status
+
+
+# ---- one Python function per C entry point, same names ----------------------
+
+def ws_status_string(status: int) -> str:
+    return lib.ws_status_string(status).decode()
+
+
+def ws_last_error() -> str:
+    return lib.ws_last_error().decode()
+
+
+def ws_version() -> int:
+    return lib.ws_version()
+
+
+def ws_device_error(clear: bool = False) -> tuple[int, int]:
+    flags = _u32(0)
+    st = lib.ws_device_error(ctypes.byref(flags), int(clear))
+    return st, flags.value
+
+
+def ws_preprocess_validate(desc: ws_preprocess_desc, batch: int) -> int:
+    return lib.ws_preprocess_validate(ctypes.byref(desc), batch)
+
+
+def ws_preprocess(desc: ws_preprocess_desc, src: int, batch: int, dst: int, stream: int = 0) -> int:
+    return lib.ws_preprocess(ctypes.byref(desc), src, batch, dst, stream)
+
+
+def ws_topk_validate(rows: int, cols: int, k: int) -> int:
+    return lib.ws_topk_validate(rows, cols, k)
+
+
+def ws_topk_workspace_bytes(rows: int, cols: int, k: int) -> tuple[int, int]:
+    n = _sz(0)
+    st = lib.ws_topk_workspace_bytes(rows, cols, k, ctypes.byref(n))
+    return st, n.value
+
+
+def ws_topk_workspace_init(workspace: int, nbytes: int, stream: int = 0) -> int:
+    return lib.ws_topk_workspace_init(workspace, nbytes, stream)
+
+
+def ws_topk(x: int, rows: int, cols: int, k: int, out_val: int, out_idx: int,
+            workspace: int | None, workspace_bytes: int, stream: int = 0) -> int:
+    return lib.ws_topk(x, rows, cols, k, out_val, out_idx, workspace or None, workspace_bytes, stream)
+
+
+def ws_lane_create(desc: ws_lane_desc) -> tuple[int, int | None]:
+    h = _vp()
+    st = lib.ws_lane_create(ctypes.byref(desc), ctypes.byref(h))
+    return st, h.value
+
+
+def ws_lane_get_buffers(lane: int) -> tuple[int, ws_lane_buffers]:
+    b = ws_lane_buffers()
+    st = lib.ws_lane_get_buffers(lane, ctypes.byref(b))
+    return st, b
+
+
+def ws_lane_acquire(lane: int) -> int:
+    return lib.ws_lane_acquire(lane)
+
+
+def ws_lane_submit(lane: int) -> int:
+    return lib.ws_lane_submit(lane)
+
+
+def ws_lane_wait(lane: int, timeout_us: int = -1) -> tuple[int, ws_lane_timing]:
+    t = ws_lane_timing()
+    st = lib.ws_lane_wait(lane, timeout_us, ctypes.byref(t))
+    return st, t
+
+
+def ws_lane_release(lane: int) -> int:
+    return lib.ws_lane_release(lane)
+
+
+def ws_lane_destroy(lane: int) -> int:
+    return lib.ws_lane_destroy(lane)
+
+
+def ws_lane_state(lane: int | None) -> int:
+    return lib.ws_lane_state(lane)
+
+
+# ---- descriptor helpers ------------------------------------------------------
+
+def preprocess_desc(src_w: int, src_h: int, dst_w: int, dst_h: int, *, letterbox: bool = False,
+                    pad_value: int = 114, norm: str = "mean_std",
+                    mean=(0.485, 0.456, 0.406), std=(0.229, 0.224, 0.225), scale: float = 1.0 / 255.0,
+                    row_stride: int | None = None, frame_stride: int | None = None) -> ws_preprocess_desc:
+    d = ws_preprocess_desc()
+    d.src_w, d.src_h, d.dst_w, d.dst_h = src_w, src_h, dst_w, dst_h
+    d.src_row_stride = 3 * src_w if row_stride is None else row_stride
+    d.src_frame_stride = d.src_row_stride * src_h if frame_stride is None else frame_stride
+    d.resize = WS_RESIZE_LETTERBOX if letterbox else WS_RESIZE_STRETCH
+    d.pad_value = pad_value
+    d.norm = WS_NORM_MEAN_STD if norm == "mean_std" else WS_NORM_SCALE
+    d.mean[:] = list(mean)
+    d.std[:] = list(std)
+    d.scale = scale
+    d.channel_order = WS_ORDER_RGB
+    return d
+
+
+def lane_desc(pre: ws_preprocess_desc, batch: int, rows: int, cols: int, k: int, *,
+              input_mode: int = WS_INPUT_DEVICE, result_mode: int = WS_RESULT_DEVICE, flags: int = 0,
+              input: int | None = None, tensor: int | None = None, logits: int | None = None,
+              result_val: int | None = None, result_idx: int | None = None, stream: int | None = None,
+              fake_polls: int = 0) -> ws_lane_desc:
+    d = ws_lane_desc()
+    d.pre = pre
+    d.batch, d.rows, d.cols, d.k = batch, rows, cols, k
+    d.input_mode, d.result_mode, d.flags = input_mode, result_mode, flags
+    d.input, d.tensor, d.logits = input, tensor, logits
+    d.result_val, d.result_idx, d.stream = result_val, result_idx, stream
+    d.fake_polls = fake_polls
+    return d

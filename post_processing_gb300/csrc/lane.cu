@@ -1,0 +1,455 @@
+// lane.cu -- fixed-shape execution lanes: preallocated buffers, one CUDA
+// Graph per lane, an explicit FREE -> ACQUIRED -> IN_FLIGHT -> FREE state
+// machine and event-timed submit / wait.
+//
+// Follows "Inside WarpStream TRT" (lane and CUDA Graph sections): every lane
+// owns its buffers, two timing events and a non-blocking stream; the work is
+// captured once (thread-local capture mode) and replayed with one launch;
+// submit records an event, launches the graph and records completion; the
+// application synchronises only in wait; a lane is never submitted unless
+// acquired nor reused while busy.  And "Streams, concurrency and CUDA Graphs"
+// (CUDA handbook, CUDA Graphs section): fixed addresses, capture once,
+// instantiate once, nothing synchronising inside the graph.  The network
+// between the two stages is not part of this library: its slot in the graph
+// is the logits buffer, which the caller fills.
+#include <chrono>
+#include <cstring>
+#include <new>
+
+#include "ws_internal.cuh"
+
+struct ws_lane {
+    ws_lane_desc d{};
+    int state = WS_LANE_FREE;
+    bool fake = false;
+    int fake_left = 0;
+
+    cudaStream_t stream = nullptr;
+    bool own_stream = false;
+
+    void* in_host = nullptr;       // MAPPED / COPY: host view
+    void* in_dev = nullptr;        // what the preprocess reads
+    bool own_in_host = false, own_in_dev = false;
+    float* tensor = nullptr;
+    bool own_tensor = false;
+    float* logits = nullptr;
+    bool own_logits = false;
+    float* rv_host = nullptr;
+    int32_t* ri_host = nullptr;
+    float* rv_dev = nullptr;
+    int32_t* ri_dev = nullptr;
+    bool own_r_host = false, own_r_dev = false;
+    void* ws = nullptr;
+    size_t ws_bytes = 0;
+
+    size_t input_bytes = 0, tensor_bytes = 0, logits_bytes = 0, result_bytes = 0;
+
+    cudaEvent_t ev_start = nullptr, ev_end = nullptr;
+    cudaEvent_t ev_pre0 = nullptr, ev_pre1 = nullptr, ev_topk1 = nullptr;
+    cudaGraph_t graph = nullptr;
+    cudaGraphExec_t exec = nullptr;
+    std::chrono::steady_clock::time_point t_submit;
+};
+
+namespace ws {
+namespace {
+
+bool stage_timing(const ws_lane* L) { return (L->d.flags & WS_LANE_FLAG_STAGE_TIMING) != 0; }
+bool use_graph(const ws_lane* L) { return (L->d.flags & WS_LANE_FLAG_NO_GRAPH) == 0; }
+
+void release_all(ws_lane* L) {
+    if (L->fake) return;
+    if (L->exec) cudaGraphExecDestroy(L->exec);
+    if (L->graph) cudaGraphDestroy(L->graph);
+    for (cudaEvent_t e : {L->ev_start, L->ev_end, L->ev_pre0, L->ev_pre1, L->ev_topk1})
+        if (e) cudaEventDestroy(e);
+    if (L->ws) cudaFree(L->ws);
+    if (L->own_r_dev) {
+        cudaFree(L->rv_dev);
+        cudaFree(L->ri_dev);
+    }
+    if (L->own_r_host) {
+        cudaFreeHost(L->rv_host);
+        cudaFreeHost(L->ri_host);
+    }
+    if (L->own_logits) cudaFree(L->logits);
+    if (L->own_tensor) cudaFree(L->tensor);
+    if (L->own_in_dev) cudaFree(L->in_dev);
+    if (L->own_in_host) cudaFreeHost(L->in_host);
+    if (L->own_stream) cudaStreamDestroy(L->stream);
+}
+
+ws_status alloc_dev(void** p, size_t bytes, const char* what) {
+    cudaError_t e = cudaMalloc(p, bytes);
+    if (e == cudaErrorMemoryAllocation) {
+        cudaGetLastError();
+        return fail(WS_ERR_OUT_OF_MEMORY, "cudaMalloc of %zu bytes for %s", bytes, what);
+    }
+    if (e != cudaSuccess) return cuda_fail(e, what);
+    return WS_OK;
+}
+
+ws_status alloc_host(void** p, size_t bytes, unsigned flags, const char* what) {
+    cudaError_t e = cudaHostAlloc(p, bytes, flags);
+    if (e == cudaErrorMemoryAllocation) {
+        cudaGetLastError();
+        return fail(WS_ERR_OUT_OF_MEMORY, "cudaHostAlloc of %zu bytes for %s", bytes, what);
+    }
+    if (e != cudaSuccess) return cuda_fail(e, what);
+    return WS_OK;
+}
+
+ws_status device_view(void* host, void** dev, const char* what) {
+    cudaError_t e = cudaHostGetDevicePointer(dev, host, 0);
+    if (e != cudaSuccess)
+        return fail(WS_ERR_INVALID_ARGUMENT, "%s is not mapped pinned memory (%s)", what, cudaGetErrorName(e));
+    return WS_OK;
+}
+
+ws_status record(cudaEvent_t ev, cudaStream_t s, bool capturing) {
+    WS_TRY_CUDA(cudaEventRecordWithFlags(ev, s, capturing ? cudaEventRecordExternal : cudaEventRecordDefault));
+    return WS_OK;
+}
+
+// The lane's whole path, enqueued on its stream: captured once into the
+// graph, and also used directly for the warm-up and NO_GRAPH lanes.
+ws_status enqueue_path(ws_lane* L, bool capturing) {
+    ws_status st;
+    if (L->d.input_mode == WS_INPUT_COPY)
+        WS_TRY_CUDA(cudaMemcpyAsync(L->in_dev, L->in_host, L->input_bytes, cudaMemcpyHostToDevice, L->stream));
+    if (stage_timing(L) && (st = record(L->ev_pre0, L->stream, capturing)) != WS_OK) return st;
+    st = ws_preprocess(&L->d.pre, static_cast<const uint8_t*>(L->in_dev), L->d.batch, L->tensor, L->stream);
+    if (st != WS_OK) return st;
+    if (stage_timing(L) && (st = record(L->ev_pre1, L->stream, capturing)) != WS_OK) return st;
+    st = ws_topk(L->logits, L->d.rows, L->d.cols, L->d.k, L->rv_dev, L->ri_dev, L->ws, L->ws_bytes, L->stream);
+    if (st != WS_OK) return st;
+    if (stage_timing(L) && (st = record(L->ev_topk1, L->stream, capturing)) != WS_OK) return st;
+    if (L->d.result_mode == WS_RESULT_COPY) {
+        const size_t n = (size_t)L->d.rows * L->d.k;
+        WS_TRY_CUDA(cudaMemcpyAsync(L->rv_host, L->rv_dev, n * 4, cudaMemcpyDeviceToHost, L->stream));
+        WS_TRY_CUDA(cudaMemcpyAsync(L->ri_host, L->ri_dev, n * 4, cudaMemcpyDeviceToHost, L->stream));
+    }
+    return WS_OK;
+}
+
+ws_status build(ws_lane* L) {
+    const ws_lane_desc& d = L->d;
+    if (d.stream) {
+        L->stream = d.stream;
+    } else {
+        WS_TRY_CUDA(cudaStreamCreateWithFlags(&L->stream, cudaStreamNonBlocking));
+        L->own_stream = true;
+    }
+    ws_status st;
+    L->input_bytes = (size_t)d.batch * (size_t)d.pre.src_frame_stride;
+    L->tensor_bytes = (size_t)d.batch * 3 * d.pre.dst_h * d.pre.dst_w * sizeof(float);
+    L->logits_bytes = (size_t)d.rows * d.cols * sizeof(float);
+    L->result_bytes = (size_t)d.rows * d.k * sizeof(float);
+
+    // producer slot
+    switch (d.input_mode) {
+        case WS_INPUT_DEVICE:
+            if (d.input) {
+                L->in_dev = d.input;
+            } else {
+                if ((st = alloc_dev(&L->in_dev, L->input_bytes, "input")) != WS_OK) return st;
+                L->own_in_dev = true;
+            }
+            break;
+        case WS_INPUT_MAPPED:
+            if (d.input) {
+                L->in_host = d.input;
+            } else {
+                if ((st = alloc_host(&L->in_host, L->input_bytes, cudaHostAllocMapped, "input")) != WS_OK)
+                    return st;
+                L->own_in_host = true;
+            }
+            if ((st = device_view(L->in_host, &L->in_dev, "input")) != WS_OK) return st;
+            break;
+        case WS_INPUT_COPY:
+            if (d.input) {
+                L->in_host = d.input;
+            } else {
+                if ((st = alloc_host(&L->in_host, L->input_bytes, cudaHostAllocDefault, "input")) != WS_OK)
+                    return st;
+                L->own_in_host = true;
+            }
+            if ((st = alloc_dev(&L->in_dev, L->input_bytes, "input copy")) != WS_OK) return st;
+            L->own_in_dev = true;
+            break;
+        default:
+            return fail(WS_ERR_INVALID_ARGUMENT, "input mode %d", d.input_mode);
+    }
+
+    if (d.tensor) {
+        L->tensor = d.tensor;
+    } else {
+        if ((st = alloc_dev((void**)&L->tensor, L->tensor_bytes, "tensor")) != WS_OK) return st;
+        L->own_tensor = true;
+    }
+    if (d.logits) {
+        L->logits = d.logits;
+    } else {
+        if ((st = alloc_dev((void**)&L->logits, L->logits_bytes, "logits")) != WS_OK) return st;
+        L->own_logits = true;
+        WS_TRY_CUDA(cudaMemsetAsync(L->logits, 0, L->logits_bytes, L->stream));
+    }
+
+    // result slot
+    if ((d.result_val == nullptr) != (d.result_idx == nullptr))
+        return fail(WS_ERR_INVALID_ARGUMENT, "result_val and result_idx must both be given or both NULL");
+    switch (d.result_mode) {
+        case WS_RESULT_DEVICE:
+            if (d.result_val) {
+                L->rv_dev = d.result_val;
+                L->ri_dev = d.result_idx;
+            } else {
+                if ((st = alloc_dev((void**)&L->rv_dev, L->result_bytes, "result")) != WS_OK) return st;
+                if ((st = alloc_dev((void**)&L->ri_dev, L->result_bytes, "result")) != WS_OK) {
+                    cudaFree(L->rv_dev);
+                    L->rv_dev = nullptr;
+                    return st;
+                }
+                L->own_r_dev = true;
+            }
+            break;
+        case WS_RESULT_MAPPED:
+        case WS_RESULT_COPY: {
+            const unsigned flags = d.result_mode == WS_RESULT_MAPPED ? cudaHostAllocMapped : cudaHostAllocDefault;
+            if (d.result_val) {
+                L->rv_host = d.result_val;
+                L->ri_host = d.result_idx;
+            } else {
+                if ((st = alloc_host((void**)&L->rv_host, L->result_bytes, flags, "result")) != WS_OK) return st;
+                if ((st = alloc_host((void**)&L->ri_host, L->result_bytes, flags, "result")) != WS_OK) {
+                    cudaFreeHost(L->rv_host);
+                    L->rv_host = nullptr;
+                    return st;
+                }
+                L->own_r_host = true;
+            }
+            if (d.result_mode == WS_RESULT_MAPPED) {
+                if ((st = device_view(L->rv_host, (void**)&L->rv_dev, "result_val")) != WS_OK) return st;
+                if ((st = device_view(L->ri_host, (void**)&L->ri_dev, "result_idx")) != WS_OK) return st;
+            } else {
+                if ((st = alloc_dev((void**)&L->rv_dev, L->result_bytes, "result")) != WS_OK) return st;
+                if ((st = alloc_dev((void**)&L->ri_dev, L->result_bytes, "result")) != WS_OK) {
+                    cudaFree(L->rv_dev);
+                    L->rv_dev = nullptr;
+                    return st;
+                }
+                L->own_r_dev = true;
+            }
+            break;
+        }
+        default:
+            return fail(WS_ERR_INVALID_ARGUMENT, "result mode %d", d.result_mode);
+    }
+
+    L->ws_bytes = topk_workspace_size(d.rows, d.cols, d.k);
+    if (L->ws_bytes) {
+        if ((st = alloc_dev(&L->ws, L->ws_bytes, "top-k workspace")) != WS_OK) return st;
+        WS_TRY_CUDA(cudaMemsetAsync(L->ws, 0, L->ws_bytes, L->stream));
+    }
+
+    WS_TRY_CUDA(cudaEventCreate(&L->ev_start));
+    WS_TRY_CUDA(cudaEventCreate(&L->ev_end));
+    if (stage_timing(L)) {
+        WS_TRY_CUDA(cudaEventCreate(&L->ev_pre0));
+        WS_TRY_CUDA(cudaEventCreate(&L->ev_pre1));
+        WS_TRY_CUDA(cudaEventCreate(&L->ev_topk1));
+    }
+
+    // Warm direct run: settles lazy module loading and kernel attributes
+    // before anything is captured.
+    if ((st = enqueue_path(L, false)) != WS_OK) return st;
+    WS_TRY_CUDA(cudaStreamSynchronize(L->stream));
+
+    if (use_graph(L)) {
+        cudaError_t e = cudaStreamBeginCapture(L->stream, cudaStreamCaptureModeThreadLocal);
+        if (e != cudaSuccess) return fail(WS_ERR_CAPTURE, "begin capture: %s", cudaGetErrorName(e));
+        st = enqueue_path(L, true);
+        cudaGraph_t g = nullptr;
+        e = cudaStreamEndCapture(L->stream, &g);
+        L->graph = g;
+        if (st != WS_OK) return st;
+        if (e != cudaSuccess) return fail(WS_ERR_CAPTURE, "end capture: %s", cudaGetErrorName(e));
+        e = cudaGraphInstantiateWithFlags(&L->exec, L->graph, 0);
+        if (e != cudaSuccess) return fail(WS_ERR_CAPTURE, "instantiate: %s", cudaGetErrorName(e));
+        // Upload once so the first submit pays no first-launch set-up.
+        e = cudaGraphUpload(L->exec, L->stream);
+        if (e != cudaSuccess) return fail(WS_ERR_CAPTURE, "upload: %s", cudaGetErrorName(e));
+        WS_TRY_CUDA(cudaStreamSynchronize(L->stream));
+    }
+    return WS_OK;
+}
+
+ws_status validate_lane(const ws_lane_desc* d) {
+    if (!d) return fail(WS_ERR_INVALID_ARGUMENT, "descriptor is NULL");
+    ws_status st = validate_preprocess(&d->pre, d->batch);
+    if (st != WS_OK) return st;
+    if ((st = validate_topk(d->rows, d->cols, d->k)) != WS_OK) return st;
+    if (d->input_mode < WS_INPUT_DEVICE || d->input_mode > WS_INPUT_COPY)
+        return fail(WS_ERR_INVALID_ARGUMENT, "input mode %d", d->input_mode);
+    if (d->result_mode < WS_RESULT_DEVICE || d->result_mode > WS_RESULT_COPY)
+        return fail(WS_ERR_INVALID_ARGUMENT, "result mode %d", d->result_mode);
+    const uint32_t known = WS_LANE_FLAG_NO_GRAPH | WS_LANE_FLAG_STAGE_TIMING | WS_LANE_FLAG_NO_DEVICE;
+    if (d->flags & ~known) return fail(WS_ERR_INVALID_ARGUMENT, "unknown flags 0x%x", d->flags & ~known);
+    if ((d->flags & WS_LANE_FLAG_NO_DEVICE) && d->fake_polls < 0)
+        return fail(WS_ERR_INVALID_ARGUMENT, "fake_polls %d < 0", d->fake_polls);
+    return WS_OK;
+}
+
+}  // namespace
+}  // namespace ws
+
+extern "C" {
+
+ws_status ws_lane_create(const ws_lane_desc* desc, ws_lane** out) {
+    using namespace ws;
+    clear_error();
+    if (!out) return fail(WS_ERR_INVALID_ARGUMENT, "lane output pointer is NULL");
+    *out = nullptr;
+    ws_status st = validate_lane(desc);
+    if (st != WS_OK) return st;
+    ws_lane* L = new (std::nothrow) ws_lane();
+    if (!L) return fail(WS_ERR_OUT_OF_MEMORY, "lane object");
+    L->d = *desc;
+    if (desc->flags & WS_LANE_FLAG_NO_DEVICE) {
+        L->fake = true;
+        *out = L;
+        return WS_OK;
+    }
+    st = build(L);
+    if (st != WS_OK) {
+        // keep the message of the failure, not of the cleanup
+        release_all(L);
+        delete L;
+        cudaGetLastError();
+        return st;
+    }
+    *out = L;
+    return WS_OK;
+}
+
+ws_status ws_lane_get_buffers(const ws_lane* L, ws_lane_buffers* b) {
+    ws::clear_error();
+    if (!L || !b) return ws::fail(WS_ERR_INVALID_ARGUMENT, "lane or buffers is NULL");
+    std::memset(b, 0, sizeof *b);
+    b->input_host = L->in_host;
+    b->input_device = L->in_dev;
+    b->tensor = L->tensor;
+    b->logits = L->logits;
+    b->result_val_host = L->rv_host;
+    b->result_idx_host = L->ri_host;
+    b->result_val_device = L->rv_dev;
+    b->result_idx_device = L->ri_dev;
+    b->input_bytes = L->input_bytes;
+    b->tensor_bytes = L->tensor_bytes;
+    b->logits_bytes = L->logits_bytes;
+    b->result_bytes = L->result_bytes;
+    b->stream = L->stream;
+    return WS_OK;
+}
+
+ws_status ws_lane_acquire(ws_lane* L) {
+    ws::clear_error();
+    if (!L) return ws::fail(WS_ERR_INVALID_ARGUMENT, "lane is NULL");
+    if (L->state != WS_LANE_FREE)
+        return ws::fail(WS_ERR_LANE_BUSY, "lane is %s", L->state == WS_LANE_ACQUIRED ? "acquired" : "in flight");
+    L->state = WS_LANE_ACQUIRED;
+    return WS_OK;
+}
+
+ws_status ws_lane_submit(ws_lane* L) {
+    using namespace ws;
+    clear_error();
+    if (!L) return fail(WS_ERR_INVALID_ARGUMENT, "lane is NULL");
+    if (L->state != WS_LANE_ACQUIRED)
+        return fail(WS_ERR_LANE_STATE, "submit needs an acquired lane (state %d)", L->state);
+    L->t_submit = std::chrono::steady_clock::now();
+    if (L->fake) {
+        L->fake_left = L->d.fake_polls;
+        L->state = WS_LANE_IN_FLIGHT;
+        return WS_OK;
+    }
+    cudaError_t e = cudaEventRecord(L->ev_start, L->stream);
+    if (e != cudaSuccess) return cuda_fail(e, "record start event");
+    if (use_graph(L)) {
+        e = cudaGraphLaunch(L->exec, L->stream);
+        if (e != cudaSuccess) return cuda_fail(e, "graph launch");
+    } else {
+        ws_status st = enqueue_path(L, false);
+        if (st != WS_OK) return st;
+    }
+    e = cudaEventRecord(L->ev_end, L->stream);
+    if (e != cudaSuccess) return cuda_fail(e, "record end event");
+    L->state = WS_LANE_IN_FLIGHT;
+    return WS_OK;
+}
+
+ws_status ws_lane_wait(ws_lane* L, int64_t timeout_us, ws_lane_timing* timing) {
+    using namespace ws;
+    clear_error();
+    if (!L) return fail(WS_ERR_INVALID_ARGUMENT, "lane is NULL");
+    if (L->state != WS_LANE_IN_FLIGHT) return fail(WS_ERR_LANE_STATE, "wait needs a lane in flight");
+    const auto t0 = std::chrono::steady_clock::now();
+    for (;;) {
+        cudaError_t e;
+        if (L->fake) {
+            e = L->fake_left > 0 ? cudaErrorNotReady : cudaSuccess;
+            if (L->fake_left > 0) --L->fake_left;
+        } else {
+            e = cudaEventQuery(L->ev_end);
+        }
+        if (e == cudaSuccess) break;
+        if (e != cudaErrorNotReady) {
+            L->state = WS_LANE_FREE;
+            return cuda_fail(e, "lane work");
+        }
+        if (timeout_us >= 0) {
+            const auto waited =
+                std::chrono::duration_cast<std::chrono::microseconds>(std::chrono::steady_clock::now() - t0);
+            if (waited.count() >= timeout_us) return fail(WS_ERR_TIMEOUT, "lane still in flight");
+        }
+    }
+    const auto t1 = std::chrono::steady_clock::now();
+    if (timing) {
+        timing->host_us = std::chrono::duration<double, std::micro>(t1 - L->t_submit).count();
+        timing->gpu_us = timing->preprocess_us = timing->topk_us = -1.f;
+        if (!L->fake) {
+            float ms = 0.f;
+            if (cudaEventElapsedTime(&ms, L->ev_start, L->ev_end) == cudaSuccess) timing->gpu_us = ms * 1000.f;
+            if (stage_timing(L)) {
+                if (cudaEventElapsedTime(&ms, L->ev_pre0, L->ev_pre1) == cudaSuccess)
+                    timing->preprocess_us = ms * 1000.f;
+                if (cudaEventElapsedTime(&ms, L->ev_pre1, L->ev_topk1) == cudaSuccess)
+                    timing->topk_us = ms * 1000.f;
+            }
+            cudaGetLastError();
+        }
+    }
+    L->state = WS_LANE_FREE;
+    return WS_OK;
+}
+
+ws_status ws_lane_release(ws_lane* L) {
+    ws::clear_error();
+    if (!L) return ws::fail(WS_ERR_INVALID_ARGUMENT, "lane is NULL");
+    if (L->state != WS_LANE_ACQUIRED) return ws::fail(WS_ERR_LANE_STATE, "release needs an acquired lane");
+    L->state = WS_LANE_FREE;
+    return WS_OK;
+}
+
+ws_status ws_lane_destroy(ws_lane* L) {
+    ws::clear_error();
+    if (!L) return ws::fail(WS_ERR_INVALID_ARGUMENT, "lane is NULL");
+    if (L->state == WS_LANE_IN_FLIGHT) return ws::fail(WS_ERR_LANE_BUSY, "lane is in flight; wait first");
+    ws::release_all(L);
+    delete L;
+    return WS_OK;
+}
+
+int32_t ws_lane_state(const ws_lane* L) { return L ? L->state : -1; }
+
+}  // extern "C"

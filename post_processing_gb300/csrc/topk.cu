@@ -1,0 +1,409 @@
+// topk.cu -- exact row-wise Top-K (K <= 32) over device FP32 logits, sm_103a.
+//
+// What it computes ("Inside WarpStream TRT", Top-K section): per row the K
+// largest values, exact, ties to the lower index, NaN ranked as -inf, and only
+// the K value/index pairs are written.  The page's own kernel repeats a
+// block-wide arg-max K times (work ~ classes x K) and says large label spaces
+// need hierarchical or radix selection instead; this kernel is built for both.
+//
+// Keys.  Each element becomes one 64-bit key: the upper word maps the float
+// (NaN -> -inf, -0 -> +0) to an unsigned integer with the same order, the
+// lower word is the bitwise complement of the index, so a larger key is a
+// larger value or, for equal values, a lower index.  Keys are unique, the
+// order is total and the Top-K set is unique: results are bit-exact.
+//
+// One block per (row, chunk of up to 8192 elements):
+//  1. Coalesced 16-byte loads; each thread keeps its 32 order-mapped values in
+//     registers and their maximum (a "delegate").
+//  2. Threshold without sorting: each warp finds the ceil(K/8)-th largest of
+//     its 32 delegates with warp max-reductions; t = the minimum over warps.
+//     Every warp then owns ceil(K/8) distinct elements >= t, so at least K
+//     elements of the chunk are >= t and the chunk's Top-K are all among them.
+//  3. Elements >= t (typically a few dozen) are appended to shared memory.
+//  4. Each candidate's rank is the number of candidates with a larger key
+//     (keys are unique, so ranks are distinct): rank < K is written in place.
+//  If more than 2048 elements pass the threshold (adversarial inputs, e.g. a
+//  constant row), an exact radix select on the 64-bit keys (8 passes of 8
+//  bits, warp-aggregated shared histograms) finds the K-th key instead.
+// Rows longer than one chunk: every chunk writes its K keys to a workspace;
+// the last block of the row to finish (an atomic ticket, reset by that block
+// so the workspace is ready for the next call or graph replay) merges the
+// chunks' keys with the same threshold / rank steps, taking as threshold the
+// largest K-th key over chunks.
+#include <cmath>
+
+#include "ws_internal.cuh"
+
+namespace ws {
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kWarps = kThreads / 32;
+constexpr int kVpt = 32;                       // values per thread
+constexpr int kChunk = kThreads * kVpt;        // 8192 elements per block
+constexpr int kCap = 2048;                     // shared candidate capacity
+constexpr int kMaxK = 32;
+constexpr unsigned kFull = 0xffffffffu;
+
+struct TopkParams {
+    const float* x;
+    long long cols;
+    int k;
+    int nchunks;
+    float* out_val;
+    int* out_idx;
+    unsigned int* tickets;        // [rows]
+    unsigned long long* keys;     // [rows][nchunks][k]
+};
+
+__device__ __forceinline__ uint32_t order_bits(float f) {
+    uint32_t b = __float_as_uint(f);
+    if ((b & 0x7fffffffu) > 0x7f800000u) b = 0xff800000u;   // NaN -> -inf
+    if (b == 0x80000000u) b = 0u;                            // -0 -> +0 (ordering only)
+    return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+
+__device__ __forceinline__ unsigned long long make_key(uint32_t u, uint32_t idx) {
+    return ((unsigned long long)u << 32) | (uint32_t)(~idx);
+}
+
+__device__ __forceinline__ uint32_t key_index(unsigned long long key) {
+    return ~(uint32_t)(key & 0xffffffffull);
+}
+
+__device__ __forceinline__ unsigned long long warp_max_u64(unsigned long long v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        const unsigned long long w = __shfl_xor_sync(kFull, v, o);
+        v = w > v ? w : v;
+    }
+    return v;
+}
+
+struct Shared {
+    unsigned long long cand[kCap];
+    unsigned long long red[kWarps];
+    uint32_t hist[256];
+    uint32_t warp_t[kWarps];
+    uint32_t cnt;
+    uint32_t sel[2];
+    int last;
+};
+
+// Exact kth-largest (1-based) of n unique 64-bit keys by radix select.
+template <class KeyAt>
+__device__ unsigned long long block_kth_largest(KeyAt key_at, int n, int kth, Shared& s) {
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    unsigned long long prefix = 0, mask = 0;
+    uint32_t remaining = (uint32_t)kth;
+    for (int shift = 56; shift >= 0; shift -= 8) {
+        for (int i = tid; i < 256; i += kThreads) s.hist[i] = 0;
+        __syncthreads();
+        for (int base = warp * 32; base < n; base += kThreads) {
+            const int i = base + lane;
+            uint32_t bin = 256;
+            if (i < n) {
+                const unsigned long long key = key_at(i);
+                if ((key & mask) == prefix) bin = (uint32_t)(key >> shift) & 255u;
+            }
+            const unsigned peers = __match_any_sync(kFull, bin);
+            if (bin < 256 && lane == __ffs(peers) - 1) atomicAdd(&s.hist[bin], (uint32_t)__popc(peers));
+        }
+        __syncthreads();
+        if (warp == 0) {
+            // lane l owns bins 255-8l down to 248-8l
+            uint32_t c[8], sum = 0;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                c[j] = s.hist[255 - 8 * lane - j];
+                sum += c[j];
+            }
+            uint32_t incl = sum;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const uint32_t v = __shfl_up_sync(kFull, incl, o);
+                if (lane >= o) incl += v;
+            }
+            const uint32_t excl = incl - sum;
+            if (excl < remaining && remaining <= incl) {
+                uint32_t acc = excl;
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    if (acc < remaining && remaining <= acc + c[j]) {
+                        s.sel[0] = 255u - 8u * lane - j;
+                        s.sel[1] = remaining - acc;
+                    }
+                    acc += c[j];
+                }
+            }
+        }
+        __syncthreads();
+        prefix |= (unsigned long long)s.sel[0] << shift;
+        mask |= 0xffull << shift;
+        remaining = s.sel[1];
+        __syncthreads();
+    }
+    return prefix;
+}
+
+// Ranks the `cnt` unique candidates in s.cand; calls emit(rank, key) for
+// ranks below `kk`.
+template <class Emit>
+__device__ __forceinline__ void rank_and_emit(const Shared& s, uint32_t cnt, int kk, Emit emit) {
+    for (uint32_t i = threadIdx.x; i < cnt; i += kThreads) {
+        const unsigned long long key = s.cand[i];
+        int rank = 0;
+        for (uint32_t j = 0; j < cnt; ++j) rank += (s.cand[j] > key) ? 1 : 0;
+        if (rank < kk) emit(rank, key);
+    }
+}
+
+template <bool kVec>
+__global__ void __launch_bounds__(kThreads) topk_kernel(const __grid_constant__ TopkParams p) {
+    __shared__ Shared s;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const long long row = blockIdx.x / p.nchunks;
+    const int chunk = (int)(blockIdx.x - row * p.nchunks);
+    const long long c0 = (long long)chunk * kChunk;
+    const int n = (int)min((long long)kChunk, p.cols - c0);
+    const float* xr = p.x + row * p.cols;
+    const int k = p.k;
+
+    // 1. load, order-map, delegate
+    uint32_t u[kVpt];
+    if (kVec) {
+#pragma unroll
+        for (int i = 0; i < kVpt / 4; ++i) {
+            const int e = (i * kThreads + tid) * 4;
+            if (e < n) {
+                const float4 v = __ldcs(reinterpret_cast<const float4*>(xr + c0 + e));
+                u[4 * i + 0] = order_bits(v.x);
+                u[4 * i + 1] = order_bits(v.y);
+                u[4 * i + 2] = order_bits(v.z);
+                u[4 * i + 3] = order_bits(v.w);
+            } else {
+                u[4 * i + 0] = u[4 * i + 1] = u[4 * i + 2] = u[4 * i + 3] = 0u;
+            }
+        }
+    } else {
+#pragma unroll
+        for (int i = 0; i < kVpt; ++i) {
+            const int e = i * kThreads + tid;
+            u[i] = e < n ? order_bits(__ldcs(xr + c0 + e)) : 0u;
+        }
+    }
+    auto elem = [&](int j) -> int {   // chunk-relative element index of u[j]
+        return kVec ? ((j >> 2) * kThreads + tid) * 4 + (j & 3) : j * kThreads + tid;
+    };
+    uint32_t d = 0;
+#pragma unroll
+    for (int j = 0; j < kVpt; ++j) d = max(d, u[j]);
+
+    // 2. threshold: min over warps of each warp's ceil(K/warps)-th largest delegate
+    const int kw = (k + kWarps - 1) / kWarps;
+    uint32_t tw = 0;
+    for (int r = 0; r < kw; ++r) {
+        const uint32_t m = __reduce_max_sync(kFull, d);
+        tw = m;
+        if (m == 0) break;
+        const unsigned who = __ballot_sync(kFull, d == m);
+        if (lane == __ffs(who) - 1) d = 0;
+    }
+    if (lane == 0) s.warp_t[warp] = tw;
+    if (tid == 0) s.cnt = 0;
+    __syncthreads();
+    // Warps that hold kw delegates each vouch for kw elements >= their own
+    // threshold; the minimum over enough such warps is a valid threshold.
+    uint32_t t = 0xffffffffu;
+    int vouching = 0;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) {
+        const uint32_t v = s.warp_t[w];
+        if (v != 0) {
+            t = min(t, v);
+            ++vouching;
+        }
+    }
+    if (vouching * kw < k) t = 1;   // too few: take every element (0 marks an empty slot)
+
+    // 3. candidates
+#pragma unroll
+    for (int j = 0; j < kVpt; ++j) {
+        if (u[j] >= t) {
+            const uint32_t pos = atomicAdd(&s.cnt, 1u);
+            if (pos < kCap) s.cand[pos] = make_key(u[j], (uint32_t)(c0 + elem(j)));
+        }
+    }
+    __syncthreads();
+    uint32_t cnt = s.cnt;
+    const int kk = min(k, n);
+    if (cnt > kCap) {
+        // exact fallback: radix select over the chunk's keys (re-read from L2)
+        auto key_at = [&](int i) { return make_key(order_bits(xr[c0 + i]), (uint32_t)(c0 + i)); };
+        const unsigned long long kth = block_kth_largest(key_at, n, kk, s);
+        if (tid == 0) s.cnt = 0;
+        __syncthreads();
+        for (int i = tid; i < n; i += kThreads) {
+            const unsigned long long key = key_at(i);
+            if (key >= kth) s.cand[atomicAdd(&s.cnt, 1u)] = key;   // exactly kk keys
+        }
+        __syncthreads();
+        cnt = s.cnt;
+    }
+
+    // 4. rank and emit
+    if (p.nchunks == 1) {
+        rank_and_emit(s, cnt, kk, [&](int rank, unsigned long long key) {
+            const uint32_t idx = key_index(key);
+            float v = xr[idx];
+            if (isnan(v)) v = -INFINITY;
+            p.out_val[row * k + rank] = v;
+            p.out_idx[row * k + rank] = (int)idx;
+        });
+        return;
+    }
+    unsigned long long* kr = p.keys + (row * p.nchunks + chunk) * k;
+    rank_and_emit(s, cnt, kk, [&](int rank, unsigned long long key) { kr[rank] = key; });
+    for (int r = kk + tid; r < k; r += kThreads) kr[r] = 0ull;   // chunk shorter than K
+
+    // Last block of the row merges.
+    __threadfence();
+    __syncthreads();
+    if (tid == 0) {
+        const unsigned prev = atomicAdd(&p.tickets[row], 1u);
+        s.last = (prev == (unsigned)p.nchunks - 1u);
+    }
+    __syncthreads();
+    if (!s.last) return;
+    __threadfence();
+
+    const unsigned long long* all = p.keys + row * p.nchunks * k;
+    const int total = p.nchunks * k;
+    unsigned long long tm = 0;
+    for (int c = tid; c < p.nchunks; c += kThreads) {
+        const unsigned long long v = __ldcg(all + (long long)c * k + (k - 1));
+        tm = v > tm ? v : tm;
+    }
+    tm = warp_max_u64(tm);
+    if (lane == 0) s.red[warp] = tm;
+    if (tid == 0) s.cnt = 0;
+    __syncthreads();
+    unsigned long long t64 = 0;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) t64 = s.red[w] > t64 ? s.red[w] : t64;
+    if (t64 == 0) t64 = 1;
+    for (int i = tid; i < total; i += kThreads) {
+        const unsigned long long key = __ldcg(all + i);
+        if (key >= t64) {
+            const uint32_t pos = atomicAdd(&s.cnt, 1u);
+            if (pos < kCap) s.cand[pos] = key;
+        }
+    }
+    __syncthreads();
+    cnt = s.cnt;
+    if (cnt > kCap) {
+        auto key_at = [&](int i) { return __ldcg(all + i); };
+        const unsigned long long kth = block_kth_largest(key_at, total, k, s);
+        if (tid == 0) s.cnt = 0;
+        __syncthreads();
+        for (int i = tid; i < total; i += kThreads) {
+            const unsigned long long key = __ldcg(all + i);
+            if (key >= kth) s.cand[atomicAdd(&s.cnt, 1u)] = key;
+        }
+        __syncthreads();
+        cnt = s.cnt;
+    }
+    rank_and_emit(s, cnt, k, [&](int rank, unsigned long long key) {
+        const uint32_t idx = key_index(key);
+        float v = xr[idx];
+        if (isnan(v)) v = -INFINITY;
+        p.out_val[row * k + rank] = v;
+        p.out_idx[row * k + rank] = (int)idx;
+    });
+    if (tid == 0) p.tickets[row] = 0u;   // ready for the next call / replay
+}
+
+size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+}  // namespace
+
+ws_status validate_topk(int64_t rows, int64_t cols, int32_t k) {
+    if (rows < 1) return fail(WS_ERR_INVALID_ARGUMENT, "rows %lld < 1", (long long)rows);
+    if (cols < 1 || cols > 2147483647LL)
+        return fail(WS_ERR_INVALID_ARGUMENT, "cols %lld outside 1 .. 2^31-1", (long long)cols);
+    if (k < 1 || k > kMaxK) return fail(WS_ERR_INVALID_ARGUMENT, "k %d outside 1..%d", k, kMaxK);
+    if (k > cols) return fail(WS_ERR_INVALID_ARGUMENT, "k %d > cols %lld", k, (long long)cols);
+    if (rows > (1LL << 40) / cols) return fail(WS_ERR_INVALID_ARGUMENT, "rows * cols too large");
+    return WS_OK;
+}
+
+size_t topk_workspace_size(int64_t rows, int64_t cols, int32_t k) {
+    const long long nchunks = (cols + kChunk - 1) / kChunk;
+    if (nchunks <= 1) return 0;
+    return round_up((size_t)rows * 4, 256) + (size_t)rows * nchunks * k * 8;
+}
+
+}  // namespace ws
+
+extern "C" {
+
+ws_status ws_topk_validate(int64_t rows, int64_t cols, int32_t k) {
+    ws::clear_error();
+    return ws::validate_topk(rows, cols, k);
+}
+
+ws_status ws_topk_workspace_bytes(int64_t rows, int64_t cols, int32_t k, size_t* bytes) {
+    ws::clear_error();
+    if (!bytes) return ws::fail(WS_ERR_INVALID_ARGUMENT, "bytes is NULL");
+    ws_status st = ws::validate_topk(rows, cols, k);
+    if (st != WS_OK) return st;
+    *bytes = ws::topk_workspace_size(rows, cols, k);
+    return WS_OK;
+}
+
+ws_status ws_topk_workspace_init(void* workspace, size_t bytes, cudaStream_t stream) {
+    ws::clear_error();
+    if (bytes == 0) return WS_OK;
+    if (!workspace) return ws::fail(WS_ERR_INVALID_ARGUMENT, "workspace is NULL");
+    WS_TRY_CUDA(cudaMemsetAsync(workspace, 0, bytes, stream));
+    return WS_OK;
+}
+
+ws_status ws_topk(const float* x, int64_t rows, int64_t cols, int32_t k, float* out_val, int32_t* out_idx,
+                  void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+    using namespace ws;
+    clear_error();
+    ws_status st = validate_topk(rows, cols, k);
+    if (st != WS_OK) return st;
+    if (!x || !out_val || !out_idx) return fail(WS_ERR_INVALID_ARGUMENT, "x, out_val or out_idx is NULL");
+    const size_t need = topk_workspace_size(rows, cols, k);
+    if (need > 0 && (!workspace || workspace_bytes < need))
+        return fail(WS_ERR_INVALID_ARGUMENT, "workspace of %zu bytes, %zu needed", workspace_bytes, need);
+    if (need > 0 && (uintptr_t)workspace % 256 != 0)
+        return fail(WS_ERR_INVALID_ARGUMENT, "workspace must be 256-byte aligned");
+
+    TopkParams p{};
+    p.x = x;
+    p.cols = cols;
+    p.k = k;
+    p.nchunks = (int)((cols + kChunk - 1) / kChunk);
+    p.out_val = out_val;
+    p.out_idx = out_idx;
+    if (need > 0) {
+        p.tickets = static_cast<unsigned int*>(workspace);
+        p.keys = reinterpret_cast<unsigned long long*>(static_cast<char*>(workspace) +
+                                                       round_up((size_t)rows * 4, 256));
+    }
+    const long long blocks = rows * p.nchunks;
+    if (blocks > 2147483647LL) return fail(WS_ERR_UNSUPPORTED, "too many blocks");
+    const bool vec = (cols % 4 == 0) && ((uintptr_t)x % 16 == 0);
+    if (vec)
+        topk_kernel<true><<<(unsigned)blocks, kThreads, 0, stream>>>(p);
+    else
+        topk_kernel<false><<<(unsigned)blocks, kThreads, 0, stream>>>(p);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(e, "top-k launch");
+    return WS_OK;
+}
+
+}  // extern "C"

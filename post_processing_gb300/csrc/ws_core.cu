@@ -1,0 +1,112 @@
+// ws_core.cu -- status strings, per-thread error text, version, the device
+// property cache and the device error word.
+#include <cstring>
+#include <mutex>
+#include <string>
+
+#include "ws_internal.cuh"
+
+// Error bits raised by kernels whose bounded waits ran out; one copy per
+// device, zero at module load.
+__device__ uint32_t g_dev_error_flags;
+
+namespace ws {
+
+namespace {
+thread_local std::string t_error;
+
+constexpr int kMaxDevices = 64;
+DeviceInfo g_info[kMaxDevices];
+bool g_have[kMaxDevices];
+uint32_t* g_err_word[kMaxDevices];
+std::mutex g_mu;
+}  // namespace
+
+ws_status fail(ws_status status, const char* fmt, ...) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof buf, fmt, ap);
+    va_end(ap);
+    t_error = buf;
+    return status;
+}
+
+void clear_error() { t_error.clear(); }
+
+ws_status cuda_fail(cudaError_t err, const char* what) {
+    return fail(WS_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(err), cudaGetErrorString(err));
+}
+
+ws_status current_device_info(int* device, const DeviceInfo** info) {
+    int dev = 0;
+    WS_TRY_CUDA(cudaGetDevice(&dev));
+    if (dev < 0 || dev >= kMaxDevices) return fail(WS_ERR_UNSUPPORTED, "device ordinal %d", dev);
+    std::lock_guard<std::mutex> lock(g_mu);
+    if (!g_have[dev]) {
+        DeviceInfo d{};
+        WS_TRY_CUDA(cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, dev));
+        WS_TRY_CUDA(cudaDeviceGetAttribute(&d.max_smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev));
+        WS_TRY_CUDA(cudaDeviceGetAttribute(&d.smem_per_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev));
+        // Device address of this device's error word (no allocation).
+        uint32_t* w = nullptr;
+        WS_TRY_CUDA(cudaGetSymbolAddress((void**)&w, g_dev_error_flags));
+        g_err_word[dev] = w;
+        g_info[dev] = d;
+        g_have[dev] = true;
+    }
+    *device = dev;
+    *info = &g_info[dev];
+    return WS_OK;
+}
+
+uint32_t* device_error_word() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+    std::lock_guard<std::mutex> lock(g_mu);
+    return g_err_word[dev];
+}
+
+}  // namespace ws
+
+extern "C" {
+
+const char* ws_status_string(ws_status s) {
+    switch (s) {
+        case WS_OK: return "WS_OK";
+        case WS_ERR_INVALID_ARGUMENT: return "WS_ERR_INVALID_ARGUMENT";
+        case WS_ERR_UNSUPPORTED: return "WS_ERR_UNSUPPORTED";
+        case WS_ERR_CUDA: return "WS_ERR_CUDA";
+        case WS_ERR_OUT_OF_MEMORY: return "WS_ERR_OUT_OF_MEMORY";
+        case WS_ERR_LANE_STATE: return "WS_ERR_LANE_STATE";
+        case WS_ERR_LANE_BUSY: return "WS_ERR_LANE_BUSY";
+        case WS_ERR_TIMEOUT: return "WS_ERR_TIMEOUT";
+        case WS_ERR_CAPTURE: return "WS_ERR_CAPTURE";
+        case WS_ERR_DEVICE: return "WS_ERR_DEVICE";
+        default: return "WS_ERR_UNKNOWN";
+    }
+}
+
+const char* ws_last_error(void) { return ws::t_error.c_str(); }
+
+int32_t ws_version(void) { return 100; }  // 0.1.0
+
+ws_status ws_device_error(uint32_t* flags, int32_t clear) {
+    ws::clear_error();
+    if (!flags) return ws::fail(WS_ERR_INVALID_ARGUMENT, "flags is NULL");
+    int dev;
+    const ws::DeviceInfo* info;
+    ws_status st = ws::current_device_info(&dev, &info);
+    if (st != WS_OK) return st;
+    uint32_t* w = ws::device_error_word();
+    uint32_t v = 0;
+    WS_TRY_CUDA(cudaMemcpy(&v, w, sizeof v, cudaMemcpyDeviceToHost));
+    if (clear) {
+        const uint32_t zero = 0;
+        WS_TRY_CUDA(cudaMemcpy(w, &zero, sizeof zero, cudaMemcpyHostToDevice));
+    }
+    *flags = v;
+    return WS_OK;
+}
+
+}  // extern "C"

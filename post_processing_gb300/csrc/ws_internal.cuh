@@ -1,0 +1,49 @@
+// ws_internal.cuh -- helpers shared by the library's translation units:
+// per-thread error text, status shorthands and a per-device property cache.
+#pragma once
+
+#include <cstdarg>
+#include <cstdint>
+#include <cstdio>
+
+#include <cuda_runtime.h>
+
+#include "ws.h"
+
+namespace ws {
+
+// Records a message for ws_last_error() and returns `status`.
+ws_status fail(ws_status status, const char* fmt, ...);
+// Clears the thread's message (called on entry of each public call).
+void clear_error();
+// WS_ERR_CUDA with the CUDA error name, or WS_OK.
+ws_status cuda_fail(cudaError_t err, const char* what);
+
+#define WS_TRY_CUDA(expr)                                        \
+    do {                                                         \
+        cudaError_t ws_e_ = (expr);                              \
+        if (ws_e_ != cudaSuccess) return ws::cuda_fail(ws_e_, #expr); \
+    } while (0)
+
+struct DeviceInfo {
+    int sm_count;
+    int max_smem_optin;     // bytes of dynamic shared memory a block may opt in to
+    int smem_per_sm;
+};
+// Properties of the current device, queried once per device.
+ws_status current_device_info(int* device, const DeviceInfo** info);
+
+// Host-side argument checks shared by the entry points and the lanes.
+ws_status validate_preprocess(const ws_preprocess_desc* d, int32_t batch);
+ws_status validate_topk(int64_t rows, int64_t cols, int32_t k);
+size_t topk_workspace_size(int64_t rows, int64_t cols, int32_t k);
+
+// Error bits kernels raise instead of waiting forever (see ws_device_error).
+enum : uint32_t {
+    kDevErrBulkCopyTimeout = 1u,
+};
+// Device address of the current device's error word; kernels receive it as a
+// parameter (no relocatable device code, so they cannot name it directly).
+uint32_t* device_error_word();
+
+}  // namespace ws

@@ -1,0 +1,150 @@
+"""GPU exact Top-K against the oracle: indices and values bit-exact.
+
+Covers the five workloads' logits at full size, row lengths around every
+block boundary (8192 per block), K from 1 to 32, ties (including ties at the
+cut and +0/-0), NaN and infinities, and adversarial rows that defeat the
+threshold (constant rows, sorted rows), which take the radix-select path;
+also a misaligned pointer (scalar loads), workspace reuse across calls and
+replay inside a captured CUDA Graph.
+"""
+import numpy as np
+import pytest
+import torch
+
+import synth
+from pins import check_topk_invariants
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def B():
+    import __graft_entry__
+    __graft_entry__.build()
+    from post_processing_gb300 import binding
+    return binding
+
+
+def gpu_topk(B, x, k, offset=0, workspace=None):
+    rows, cols = x.shape
+    flat = torch.zeros(rows * cols + offset + 8, dtype=torch.float32, device="cuda")
+    flat[offset:offset + rows * cols] = torch.from_numpy(x.reshape(-1)).cuda()
+    val = torch.full((rows, k), 7.0, dtype=torch.float32, device="cuda")
+    idx = torch.full((rows, k), -9, dtype=torch.int32, device="cuda")
+    st, n = B.ws_topk_workspace_bytes(rows, cols, k)
+    B.check(st)
+    s = torch.cuda.current_stream().cuda_stream
+    if workspace is None and n:
+        workspace = torch.empty(n + 256, dtype=torch.uint8, device="cuda")
+    wptr = 0
+    if n:
+        wptr = workspace.data_ptr() + (-workspace.data_ptr()) % 256
+        B.check(B.ws_topk_workspace_init(wptr, n, s))
+    B.check(B.ws_topk(flat.data_ptr() + 4 * offset, rows, cols, k, val.data_ptr(), idx.data_ptr(),
+                      wptr or None, n, s))
+    torch.cuda.synchronize()
+    return val.cpu().numpy(), idx.cpu().numpy()
+
+
+def assert_exact(got, want):
+    gv, gi = got
+    wv, wi = want
+    assert np.array_equal(gi, wi), f"indices differ in rows {np.nonzero((gi != wi).any(1))[0][:8]}"
+    assert np.array_equal(gv.view(np.uint32), wv.view(np.uint32)), "values differ"
+
+
+@pytest.mark.parametrize("name", list(synth.WORKLOADS))
+def test_workload_parity(B, oracle, name):
+    w = synth.WORKLOADS[name]
+    x = synth.make_logits(name)
+    assert_exact(gpu_topk(B, x, w["k"]), oracle.topk(x, w["k"]))
+
+
+@pytest.mark.parametrize("cols", [1, 2, 3, 31, 32, 33, 100, 1000, 4097, 8191, 8192, 8193, 16384, 20001,
+                                  65536 + 3])
+@pytest.mark.parametrize("k", [1, 5, 32])
+def test_lengths(B, oracle, cols, k):
+    if k > cols:
+        pytest.skip("k > cols is rejected")
+    x = synth.logits_with_ties(cols * 31 + k, 3, cols, frac=0.1)
+    assert_exact(gpu_topk(B, x, k), oracle.topk(x, k))
+
+
+def special_rows(cols, rng):
+    rows = []
+    rows.append(np.zeros(cols, np.float32))                                  # constant
+    rows.append(np.full(cols, np.nan, np.float32))                           # all NaN
+    z = np.zeros(cols, np.float32); z[::2] = -0.0; rows.append(z)          # +0 / -0 ties
+    rows.append(np.arange(cols, dtype=np.float32))                           # ascending
+    rows.append(-np.arange(cols, dtype=np.float32))                          # descending
+    r = rng.integers(0, 3, cols).astype(np.float32); rows.append(r)         # three values
+    r = rng.standard_normal(cols).astype(np.float32)
+    r[rng.integers(0, cols, cols // 10)] = np.nan
+    r[rng.integers(0, cols, 5)] = np.inf
+    r[rng.integers(0, cols, 5)] = -np.inf
+    rows.append(r)
+    r = rng.standard_normal(cols).astype(np.float32)                        # ties at the cut
+    top = np.sort(r)[-20]
+    r[rng.integers(0, cols, 40)] = top
+    rows.append(r)
+    r = np.full(cols, -1.0, np.float32); r[: min(cols, 300)] = 5.0          # one hot region
+    rows.append(r)
+    r = np.full(cols, 1.0, np.float32); r[-min(cols, 300):] = 2.0           # hot region at the end
+    rows.append(r)
+    return np.stack(rows)
+
+
+@pytest.mark.parametrize("cols", [40, 1000, 8192, 30000])
+@pytest.mark.parametrize("k", [1, 17, 32])
+def test_special_rows(B, oracle, cols, k):
+    x = special_rows(cols, np.random.default_rng(cols + k))
+    got = gpu_topk(B, x, k)
+    assert_exact(got, oracle.topk(x, k))
+    check_topk_invariants(x, got[0], got[1], k)
+
+
+def test_misaligned_pointer_scalar_path(B, oracle):
+    x = synth.logits_normal(5, 4, 10001)
+    assert_exact(gpu_topk(B, x, 32, offset=1), oracle.topk(x, 32))
+    x = synth.logits_normal(6, 2, 1000)
+    assert_exact(gpu_topk(B, x, 5, offset=3), oracle.topk(x, 5))
+
+
+def test_workspace_reuse_and_graph_replay(B, oracle):
+    rows, cols, k = 8, 50000, 32
+    xs = [synth.logits_with_ties(40 + i, rows, cols) for i in range(3)]
+    st, n = B.ws_topk_workspace_bytes(rows, cols, k)
+    ws = torch.empty(n, dtype=torch.uint8, device="cuda")
+    s = torch.cuda.Stream()
+    x_dev = torch.empty((rows, cols), dtype=torch.float32, device="cuda")
+    val = torch.empty((rows, k), dtype=torch.float32, device="cuda")
+    idx = torch.empty((rows, k), dtype=torch.int32, device="cuda")
+    with torch.cuda.stream(s):
+        B.check(B.ws_topk_workspace_init(ws.data_ptr(), n, s.cuda_stream))
+        # plain calls, one after another on one workspace
+        for x in xs:
+            x_dev.copy_(torch.from_numpy(x))
+            B.check(B.ws_topk(x_dev.data_ptr(), rows, cols, k, val.data_ptr(), idx.data_ptr(),
+                              ws.data_ptr(), n, s.cuda_stream))
+            s.synchronize()
+            assert_exact((val.cpu().numpy(), idx.cpu().numpy()), oracle.topk(x, k))
+        # captured once, replayed with new inputs in the same buffers
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            B.check(B.ws_topk(x_dev.data_ptr(), rows, cols, k, val.data_ptr(), idx.data_ptr(),
+                              ws.data_ptr(), n, s.cuda_stream))
+        for x in reversed(xs):
+            x_dev.copy_(torch.from_numpy(x))
+            g.replay()
+            s.synchronize()
+            assert_exact((val.cpu().numpy(), idx.cpu().numpy()), oracle.topk(x, k))
+
+
+def test_torch_sort_agrees(B):
+    """Library special case: a stable descending sort after NaN -> -inf."""
+    x = synth.logits_with_ties(77, 16, 4096, frac=0.3)
+    x[3, ::7] = np.nan
+    v, i = gpu_topk(B, x, 32)
+    t = torch.from_numpy(np.where(np.isnan(x), -np.inf, x)) + 0.0
+    sv, si = torch.sort(t, dim=1, descending=True, stable=True)
+    assert np.array_equal(i, si[:, :32].numpy().astype(np.int32))
