@@ -167,6 +167,40 @@ ws_status ws_topk(const float* x, int64_t rows, int64_t cols, int32_t k,
                   float* out_val, int32_t* out_idx,
                   void* workspace, size_t workspace_bytes, cudaStream_t stream);
 
+/* Top-K for callers that cannot allocate device memory.  Same result as
+ * ws_topk (same kernel, bit-exact), but its scratch lives in a fixed 1 MiB
+ * array inside the library's device image instead of a caller workspace.
+ * The pages have no counterpart of this call.
+ *
+ * Who needs it: code that is handed only its input and output buffers and has
+ * no allocator of its own (a plugin or callback running inside another
+ * framework's enqueue), and latency-critical loops that must not call
+ * cudaMalloc after start-up (allocation can synchronise the device and take
+ * driver locks, which shows up as tail latency).  They cannot size, own or
+ * free a workspace; this call needs none.
+ *
+ * Arguments: as ws_topk (x device [rows][cols]; out_val / out_idx device
+ * [rows][k]); nothing is allocated and no workspace is passed.
+ * Limits and behaviour:
+ *  - The scratch a shape needs is ws_topk_workspace_bytes(rows, cols, k);
+ *    shapes needing more than 1 MiB (1048576 bytes) are rejected with
+ *    WS_ERR_UNSUPPORTED and a message giving both sizes; nothing is enqueued.
+ *    Rows of at most 8192 entries need no scratch at all.
+ *  - The array costs 1 MiB of device memory on every GPU that loads the
+ *    library, held until the process exits.
+ *  - The first call on each device looks up the array's device address
+ *    (cudaGetSymbolAddress, no allocation) with that device current; make that
+ *    first call before any stream capture.
+ *  - Every call shares the one array, which keeps the last call's contents;
+ *    each call therefore clears its row tickets first (one cudaMemsetAsync of
+ *    rows * 4 bytes on `stream`).  Calls that overlap on the GPU (for example
+ *    on two streams at once) race on the array and give wrong results:
+ *    serialise them.
+ * Errors: WS_ERR_INVALID_ARGUMENT (shape, K, NULL pointer), WS_ERR_UNSUPPORTED
+ * (scratch above the limit), WS_ERR_CUDA (set-up, clearing or launch failed). */
+ws_status ws_topk_noalloc(const float* x, int64_t rows, int64_t cols, int32_t k,
+                          float* out_val, int32_t* out_idx, cudaStream_t stream);
+
 /* ------------------------------------------------------------------- lanes */
 
 #define WS_INPUT_DEVICE 0   /* producer writes a device buffer                       */

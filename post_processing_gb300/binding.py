@@ -77,6 +77,7 @@ SIGNATURES = {
     "ws_topk_workspace_bytes": (_i32, [_i64, _i64, _i32, ctypes.POINTER(_sz)]),
     "ws_topk_workspace_init": (_i32, [_vp, _sz, _vp]),
     "ws_topk": (_i32, [_vp, _i64, _i64, _i32, _vp, _vp, _vp, _sz, _vp]),
+    "ws_topk_noalloc": (_i32, [_vp, _i64, _i64, _i32, _vp, _vp, _vp]),
     "ws_lane_create": (_i32, [ctypes.POINTER(ws_lane_desc), ctypes.POINTER(_vp)]),
     "ws_lane_get_buffers": (_i32, [_vp, ctypes.POINTER(ws_lane_buffers)]),
     "ws_lane_acquire": (_i32, [_vp]),
@@ -163,6 +164,11 @@ def ws_topk_workspace_init(workspace: int, nbytes: int, stream: int = 0) -> int:
 def ws_topk(x: int, rows: int, cols: int, k: int, out_val: int, out_idx: int,
             workspace: int | None, workspace_bytes: int, stream: int = 0) -> int:
     return lib.ws_topk(x, rows, cols, k, out_val, out_idx, workspace or None, workspace_bytes, stream)
+
+
+def ws_topk_noalloc(x: int, rows: int, cols: int, k: int, out_val: int, out_idx: int,
+                    stream: int = 0) -> int:
+    return lib.ws_topk_noalloc(x, rows, cols, k, out_val, out_idx, stream)
 
 
 def ws_lane_create(desc: ws_lane_desc) -> tuple[int, int | None]:

@@ -31,6 +31,7 @@
 // chunks' keys with the same threshold / rank steps, taking as threshold the
 // largest K-th key over chunks.
 #include <cmath>
+#include <mutex>
 
 #include "ws_internal.cuh"
 
@@ -407,3 +408,60 @@ ws_status ws_topk(const float* x, int64_t rows, int64_t cols, int32_t k, float* 
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// ws_topk_noalloc: the same Top-K for callers that cannot allocate device
+// memory.  Its scratch (row tickets + per-block keys, laid out exactly like a
+// ws_topk workspace) is this fixed array in the library's device image: every
+// GPU that loads the library holds it until the process exits.
+// ---------------------------------------------------------------------------
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = 1u << 20;   // 1 MiB per device
+static __device__ __align__(256) unsigned char g_topk_noalloc_scratch[kNoAllocScratchBytes];
+
+std::mutex g_noalloc_mu;
+void* g_noalloc_ptr[64];
+
+// Device address of this device's scratch array.  The array's name is only a
+// host-side stand-in in host code, so the address is looked up once per
+// device, with that device current, and cached.
+ws_status noalloc_scratch(void** out) {
+    int dev;
+    const ws::DeviceInfo* info;
+    ws_status st = ws::current_device_info(&dev, &info);
+    if (st != WS_OK) return st;
+    std::lock_guard<std::mutex> lock(g_noalloc_mu);
+    if (!g_noalloc_ptr[dev]) {
+        void* p = nullptr;
+        cudaError_t e = cudaGetSymbolAddress(&p, g_topk_noalloc_scratch);
+        if (e != cudaSuccess) return ws::cuda_fail(e, "cudaGetSymbolAddress of the Top-K scratch array");
+        g_noalloc_ptr[dev] = p;
+    }
+    *out = g_noalloc_ptr[dev];
+    return WS_OK;
+}
+
+}  // namespace
+
+extern "C" ws_status ws_topk_noalloc(const float* x, int64_t rows, int64_t cols, int32_t k, float* out_val,
+                                     int32_t* out_idx, cudaStream_t stream) {
+    ws::clear_error();
+    ws_status st = ws::validate_topk(rows, cols, k);
+    if (st != WS_OK) return st;
+    const size_t need = ws::topk_workspace_size(rows, cols, k);
+    if (need > kNoAllocScratchBytes)
+        return ws::fail(WS_ERR_UNSUPPORTED,
+                        "rows=%lld cols=%lld k=%d needs %zu bytes of scratch; ws_topk_noalloc has a fixed "
+                        "%zu-byte array (use ws_topk with a caller workspace)",
+                        (long long)rows, (long long)cols, k, need, kNoAllocScratchBytes);
+    void* scratch = nullptr;
+    if (need > 0) {
+        if ((st = noalloc_scratch(&scratch)) != WS_OK) return st;
+        // The array keeps the previous call's contents; the row tickets must
+        // start at zero.
+        cudaError_t e = cudaMemsetAsync(scratch, 0, (size_t)rows * sizeof(unsigned int), stream);
+        if (e != cudaSuccess) return ws::cuda_fail(e, "clearing the Top-K scratch tickets");
+    }
+    return ws_topk(x, rows, cols, k, out_val, out_idx, scratch, need > 0 ? kNoAllocScratchBytes : 0, stream);
+}
