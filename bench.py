@@ -11,8 +11,9 @@ HBM-throughput configuration.  Also measured on every run:
   clock, graph and no-graph) on one 1920x1080 frame -> 224x224, Top-5 of 1000;
 * end-to-end throughput through the lane API with host buffers: the graph
   copies the frames from pinned host memory and the result back;
-* the roofline of the dominant kernel (the preprocess) from in-graph event
-  nodes around it, against the measured HBM copy bandwidth;
+* the roofline of the dominant kernel (the preprocess): its average launch
+  duration from CUDA events around back-to-back launches on the lanes'
+  buffers, against the measured HBM copy bandwidth;
 * the CPU oracle on the host cores (a bounded sample), as a reported baseline.
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
@@ -45,14 +46,14 @@ LATENCY_WORKLOAD = "b1_1080p_to_224"
 FALLBACK_HBM_GBS = 6800.0
 LANES = 3
 
-# DRAM traffic of the staged preprocess kernel per launch from one ncu
+# DRAM traffic of the preprocess kernel per launch from one ncu
 # capture (dram__bytes_read.sum + dram__bytes_write.sum), keyed by the SHA-256
 # of the kernel source it was taken on; reported only while that source is
 # unchanged.  Filled from the committed ncu summary under profiles/.
 NCU_TRAFFIC = {
     "b64_1080p_to_224": {
-        "bytes": 165_189_632 + 22_113_024,
-        "source_sha": "fc82e5cd0da2fca242797cc4127f42558d70faef4c9e06d1eabe9ace5c57a5a9",
+        "bytes": 185_469_952,
+        "source_sha": "8b6a78888ca824840ba02ea5c31d683162c384af7d56a9392c98bc696bd04f21",
     },
 }
 
@@ -331,45 +332,74 @@ def main():
         src = frames_dev.clone()
         lg = logits_dev.clone()
         keep += [src, lg]
+        # throughput lanes: only a completion event per submit (no timing pair)
         d = B.lane_desc(pre, w["batch"], w["rows"], w["cols"], w["k"], input=src.data_ptr(), logits=lg.data_ptr(),
-                        stream=stream.cuda_stream, flags=B.WS_LANE_FLAG_STAGE_TIMING)
+                        stream=stream.cuda_stream, flags=B.WS_LANE_FLAG_NO_TIMING)
         lanes.append(Lane(d))
     torch.cuda.synchronize()
     alg = algorithmic_bytes(w)
     touched_per_rotation = LANES * alg["total"]
 
-    def run_steps(n, record):
+    def run_steps(n):
         inflight = []
         for s in range(n):
             lane = lanes[s % LANES]
             if lane.state == B.WS_LANE_IN_FLIGHT:
-                t = lane.wait()
+                lane.wait()
                 inflight.remove(lane)
-                if record is not None:
-                    record.append((t.preprocess_us, t.topk_us))
             lane.acquire()
             lane.submit()
             inflight.append(lane)
         for lane in inflight:
-            t = lane.wait()
-            if record is not None:
-                record.append((t.preprocess_us, t.topk_us))
+            lane.wait()
 
-    run_steps(args.warmup, None)
+    run_steps(args.warmup)
     torch.cuda.synchronize()
     if world > 1:
         torch.distributed.barrier()
     clocks.start()
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    stage = []
     torch.cuda.synchronize()
     ev0.record(stream)
-    run_steps(args.steps, stage)
+    run_steps(args.steps)
     ev1.record(stream)
     torch.cuda.synchronize()
     elapsed_s = ev0.elapsed_time(ev1) / 1000.0
     if world > 1:
         torch.distributed.barrier()
+
+    # Per-kernel durations for the roofline: the same kernels on the same
+    # stream and the lanes' own buffers (rotating, so inputs stay larger than
+    # L2), launched back to back through the C ABI and bracketed by CUDA
+    # events, right after the timed region.
+    kernel_launches = min(args.steps, 2000)
+    bufs = [lane.buffers for lane in lanes]
+    st_ws = [B.ws_topk_workspace_bytes(w["rows"], w["cols"], w["k"])[1] for _ in lanes]
+    topk_ws = [torch.zeros(max(n, 1), dtype=torch.uint8, device=device) for n in st_ws]
+
+    def time_kernel(launch, n):
+        for i in range(8):
+            launch(i)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        e0.record(stream)
+        for i in range(n):
+            launch(i)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) * 1000.0 / n
+
+    def launch_pre(i):
+        b = bufs[i % LANES]
+        B.check(B.ws_preprocess(pre, b.input_device, w["batch"], b.tensor, stream.cuda_stream))
+
+    def launch_topk(i):
+        b, ws_t, n = bufs[i % LANES], topk_ws[i % LANES], st_ws[i % LANES]
+        B.check(B.ws_topk(b.logits, w["rows"], w["cols"], w["k"], b.result_val_device, b.result_idx_device,
+                          ws_t.data_ptr() if n else None, n, stream.cuda_stream))
+
+    pre_avg_us = time_kernel(launch_pre, kernel_launches)
+    topk_avg_us = time_kernel(launch_topk, kernel_launches)
 
     # batch-1 latency: one lane, submit -> wait, graph and direct launches
     lw = synth.WORKLOADS[LATENCY_WORKLOAD]
@@ -378,7 +408,12 @@ def main():
     lpre = B.preprocess_desc(lw["src_w"], lw["src_h"], lw["dst_w"], lw["dst_h"], norm=lw["norm"])
     latency = {"workload": workload_config(LATENCY_WORKLOAD, lw)["workload"], "samples": args.latency_samples,
                "warmup": min(1000, args.latency_samples), "input": "device-resident"}
-    for label, flags in (("graph", 0), ("no_graph", B.WS_LANE_FLAG_NO_GRAPH)):
+    # "graph": the page's measurement, timing events just before the graph
+    # launch and after the Top-K (GPU interval) plus the host steady clock;
+    # "graph_no_timing": the same replay with only a completion event (host
+    # clock); "no_graph": direct launches with the timing events.
+    for label, flags in (("graph", 0), ("graph_no_timing", B.WS_LANE_FLAG_NO_TIMING),
+                         ("no_graph", B.WS_LANE_FLAG_NO_GRAPH)):
         d = B.lane_desc(lpre, 1, 1, lw["cols"], lw["k"], input=lframes.data_ptr(), logits=llogits.data_ptr(),
                         flags=flags)
         with Lane(d) as lane:
@@ -390,7 +425,9 @@ def main():
                 if i >= latency["warmup"]:
                     gpu.append(t.gpu_us)
                     host.append(t.host_us)
-            latency[label] = {"gpu_us": percentiles(gpu), "host_us": percentiles(host)}
+            latency[label] = {"host_us": percentiles(host)}
+            if flags & B.WS_LANE_FLAG_NO_TIMING == 0:
+                latency[label]["gpu_us"] = percentiles(gpu)
     clk = clocks.stop()
 
     # end to end through the lane API with host buffers: pinned frames in, result out
@@ -399,7 +436,8 @@ def main():
         e_lanes = []
         for _ in range(2):
             d = B.lane_desc(pre, w["batch"], w["rows"], w["cols"], w["k"], input_mode=B.WS_INPUT_COPY,
-                            result_mode=B.WS_RESULT_COPY, logits=logits_dev.data_ptr())
+                            result_mode=B.WS_RESULT_COPY, logits=logits_dev.data_ptr(),
+                            flags=B.WS_LANE_FLAG_NO_TIMING)
             lane = Lane(d)
             import ctypes
             buf = (ctypes.c_char * frames.nbytes).from_address(lane.buffers.input_host)
@@ -434,14 +472,12 @@ def main():
         lane.close()
 
     value, t_max = whole_job_rate(w["batch"] * args.steps, elapsed_s, world, device)
-    pre_us = np.array([s[0] for s in stage], dtype=np.float64)
-    topk_us = np.array([s[1] for s in stage], dtype=np.float64)
     peaks_path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(peaks_path):
         peak, peak_src = float(json.load(open(peaks_path))["hbm_gbs"]), "measured"
     else:
         peak, peak_src = FALLBACK_HBM_GBS, "fallback"
-    achieved = alg["preprocess"] / (pre_us.mean() * 1e-6) / 1e9
+    achieved = alg["preprocess"] / (pre_avg_us * 1e-6) / 1e9
     sha = source_sha(os.path.join(ROOT, "post_processing_gb300", "csrc", "preprocess.cu"))
     traffic = NCU_TRAFFIC.get(args.workload)
     traffic = traffic["bytes"] if traffic and traffic.get("source_sha") == sha else None
@@ -461,11 +497,14 @@ def main():
                            parallelism=f"replicas x{world}", graph=True,
                            algorithmic_bytes_per_step=alg["total"]),
             "hbm_gbs_step": alg["total"] * args.steps * world / t_max / 1e9,
-            "roofline": {"bound": "hbm", "kernel": "pre_staged_kernel", "achieved": achieved, "peak": peak,
+            "roofline": {"bound": "hbm", "kernel": "pre_ring_kernel", "achieved": achieved, "peak": peak,
                          "unit": "GB/s", "frac": achieved / peak, "peak_source": peak_src,
                          "traffic": traffic, "algorithmic_bytes_per_launch": alg["preprocess"],
-                         "avg_launch_us": float(pre_us.mean()), "p50_launch_us": float(np.median(pre_us)),
-                         "topk_avg_launch_us": float(topk_us.mean())},
+                         "avg_launch_us": pre_avg_us, "launches_timed": kernel_launches,
+                         "timing": "CUDA events on the launching stream around back-to-back launches "
+                                   "on the lanes' rotating buffers, after the timed region",
+                         "topk_avg_launch_us": topk_avg_us,
+                         "topk_gbs": alg["topk"] / (topk_avg_us * 1e-6) / 1e9},
             "latency_b1": latency,
             "e2e": e2e,
             "gpu_launches": 2 * args.steps,

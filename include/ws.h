@@ -213,6 +213,11 @@ ws_status ws_topk_noalloc(const float* x, int64_t rows, int64_t cols, int32_t k,
 
 #define WS_LANE_FLAG_NO_GRAPH     1u  /* replay by direct launches instead of the CUDA Graph   */
 #define WS_LANE_FLAG_STAGE_TIMING 2u  /* event nodes around each stage for per-stage times   */
+#define WS_LANE_FLAG_NO_TIMING    4u  /* submit records only a completion event (timing
+                                         disabled) instead of the start / end timing pair:
+                                         each timing event costs the GPU a short bubble, so
+                                         back-to-back throughput lanes run faster without
+                                         them; ws_lane_timing.gpu_us is then -1 */
 #define WS_LANE_FLAG_NO_DEVICE    8u  /* host-only lane: no CUDA resource is made; submit marks
                                          it in flight and the "GPU" finishes after fake_polls
                                          completion queries.  Exercises the state machine on
@@ -262,7 +267,8 @@ typedef struct ws_lane_buffers {
 
 /* Times of one completed submit. */
 typedef struct ws_lane_timing {
-    float  gpu_us;         /* event before the graph launch -> event after the last stage */
+    float  gpu_us;         /* event before the graph launch -> event after the last stage
+                              (-1 on WS_LANE_FLAG_NO_TIMING lanes) */
     float  preprocess_us;  /* STAGE_TIMING lanes: preprocess kernel alone, else -1   */
     float  topk_us;        /* STAGE_TIMING lanes: Top-K kernel alone, else -1        */
     double host_us;        /* steady clock, entry of submit -> return of wait       */

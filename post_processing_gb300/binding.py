@@ -34,6 +34,7 @@ WS_INPUT_DEVICE, WS_INPUT_MAPPED, WS_INPUT_COPY = 0, 1, 2
 WS_RESULT_DEVICE, WS_RESULT_MAPPED, WS_RESULT_COPY = 0, 1, 2
 WS_LANE_FLAG_NO_GRAPH = 1
 WS_LANE_FLAG_STAGE_TIMING = 2
+WS_LANE_FLAG_NO_TIMING = 4
 WS_LANE_FLAG_NO_DEVICE = 8
 WS_LANE_FREE, WS_LANE_ACQUIRED, WS_LANE_IN_FLIGHT = 0, 1, 2
 

@@ -55,6 +55,7 @@ namespace ws {
 namespace {
 
 bool stage_timing(const ws_lane* L) { return (L->d.flags & WS_LANE_FLAG_STAGE_TIMING) != 0; }
+bool submit_timing(const ws_lane* L) { return (L->d.flags & WS_LANE_FLAG_NO_TIMING) == 0; }
 bool use_graph(const ws_lane* L) { return (L->d.flags & WS_LANE_FLAG_NO_GRAPH) == 0; }
 
 void release_all(ws_lane* L) {
@@ -252,8 +253,13 @@ ws_status build(ws_lane* L) {
         WS_TRY_CUDA(cudaMemsetAsync(L->ws, 0, L->ws_bytes, L->stream));
     }
 
-    WS_TRY_CUDA(cudaEventCreate(&L->ev_start));
-    WS_TRY_CUDA(cudaEventCreate(&L->ev_end));
+    if (submit_timing(L)) {
+        WS_TRY_CUDA(cudaEventCreate(&L->ev_start));
+        WS_TRY_CUDA(cudaEventCreate(&L->ev_end));
+    } else {
+        // completion only: a timing-disabled event is the lightest marker
+        WS_TRY_CUDA(cudaEventCreateWithFlags(&L->ev_end, cudaEventDisableTiming));
+    }
     if (stage_timing(L)) {
         WS_TRY_CUDA(cudaEventCreate(&L->ev_pre0));
         WS_TRY_CUDA(cudaEventCreate(&L->ev_pre1));
@@ -293,7 +299,8 @@ ws_status validate_lane(const ws_lane_desc* d) {
         return fail(WS_ERR_INVALID_ARGUMENT, "input mode %d", d->input_mode);
     if (d->result_mode < WS_RESULT_DEVICE || d->result_mode > WS_RESULT_COPY)
         return fail(WS_ERR_INVALID_ARGUMENT, "result mode %d", d->result_mode);
-    const uint32_t known = WS_LANE_FLAG_NO_GRAPH | WS_LANE_FLAG_STAGE_TIMING | WS_LANE_FLAG_NO_DEVICE;
+    const uint32_t known =
+        WS_LANE_FLAG_NO_GRAPH | WS_LANE_FLAG_STAGE_TIMING | WS_LANE_FLAG_NO_TIMING | WS_LANE_FLAG_NO_DEVICE;
     if (d->flags & ~known) return fail(WS_ERR_INVALID_ARGUMENT, "unknown flags 0x%x", d->flags & ~known);
     if ((d->flags & WS_LANE_FLAG_NO_DEVICE) && d->fake_polls < 0)
         return fail(WS_ERR_INVALID_ARGUMENT, "fake_polls %d < 0", d->fake_polls);
@@ -373,8 +380,11 @@ ws_status ws_lane_submit(ws_lane* L) {
         L->state = WS_LANE_IN_FLIGHT;
         return WS_OK;
     }
-    cudaError_t e = cudaEventRecord(L->ev_start, L->stream);
-    if (e != cudaSuccess) return cuda_fail(e, "record start event");
+    cudaError_t e = cudaSuccess;
+    if (submit_timing(L)) {
+        e = cudaEventRecord(L->ev_start, L->stream);
+        if (e != cudaSuccess) return cuda_fail(e, "record start event");
+    }
     if (use_graph(L)) {
         e = cudaGraphLaunch(L->exec, L->stream);
         if (e != cudaSuccess) return cuda_fail(e, "graph launch");
@@ -394,6 +404,15 @@ ws_status ws_lane_wait(ws_lane* L, int64_t timeout_us, ws_lane_timing* timing) {
     if (!L) return fail(WS_ERR_INVALID_ARGUMENT, "lane is NULL");
     if (L->state != WS_LANE_IN_FLIGHT) return fail(WS_ERR_LANE_STATE, "wait needs a lane in flight");
     const auto t0 = std::chrono::steady_clock::now();
+    if (!L->fake && timeout_us < 0) {
+        // no deadline: the driver's own wait on the completion event reacts
+        // faster than polling cudaEventQuery
+        cudaError_t e = cudaEventSynchronize(L->ev_end);
+        if (e != cudaSuccess) {
+            L->state = WS_LANE_FREE;
+            return cuda_fail(e, "lane work");
+        }
+    }
     for (;;) {
         cudaError_t e;
         if (L->fake) {
@@ -419,7 +438,8 @@ ws_status ws_lane_wait(ws_lane* L, int64_t timeout_us, ws_lane_timing* timing) {
         timing->gpu_us = timing->preprocess_us = timing->topk_us = -1.f;
         if (!L->fake) {
             float ms = 0.f;
-            if (cudaEventElapsedTime(&ms, L->ev_start, L->ev_end) == cudaSuccess) timing->gpu_us = ms * 1000.f;
+            if (submit_timing(L) && cudaEventElapsedTime(&ms, L->ev_start, L->ev_end) == cudaSuccess)
+                timing->gpu_us = ms * 1000.f;
             if (stage_timing(L)) {
                 if (cudaEventElapsedTime(&ms, L->ev_pre0, L->ev_pre1) == cudaSuccess)
                     timing->preprocess_us = ms * 1000.f;

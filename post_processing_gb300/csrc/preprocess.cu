@@ -8,18 +8,19 @@
 // its channel plane of the NCHW tensor.  Nothing else is materialised.
 //
 // How (GB300 design, not the page's one-thread-per-pixel gather):
-//  * Staged kernel (16-byte aligned rows).  A block owns one frame and a band
-//    of output rows.  One thread works out which source rows the band needs
-//    (two per output row on a downscale, fewer on an upscale, none for
-//    letterbox padding rows) and pulls each whole row into shared memory
-//    with one bulk copy (cp.async.bulk, completion counted on an mbarrier).
-//    On a 4-9x downscale the bilinear taps of a row touch every 32-byte
-//    sector, so streaming whole rows is the least DRAM traffic any reader
-//    can have; the bulk copy engine moves them without spending registers.
-//    While the copies fly, the threads build the column tap table (byte
-//    offsets and weights) in shared memory.  Each thread then produces four
-//    consecutive x of one output row and writes them as one 16-byte store per
-//    channel plane, so the NCHW planes are written fully coalesced.
+//  * Ring kernel (16-byte aligned rows), persistent.  The work is cut into
+//    units of (frame, band of output rows); each resident block walks its
+//    share of units.  Warp 0 plans a unit (one lane per output row works out
+//    its two source rows and weight) and pulls each needed source row, whole,
+//    into a stage of a shared-memory ring with one bulk copy (cp.async.bulk),
+//    completion counted on the stage's mbarrier.  While the block computes
+//    unit i from its stage, the copies of the next units are already in
+//    flight, so HBM sees a steady stream instead of load-then-compute bursts.
+//    On a 4-9x downscale the taps of a row touch every 32-byte sector, so
+//    whole rows are also the least DRAM traffic any reader can have.  The
+//    column tap table (byte offsets and weights) is built once per block.
+//    Each thread produces four consecutive x of one output row and writes one
+//    16-byte store per channel plane: the NCHW planes are written coalesced.
 //  * Direct kernel (any alignment): one thread per output pixel with plain
 //    byte loads; same arithmetic, same results.
 //
@@ -33,16 +34,27 @@
 #include "ws_internal.cuh"
 
 namespace ws {
+
+// Tuning of one launch of the ring kernel.
+struct PreTuning {
+    int band, stages, blocks_per_sm, threads;
+};
+
 namespace {
 
-constexpr int kPreThreads = 256;
-constexpr int kMaxBand = 16;
-constexpr int kMaxSlots = 2 * kMaxBand;
-constexpr int kSmemTarget = 56 * 1024;     // about four blocks per SM
+constexpr int kMaxBand = 8;            // output rows per unit
+constexpr int kMaxStages = 8;
+constexpr int kMaxThreads = 512;
 constexpr int kMaxTableCols = 8192;
-constexpr int kHeaderBytes = 16 + 4 * (3 * kMaxBand + kMaxSlots + 1);
-constexpr int kOffCols = (kHeaderBytes + 15) / 16 * 16;
 constexpr unsigned long long kWaitLimitNs = 1ull << 30;   // ~1.07 s
+constexpr unsigned kFull = 0xffffffffu;
+
+struct StagePlan {
+    int frame, y0, nrows, pad_;
+    int a[kMaxBand];     // byte offset in the stage of output row r's upper source row, -1 = padding row
+    int b[kMaxBand];     // ... of its lower source row
+    float wy[kMaxBand];
+};
 
 struct PreParams {
     const uint8_t* src;
@@ -52,11 +64,16 @@ struct PreParams {
     float M[3], R[3];         // out = (v - M) * R
     float pad;                // padding byte value
     float* dst;
-    int band;                 // staged: output rows per block
-    int slot_bytes;           // staged: shared bytes per staged source row (multiple of 16)
-    int bulk_bytes;           // staged: leading bytes of a row moved by the bulk copy
+    // ring kernel
+    int band;                 // output rows per unit
+    int stages;               // ring depth
+    int slot_bytes;           // shared bytes per staged source row (multiple of 16)
+    int bulk_bytes;           // leading bytes of a row moved by the bulk copy (multiple of 16)
     int row_bytes;            // 3 * sw
-    int off_slots;            // staged: shared offset of the row slots
+    int stage_bytes;          // 2 * band * slot_bytes
+    int off_plan, off_cols, off_slots;
+    int nbands;               // units per frame
+    long long units;          // batch * nbands
     uint32_t* err;            // device error word
 };
 
@@ -64,9 +81,20 @@ struct PreParams {
 __device__ __forceinline__ void axis_taps(int x, int S, int D, int& lo, int& hi, float& w) {
     const long long num = (2LL * x + 1) * S - D;
     const long long den = 2LL * D;
-    long long q = num / den;                  // truncates toward zero
-    if (num < 0 && q * den != num) --q;       // floor
-    const long long rem = num - q * den;      // 0 <= rem < den
+    long long q, rem;
+    if (num >= -0x3fffffffLL && num <= 0x3fffffffLL && den <= 0x3fffffffLL) {
+        // same integer arithmetic in 32 bits (every size up to ~23k pixels)
+        const int n32 = (int)num, d32 = (int)den;
+        int q32 = n32 / d32;                  // truncates toward zero
+        if (n32 < 0 && q32 * d32 != n32) --q32;
+        q = q32;
+        rem = n32 - q32 * d32;
+    } else {
+        q = num / den;
+        if (num < 0 && q * den != num) --q;   // floor
+        rem = num - q * den;
+    }
+    // 0 <= rem < den
     w = __fdiv_rn((float)rem, (float)den);
     lo = (int)(q < 0 ? 0 : (q > S - 1 ? S - 1 : q));
     const long long q1 = q + 1;
@@ -79,6 +107,9 @@ __device__ __forceinline__ uint32_t smem_u32(const void* p) {
 
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init() {
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
 }
 
@@ -116,6 +147,7 @@ __device__ __forceinline__ unsigned long long global_ns() {
 
 // Waits for phase `parity` of `bar`, giving up after `limit_ns`.
 __device__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, unsigned long long limit_ns) {
+    if (mbar_try_wait(bar, parity)) return true;
     const unsigned long long t0 = global_ns();
     while (!mbar_try_wait(bar, parity)) {
         if (global_ns() - t0 > limit_ns) return false;
@@ -123,113 +155,86 @@ __device__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, unsigned long 
     return true;
 }
 
-__device__ __forceinline__ int find_or_add(int* rows, int& n, int j) {
-    for (int s = 0; s < n; ++s)
-        if (rows[s] == j) return s;
-    rows[n] = j;
-    return n++;
+// Warp 0: plan unit `u` into stage `s` and start its copies.  Lane r handles
+// output row r of the unit; its rows go to slots 2r and 2r+1 of the stage.
+__device__ void issue_unit(const PreParams& p, long long u, uint64_t* bar, StagePlan* plan,
+                           unsigned char* stage) {
+    const int lane = threadIdx.x & 31;
+    const int frame = (int)(u / p.nbands);
+    const int y0 = (int)(u - (long long)frame * p.nbands) * p.band;
+    const int nrows = min(p.band, p.dh - y0);
+    const uint8_t* fr = p.src + (long long)frame * p.frame_stride;
+    int ja = -1, jb = -1;
+    uint32_t bytes = 0;
+    if (lane < nrows) {
+        const int y = y0 + lane;
+        int a = -1, b = -1;
+        float wy = 0.f;
+        if (y >= p.top && y < p.top + p.nh) {
+            int j0, j1;
+            axis_taps(y - p.top, p.sh, p.nh, j0, j1, wy);
+            a = 2 * lane * p.slot_bytes;
+            ja = j0;
+            bytes += p.bulk_bytes;
+            if (wy != 0.f && j1 != j0) {   // a zero weight needs no second row (v = t exactly)
+                b = a + p.slot_bytes;
+                jb = j1;
+                bytes += p.bulk_bytes;
+            } else {
+                b = a;
+            }
+        }
+        plan->a[lane] = a;
+        plan->b[lane] = b;
+        plan->wy[lane] = wy;
+    }
+    if (lane == 0) {
+        plan->frame = frame;
+        plan->y0 = y0;
+        plan->nrows = nrows;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) bytes += __shfl_xor_sync(kFull, bytes, o);
+    // The expected bytes are registered (with the one arrival) before any copy
+    // can complete; a band of padding rows completes the phase at once.
+    if (lane == 0) mbar_arrive_expect_tx(bar, bytes);
+    __syncwarp();
+    if (p.bulk_bytes > 0) {
+        if (ja >= 0) bulk_g2s(stage + 2 * lane * p.slot_bytes, fr + (long long)ja * p.row_stride, p.bulk_bytes, bar);
+        if (jb >= 0)
+            bulk_g2s(stage + (2 * lane + 1) * p.slot_bytes, fr + (long long)jb * p.row_stride, p.bulk_bytes, bar);
+    }
+    // Ragged row ends (< 16 bytes) by plain loads; consumers see them after
+    // the block barriers that separate issue from use.
+    for (int t = p.bulk_bytes; t < p.row_bytes; ++t) {
+        if (ja >= 0) stage[2 * lane * p.slot_bytes + t] = fr[(long long)ja * p.row_stride + t];
+        if (jb >= 0) stage[(2 * lane + 1) * p.slot_bytes + t] = fr[(long long)jb * p.row_stride + t];
+    }
 }
 
 template <bool kVecStore>
-__global__ void __launch_bounds__(kPreThreads) pre_staged_kernel(const __grid_constant__ PreParams p) {
-    extern __shared__ __align__(128) unsigned char smem[];
-    uint64_t* bar = reinterpret_cast<uint64_t*>(smem);
-    int* s_slot_a = reinterpret_cast<int*>(smem + 16);   // [kMaxBand] slot of the upper row, -1 = padding row
-    int* s_slot_b = s_slot_a + kMaxBand;                  // [kMaxBand] slot of the lower row
-    float* s_wy = reinterpret_cast<float*>(s_slot_b + kMaxBand);  // [kMaxBand]
-    int* s_rows = reinterpret_cast<int*>(s_wy + kMaxBand);        // [kMaxSlots] source row per slot
-    int* s_nslots = s_rows + kMaxSlots;
-    int* s_off0 = reinterpret_cast<int*>(smem + kOffCols);        // [dw] byte offset of the left tap
-    int* s_off1 = s_off0 + p.dw;                                  // [dw] byte offset of the right tap
-    float* s_wx = reinterpret_cast<float*>(s_off1 + p.dw);        // [dw]
-    unsigned char* slots = smem + p.off_slots;
-
-    const int tid = threadIdx.x;
-    const int b = blockIdx.y;
-    const int y0 = blockIdx.x * p.band;
-    const int nrows = min(p.band, p.dh - y0);
-    const uint8_t* frame = p.src + (long long)b * p.frame_stride;
-
-    if (tid == 0) {
-        int n = 0;
-        for (int r = 0; r < nrows; ++r) {
-            const int y = y0 + r;
-            int a = -1, c = -1;
-            float wy = 0.f;
-            if (y >= p.top && y < p.top + p.nh) {
-                int j0, j1;
-                axis_taps(y - p.top, p.sh, p.nh, j0, j1, wy);
-                a = find_or_add(s_rows, n, j0);
-                // a zero weight needs no second row (v = t exactly)
-                c = (wy != 0.f && j1 != j0) ? find_or_add(s_rows, n, j1) : a;
-            }
-            s_slot_a[r] = a;
-            s_slot_b[r] = c;
-            s_wy[r] = wy;
-        }
-        *s_nslots = n;
-        if (n > 0 && p.bulk_bytes > 0) {
-            mbar_init(bar, 1);
-            mbar_arrive_expect_tx(bar, (uint32_t)n * (uint32_t)p.bulk_bytes);
-            for (int s = 0; s < n; ++s)
-                bulk_g2s(slots + (size_t)s * p.slot_bytes, frame + (long long)s_rows[s] * p.row_stride,
-                         (uint32_t)p.bulk_bytes, bar);
-        }
-    }
-
-    // Column taps while the rows are in flight.
-    for (int x = tid; x < p.dw; x += kPreThreads) {
-        int i0 = 0, i1 = 0;
-        float wx = 0.f;
-        if (x >= p.left && x < p.left + p.nw) axis_taps(x - p.left, p.sw, p.nw, i0, i1, wx);
-        s_off0[x] = 3 * i0;
-        s_off1[x] = 3 * i1;
-        s_wx[x] = wx;
-    }
-    __syncthreads();
-
-    const int nslots = *s_nslots;
-    const int tail = p.row_bytes - p.bulk_bytes;   // < 16 trailing bytes moved by plain loads
-    if (tail > 0) {
-        for (int i = tid; i < nslots * tail; i += kPreThreads) {
-            const int s = i / tail, t = p.bulk_bytes + i % tail;
-            slots[(size_t)s * p.slot_bytes + t] = frame[(long long)s_rows[s] * p.row_stride + t];
-        }
-    }
-    int ok = 1;
-    if (nslots > 0 && p.bulk_bytes > 0) ok = mbar_wait_bounded(bar, 0, kWaitLimitNs) ? 1 : 0;
-    if (!__syncthreads_and(ok)) {
-        // A copy never completed: report it, give copies in flight a last
-        // bounded chance to land in this block's memory, and leave.
-        if (tid == 0) atomicOr(p.err, kDevErrBulkCopyTimeout);
-        if (!ok) mbar_wait_bounded(bar, 0, kWaitLimitNs);
-        return;
-    }
-
-    float padn[3];
-#pragma unroll
-    for (int c = 0; c < 3; ++c) padn[c] = (p.pad - p.M[c]) * p.R[c];
-
+__device__ __forceinline__ void compute_unit(const PreParams& p, const StagePlan& plan, const unsigned char* stage,
+                                             const int* s_off0, const int* s_off1, const float* s_wx,
+                                             const float (&padn)[3]) {
     const int groups = (p.dw + 3) >> 2;
-    const int items = nrows * groups;
+    const int items = plan.nrows * groups;
     const size_t plane = (size_t)p.dh * p.dw;
-    float* out_b = p.dst + (size_t)b * 3 * plane;
-
-    for (int it = tid; it < items; it += kPreThreads) {
+    float* out_b = p.dst + (size_t)plan.frame * 3 * plane;
+    for (int it = threadIdx.x; it < items; it += blockDim.x) {
         const int r = it / groups;
         const int x0 = (it - r * groups) * 4;
-        const int y = y0 + r;
+        const int y = plan.y0 + r;
         float o[3][4];
-        const int sa = s_slot_a[r];
+        const int sa = plan.a[r];
         if (sa < 0) {
 #pragma unroll
             for (int q = 0; q < 4; ++q)
 #pragma unroll
                 for (int c = 0; c < 3; ++c) o[c][q] = padn[c];
         } else {
-            const unsigned char* A = slots + (size_t)sa * p.slot_bytes;
-            const unsigned char* B = slots + (size_t)s_slot_b[r] * p.slot_bytes;
-            const float wy = s_wy[r];
+            const unsigned char* A = stage + sa;
+            const unsigned char* B = stage + plan.b[r];
+            const float wy = plan.wy[r];
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
                 const int x = x0 + q;
@@ -266,8 +271,73 @@ __global__ void __launch_bounds__(kPreThreads) pre_staged_kernel(const __grid_co
     }
 }
 
+template <bool kVecStore>
+__global__ void __launch_bounds__(kMaxThreads) pre_ring_kernel(const __grid_constant__ PreParams p) {
+    extern __shared__ __align__(128) unsigned char smem[];
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem);                    // [stages]
+    StagePlan* plans = reinterpret_cast<StagePlan*>(smem + p.off_plan);   // [stages]
+    int* s_off0 = reinterpret_cast<int*>(smem + p.off_cols);              // [dw] byte offset of the left tap
+    int* s_off1 = s_off0 + p.dw;                                          // [dw] byte offset of the right tap
+    float* s_wx = reinterpret_cast<float*>(s_off1 + p.dw);                // [dw]
+    unsigned char* slots = smem + p.off_slots;
+
+    // Let a programmatic dependent (the Top-K) be launched now; it waits for
+    // this grid's completion before it reads anything.
+    asm volatile("griddepcontrol.launch_dependents;");
+    const int tid = threadIdx.x;
+    const long long G = gridDim.x;
+    const long long first = blockIdx.x;
+    const int n_my = p.units > first ? (int)((p.units - 1 - first) / G + 1) : 0;
+
+    if (tid < 32) {
+        if (tid == 0) {
+            for (int s = 0; s < p.stages; ++s) mbar_init(&bars[s], 1);
+            fence_mbar_init();
+        }
+        __syncwarp();
+        const int pre = min(p.stages, n_my);
+        for (int i = 0; i < pre; ++i)
+            issue_unit(p, first + i * G, &bars[i], &plans[i], slots + (size_t)i * p.stage_bytes);
+    }
+    // Column taps, once per block, while the first rows are in flight.
+    for (int x = tid; x < p.dw; x += blockDim.x) {
+        int i0 = 0, i1 = 0;
+        float wx = 0.f;
+        if (x >= p.left && x < p.left + p.nw) axis_taps(x - p.left, p.sw, p.nw, i0, i1, wx);
+        s_off0[x] = 3 * i0;
+        s_off1[x] = 3 * i1;
+        s_wx[x] = wx;
+    }
+    float padn[3];
+#pragma unroll
+    for (int c = 0; c < 3; ++c) padn[c] = (p.pad - p.M[c]) * p.R[c];
+    __syncthreads();
+
+    for (int i = 0; i < n_my; ++i) {
+        const int s = i % p.stages;
+        const uint32_t parity = (uint32_t)(i / p.stages) & 1u;
+        const bool ok = mbar_wait_bounded(&bars[s], parity, kWaitLimitNs);
+        if (ok)
+            compute_unit<kVecStore>(p, plans[s], slots + (size_t)s * p.stage_bytes, s_off0, s_off1, s_wx, padn);
+        // Everyone is done with stage s (and agrees on whether a copy hung).
+        if (__syncthreads_or(!ok)) {
+            if (tid == 0) {
+                atomicOr(p.err, kDevErrBulkCopyTimeout);
+                // let the copies still in flight land in this block's memory
+                for (int j = i; j < min(n_my, i + p.stages); ++j)
+                    mbar_wait_bounded(&bars[j % p.stages], (uint32_t)(j / p.stages) & 1u, kWaitLimitNs);
+            }
+            return;
+        }
+        if (tid < 32 && i + p.stages < n_my)
+            issue_unit(p, first + (long long)(i + p.stages) * G, &bars[s], &plans[s],
+                       slots + (size_t)s * p.stage_bytes);
+    }
+}
+
 // One thread per destination pixel, plain byte loads; any alignment.
 __global__ void __launch_bounds__(256) pre_direct_kernel(const __grid_constant__ PreParams p, long long total) {
+    asm volatile("griddepcontrol.launch_dependents;");
     const size_t plane = (size_t)p.dh * p.dw;
     for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < total;
          i += (long long)gridDim.x * blockDim.x) {
@@ -324,7 +394,56 @@ void inner_box(const ws_preprocess_desc& d, int* nw, int* nh, int* left, int* to
     *top = (int)((dh - h) / 2);
 }
 
-bool g_staged_attr_set[64][2];
+size_t align16(size_t v) { return (v + 15) / 16 * 16; }
+
+// Shared-memory layout of the ring kernel for a tuning; returns total bytes.
+size_t ring_layout(PreParams& p, const PreTuning& t) {
+    p.band = t.band;
+    p.stages = t.stages;
+    p.stage_bytes = 2 * t.band * p.slot_bytes;
+    p.off_plan = (int)align16(8 * kMaxStages);
+    p.off_cols = (int)align16(p.off_plan + sizeof(StagePlan) * kMaxStages);
+    p.off_slots = (int)align16(p.off_cols + 12 * (size_t)p.dw);
+    return (size_t)p.off_slots + (size_t)t.stages * p.stage_bytes;
+}
+
+// Default tuning (from a sweep of rows per unit, ring depth and blocks per SM
+// on GB300, 64 x 1080p -> 224 and 8 x 4K -> 512): three resident blocks per
+// SM, each a ring of ~70 KB, so that with one stage being computed the others
+// keep >= ~64 KB of source rows in flight per SM (HBM bandwidth x loaded
+// latency); about 128 threads of 4-column items per unit; single-frame work
+// spread thin for latency.
+PreTuning default_tuning(const PreParams& p, int batch, const DeviceInfo& info) {
+    const int groups = (p.dw + 3) / 4;
+    const size_t fixed = align16(8 * kMaxStages) + sizeof(StagePlan) * kMaxStages + align16(12 * (size_t)p.dw) + 64;
+    PreTuning t{};
+    for (int bps = 3; bps >= 1; --bps) {
+        const size_t budget =
+            std::min<size_t>((size_t)info.smem_per_sm / bps - 1024, (size_t)info.max_smem_optin);
+        int band = std::max(1, std::min(kMaxBand, 128 / std::max(groups, 1)));
+        // keep at least ~2 units per resident block when the batch is large enough
+        const long long slots_total = (long long)info.sm_count * bps;
+        while (band > 1 && (long long)batch * ((p.dh + band - 1) / band) < 2 * slots_total) band /= 2;
+        int stages = 0;
+        for (;;) {
+            const size_t stage = 2ull * band * p.slot_bytes;
+            stages = (int)std::min<size_t>(kMaxStages, (budget > fixed ? budget - fixed : 0) / stage);
+            if (stages >= 2 || band == 1) break;
+            band /= 2;
+        }
+        t.blocks_per_sm = bps;
+        t.band = band;
+        t.stages = std::max(1, std::min(stages, 3));
+        t.threads = std::min(kMaxThreads, std::max(64, (band * groups + 31) / 32 * 32));
+        // blocks that get a single unit (small batches) are latency-bound:
+        // more threads build the column table and issue the loads sooner
+        if ((long long)batch * ((p.dh + band - 1) / band) <= slots_total) t.threads = std::max(t.threads, 128);
+        if (stages >= 2) break;   // else: very wide rows, fewer blocks with more memory each
+    }
+    return t;
+}
+
+bool g_ring_attr_set[64][2];
 
 }  // namespace
 
@@ -365,19 +484,9 @@ ws_status validate_preprocess(const ws_preprocess_desc* d, int32_t batch) {
     return WS_OK;
 }
 
-}  // namespace ws
-
-extern "C" {
-
-ws_status ws_preprocess_validate(const ws_preprocess_desc* desc, int32_t batch) {
-    ws::clear_error();
-    return ws::validate_preprocess(desc, batch);
-}
-
-ws_status ws_preprocess(const ws_preprocess_desc* d, const uint8_t* src, int32_t batch, float* dst,
-                        cudaStream_t stream) {
-    using namespace ws;
-    clear_error();
+// Launch with an explicit ring tuning (NULL = the default policy).
+ws_status preprocess_launch(const ws_preprocess_desc* d, const uint8_t* src, int32_t batch, float* dst,
+                            cudaStream_t stream, const PreTuning* tuning) {
     ws_status st = validate_preprocess(d, batch);
     if (st != WS_OK) return st;
     if (!src || !dst) return fail(WS_ERR_INVALID_ARGUMENT, "src or dst is NULL");
@@ -405,41 +514,35 @@ ws_status ws_preprocess(const ws_preprocess_desc* d, const uint8_t* src, int32_t
     p.pad = (float)d->pad_value;
     p.dst = dst;
     p.row_bytes = 3 * d->src_w;
+    p.slot_bytes = (int)align16(p.row_bytes);
+    p.bulk_bytes = p.row_bytes / 16 * 16;
     p.err = device_error_word();
 
     const bool aligned = ((uintptr_t)src % 16 == 0) && (d->src_row_stride % 16 == 0) &&
                          (batch == 1 || d->src_frame_stride % 16 == 0);
-    const int slot_bytes = (p.row_bytes + 15) / 16 * 16;
-    const int off_slots = kOffCols + (12 * d->dst_w + 15) / 16 * 16;
-    const long long min_smem = (long long)off_slots + 2LL * slot_bytes;
-    if (aligned && d->dst_w <= kMaxTableCols && min_smem <= info->max_smem_optin) {
-        int band = 1;
-        while (band < kMaxBand && off_slots + 2LL * (band + 1) * slot_bytes <= kSmemTarget) ++band;
-        // keep at least two blocks per SM in the grid
-        while (band > 1 && (long long)((d->dst_h + band - 1) / band) * batch < 2LL * info->sm_count) band /= 2;
-        p.band = band;
-        p.slot_bytes = slot_bytes;
-        p.bulk_bytes = p.row_bytes / 16 * 16;
-        p.off_slots = off_slots;
-        const size_t smem = (size_t)off_slots + 2ull * band * slot_bytes;
+    PreTuning t = tuning ? *tuning : default_tuning(p, batch, *info);
+    const size_t smem = ring_layout(p, t);
+    const bool ring_ok = aligned && d->dst_w <= kMaxTableCols && t.band >= 1 && t.band <= kMaxBand &&
+                         t.stages >= 1 && t.stages <= kMaxStages && t.threads >= 32 &&
+                         t.threads <= kMaxThreads && smem <= (size_t)info->max_smem_optin;
+    if (ring_ok) {
+        p.nbands = (d->dst_h + t.band - 1) / t.band;
+        p.units = (long long)batch * p.nbands;
         const bool vec = (d->dst_w % 4 == 0) && ((uintptr_t)dst % 16 == 0);
-        if (!g_staged_attr_set[dev][vec]) {
+        if (!g_ring_attr_set[dev][vec]) {
             if (vec)
-                WS_TRY_CUDA(cudaFuncSetAttribute(pre_staged_kernel<true>,
-                                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
+                WS_TRY_CUDA(cudaFuncSetAttribute(pre_ring_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                  info->max_smem_optin));
             else
-                WS_TRY_CUDA(cudaFuncSetAttribute(pre_staged_kernel<false>,
-                                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
+                WS_TRY_CUDA(cudaFuncSetAttribute(pre_ring_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                  info->max_smem_optin));
-            g_staged_attr_set[dev][vec] = true;
+            g_ring_attr_set[dev][vec] = true;
         }
-        const dim3 grid((d->dst_h + band - 1) / band, batch);
-        if (grid.y > 65535) return fail(WS_ERR_UNSUPPORTED, "batch %d > 65535", batch);
+        const long long blocks = std::min<long long>(p.units, (long long)info->sm_count * t.blocks_per_sm);
         if (vec)
-            pre_staged_kernel<true><<<grid, kPreThreads, smem, stream>>>(p);
+            pre_ring_kernel<true><<<(unsigned)blocks, t.threads, smem, stream>>>(p);
         else
-            pre_staged_kernel<false><<<grid, kPreThreads, smem, stream>>>(p);
+            pre_ring_kernel<false><<<(unsigned)blocks, t.threads, smem, stream>>>(p);
     } else {
         const long long total = (long long)batch * d->dst_h * d->dst_w;
         const long long blocks = std::min<long long>((total + 255) / 256, (long long)info->sm_count * 16);
@@ -448,6 +551,21 @@ ws_status ws_preprocess(const ws_preprocess_desc* d, const uint8_t* src, int32_t
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e, "preprocess launch");
     return WS_OK;
+}
+
+}  // namespace ws
+
+extern "C" {
+
+ws_status ws_preprocess_validate(const ws_preprocess_desc* desc, int32_t batch) {
+    ws::clear_error();
+    return ws::validate_preprocess(desc, batch);
+}
+
+ws_status ws_preprocess(const ws_preprocess_desc* d, const uint8_t* src, int32_t batch, float* dst,
+                        cudaStream_t stream) {
+    ws::clear_error();
+    return ws::preprocess_launch(d, src, batch, dst, stream, nullptr);
 }
 
 }  // extern "C"

@@ -44,6 +44,7 @@ constexpr int kVpt = 32;                       // values per thread
 constexpr int kChunk = kThreads * kVpt;        // 8192 elements per block
 constexpr int kCap = 2048;                     // shared candidate capacity
 constexpr int kMaxK = 32;
+constexpr int kMergeBatch = 8;                 // keys each merging thread loads at once
 constexpr unsigned kFull = 0xffffffffu;
 
 struct TopkParams {
@@ -62,6 +63,15 @@ __device__ __forceinline__ uint32_t order_bits(float f) {
     if ((b & 0x7fffffffu) > 0x7f800000u) b = 0xff800000u;   // NaN -> -inf
     if (b == 0x80000000u) b = 0u;                            // -0 -> +0 (ordering only)
     return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+
+// Inverse of order_bits on the canonical value: the float bits of a key's
+// value.  Only the sign of a zero is lost, so zeros are read back from x.
+__device__ __forceinline__ float key_value(unsigned long long key, const float* xr) {
+    const uint32_t u = (uint32_t)(key >> 32);
+    const uint32_t b = (u & 0x80000000u) ? (u & 0x7fffffffu) : ~u;
+    if (b == 0u) return xr[~(uint32_t)(key & 0xffffffffull)];   // +0 or -0 as stored
+    return __uint_as_float(b);                                   // NaN came in as -inf
 }
 
 __device__ __forceinline__ unsigned long long make_key(uint32_t u, uint32_t idx) {
@@ -162,6 +172,10 @@ __device__ __forceinline__ void rank_and_emit(const Shared& s, uint32_t cnt, int
 template <bool kVec>
 __global__ void __launch_bounds__(kThreads) topk_kernel(const __grid_constant__ TopkParams p) {
     __shared__ Shared s;
+    // Launched as a programmatic dependent of the previous kernel on the
+    // stream: wait here until that grid has finished and its writes (the
+    // logits) are visible.  A no-op for an ordinary launch.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const long long row = blockIdx.x / p.nchunks;
     const int chunk = (int)(blockIdx.x - row * p.nchunks);
@@ -170,35 +184,41 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(const __grid_constant__ 
     const float* xr = p.x + row * p.cols;
     const int k = p.k;
 
-    // 1. load, order-map, delegate
-    uint32_t u[kVpt];
+    // 1. load and delegate.  Every load is issued unconditionally
+    // (out-of-range slots re-read the chunk's last element) so that all of a
+    // thread's loads are in flight at once; out-of-range slots then hold NaN,
+    // which no comparison below lets through.
+    float v[kVpt];
     if (kVec) {
+        const float4* base = reinterpret_cast<const float4*>(xr + c0);
+        const int n4 = n >> 2;   // n is a multiple of 4 on this path
+        float4 q[kVpt / 4];
+#pragma unroll
+        for (int i = 0; i < kVpt / 4; ++i) q[i] = __ldcs(base + min(i * kThreads + tid, n4 - 1));
 #pragma unroll
         for (int i = 0; i < kVpt / 4; ++i) {
-            const int e = (i * kThreads + tid) * 4;
-            if (e < n) {
-                const float4 v = __ldcs(reinterpret_cast<const float4*>(xr + c0 + e));
-                u[4 * i + 0] = order_bits(v.x);
-                u[4 * i + 1] = order_bits(v.y);
-                u[4 * i + 2] = order_bits(v.z);
-                u[4 * i + 3] = order_bits(v.w);
-            } else {
-                u[4 * i + 0] = u[4 * i + 1] = u[4 * i + 2] = u[4 * i + 3] = 0u;
-            }
+            const bool in = i * kThreads + tid < n4;
+            v[4 * i + 0] = in ? q[i].x : __int_as_float(0x7fffffff);
+            v[4 * i + 1] = in ? q[i].y : __int_as_float(0x7fffffff);
+            v[4 * i + 2] = in ? q[i].z : __int_as_float(0x7fffffff);
+            v[4 * i + 3] = in ? q[i].w : __int_as_float(0x7fffffff);
         }
     } else {
 #pragma unroll
-        for (int i = 0; i < kVpt; ++i) {
-            const int e = i * kThreads + tid;
-            u[i] = e < n ? order_bits(__ldcs(xr + c0 + e)) : 0u;
-        }
+        for (int i = 0; i < kVpt; ++i) v[i] = __ldcs(xr + c0 + min(i * kThreads + tid, n - 1));
+#pragma unroll
+        for (int i = 0; i < kVpt; ++i)
+            if (i * kThreads + tid >= n) v[i] = __int_as_float(0x7fffffff);
     }
-    auto elem = [&](int j) -> int {   // chunk-relative element index of u[j]
+    auto elem = [&](int j) -> int {   // chunk-relative element index of v[j]
         return kVec ? ((j >> 2) * kThreads + tid) * 4 + (j & 3) : j * kThreads + tid;
     };
-    uint32_t d = 0;
+    // The delegate is the thread's largest element (fmaxf skips NaN, so a NaN
+    // counts as -inf); threads without elements have none (0).
+    float dm = -INFINITY;
 #pragma unroll
-    for (int j = 0; j < kVpt; ++j) d = max(d, u[j]);
+    for (int j = 0; j < kVpt; ++j) dm = fmaxf(dm, v[j]);
+    uint32_t d = elem(0) < n ? order_bits(dm) : 0u;
 
     // 2. threshold: min over warps of each warp's ceil(K/warps)-th largest delegate
     const int kw = (k + kWarps - 1) / kWarps;
@@ -219,20 +239,35 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(const __grid_constant__ 
     int vouching = 0;
 #pragma unroll
     for (int w = 0; w < kWarps; ++w) {
-        const uint32_t v = s.warp_t[w];
-        if (v != 0) {
-            t = min(t, v);
+        const uint32_t tv = s.warp_t[w];
+        if (tv != 0) {
+            t = min(t, tv);
             ++vouching;
         }
     }
-    if (vouching * kw < k) t = 1;   // too few: take every element (0 marks an empty slot)
 
-    // 3. candidates
+    // 3. candidates.  Above -inf the threshold is tested as a float, one
+    // compare per element (NaN fails it, +0 and -0 both pass a zero); only
+    // the few survivors become keys.
+    const uint32_t kOrderNegInf = 0x007fffffu;   // order_bits(-inf)
+    if (vouching * kw >= k && t > kOrderNegInf) {
+        const float tf = __uint_as_float((t & 0x80000000u) ? (t & 0x7fffffffu) : ~t);
 #pragma unroll
-    for (int j = 0; j < kVpt; ++j) {
-        if (u[j] >= t) {
-            const uint32_t pos = atomicAdd(&s.cnt, 1u);
-            if (pos < kCap) s.cand[pos] = make_key(u[j], (uint32_t)(c0 + elem(j)));
+        for (int j = 0; j < kVpt; ++j) {
+            if (v[j] >= tf) {
+                const uint32_t pos = atomicAdd(&s.cnt, 1u);
+                if (pos < kCap) s.cand[pos] = make_key(order_bits(v[j]), (uint32_t)(c0 + elem(j)));
+            }
+        }
+    } else {
+        // too few vouching warps, or a threshold of -inf: every element is a
+        // candidate (this chunk then usually takes the radix select below)
+#pragma unroll
+        for (int j = 0; j < kVpt; ++j) {
+            if (elem(j) < n) {
+                const uint32_t pos = atomicAdd(&s.cnt, 1u);
+                if (pos < kCap) s.cand[pos] = make_key(order_bits(v[j]), (uint32_t)(c0 + elem(j)));
+            }
         }
     }
     __syncthreads();
@@ -255,11 +290,8 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(const __grid_constant__ 
     // 4. rank and emit
     if (p.nchunks == 1) {
         rank_and_emit(s, cnt, kk, [&](int rank, unsigned long long key) {
-            const uint32_t idx = key_index(key);
-            float v = xr[idx];
-            if (isnan(v)) v = -INFINITY;
-            p.out_val[row * k + rank] = v;
-            p.out_idx[row * k + rank] = (int)idx;
+            p.out_val[row * k + rank] = key_value(key, xr);
+            p.out_idx[row * k + rank] = (int)key_index(key);
         });
         return;
     }
@@ -280,24 +312,60 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(const __grid_constant__ 
 
     const unsigned long long* all = p.keys + row * p.nchunks * k;
     const int total = p.nchunks * k;
-    unsigned long long tm = 0;
-    for (int c = tid; c < p.nchunks; c += kThreads) {
-        const unsigned long long v = __ldcg(all + (long long)c * k + (k - 1));
-        tm = v > tm ? v : tm;
-    }
-    tm = warp_max_u64(tm);
-    if (lane == 0) s.red[warp] = tm;
-    if (tid == 0) s.cnt = 0;
-    __syncthreads();
-    unsigned long long t64 = 0;
+    // Threshold from the sorted chunk lists: the first m = ceil(K / chunks)
+    // keys of every chunk hold at least K keys, so the K-th largest of that
+    // union has at least K keys at or above it, and every key of the row's
+    // Top-K is at or above it.  It is found by counting, like the ranks.
+    const int m = (k + p.nchunks - 1) / p.nchunks;
+    const int U = m * p.nchunks;
+    unsigned long long t64;
+    if (U <= kCap) {
+        for (int i = tid; i < U; i += kThreads) {
+            const int c = i / m;
+            s.cand[i] = __ldcg(all + (long long)c * k + (i - c * m));
+        }
+        if (tid == 0) s.red[0] = ~0ull;
+        __syncthreads();
+        for (int i = tid; i < U; i += kThreads) {
+            const unsigned long long key = s.cand[i];
+            int rank = 0;
+            for (int j = 0; j < U; ++j) rank += (s.cand[j] > key) ? 1 : 0;
+            if (rank < k) atomicMin(&s.red[0], key);   // min of the top K = the K-th largest
+        }
+        if (tid == 0) s.cnt = 0;
+        __syncthreads();
+        t64 = s.red[0];
+        __syncthreads();   // everyone has read the threshold before cand is reused
+    } else {
+        // very many chunks: the largest K-th key over chunks (always valid)
+        unsigned long long tm = 0;
+        for (int c0m = 0; c0m < p.nchunks; c0m += kThreads * kMergeBatch) {
+            unsigned long long v[kMergeBatch];
 #pragma unroll
-    for (int w = 0; w < kWarps; ++w) t64 = s.red[w] > t64 ? s.red[w] : t64;
-    if (t64 == 0) t64 = 1;
-    for (int i = tid; i < total; i += kThreads) {
-        const unsigned long long key = __ldcg(all + i);
-        if (key >= t64) {
-            const uint32_t pos = atomicAdd(&s.cnt, 1u);
-            if (pos < kCap) s.cand[pos] = key;
+            for (int j = 0; j < kMergeBatch; ++j)
+                v[j] = __ldcg(all + (long long)min(c0m + j * kThreads + tid, p.nchunks - 1) * k + (k - 1));
+#pragma unroll
+            for (int j = 0; j < kMergeBatch; ++j) tm = v[j] > tm ? v[j] : tm;
+        }
+        tm = warp_max_u64(tm);
+        if (lane == 0) s.red[warp] = tm;
+        if (tid == 0) s.cnt = 0;
+        __syncthreads();
+        t64 = 0;
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w) t64 = s.red[w] > t64 ? s.red[w] : t64;
+    }
+    if (t64 == 0) t64 = 1;   // padding keys (0) never pass
+    for (int i0 = 0; i0 < total; i0 += kThreads * kMergeBatch) {
+        unsigned long long v[kMergeBatch];
+#pragma unroll
+        for (int j = 0; j < kMergeBatch; ++j) v[j] = __ldcg(all + min(i0 + j * kThreads + tid, total - 1));
+#pragma unroll
+        for (int j = 0; j < kMergeBatch; ++j) {
+            if (i0 + j * kThreads + tid < total && v[j] >= t64) {
+                const uint32_t pos = atomicAdd(&s.cnt, 1u);
+                if (pos < kCap) s.cand[pos] = v[j];
+            }
         }
     }
     __syncthreads();
@@ -315,11 +383,8 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(const __grid_constant__ 
         cnt = s.cnt;
     }
     rank_and_emit(s, cnt, k, [&](int rank, unsigned long long key) {
-        const uint32_t idx = key_index(key);
-        float v = xr[idx];
-        if (isnan(v)) v = -INFINITY;
-        p.out_val[row * k + rank] = v;
-        p.out_idx[row * k + rank] = (int)idx;
+        p.out_val[row * k + rank] = key_value(key, xr);
+        p.out_idx[row * k + rank] = (int)key_index(key);
     });
     if (tid == 0) p.tickets[row] = 0u;   // ready for the next call / replay
 }
@@ -398,11 +463,23 @@ ws_status ws_topk(const float* x, int64_t rows, int64_t cols, int32_t k, float* 
     const long long blocks = rows * p.nchunks;
     if (blocks > 2147483647LL) return fail(WS_ERR_UNSUPPORTED, "too many blocks");
     const bool vec = (cols % 4 == 0) && ((uintptr_t)x % 16 == 0);
-    if (vec)
-        topk_kernel<true><<<(unsigned)blocks, kThreads, 0, stream>>>(p);
-    else
-        topk_kernel<false><<<(unsigned)blocks, kThreads, 0, stream>>>(p);
-    cudaError_t e = cudaGetLastError();
+    // Programmatic dependent launch ("Streams, concurrency and CUDA Graphs",
+    // PDL section): the grid may be launched while the previous kernel on the
+    // stream is still running and waits in griddepcontrol.wait, which hides
+    // the launch gap between the preprocess and the Top-K.
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3((unsigned)blocks);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e = vec ? cudaLaunchKernelEx(&cfg, topk_kernel<true>, p) : cudaLaunchKernelEx(&cfg, topk_kernel<false>, p);
+    if (e != cudaSuccess) return cuda_fail(e, "top-k launch");
+    e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e, "top-k launch");
     return WS_OK;
 }

@@ -81,6 +81,8 @@ ODD = [
     (1920, 1080, 224, 224, False, "mean_std", 0, 0, 1, 1),   # config shape, misaligned base
     (4000, 3, 512, 7, False, "mean_std", 0, 0, 0, 1),        # 12000-byte rows, 2 rows
     (21, 700, 8, 300, False, "scale", 0, 0, 0, 2),            # 63-byte rows: bulk part 48 + tail 15
+    (2, 50000, 3, 60000, False, "scale", 10, 0, 0, 1),       # tall: 64-bit y taps, tail-only rows
+    (40000, 2, 30000, 1, False, "mean_std", 0, 0, 0, 1),     # wide: per-pixel kernel, 64-bit x taps
 ]
 
 
