@@ -430,16 +430,21 @@ def main():
                 latency[label]["gpu_us"] = percentiles(gpu)
     clk = clocks.stop()
 
-    # end to end through the lane API with host buffers: pinned frames in, result out
+    # End to end through the lane API with host buffers: the producer writes
+    # the frames into the lane's mapped pinned input slot, the preprocess
+    # reads the rows it needs in place across the host link, and the Top-K
+    # writes the K pairs straight into mapped pinned host memory (the
+    # producer / result path of the WarpStream write-up).  Two lanes, each on
+    # its own stream.
     e2e = None
     if args.e2e_steps > 0:
+        import ctypes
         e_lanes = []
         for _ in range(2):
-            d = B.lane_desc(pre, w["batch"], w["rows"], w["cols"], w["k"], input_mode=B.WS_INPUT_COPY,
-                            result_mode=B.WS_RESULT_COPY, logits=logits_dev.data_ptr(),
+            d = B.lane_desc(pre, w["batch"], w["rows"], w["cols"], w["k"], input_mode=B.WS_INPUT_MAPPED,
+                            result_mode=B.WS_RESULT_MAPPED, logits=logits_dev.data_ptr(),
                             flags=B.WS_LANE_FLAG_NO_TIMING)
             lane = Lane(d)
-            import ctypes
             buf = (ctypes.c_char * frames.nbytes).from_address(lane.buffers.input_host)
             np.frombuffer(buf, dtype=np.uint8)[:] = frames.reshape(-1)
             e_lanes.append(lane)
@@ -449,7 +454,6 @@ def main():
         if world > 1:
             torch.distributed.barrier()
         t0 = time.perf_counter()
-        pending = []
         for s in range(args.e2e_steps):
             lane = e_lanes[s % 2]
             if lane.state == B.WS_LANE_IN_FLIGHT:
@@ -461,10 +465,13 @@ def main():
                 lane.wait()
         e_dt = time.perf_counter() - t0
         e_rate, _ = whole_job_rate(w["batch"] * args.e2e_steps, e_dt, world, device)
-        e2e = {"value": e_rate, "unit": "frames/s", "h2d_bytes_per_step": int(frames.nbytes),
+        e2e = {"value": e_rate, "unit": "frames/s", "h2d_bytes_per_step": int(alg["source"]),
                "d2h_bytes_per_step": int(w["rows"] * w["k"] * 8),
-               "path": "ws_lane_submit/wait, input_mode=COPY (pinned host frames, H2D inside the graph), "
-                       "result_mode=COPY (D2H of the K pairs inside the graph), 2 lanes on their own streams"}
+               "path": "ws_lane_submit/wait on host buffers: input_mode=MAPPED (frames written by the host "
+                       "into mapped pinned memory; the kernel reads the needed rows, h2d_bytes_per_step, "
+                       "in place), result_mode=MAPPED (the K pairs written into pinned host memory); "
+                       "2 lanes on their own streams; host clock",
+               "frames_bytes_per_step": int(frames.nbytes)}
         for lane in e_lanes:
             lane.close()
 

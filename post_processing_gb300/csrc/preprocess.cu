@@ -32,6 +32,7 @@
 #include <cmath>
 
 #include "ws_internal.cuh"
+#include "ws_ptx.cuh"
 
 namespace ws {
 
@@ -46,7 +47,6 @@ constexpr int kMaxBand = 8;            // output rows per unit
 constexpr int kMaxStages = 8;
 constexpr int kMaxThreads = 512;
 constexpr int kMaxTableCols = 8192;
-constexpr unsigned long long kWaitLimitNs = 1ull << 30;   // ~1.07 s
 constexpr unsigned kFull = 0xffffffffu;
 
 struct StagePlan {
@@ -99,60 +99,6 @@ __device__ __forceinline__ void axis_taps(int x, int S, int D, int& lo, int& hi,
     lo = (int)(q < 0 ? 0 : (q > S - 1 ? S - 1 : q));
     const long long q1 = q + 1;
     hi = (int)(q1 < 0 ? 0 : (q1 > S - 1 ? S - 1 : q1));
-}
-
-__device__ __forceinline__ uint32_t smem_u32(const void* p) {
-    return (uint32_t)__cvta_generic_to_shared(p);
-}
-
-__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
-}
-
-__device__ __forceinline__ void fence_mbar_init() {
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
-                 : "memory");
-}
-
-// One bulk copy global -> this block's shared memory, completion on `bar`.
-__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
-    asm volatile(
-        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-            smem_u32(dst)),
-        "l"(src), "r"(bytes), "r"(smem_u32(bar))
-        : "memory");
-}
-
-__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}\n"
-        : "=r"(ok)
-        : "r"(smem_u32(bar)), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
-
-__device__ __forceinline__ unsigned long long global_ns() {
-    unsigned long long t;
-    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-    return t;
-}
-
-// Waits for phase `parity` of `bar`, giving up after `limit_ns`.
-__device__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, unsigned long long limit_ns) {
-    if (mbar_try_wait(bar, parity)) return true;
-    const unsigned long long t0 = global_ns();
-    while (!mbar_try_wait(bar, parity)) {
-        if (global_ns() - t0 > limit_ns) return false;
-    }
-    return true;
 }
 
 // Warp 0: plan unit `u` into stage `s` and start its copies.  Lane r handles

@@ -30,10 +30,12 @@
 // so the workspace is ready for the next call or graph replay) merges the
 // chunks' keys with the same threshold / rank steps, taking as threshold the
 // largest K-th key over chunks.
+#include <algorithm>
 #include <cmath>
 #include <mutex>
 
 #include "ws_internal.cuh"
+#include "ws_ptx.cuh"
 
 namespace ws {
 namespace {
@@ -45,6 +47,7 @@ constexpr int kChunk = kThreads * kVpt;        // 8192 elements per block
 constexpr int kCap = 2048;                     // shared candidate capacity
 constexpr int kMaxK = 32;
 constexpr int kMergeBatch = 8;                 // keys each merging thread loads at once
+constexpr int kMergeRegs = 12;                 // chunk lists per warp held in registers (<= 96 chunks)
 constexpr unsigned kFull = 0xffffffffu;
 
 struct TopkParams {
@@ -56,6 +59,7 @@ struct TopkParams {
     int* out_idx;
     unsigned int* tickets;        // [rows]
     unsigned long long* keys;     // [rows][nchunks][k]
+    uint32_t* err;                // device error word
 };
 
 __device__ __forceinline__ uint32_t order_bits(float f) {
@@ -91,15 +95,19 @@ __device__ __forceinline__ unsigned long long warp_max_u64(unsigned long long v)
     return v;
 }
 
-struct Shared {
+struct __align__(16) Shared {
     unsigned long long cand[kCap];
     unsigned long long red[kWarps];
     uint32_t hist[256];
     uint32_t warp_t[kWarps];
+    int warp_cnt[kWarps];
     uint32_t cnt;
     uint32_t sel[2];
     int last;
 };
+
+constexpr int kSharedBytes = (int)((sizeof(Shared) + 127) / 128 * 128);
+constexpr int kDynSmem = kSharedBytes + kChunk * 4;
 
 // Exact kth-largest (1-based) of n unique 64-bit keys by radix select.
 template <class KeyAt>
@@ -157,6 +165,30 @@ __device__ unsigned long long block_kth_largest(KeyAt key_at, int n, int kth, Sh
     return prefix;
 }
 
+// Block-wide placement without atomics: every thread contributes `mine`
+// items; returns the thread's first slot and sets `total` for the block.
+// Contains one __syncthreads.
+__device__ __forceinline__ int block_offsets(int mine, int& total, Shared& s) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    int incl = mine;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(kFull, incl, o);
+        if (lane >= o) incl += y;
+    }
+    if (lane == 31) s.warp_cnt[warp] = incl;
+    __syncthreads();
+    int base = 0;
+    total = 0;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) {
+        const int c = s.warp_cnt[w];
+        base += (w < warp) ? c : 0;
+        total += c;
+    }
+    return base + incl - mine;
+}
+
 // Ranks the `cnt` unique candidates in s.cand; calls emit(rank, key) for
 // ranks below `kk`.
 template <class Emit>
@@ -164,14 +196,18 @@ __device__ __forceinline__ void rank_and_emit(const Shared& s, uint32_t cnt, int
     for (uint32_t i = threadIdx.x; i < cnt; i += kThreads) {
         const unsigned long long key = s.cand[i];
         int rank = 0;
+#pragma unroll 8
         for (uint32_t j = 0; j < cnt; ++j) rank += (s.cand[j] > key) ? 1 : 0;
         if (rank < kk) emit(rank, key);
     }
 }
 
 template <bool kVec>
-__global__ void __launch_bounds__(kThreads) topk_kernel(const __grid_constant__ TopkParams p) {
-    __shared__ Shared s;
+__global__ void __launch_bounds__(kThreads, 4) topk_kernel(const __grid_constant__ TopkParams p) {
+    extern __shared__ __align__(128) unsigned char dsmem[];
+    Shared& s = *reinterpret_cast<Shared*>(dsmem);
+    float* sx = reinterpret_cast<float*>(dsmem + kSharedBytes);   // [kChunk] the staged chunk
+    __shared__ uint64_t bar;
     // Launched as a programmatic dependent of the previous kernel on the
     // stream: wait here until that grid has finished and its writes (the
     // logits) are visible.  A no-op for an ordinary launch.
@@ -184,41 +220,45 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(const __grid_constant__ 
     const float* xr = p.x + row * p.cols;
     const int k = p.k;
 
-    // 1. load and delegate.  Every load is issued unconditionally
-    // (out-of-range slots re-read the chunk's last element) so that all of a
-    // thread's loads are in flight at once; out-of-range slots then hold NaN,
-    // which no comparison below lets through.
-    float v[kVpt];
+    // 1. stage the chunk in shared memory: one bulk copy (16-byte aligned
+    // rows), else coalesced loads.
     if (kVec) {
-        const float4* base = reinterpret_cast<const float4*>(xr + c0);
-        const int n4 = n >> 2;   // n is a multiple of 4 on this path
-        float4 q[kVpt / 4];
-#pragma unroll
-        for (int i = 0; i < kVpt / 4; ++i) q[i] = __ldcs(base + min(i * kThreads + tid, n4 - 1));
-#pragma unroll
-        for (int i = 0; i < kVpt / 4; ++i) {
-            const bool in = i * kThreads + tid < n4;
-            v[4 * i + 0] = in ? q[i].x : __int_as_float(0x7fffffff);
-            v[4 * i + 1] = in ? q[i].y : __int_as_float(0x7fffffff);
-            v[4 * i + 2] = in ? q[i].z : __int_as_float(0x7fffffff);
-            v[4 * i + 3] = in ? q[i].w : __int_as_float(0x7fffffff);
+        if (tid == 0) {
+            mbar_init(&bar, 1);
+            fence_mbar_init();
+            mbar_arrive_expect_tx(&bar, (uint32_t)n * 4u);
+            bulk_g2s(sx, xr + c0, (uint32_t)n * 4u, &bar);
+        }
+        __syncthreads();
+        const bool ok = mbar_wait_bounded(&bar, 0, kWaitLimitNs);
+        if (__syncthreads_or(!ok)) {
+            if (tid == 0) {
+                atomicOr(p.err, kDevErrBulkCopyTimeout);
+                mbar_wait_bounded(&bar, 0, kWaitLimitNs);   // let the copy land before leaving
+            }
+            return;
         }
     } else {
-#pragma unroll
-        for (int i = 0; i < kVpt; ++i) v[i] = __ldcs(xr + c0 + min(i * kThreads + tid, n - 1));
-#pragma unroll
-        for (int i = 0; i < kVpt; ++i)
-            if (i * kThreads + tid >= n) v[i] = __int_as_float(0x7fffffff);
+        for (int i = tid; i < n; i += kThreads) sx[i] = __ldcs(xr + c0 + i);
+        __syncthreads();
     }
-    auto elem = [&](int j) -> int {   // chunk-relative element index of v[j]
-        return kVec ? ((j >> 2) * kThreads + tid) * 4 + (j & 3) : j * kThreads + tid;
-    };
+    // Thread tid owns the 4-element groups tid, tid + 256, ... of the chunk
+    // (scalar path: the elements tid, tid + 256, ...).
+    const int n4 = n >> 2;
+    const float4* sx4 = reinterpret_cast<const float4*>(sx);
+
     // The delegate is the thread's largest element (fmaxf skips NaN, so a NaN
     // counts as -inf); threads without elements have none (0).
     float dm = -INFINITY;
-#pragma unroll
-    for (int j = 0; j < kVpt; ++j) dm = fmaxf(dm, v[j]);
-    uint32_t d = elem(0) < n ? order_bits(dm) : 0u;
+    if (kVec) {
+        for (int i = tid; i < n4; i += kThreads) {
+            const float4 f = sx4[i];
+            dm = fmaxf(dm, fmaxf(fmaxf(f.x, f.y), fmaxf(f.z, f.w)));
+        }
+    } else {
+        for (int i = tid; i < n; i += kThreads) dm = fmaxf(dm, sx[i]);
+    }
+    uint32_t d = (kVec ? tid < n4 : tid < n) ? order_bits(dm) : 0u;
 
     // 2. threshold: min over warps of each warp's ceil(K/warps)-th largest delegate
     const int kw = (k + kWarps - 1) / kWarps;
@@ -231,7 +271,6 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(const __grid_constant__ 
         if (lane == __ffs(who) - 1) d = 0;
     }
     if (lane == 0) s.warp_t[warp] = tw;
-    if (tid == 0) s.cnt = 0;
     __syncthreads();
     // Warps that hold kw delegates each vouch for kw elements >= their own
     // threshold; the minimum over enough such warps is a valid threshold.
@@ -248,34 +287,47 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(const __grid_constant__ 
 
     // 3. candidates.  Above -inf the threshold is tested as a float, one
     // compare per element (NaN fails it, +0 and -0 both pass a zero); only
-    // the few survivors become keys.
+    // the few survivors become keys.  Too few vouching warps, or a threshold
+    // of -inf, make every element a candidate (the chunk then usually takes
+    // the radix select below).  Slots come from counts and a scan, not from
+    // atomics.
     const uint32_t kOrderNegInf = 0x007fffffu;   // order_bits(-inf)
-    if (vouching * kw >= k && t > kOrderNegInf) {
-        const float tf = __uint_as_float((t & 0x80000000u) ? (t & 0x7fffffffu) : ~t);
-#pragma unroll
-        for (int j = 0; j < kVpt; ++j) {
-            if (v[j] >= tf) {
-                const uint32_t pos = atomicAdd(&s.cnt, 1u);
-                if (pos < kCap) s.cand[pos] = make_key(order_bits(v[j]), (uint32_t)(c0 + elem(j)));
-            }
+    const bool by_value = vouching * kw >= k && t > kOrderNegInf;
+    const float tf = __uint_as_float((t & 0x80000000u) ? (t & 0x7fffffffu) : ~t);
+    int mine = 0;
+    if (kVec) {
+        for (int i = tid; i < n4; i += kThreads) {
+            const float4 f = sx4[i];
+            mine += by_value ? (f.x >= tf) + (f.y >= tf) + (f.z >= tf) + (f.w >= tf) : 4;
         }
     } else {
-        // too few vouching warps, or a threshold of -inf: every element is a
-        // candidate (this chunk then usually takes the radix select below)
-#pragma unroll
-        for (int j = 0; j < kVpt; ++j) {
-            if (elem(j) < n) {
-                const uint32_t pos = atomicAdd(&s.cnt, 1u);
-                if (pos < kCap) s.cand[pos] = make_key(order_bits(v[j]), (uint32_t)(c0 + elem(j)));
+        for (int i = tid; i < n; i += kThreads) mine += by_value ? (sx[i] >= tf) : 1;
+    }
+    int ctotal;
+    int pos = block_offsets(mine, ctotal, s);
+    if (ctotal <= kCap && mine > 0) {
+        auto put = [&](float v, int e) {
+            if (!by_value || v >= tf) s.cand[pos++] = make_key(order_bits(v), (uint32_t)(c0 + e));
+        };
+        if (kVec) {
+            for (int i = tid; i < n4; i += kThreads) {
+                const float4 f = sx4[i];
+                put(f.x, 4 * i);
+                put(f.y, 4 * i + 1);
+                put(f.z, 4 * i + 2);
+                put(f.w, 4 * i + 3);
             }
+        } else {
+            for (int i = tid; i < n; i += kThreads) put(sx[i], i);
         }
     }
+    if (tid == 0) s.cnt = (uint32_t)ctotal;
     __syncthreads();
     uint32_t cnt = s.cnt;
     const int kk = min(k, n);
     if (cnt > kCap) {
-        // exact fallback: radix select over the chunk's keys (re-read from L2)
-        auto key_at = [&](int i) { return make_key(order_bits(xr[c0 + i]), (uint32_t)(c0 + i)); };
+        // exact fallback: radix select over the chunk's keys
+        auto key_at = [&](int i) { return make_key(order_bits(sx[i]), (uint32_t)(c0 + i)); };
         const unsigned long long kth = block_kth_largest(key_at, n, kk, s);
         if (tid == 0) s.cnt = 0;
         __syncthreads();
@@ -318,26 +370,51 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(const __grid_constant__ 
     // Top-K is at or above it.  It is found by counting, like the ranks.
     const int m = (k + p.nchunks - 1) / p.nchunks;
     const int U = m * p.nchunks;
-    unsigned long long t64;
-    if (U <= kCap) {
-        for (int i = tid; i < U; i += kThreads) {
-            const int c = i / m;
-            s.cand[i] = __ldcg(all + (long long)c * k + (i - c * m));
+    if (p.nchunks <= kWarps * kMergeRegs && U <= kCap) {
+        // One round trip: warp w holds the lists of chunks w, w + 8, ... in
+        // registers, lane i the i-th key of each.  As the lists are sorted,
+        // the keys at or above the threshold are a prefix of each list.
+        unsigned long long key[kMergeRegs];
+#pragma unroll
+        for (int r = 0; r < kMergeRegs; ++r)
+            key[r] = __ldcg(all + (long long)min(warp + r * kWarps, p.nchunks - 1) * k + min(lane, k - 1));
+#pragma unroll
+        for (int r = 0; r < kMergeRegs; ++r) {
+            const int c = warp + r * kWarps;
+            if (c >= p.nchunks || lane >= k) key[r] = 0ull;
+            else if (lane < m) s.cand[c * m + lane] = key[r];
         }
         if (tid == 0) s.red[0] = ~0ull;
         __syncthreads();
         for (int i = tid; i < U; i += kThreads) {
-            const unsigned long long key = s.cand[i];
+            const unsigned long long kv = s.cand[i];
             int rank = 0;
-            for (int j = 0; j < U; ++j) rank += (s.cand[j] > key) ? 1 : 0;
-            if (rank < k) atomicMin(&s.red[0], key);   // min of the top K = the K-th largest
+#pragma unroll 8
+            for (int j = 0; j < U; ++j) rank += (s.cand[j] > kv) ? 1 : 0;
+            if (rank < k) atomicMin(&s.red[0], kv);   // min of the top K = the K-th largest
         }
-        if (tid == 0) s.cnt = 0;
         __syncthreads();
-        t64 = s.red[0];
-        __syncthreads();   // everyone has read the threshold before cand is reused
+        unsigned long long t64 = s.red[0];
+        if (t64 == 0) t64 = 1;   // padding keys (0) never pass
+        int warp_total = 0;
+#pragma unroll
+        for (int r = 0; r < kMergeRegs; ++r) warp_total += __popc(__ballot_sync(kFull, key[r] >= t64));
+        int all_total;
+        int off = block_offsets(lane == 0 ? warp_total : 0, all_total, s);
+        off = __shfl_sync(kFull, off, 0);   // the warp's first slot
+        if (all_total <= kCap) {
+            const unsigned below = (1u << lane) - 1u;
+#pragma unroll
+            for (int r = 0; r < kMergeRegs; ++r) {
+                const unsigned mask = __ballot_sync(kFull, key[r] >= t64);
+                if ((mask >> lane) & 1u) s.cand[off + __popc(mask & below)] = key[r];
+                off += __popc(mask);
+            }
+        }
+        if (tid == 0) s.cnt = (uint32_t)all_total;
     } else {
-        // very many chunks: the largest K-th key over chunks (always valid)
+        // very many chunks: the largest K-th key over chunks (always valid),
+        // keys gathered from global memory in batches
         unsigned long long tm = 0;
         for (int c0m = 0; c0m < p.nchunks; c0m += kThreads * kMergeBatch) {
             unsigned long long v[kMergeBatch];
@@ -351,20 +428,20 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(const __grid_constant__ 
         if (lane == 0) s.red[warp] = tm;
         if (tid == 0) s.cnt = 0;
         __syncthreads();
-        t64 = 0;
+        unsigned long long t64 = 0;
 #pragma unroll
         for (int w = 0; w < kWarps; ++w) t64 = s.red[w] > t64 ? s.red[w] : t64;
-    }
-    if (t64 == 0) t64 = 1;   // padding keys (0) never pass
-    for (int i0 = 0; i0 < total; i0 += kThreads * kMergeBatch) {
-        unsigned long long v[kMergeBatch];
+        if (t64 == 0) t64 = 1;
+        for (int i0 = 0; i0 < total; i0 += kThreads * kMergeBatch) {
+            unsigned long long v[kMergeBatch];
 #pragma unroll
-        for (int j = 0; j < kMergeBatch; ++j) v[j] = __ldcg(all + min(i0 + j * kThreads + tid, total - 1));
+            for (int j = 0; j < kMergeBatch; ++j) v[j] = __ldcg(all + min(i0 + j * kThreads + tid, total - 1));
 #pragma unroll
-        for (int j = 0; j < kMergeBatch; ++j) {
-            if (i0 + j * kThreads + tid < total && v[j] >= t64) {
-                const uint32_t pos = atomicAdd(&s.cnt, 1u);
-                if (pos < kCap) s.cand[pos] = v[j];
+            for (int j = 0; j < kMergeBatch; ++j) {
+                if (i0 + j * kThreads + tid < total && v[j] >= t64) {
+                    const uint32_t pos = atomicAdd(&s.cnt, 1u);
+                    if (pos < kCap) s.cand[pos] = v[j];
+                }
             }
         }
     }
@@ -390,6 +467,8 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(const __grid_constant__ 
 }
 
 size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+bool g_topk_attr_set[64];
 
 }  // namespace
 
@@ -467,10 +546,21 @@ ws_status ws_topk(const float* x, int64_t rows, int64_t cols, int32_t k, float* 
     // PDL section): the grid may be launched while the previous kernel on the
     // stream is still running and waits in griddepcontrol.wait, which hides
     // the launch gap between the preprocess and the Top-K.
+    int dev;
+    const DeviceInfo* info;
+    st = current_device_info(&dev, &info);
+    if (st != WS_OK) return st;
+    if (!g_topk_attr_set[dev]) {
+        WS_TRY_CUDA(cudaFuncSetAttribute(topk_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kDynSmem));
+        WS_TRY_CUDA(cudaFuncSetAttribute(topk_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kDynSmem));
+        g_topk_attr_set[dev] = true;
+    }
+    p.err = device_error_word();
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = dim3((unsigned)blocks);
     cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = 0;
+    // the staged chunk only needs the row's length when the row is short
+    cfg.dynamicSmemBytes = (size_t)kSharedBytes + (size_t)(std::min<long long>(cols, kChunk) + 3) / 4 * 16;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;

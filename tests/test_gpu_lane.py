@@ -143,3 +143,39 @@ def test_borrowed_buffers(B, oracle):
         assert np.max(np.abs(tensor.cpu().numpy() - want)) <= 1e-5
         wv, wi = oracle.topk(logits, 5)
         assert np.array_equal(idx.cpu().numpy(), wi)
+
+
+def test_bench_throughput_configuration(B, oracle):
+    """The benchmark's throughput setup: three 64-frame 1080p lanes without
+    timing events sharing one stream, replayed in rotation; every replay's
+    tensor and Top-K equal the oracle's."""
+    from post_processing_gb300 import Lane
+    name = "b64_1080p_to_224"
+    w = synth.WORKLOADS[name]
+    frames = synth.make_frames(name)
+    logits = synth.make_logits(name)
+    want_t = oracle.preprocess(frames, 1920, 1080, 224, 224)
+    want_v, want_i = oracle.topk(logits, 32)
+    s = torch.cuda.Stream()
+    pre = B.preprocess_desc(1920, 1080, 224, 224)
+    lanes = [Lane(B.lane_desc(pre, 64, 64, 1000, 32, stream=s.cuda_stream, flags=B.WS_LANE_FLAG_NO_TIMING))
+             for _ in range(3)]
+    try:
+        for ln in lanes:
+            fill_lane(B, ln, frames, logits)
+        for step in range(9):
+            ln = lanes[step % 3]
+            if ln.state == B.WS_LANE_IN_FLIGHT:
+                ln.wait()
+            ln.acquire()
+            ln.submit()
+        for ln in lanes:
+            if ln.state == B.WS_LANE_IN_FLIGHT:
+                t = ln.wait()
+                assert t.gpu_us == -1.0
+            tensor, v, i = read_lane(B, ln, 64, 224, 224, 64, 32)
+            assert np.max(np.abs(tensor - want_t)) <= 1e-5
+            assert np.array_equal(i, want_i) and np.array_equal(v.view(np.uint32), want_v.view(np.uint32))
+    finally:
+        for ln in lanes:
+            ln.close()
