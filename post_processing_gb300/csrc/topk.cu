@@ -48,6 +48,8 @@ constexpr int kCap = 2048;                     // shared candidate capacity
 constexpr int kMaxK = 32;
 constexpr int kMergeBatch = 8;                 // keys each merging thread loads at once
 constexpr int kMergeRegs = 12;                 // chunk lists per warp held in registers (<= 96 chunks)
+constexpr int kMergeChunks = 8 * kMergeRegs;   // blocks per row the one-round-trip merge handles
+constexpr int kMinChunk = 2048;                // shortest chunk a long row is cut into
 constexpr unsigned kFull = 0xffffffffu;
 
 struct TopkParams {
@@ -55,6 +57,7 @@ struct TopkParams {
     long long cols;
     int k;
     int nchunks;
+    int chunk;                    // elements per block (a multiple of 4, <= kChunk)
     float* out_val;
     int* out_idx;
     unsigned int* tickets;        // [rows]
@@ -215,8 +218,8 @@ __global__ void __launch_bounds__(kThreads, 4) topk_kernel(const __grid_constant
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const long long row = blockIdx.x / p.nchunks;
     const int chunk = (int)(blockIdx.x - row * p.nchunks);
-    const long long c0 = (long long)chunk * kChunk;
-    const int n = (int)min((long long)kChunk, p.cols - c0);
+    const long long c0 = (long long)chunk * p.chunk;
+    const int n = (int)min((long long)p.chunk, p.cols - c0);
     const float* xr = p.x + row * p.cols;
     const int k = p.k;
 
@@ -229,8 +232,9 @@ __global__ void __launch_bounds__(kThreads, 4) topk_kernel(const __grid_constant
             mbar_arrive_expect_tx(&bar, (uint32_t)n * 4u);
             bulk_g2s(sx, xr + c0, (uint32_t)n * 4u, &bar);
         }
-        __syncthreads();
-        const bool ok = mbar_wait_bounded(&bar, 0, kWaitLimitNs);
+        // One thread polls the barrier; the others sleep in the block barrier
+        // (which costs no issue slots) instead of spinning beside it.
+        const bool ok = tid == 0 ? mbar_wait_bounded(&bar, 0, kWaitLimitNs) : true;
         if (__syncthreads_or(!ok)) {
             if (tid == 0) {
                 atomicOr(p.err, kDevErrBulkCopyTimeout);
@@ -238,27 +242,41 @@ __global__ void __launch_bounds__(kThreads, 4) topk_kernel(const __grid_constant
             }
             return;
         }
+        // The phase is complete: each thread's own (immediately satisfied)
+        // wait is its acquire of the bytes the bulk copy wrote.
+        if (tid != 0) mbar_wait_bounded(&bar, 0, kWaitLimitNs);
     } else {
         for (int i = tid; i < n; i += kThreads) sx[i] = __ldcs(xr + c0 + i);
         __syncthreads();
     }
     // Thread tid owns the 4-element groups tid, tid + 256, ... of the chunk
-    // (scalar path: the elements tid, tid + 256, ...).
-    const int n4 = n >> 2;
+    // (the last group padded with NaN), and keeps each group's maximum in a
+    // register: the candidate pass then re-reads only the rare groups whose
+    // maximum reaches the threshold.
+    const int ng = (n + 3) >> 2;
+    const float qnan = __int_as_float(0x7fffffff);
     const float4* sx4 = reinterpret_cast<const float4*>(sx);
-
-    // The delegate is the thread's largest element (fmaxf skips NaN, so a NaN
-    // counts as -inf); threads without elements have none (0).
-    float dm = -INFINITY;
-    if (kVec) {
-        for (int i = tid; i < n4; i += kThreads) {
-            const float4 f = sx4[i];
-            dm = fmaxf(dm, fmaxf(fmaxf(f.x, f.y), fmaxf(f.z, f.w)));
+    auto group = [&](int i) -> float4 {
+        if (kVec) return sx4[i];   // n is a multiple of 4 on this path
+        const int e = 4 * i;
+        return make_float4(e < n ? sx[e] : qnan, e + 1 < n ? sx[e + 1] : qnan, e + 2 < n ? sx[e + 2] : qnan,
+                           e + 3 < n ? sx[e + 3] : qnan);
+    };
+    constexpr int kG = kChunk / 4 / kThreads;   // groups per thread
+    float gmax[kG];
+    float dm = -INFINITY;   // the delegate: fmaxf skips NaN, so a NaN counts as -inf
+#pragma unroll
+    for (int g = 0; g < kG; ++g) {
+        const int i = g * kThreads + tid;
+        float mx = qnan;
+        if (i < ng) {
+            const float4 f = group(i);
+            mx = fmaxf(fmaxf(f.x, f.y), fmaxf(f.z, f.w));
         }
-    } else {
-        for (int i = tid; i < n; i += kThreads) dm = fmaxf(dm, sx[i]);
+        gmax[g] = mx;
+        dm = fmaxf(dm, mx);
     }
-    uint32_t d = (kVec ? tid < n4 : tid < n) ? order_bits(dm) : 0u;
+    uint32_t d = tid < ng ? order_bits(dm) : 0u;   // threads without elements have no delegate
 
     // 2. threshold: min over warps of each warp's ceil(K/warps)-th largest delegate
     const int kw = (k + kWarps - 1) / kWarps;
@@ -285,40 +303,43 @@ __global__ void __launch_bounds__(kThreads, 4) topk_kernel(const __grid_constant
         }
     }
 
-    // 3. candidates.  Above -inf the threshold is tested as a float, one
-    // compare per element (NaN fails it, +0 and -0 both pass a zero); only
-    // the few survivors become keys.  Too few vouching warps, or a threshold
-    // of -inf, make every element a candidate (the chunk then usually takes
-    // the radix select below).  Slots come from counts and a scan, not from
-    // atomics.
+    // 3. candidates.  Each thread marks the groups whose maximum reaches the
+    // threshold (usually none or one) and visits only those, once to count
+    // and once to write; a warp scan and a block scan give every candidate
+    // its slot.  Above -inf the threshold is tested as a float (NaN fails it,
+    // +0 and -0 both pass a zero).  Too few vouching warps, or a threshold of
+    // -inf, make every element a candidate (the chunk then usually takes the
+    // radix select below).
     const uint32_t kOrderNegInf = 0x007fffffu;   // order_bits(-inf)
     const bool by_value = vouching * kw >= k && t > kOrderNegInf;
     const float tf = __uint_as_float((t & 0x80000000u) ? (t & 0x7fffffffu) : ~t);
+    unsigned hits = 0;
+#pragma unroll
+    for (int g = 0; g < kG; ++g) {
+        const int i = g * kThreads + tid;
+        if (i < ng && (!by_value || gmax[g] >= tf)) hits |= 1u << g;
+    }
     int mine = 0;
-    if (kVec) {
-        for (int i = tid; i < n4; i += kThreads) {
-            const float4 f = sx4[i];
-            mine += by_value ? (f.x >= tf) + (f.y >= tf) + (f.z >= tf) + (f.w >= tf) : 4;
+    for (unsigned m = hits; m; m &= m - 1) {
+        const int i = (__ffs(m) - 1) * kThreads + tid;
+        const float4 f = group(i);
+        if (by_value) {
+            mine += (f.x >= tf) + (f.y >= tf) + (f.z >= tf) + (f.w >= tf);
+        } else {
+            mine += min(4, n - 4 * i);
         }
-    } else {
-        for (int i = tid; i < n; i += kThreads) mine += by_value ? (sx[i] >= tf) : 1;
     }
     int ctotal;
     int pos = block_offsets(mine, ctotal, s);
-    if (ctotal <= kCap && mine > 0) {
-        auto put = [&](float v, int e) {
-            if (!by_value || v >= tf) s.cand[pos++] = make_key(order_bits(v), (uint32_t)(c0 + e));
-        };
-        if (kVec) {
-            for (int i = tid; i < n4; i += kThreads) {
-                const float4 f = sx4[i];
-                put(f.x, 4 * i);
-                put(f.y, 4 * i + 1);
-                put(f.z, 4 * i + 2);
-                put(f.w, 4 * i + 3);
-            }
-        } else {
-            for (int i = tid; i < n; i += kThreads) put(sx[i], i);
+    if (ctotal <= kCap) {
+        for (unsigned m = hits; m; m &= m - 1) {
+            const int i = (__ffs(m) - 1) * kThreads + tid;
+            const float4 f = group(i);
+            const float e[4] = {f.x, f.y, f.z, f.w};
+#pragma unroll
+            for (int c = 0; c < 4; ++c)
+                if (by_value ? e[c] >= tf : 4 * i + c < n)
+                    s.cand[pos++] = make_key(order_bits(e[c]), (uint32_t)(c0 + 4 * i + c));
         }
     }
     if (tid == 0) s.cnt = (uint32_t)ctotal;
@@ -482,9 +503,33 @@ ws_status validate_topk(int64_t rows, int64_t cols, int32_t k) {
     return WS_OK;
 }
 
+// Blocks per row.  Rows up to kChunk elements take one block.  Longer rows
+// take 8192-element blocks, except that when that leaves a launch short of
+// one full wave (4 blocks on every SM) the rows are cut finer, down to
+// kMinChunk elements and at most kMergeChunks blocks per row, so that the
+// wave is full and even.
+int blocks_per_row(int64_t rows, int64_t cols, int sm_count) {
+    const long long base = (cols + kChunk - 1) / kChunk;
+    if (base <= 1) return 1;
+    const long long cap = std::max<long long>(base, std::min<long long>((cols + kMinChunk - 1) / kMinChunk,
+                                                                        kMergeChunks));
+    const long long want = (long long)sm_count * 4 / std::max<int64_t>(rows, 1);
+    return (int)std::min<long long>(cap, std::max<long long>(base, want));
+}
+
+// Chunk length for a number of blocks per row: a multiple of 4 elements.
+int chunk_len(int64_t cols, int nchunks) {
+    const long long c = (cols + nchunks - 1) / nchunks;
+    return (int)std::min<long long>(kChunk, (c + 3) / 4 * 4);
+}
+
 size_t topk_workspace_size(int64_t rows, int64_t cols, int32_t k) {
-    const long long nchunks = (cols + kChunk - 1) / kChunk;
-    if (nchunks <= 1) return 0;
+    // Upper bound over every launch shape blocks_per_row() can choose, so it
+    // depends on (rows, cols, k) only.
+    const long long base = (cols + kChunk - 1) / kChunk;
+    if (base <= 1) return 0;
+    const long long nchunks =
+        std::max<long long>(base, std::min<long long>((cols + kMinChunk - 1) / kMinChunk, kMergeChunks));
     return round_up((size_t)rows * 4, 256) + (size_t)rows * nchunks * k * 8;
 }
 
@@ -531,7 +576,13 @@ ws_status ws_topk(const float* x, int64_t rows, int64_t cols, int32_t k, float* 
     p.x = x;
     p.cols = cols;
     p.k = k;
-    p.nchunks = (int)((cols + kChunk - 1) / kChunk);
+    int dev;
+    const DeviceInfo* info;
+    st = current_device_info(&dev, &info);
+    if (st != WS_OK) return st;
+    p.nchunks = blocks_per_row(rows, cols, info->sm_count);
+    p.chunk = chunk_len(cols, p.nchunks);
+    p.nchunks = (int)((cols + p.chunk - 1) / p.chunk);
     p.out_val = out_val;
     p.out_idx = out_idx;
     if (need > 0) {
@@ -546,10 +597,6 @@ ws_status ws_topk(const float* x, int64_t rows, int64_t cols, int32_t k, float* 
     // PDL section): the grid may be launched while the previous kernel on the
     // stream is still running and waits in griddepcontrol.wait, which hides
     // the launch gap between the preprocess and the Top-K.
-    int dev;
-    const DeviceInfo* info;
-    st = current_device_info(&dev, &info);
-    if (st != WS_OK) return st;
     if (!g_topk_attr_set[dev]) {
         WS_TRY_CUDA(cudaFuncSetAttribute(topk_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kDynSmem));
         WS_TRY_CUDA(cudaFuncSetAttribute(topk_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kDynSmem));
@@ -560,7 +607,7 @@ ws_status ws_topk(const float* x, int64_t rows, int64_t cols, int32_t k, float* 
     cfg.gridDim = dim3((unsigned)blocks);
     cfg.blockDim = dim3(kThreads);
     // the staged chunk only needs the row's length when the row is short
-    cfg.dynamicSmemBytes = (size_t)kSharedBytes + (size_t)(std::min<long long>(cols, kChunk) + 3) / 4 * 16;
+    cfg.dynamicSmemBytes = (size_t)kSharedBytes + (size_t)(p.chunk + 3) / 4 * 16;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
