@@ -52,8 +52,8 @@ LANES = 3
 # unchanged.  Filled from the committed ncu summary under profiles/.
 NCU_TRAFFIC = {
     "b64_1080p_to_224": {
-        "bytes": 185_469_952,
-        "source_sha": "8b6a78888ca824840ba02ea5c31d683162c384af7d56a9392c98bc696bd04f21",
+        "bytes": 185_634_304,
+        "source_sha": "496b1bf9f80e075404ad000953a871a5d4ea863875d6d9363f955b4989dae4e7",
     },
 }
 
