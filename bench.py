@@ -86,7 +86,7 @@ def _box(sw, sh, dw, dh, letterbox):
     return max(1, (2 * sw * dh + sh) // (2 * sh)), dh
 
 
-def algorithmic_bytes(w: dict) -> dict:
+def algorithmic_bytes(w: dict, out_bytes: int = 4) -> dict:
     nw, nh = _box(w["src_w"], w["src_h"], w["dst_w"], w["dst_h"], w["resize"] == "letterbox")
     lo, hi, nz = _axis(w["src_h"], nh)
     rows = np.unique(np.concatenate([lo, hi[nz]]))
@@ -98,7 +98,7 @@ def algorithmic_bytes(w: dict) -> dict:
     for j in rows:                                   # rows start at j * row_bytes in a packed frame
         src_sectors += np.unique((j * row_bytes + col_bytes) // 32).size
     src = src_sectors * 32 * w["batch"]
-    dst = w["batch"] * 3 * w["dst_w"] * w["dst_h"] * 4
+    dst = w["batch"] * 3 * w["dst_w"] * w["dst_h"] * out_bytes
     topk = w["rows"] * w["cols"] * 4 + w["rows"] * w["k"] * 8
     return {"preprocess": int(src + dst), "source": int(src), "tensor": int(dst), "topk": int(topk),
             "total": int(src + dst + topk)}
@@ -283,6 +283,8 @@ def main():
     ap.add_argument("--latency-samples", type=int, default=10000)
     ap.add_argument("--e2e-steps", type=int, default=60)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--out-dtype", default="f32", choices=["f32", "f16", "bf16"],
+                    help="element type of the NCHW tensor (the workloads specify FP32)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -325,8 +327,10 @@ def main():
     logits_dev = torch.from_numpy(logits).to(device)
 
     stream = torch.cuda.Stream(device)
+    dst_type = {"f32": B.WS_DTYPE_F32, "f16": B.WS_DTYPE_F16, "bf16": B.WS_DTYPE_BF16}[args.out_dtype]
+    out_bytes = 4 if args.out_dtype == "f32" else 2
     pre = B.preprocess_desc(w["src_w"], w["src_h"], w["dst_w"], w["dst_h"],
-                            letterbox=w["resize"] == "letterbox", norm=w["norm"])
+                            letterbox=w["resize"] == "letterbox", norm=w["norm"], dst_type=dst_type)
     lanes, keep = [], []
     for _ in range(LANES):
         src = frames_dev.clone()
@@ -337,7 +341,7 @@ def main():
                         stream=stream.cuda_stream, flags=B.WS_LANE_FLAG_NO_TIMING)
         lanes.append(Lane(d))
     torch.cuda.synchronize()
-    alg = algorithmic_bytes(w)
+    alg = algorithmic_bytes(w, out_bytes)
     touched_per_rotation = LANES * alg["total"]
 
     def run_steps(n):
@@ -497,7 +501,7 @@ def main():
             "metric": METRIC, "value": value, "unit": "frames/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": 1000.0 * t_max / args.steps, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-            "config": dict(workload_config(args.workload, w),
+            "config": dict(workload_config(args.workload, w), out_dtype=args.out_dtype,
                            l2=f"{LANES} lanes rotate, {touched_per_rotation / 1e6:.0f} MB touched per rotation "
                               f"(> {touched_per_rotation / l2:.1f}x the {l2 / 2 ** 20:.0f} MiB L2): inputs larger "
                                 "than L2",

@@ -92,6 +92,12 @@ ws_status ws_device_error(uint32_t* flags, int32_t clear);
 #define WS_NORM_SCALE    1     /* out = v * scale                                       */
 
 #define WS_ORDER_RGB 0         /* source bytes are R, G, B; planes are written R, G, B  */
+#define WS_ORDER_BGR 1         /* source bytes are B, G, R; planes are still written R, G, B
+                                  (yolo.cu README: its engine takes BGR frames) */
+
+#define WS_DTYPE_F32  0        /* destination float32                                    */
+#define WS_DTYPE_F16  1        /* destination IEEE half, the FP32 value rounded to nearest even */
+#define WS_DTYPE_BF16 2        /* destination bfloat16, the FP32 value rounded to nearest even  */
 
 /* Geometry and normalisation of the fused preprocess.
  *
@@ -117,7 +123,10 @@ typedef struct ws_preprocess_desc {
     float   mean[3];              /* WS_NORM_MEAN_STD, in [0,1] units, per channel   */
     float   std[3];               /* WS_NORM_MEAN_STD, > 0, in [0,1] units           */
     float   scale;                /* WS_NORM_SCALE (e.g. 1/255)                      */
-    int32_t channel_order;        /* WS_ORDER_RGB                                    */
+    int32_t channel_order;        /* WS_ORDER_RGB or WS_ORDER_BGR                    */
+    int32_t dst_type;             /* WS_DTYPE_F32 (default 0), _F16 or _BF16 ("Inside
+                                     WarpStream TRT", next steps: precision-specialised
+                                     preprocessing); half outputs halve the bytes written */
 } ws_preprocess_desc;
 
 /* Host-only check of a descriptor for a batch; enqueues nothing. */
@@ -126,14 +135,15 @@ ws_status ws_preprocess_validate(const ws_preprocess_desc* desc, int32_t batch);
 /* Fused preprocess of `batch` frames.
  *   src: device, uint8; byte (b, row j, column i, channel c) is at
  *        src[b * src_frame_stride + j * src_row_stride + 3 * i + c].
- *   dst: device, float32 [batch][3][dst_h][dst_w] (NCHW, contiguous).
+ *   dst: device, [batch][3][dst_h][dst_w] (NCHW, contiguous) of the element
+ *        type desc->dst_type (float32, half or bfloat16).
  * One kernel launch on `stream`.  Any alignment is accepted; a 16-byte
  * aligned src, row stride and frame stride select the staged bulk-copy
  * kernel, anything else a per-pixel kernel with the same results.
  * Errors: WS_ERR_INVALID_ARGUMENT (NULL pointer, batch < 1, bad descriptor),
  * WS_ERR_CUDA (launch failed). */
 ws_status ws_preprocess(const ws_preprocess_desc* desc, const uint8_t* src, int32_t batch,
-                        float* dst, cudaStream_t stream);
+                        void* dst, cudaStream_t stream);
 
 /* ------------------------------------------------------------------- top-k */
 
@@ -241,7 +251,7 @@ typedef struct ws_lane_desc {
     void*    input;               /* DEVICE: device buffer; MAPPED: host pointer of a
                                      cudaHostAllocMapped allocation; COPY: pinned host
                                      buffer.  batch * src_frame_stride bytes.       */
-    float*   tensor;              /* device, [batch][3][dst_h][dst_w]               */
+    void*    tensor;              /* device, [batch][3][dst_h][dst_w] of pre.dst_type */
     float*   logits;              /* device, [rows][cols]; the network's output slot */
     float*   result_val;          /* DEVICE: device; MAPPED: mapped host; COPY: pinned host; [rows][k] */
     int32_t* result_idx;          /* same, int32 [rows][k]                          */
@@ -255,7 +265,7 @@ typedef struct ws_lane ws_lane;
 typedef struct ws_lane_buffers {
     void*    input_host;          /* host view of the producer slot (MAPPED, COPY) or NULL */
     void*    input_device;        /* device buffer the preprocess reads             */
-    float*   tensor;              /* device NCHW tensor                             */
+    void*    tensor;              /* device NCHW tensor (pre.dst_type elements)     */
     float*   logits;              /* device logits                                  */
     float*   result_val_host;     /* host view of the result (MAPPED, COPY) or NULL */
     int32_t* result_idx_host;

@@ -24,7 +24,9 @@ def preprocess(frames: torch.Tensor, desc: B.ws_preprocess_desc, batch: int | No
     if batch is None:
         batch = frames.shape[0]
     if out is None:
-        out = torch.empty((batch, 3, desc.dst_h, desc.dst_w), dtype=torch.float32, device=frames.device)
+        dtype = {B.WS_DTYPE_F32: torch.float32, B.WS_DTYPE_F16: torch.float16,
+                 B.WS_DTYPE_BF16: torch.bfloat16}[desc.dst_type]
+        out = torch.empty((batch, 3, desc.dst_h, desc.dst_w), dtype=dtype, device=frames.device)
     B.check(B.ws_preprocess(desc, frames.data_ptr(), batch, out.data_ptr(), _stream(stream)))
     return out
 

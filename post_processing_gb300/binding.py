@@ -29,7 +29,8 @@ WS_ERR_DEVICE = 9
 
 WS_RESIZE_STRETCH, WS_RESIZE_LETTERBOX = 0, 1
 WS_NORM_MEAN_STD, WS_NORM_SCALE = 0, 1
-WS_ORDER_RGB = 0
+WS_ORDER_RGB, WS_ORDER_BGR = 0, 1
+WS_DTYPE_F32, WS_DTYPE_F16, WS_DTYPE_BF16 = 0, 1, 2
 WS_INPUT_DEVICE, WS_INPUT_MAPPED, WS_INPUT_COPY = 0, 1, 2
 WS_RESULT_DEVICE, WS_RESULT_MAPPED, WS_RESULT_COPY = 0, 1, 2
 WS_LANE_FLAG_NO_GRAPH = 1
@@ -45,7 +46,8 @@ _vp, _sz = ctypes.c_void_p, ctypes.c_size_t
 class ws_preprocess_desc(ctypes.Structure):
     _fields_ = [("src_w", _i32), ("src_h", _i32), ("src_row_stride", _i64), ("src_frame_stride", _i64),
                 ("dst_w", _i32), ("dst_h", _i32), ("resize", _i32), ("pad_value", _i32), ("norm", _i32),
-                ("mean", _f32 * 3), ("std", _f32 * 3), ("scale", _f32), ("channel_order", _i32)]
+                ("mean", _f32 * 3), ("std", _f32 * 3), ("scale", _f32), ("channel_order", _i32),
+                ("dst_type", _i32)]
 
 
 class ws_lane_desc(ctypes.Structure):
@@ -215,7 +217,8 @@ def ws_lane_state(lane: int | None) -> int:
 def preprocess_desc(src_w: int, src_h: int, dst_w: int, dst_h: int, *, letterbox: bool = False,
                     pad_value: int = 114, norm: str = "mean_std",
                     mean=(0.485, 0.456, 0.406), std=(0.229, 0.224, 0.225), scale: float = 1.0 / 255.0,
-                    row_stride: int | None = None, frame_stride: int | None = None) -> ws_preprocess_desc:
+                    row_stride: int | None = None, frame_stride: int | None = None,
+                    channel_order: int = WS_ORDER_RGB, dst_type: int = WS_DTYPE_F32) -> ws_preprocess_desc:
     d = ws_preprocess_desc()
     d.src_w, d.src_h, d.dst_w, d.dst_h = src_w, src_h, dst_w, dst_h
     d.src_row_stride = 3 * src_w if row_stride is None else row_stride
@@ -226,7 +229,8 @@ def preprocess_desc(src_w: int, src_h: int, dst_w: int, dst_h: int, *, letterbox
     d.mean[:] = list(mean)
     d.std[:] = list(std)
     d.scale = scale
-    d.channel_order = WS_ORDER_RGB
+    d.channel_order = channel_order
+    d.dst_type = dst_type
     return d
 
 

@@ -30,7 +30,7 @@ struct ws_lane {
     void* in_host = nullptr;       // MAPPED / COPY: host view
     void* in_dev = nullptr;        // what the preprocess reads
     bool own_in_host = false, own_in_dev = false;
-    float* tensor = nullptr;
+    void* tensor = nullptr;
     bool own_tensor = false;
     float* logits = nullptr;
     bool own_logits = false;
@@ -143,7 +143,8 @@ ws_status build(ws_lane* L) {
     }
     ws_status st;
     L->input_bytes = (size_t)d.batch * (size_t)d.pre.src_frame_stride;
-    L->tensor_bytes = (size_t)d.batch * 3 * d.pre.dst_h * d.pre.dst_w * sizeof(float);
+    const size_t elem = d.pre.dst_type == WS_DTYPE_F32 ? 4 : 2;
+    L->tensor_bytes = (size_t)d.batch * 3 * d.pre.dst_h * d.pre.dst_w * elem;
     L->logits_bytes = (size_t)d.rows * d.cols * sizeof(float);
     L->result_bytes = (size_t)d.rows * d.k * sizeof(float);
 
@@ -185,7 +186,7 @@ ws_status build(ws_lane* L) {
     if (d.tensor) {
         L->tensor = d.tensor;
     } else {
-        if ((st = alloc_dev((void**)&L->tensor, L->tensor_bytes, "tensor")) != WS_OK) return st;
+        if ((st = alloc_dev(&L->tensor, L->tensor_bytes, "tensor")) != WS_OK) return st;
         L->own_tensor = true;
     }
     if (d.logits) {

@@ -31,6 +31,9 @@
 #include <algorithm>
 #include <cmath>
 
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
 #include "ws_internal.cuh"
 #include "ws_ptx.cuh"
 
@@ -63,7 +66,8 @@ struct PreParams {
     int nw, nh, left, top;    // inner box (the whole destination when stretching)
     float M[3], R[3];         // out = (v - M) * R
     float pad;                // padding byte value
-    float* dst;
+    int cmap[3];              // byte of a source pixel that feeds output plane c (RGB or BGR)
+    void* dst;                // [batch][3][dh][dw] of the output type
     // ring kernel
     int band;                 // output rows per unit
     int stages;               // ring depth
@@ -99,6 +103,28 @@ __device__ __forceinline__ void axis_taps(int x, int S, int D, int& lo, int& hi,
     lo = (int)(q < 0 ? 0 : (q > S - 1 ? S - 1 : q));
     const long long q1 = q + 1;
     hi = (int)(q1 < 0 ? 0 : (q1 > S - 1 ? S - 1 : q1));
+}
+
+// Output element conversion (round to nearest even for the half types).
+template <typename OutT> __device__ __forceinline__ OutT to_out(float v);
+template <> __device__ __forceinline__ float to_out<float>(float v) { return v; }
+template <> __device__ __forceinline__ __half to_out<__half>(float v) { return __float2half_rn(v); }
+template <> __device__ __forceinline__ __nv_bfloat16 to_out<__nv_bfloat16>(float v) { return __float2bfloat16_rn(v); }
+
+// Four consecutive outputs of one plane in one store (16 bytes for float,
+// 8 for the half types); the address is aligned to the store's size.
+template <typename OutT>
+__device__ __forceinline__ void store4(OutT* dst, float a, float b, float c, float d) {
+    if constexpr (sizeof(OutT) == 4) {
+        *reinterpret_cast<float4*>(dst) = make_float4(a, b, c, d);
+    } else {
+        union { OutT h[4]; uint2 u; } pk;
+        pk.h[0] = to_out<OutT>(a);
+        pk.h[1] = to_out<OutT>(b);
+        pk.h[2] = to_out<OutT>(c);
+        pk.h[3] = to_out<OutT>(d);
+        *reinterpret_cast<uint2*>(dst) = pk.u;
+    }
 }
 
 // Warp 0: plan unit `u` into stage `s` and start its copies.  Lane r handles
@@ -158,14 +184,14 @@ __device__ void issue_unit(const PreParams& p, long long u, uint64_t* bar, Stage
     }
 }
 
-template <bool kVecStore>
+template <typename OutT, bool kVecStore>
 __device__ __forceinline__ void compute_unit(const PreParams& p, const StagePlan& plan, const unsigned char* stage,
                                              const int* s_off0, const int* s_off1, const float* s_wx,
                                              const float (&padn)[3]) {
     const int groups = (p.dw + 3) >> 2;
     const int items = plan.nrows * groups;
     const size_t plane = (size_t)p.dh * p.dw;
-    float* out_b = p.dst + (size_t)plan.frame * 3 * plane;
+    OutT* out_b = static_cast<OutT*>(p.dst) + (size_t)plan.frame * 3 * plane;
     for (int it = threadIdx.x; it < items; it += blockDim.x) {
         const int r = it / groups;
         const int x0 = (it - r * groups) * 4;
@@ -189,8 +215,9 @@ __device__ __forceinline__ void compute_unit(const PreParams& p, const StagePlan
                     const float wx = s_wx[x];
 #pragma unroll
                     for (int c = 0; c < 3; ++c) {
-                        const float p00 = A[o0 + c], p01 = A[o1 + c];
-                        const float p10 = B[o0 + c], p11 = B[o1 + c];
+                        const int sc = p.cmap[c];
+                        const float p00 = A[o0 + sc], p01 = A[o1 + sc];
+                        const float p10 = B[o0 + sc], p11 = B[o1 + sc];
                         const float t = p00 + wx * (p01 - p00);
                         const float u = p10 + wx * (p11 - p10);
                         const float v = t + wy * (u - t);
@@ -202,22 +229,21 @@ __device__ __forceinline__ void compute_unit(const PreParams& p, const StagePlan
                 }
             }
         }
-        float* row0 = out_b + (size_t)y * p.dw + x0;
+        OutT* row0 = out_b + (size_t)y * p.dw + x0;
         if (kVecStore) {
 #pragma unroll
-            for (int c = 0; c < 3; ++c)
-                *reinterpret_cast<float4*>(row0 + c * plane) = make_float4(o[c][0], o[c][1], o[c][2], o[c][3]);
+            for (int c = 0; c < 3; ++c) store4<OutT>(row0 + c * plane, o[c][0], o[c][1], o[c][2], o[c][3]);
         } else {
 #pragma unroll
             for (int q = 0; q < 4; ++q)
                 if (x0 + q < p.dw)
 #pragma unroll
-                    for (int c = 0; c < 3; ++c) row0[c * plane + q] = o[c][q];
+                    for (int c = 0; c < 3; ++c) row0[c * plane + q] = to_out<OutT>(o[c][q]);
         }
     }
 }
 
-template <bool kVecStore>
+template <typename OutT, bool kVecStore>
 __global__ void __launch_bounds__(kMaxThreads) pre_ring_kernel(const __grid_constant__ PreParams p) {
     extern __shared__ __align__(128) unsigned char smem[];
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem);                    // [stages]
@@ -264,7 +290,7 @@ __global__ void __launch_bounds__(kMaxThreads) pre_ring_kernel(const __grid_cons
         const uint32_t parity = (uint32_t)(i / p.stages) & 1u;
         const bool ok = mbar_wait_bounded(&bars[s], parity, kWaitLimitNs);
         if (ok)
-            compute_unit<kVecStore>(p, plans[s], slots + (size_t)s * p.stage_bytes, s_off0, s_off1, s_wx, padn);
+            compute_unit<OutT, kVecStore>(p, plans[s], slots + (size_t)s * p.stage_bytes, s_off0, s_off1, s_wx, padn);
         // Everyone is done with stage s (and agrees on whether a copy hung).
         if (__syncthreads_or(!ok)) {
             if (tid == 0) {
@@ -282,6 +308,7 @@ __global__ void __launch_bounds__(kMaxThreads) pre_ring_kernel(const __grid_cons
 }
 
 // One thread per destination pixel, plain byte loads; any alignment.
+template <typename OutT>
 __global__ void __launch_bounds__(256) pre_direct_kernel(const __grid_constant__ PreParams p, long long total) {
     asm volatile("griddepcontrol.launch_dependents;");
     const size_t plane = (size_t)p.dh * p.dw;
@@ -302,8 +329,9 @@ __global__ void __launch_bounds__(256) pre_direct_kernel(const __grid_constant__
             const uint8_t* B = f + (long long)j1 * p.row_stride;
 #pragma unroll
             for (int c = 0; c < 3; ++c) {
-                const float p00 = __ldg(A + 3 * i0 + c), p01 = __ldg(A + 3 * i1 + c);
-                const float p10 = __ldg(B + 3 * i0 + c), p11 = __ldg(B + 3 * i1 + c);
+                const int sc = p.cmap[c];
+                const float p00 = __ldg(A + 3 * i0 + sc), p01 = __ldg(A + 3 * i1 + sc);
+                const float p10 = __ldg(B + 3 * i0 + sc), p11 = __ldg(B + 3 * i1 + sc);
                 const float tt = p00 + wx * (p01 - p00);
                 const float u = p10 + wx * (p11 - p10);
                 v[c] = tt + wy * (u - tt);
@@ -311,9 +339,9 @@ __global__ void __launch_bounds__(256) pre_direct_kernel(const __grid_constant__
         } else {
             v[0] = v[1] = v[2] = p.pad;
         }
-        float* o = p.dst + (size_t)b * 3 * plane + (size_t)y * p.dw + x;
+        OutT* o = static_cast<OutT*>(p.dst) + (size_t)b * 3 * plane + (size_t)y * p.dw + x;
 #pragma unroll
-        for (int c = 0; c < 3; ++c) o[c * plane] = (v[c] - p.M[c]) * p.R[c];
+        for (int c = 0; c < 3; ++c) o[c * plane] = to_out<OutT>((v[c] - p.M[c]) * p.R[c]);
     }
 }
 
@@ -389,7 +417,29 @@ PreTuning default_tuning(const PreParams& p, int batch, const DeviceInfo& info) 
     return t;
 }
 
-bool g_ring_attr_set[64][2];
+bool g_ring_attr_set[64][3][2];
+
+template <typename OutT, bool kVec>
+ws_status launch_ring(const PreParams& p, int dev, const DeviceInfo& info, unsigned blocks, int threads, size_t smem,
+                      int type_slot, cudaStream_t stream) {
+    if (!g_ring_attr_set[dev][type_slot][kVec]) {
+        WS_TRY_CUDA(cudaFuncSetAttribute(pre_ring_kernel<OutT, kVec>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         info.max_smem_optin));
+        g_ring_attr_set[dev][type_slot][kVec] = true;
+    }
+    pre_ring_kernel<OutT, kVec><<<blocks, threads, smem, stream>>>(p);
+    return WS_OK;
+}
+
+template <typename OutT>
+ws_status launch_any(const PreParams& p, bool ring, bool vec, int dev, const DeviceInfo& info, unsigned blocks,
+                     int threads, size_t smem, int type_slot, long long total, cudaStream_t stream) {
+    if (ring)
+        return vec ? launch_ring<OutT, true>(p, dev, info, blocks, threads, smem, type_slot, stream)
+                   : launch_ring<OutT, false>(p, dev, info, blocks, threads, smem, type_slot, stream);
+    pre_direct_kernel<OutT><<<blocks, 256, 0, stream>>>(p, total);
+    return WS_OK;
+}
 
 }  // namespace
 
@@ -413,8 +463,10 @@ ws_status validate_preprocess(const ws_preprocess_desc* d, int32_t batch) {
         return fail(WS_ERR_INVALID_ARGUMENT, "resize mode %d", d->resize);
     if (d->pad_value < 0 || d->pad_value > 255)
         return fail(WS_ERR_INVALID_ARGUMENT, "pad value %d outside 0..255", d->pad_value);
-    if (d->channel_order != WS_ORDER_RGB)
-        return fail(WS_ERR_UNSUPPORTED, "channel order %d", d->channel_order);
+    if (d->channel_order != WS_ORDER_RGB && d->channel_order != WS_ORDER_BGR)
+        return fail(WS_ERR_INVALID_ARGUMENT, "channel order %d", d->channel_order);
+    if (d->dst_type != WS_DTYPE_F32 && d->dst_type != WS_DTYPE_F16 && d->dst_type != WS_DTYPE_BF16)
+        return fail(WS_ERR_INVALID_ARGUMENT, "destination type %d", d->dst_type);
     if (d->norm == WS_NORM_MEAN_STD) {
         for (int c = 0; c < 3; ++c) {
             if (!(d->std[c] > 0.f) || !std::isfinite(d->std[c]) || !std::isfinite(d->mean[c]))
@@ -431,7 +483,7 @@ ws_status validate_preprocess(const ws_preprocess_desc* d, int32_t batch) {
 }
 
 // Launch with an explicit ring tuning (NULL = the default policy).
-ws_status preprocess_launch(const ws_preprocess_desc* d, const uint8_t* src, int32_t batch, float* dst,
+ws_status preprocess_launch(const ws_preprocess_desc* d, const uint8_t* src, int32_t batch, void* dst,
                             cudaStream_t stream, const PreTuning* tuning) {
     ws_status st = validate_preprocess(d, batch);
     if (st != WS_OK) return st;
@@ -458,6 +510,7 @@ ws_status preprocess_launch(const ws_preprocess_desc* d, const uint8_t* src, int
         }
     }
     p.pad = (float)d->pad_value;
+    for (int c = 0; c < 3; ++c) p.cmap[c] = d->channel_order == WS_ORDER_BGR ? 2 - c : c;
     p.dst = dst;
     p.row_bytes = 3 * d->src_w;
     p.slot_bytes = (int)align16(p.row_bytes);
@@ -471,29 +524,29 @@ ws_status preprocess_launch(const ws_preprocess_desc* d, const uint8_t* src, int
     const bool ring_ok = aligned && d->dst_w <= kMaxTableCols && t.band >= 1 && t.band <= kMaxBand &&
                          t.stages >= 1 && t.stages <= kMaxStages && t.threads >= 32 &&
                          t.threads <= kMaxThreads && smem <= (size_t)info->max_smem_optin;
+    bool vec = false;
+    unsigned blocks;
+    long long total = 0;
     if (ring_ok) {
         p.nbands = (d->dst_h + t.band - 1) / t.band;
         p.units = (long long)batch * p.nbands;
-        const bool vec = (d->dst_w % 4 == 0) && ((uintptr_t)dst % 16 == 0);
-        if (!g_ring_attr_set[dev][vec]) {
-            if (vec)
-                WS_TRY_CUDA(cudaFuncSetAttribute(pre_ring_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                 info->max_smem_optin));
-            else
-                WS_TRY_CUDA(cudaFuncSetAttribute(pre_ring_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                 info->max_smem_optin));
-            g_ring_attr_set[dev][vec] = true;
-        }
-        const long long blocks = std::min<long long>(p.units, (long long)info->sm_count * t.blocks_per_sm);
-        if (vec)
-            pre_ring_kernel<true><<<(unsigned)blocks, t.threads, smem, stream>>>(p);
-        else
-            pre_ring_kernel<false><<<(unsigned)blocks, t.threads, smem, stream>>>(p);
+        vec = (d->dst_w % 4 == 0) && ((uintptr_t)dst % 16 == 0);
+        blocks = (unsigned)std::min<long long>(p.units, (long long)info->sm_count * t.blocks_per_sm);
     } else {
-        const long long total = (long long)batch * d->dst_h * d->dst_w;
-        const long long blocks = std::min<long long>((total + 255) / 256, (long long)info->sm_count * 16);
-        pre_direct_kernel<<<(unsigned)blocks, 256, 0, stream>>>(p, total);
+        total = (long long)batch * d->dst_h * d->dst_w;
+        blocks = (unsigned)std::min<long long>((total + 255) / 256, (long long)info->sm_count * 16);
     }
+    switch (d->dst_type) {
+        case WS_DTYPE_F16:
+            st = launch_any<__half>(p, ring_ok, vec, dev, *info, blocks, t.threads, smem, 1, total, stream);
+            break;
+        case WS_DTYPE_BF16:
+            st = launch_any<__nv_bfloat16>(p, ring_ok, vec, dev, *info, blocks, t.threads, smem, 2, total, stream);
+            break;
+        default:
+            st = launch_any<float>(p, ring_ok, vec, dev, *info, blocks, t.threads, smem, 0, total, stream);
+    }
+    if (st != WS_OK) return st;
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e, "preprocess launch");
     return WS_OK;
@@ -508,7 +561,7 @@ ws_status ws_preprocess_validate(const ws_preprocess_desc* desc, int32_t batch) 
     return ws::validate_preprocess(desc, batch);
 }
 
-ws_status ws_preprocess(const ws_preprocess_desc* d, const uint8_t* src, int32_t batch, float* dst,
+ws_status ws_preprocess(const ws_preprocess_desc* d, const uint8_t* src, int32_t batch, void* dst,
                         cudaStream_t stream) {
     ws::clear_error();
     return ws::preprocess_launch(d, src, batch, dst, stream, nullptr);

@@ -66,7 +66,8 @@ def test_status_strings(B):
 
 @pytest.mark.parametrize("field,value", [
     ("src_w", 0), ("src_h", -1), ("dst_w", 0), ("dst_h", 70000), ("src_row_stride", 5),
-    ("src_frame_stride", 10), ("resize", 7), ("pad_value", 256), ("norm", 3), ("channel_order", 1)])
+    ("src_frame_stride", 10), ("resize", 7), ("pad_value", 256), ("norm", 3), ("channel_order", 2),
+    ("dst_type", 3), ("dst_type", -1)])
 def test_preprocess_descriptor_rejected(B, field, value):
     d = B.preprocess_desc(32, 16, 8, 8)
     setattr(d, field, value)

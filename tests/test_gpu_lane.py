@@ -179,3 +179,23 @@ def test_bench_throughput_configuration(B, oracle):
     finally:
         for ln in lanes:
             ln.close()
+
+
+def test_bf16_bgr_lane(B, oracle):
+    """A lane with a BGR producer and a bfloat16 network input."""
+    from post_processing_gb300 import Lane
+    rgb = synth.frames_uniform(12, 4, 240, 320)
+    bgr = rgb.reshape(4, 240, 320, 3)[..., ::-1].copy().reshape(rgb.shape)
+    logits = synth.logits_normal(13, 4, 1000)
+    pre = B.preprocess_desc(320, 240, 128, 96, channel_order=B.WS_ORDER_BGR, dst_type=B.WS_DTYPE_BF16)
+    with Lane(B.lane_desc(pre, 4, 4, 1000, 5)) as lane:
+        assert lane.buffers.tensor_bytes == 4 * 3 * 96 * 128 * 2
+        fill_lane(B, lane, bgr, logits)
+        lane.acquire()
+        lane.submit()
+        lane.wait()
+        raw = np.empty(4 * 3 * 96 * 128, np.uint16)
+        memcpy(raw.ctypes.data, lane.buffers.tensor, raw.nbytes)
+        got = torch.from_numpy(raw.view(np.int16)).view(torch.bfloat16).float().reshape(4, 3, 96, 128)
+        want = torch.from_numpy(oracle.preprocess(rgb, 320, 240, 128, 96)).to(torch.bfloat16).float()
+        assert float((got - want).abs().max()) <= 2.0 ** -6 * 4    # at most one bf16 ulp at |x| < 4

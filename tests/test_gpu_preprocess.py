@@ -119,3 +119,87 @@ def test_repeat_calls_are_identical(B):
 def test_no_device_error_raised(B):
     st, flags = B.ws_device_error(False)
     assert st == B.WS_OK and flags == 0
+
+
+# ---- precision- and format-specialised outputs ------------------------------
+
+def run_gpu_typed(B, frames, sw, sh, dw, dh, dst_type, channel_order=0, letterbox=False, norm="mean_std",
+                  offset=0):
+    batch = frames.shape[0]
+    flat = np.zeros(offset + frames.size + 64, np.uint8)
+    flat[offset:offset + frames.size] = frames.reshape(-1)
+    dev = torch.from_numpy(flat).cuda()
+    tdt = {B.WS_DTYPE_F32: torch.float32, B.WS_DTYPE_F16: torch.float16, B.WS_DTYPE_BF16: torch.bfloat16}[dst_type]
+    out = torch.full((batch, 3, dh, dw), float("nan"), dtype=tdt, device="cuda")
+    d = B.preprocess_desc(sw, sh, dw, dh, letterbox=letterbox, norm=norm, channel_order=channel_order,
+                          dst_type=dst_type)
+    B.check(B.ws_preprocess(d, dev.data_ptr() + offset, batch, out.data_ptr(),
+                            torch.cuda.current_stream().cuda_stream))
+    torch.cuda.synchronize()
+    return out.cpu()
+
+
+def rounded(oracle_f32, dst_type, B):
+    """The FP32 oracle rounded to the output format (torch: round to nearest even)."""
+    tdt = {B.WS_DTYPE_F16: torch.float16, B.WS_DTYPE_BF16: torch.bfloat16}[dst_type]
+    return torch.from_numpy(oracle_f32).to(tdt)
+
+
+def ulp_of(x, dst_type, B):
+    """Spacing of the format at |x| (one unit in the last place)."""
+    mant = 10 if dst_type == B.WS_DTYPE_F16 else 7
+    # exact binade from the float's exponent (a float log2 of 2.0 may land
+    # just below 1); clamped to the smallest normal exponent of the format
+    _, e = torch.frexp(x.float())
+    e = torch.clamp(e.float() - 1, min=-14.0 if dst_type == B.WS_DTYPE_F16 else -126.0)
+    return torch.pow(2.0, e - mant)
+
+
+SHAPES_TYPED = [("b64_1080p_to_224", 8), ("b1_720p_letterbox_640", 1), ("b8_4k_to_512", 2), (None, 2)]
+
+
+@pytest.mark.parametrize("dst", ["f16", "bf16"])
+@pytest.mark.parametrize("name,batch", SHAPES_TYPED, ids=[str(s[0]) for s in SHAPES_TYPED])
+def test_half_outputs(B, oracle, dst, name, batch):
+    """Half outputs equal the FP32 oracle rounded to the format, except where
+    the two FP32 values (within 1e-5 of each other) straddle a rounding
+    boundary: there an element may differ by one unit in the last place, plus
+    the FP32 difference itself."""
+    dst_type = B.WS_DTYPE_F16 if dst == "f16" else B.WS_DTYPE_BF16
+    if name is None:   # ragged shape, per-pixel kernel (misaligned base)
+        sw, sh, dw, dh, lb, norm, off = 101, 67, 37, 29, False, "mean_std", 3
+        frames = synth.frames_uniform(5, batch, sh, sw)
+    else:
+        w = synth.WORKLOADS[name]
+        sw, sh, dw, dh, lb, norm, off = (w["src_w"], w["src_h"], w["dst_w"], w["dst_h"],
+                                          w["resize"] == "letterbox", w["norm"], 0)
+        frames = synth.make_frames(name, batch=batch)
+    got = run_gpu_typed(B, frames, sw, sh, dw, dh, dst_type, letterbox=lb, norm=norm, offset=off)
+    want32 = oracle.preprocess(frames, sw, sh, dw, dh, letterbox=lb, norm=norm)
+    want = rounded(want32, dst_type, B)
+    diff = (got.float() - want.float()).abs()
+    assert not torch.isnan(got.float()).any()
+    # |round(a) - round(b)| <= |a - b| + one ulp, and |a - b| <= 1e-5 for the
+    # FP32 values (near zero that 1e-5 spans several half ulps)
+    assert torch.all(diff <= ulp_of(want, dst_type, B) + TOL), float(diff.max())
+    assert float((diff > 0).float().mean()) < 1e-3          # boundary cases only
+    # and the value is the FP32 result within the format's rounding (one ulp
+    # covers a rounding that lands on the next binade)
+    assert torch.all((got.float() - torch.from_numpy(want32)).abs() <= ulp_of(want, dst_type, B) + 1e-5)
+
+
+@pytest.mark.parametrize("name", ["b1_1080p_to_224", "b1_720p_letterbox_640"])
+def test_bgr_source(B, oracle, name):
+    """A BGR frame gives exactly the planes of the same picture stored as RGB."""
+    w = synth.WORKLOADS[name]
+    rgb = synth.make_frames(name)
+    bgr = rgb.reshape(rgb.shape[0], w["src_h"], w["src_w"], 3)[..., ::-1].copy().reshape(rgb.shape)
+    lb = w["resize"] == "letterbox"
+    got = run_gpu_typed(B, bgr, w["src_w"], w["src_h"], w["dst_w"], w["dst_h"], B.WS_DTYPE_F32,
+                        channel_order=B.WS_ORDER_BGR, letterbox=lb, norm=w["norm"]).numpy()
+    want = oracle.preprocess(rgb, w["src_w"], w["src_h"], w["dst_w"], w["dst_h"], letterbox=lb, norm=w["norm"])
+    compare(got, want)
+    # the per-pixel kernel too (misaligned base)
+    got2 = run_gpu_typed(B, bgr, w["src_w"], w["src_h"], w["dst_w"], w["dst_h"], B.WS_DTYPE_F32,
+                         channel_order=B.WS_ORDER_BGR, letterbox=lb, norm=w["norm"], offset=1).numpy()
+    compare(got2, want)
