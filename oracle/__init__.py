@@ -1,4 +1,5 @@
-"""The oracle: a plain CPU definition of the preprocess and the exact Top-K.
+"""The oracle: a plain CPU definition of the preprocess, the exact Top-K and
+the detection decode + NMS.
 
 TEST INFRASTRUCTURE.  Only ``tests/``, ``__graft_entry__.smoke()`` and the
 ``cpu_baseline`` / ``--impl reference`` legs of ``bench.py`` may import this
@@ -52,6 +53,15 @@ def load(path: str | None = None):
     lib.oracle_preprocess.restype = i32
     lib.oracle_topk.argtypes = [ctypes.c_void_p, i64, i64, i32, ctypes.c_void_p, ctypes.c_void_p]
     lib.oracle_topk.restype = i32
+    vp = ctypes.c_void_p
+    lib.oracle_anchor.argtypes = [i64, i32, i32, vp, i32, ctypes.POINTER(ctypes.c_double),
+                                  ctypes.POINTER(ctypes.c_double), ctypes.POINTER(i32)]
+    lib.oracle_anchor.restype = i32
+    lib.oracle_decode.argtypes = [vp, i64, i32, i32, i32, i32, vp, i32, ctypes.c_float, i32,
+                                  vp, vp, vp, vp, vp, ctypes.POINTER(i32)]
+    lib.oracle_decode.restype = i32
+    lib.oracle_nms.argtypes = [vp, vp, vp, vp, i32, ctypes.c_float, i32, vp]
+    lib.oracle_nms.restype = i32
     if path is None:
         _lib = lib
     return lib
@@ -110,3 +120,48 @@ class Oracle:
         if rc != 0:
             raise ValueError("oracle_topk rejected its arguments")
         return val, idx
+
+    # ---- detection decode + NMS ------------------------------------------------
+
+    def anchor(self, a, in_w, in_h, strides):
+        st = np.ascontiguousarray(strides, dtype=np.int32)
+        cx, cy, s = ctypes.c_double(), ctypes.c_double(), ctypes.c_int()
+        if self.lib.oracle_anchor(a, in_w, in_h, st.ctypes.data, st.size, ctypes.byref(cx),
+                                  ctypes.byref(cy), ctypes.byref(s)):
+            raise ValueError("anchor out of range")
+        return cx.value, cy.value, s.value
+
+    def decode(self, head: np.ndarray, reg_max: int, num_classes: int, in_w: int, in_h: int, strides,
+               logit_thr: float, max_cand: int = 1 << 20):
+        """head: float32 [4*reg_max + num_classes, A] of one image."""
+        head = np.ascontiguousarray(head, dtype=np.float32)
+        A = head.shape[1]
+        st = np.ascontiguousarray(strides, dtype=np.int32)
+        cap = min(max_cand, A)
+        boxes = np.empty((cap, 4), np.float32)
+        logits = np.empty(cap, np.float32)
+        scores = np.empty(cap, np.float32)
+        classes = np.empty(cap, np.int32)
+        anchors = np.empty(cap, np.int32)
+        total = ctypes.c_int()
+        n = self.lib.oracle_decode(head.ctypes.data, A, reg_max, num_classes, in_w, in_h, st.ctypes.data,
+                                   st.size, ctypes.c_float(logit_thr), cap, boxes.ctypes.data,
+                                   logits.ctypes.data, scores.ctypes.data, classes.ctypes.data,
+                                   anchors.ctypes.data, ctypes.byref(total))
+        if n < 0:
+            raise ValueError("oracle_decode rejected its arguments")
+        return dict(boxes=boxes[:n], logits=logits[:n], scores=scores[:n], classes=classes[:n],
+                    anchors=anchors[:n], total=total.value)
+
+    def nms(self, boxes, logits, classes, anchors, iou_thr: float, max_det: int):
+        boxes = np.ascontiguousarray(boxes, dtype=np.float32).reshape(-1, 4)
+        logits = np.ascontiguousarray(logits, dtype=np.float32)
+        classes = np.ascontiguousarray(classes, dtype=np.int32)
+        anchors = np.ascontiguousarray(anchors, dtype=np.int32)
+        n = boxes.shape[0]
+        keep = np.empty(max(max_det, 1), np.int32)
+        k = self.lib.oracle_nms(boxes.ctypes.data, logits.ctypes.data, classes.ctypes.data, anchors.ctypes.data,
+                                n, ctypes.c_float(iou_thr), max_det, keep.ctypes.data)
+        if k < 0:
+            raise ValueError("oracle_nms rejected its arguments")
+        return keep[:k]

@@ -1,5 +1,6 @@
 // ws_oracle.cpp -- the oracle: a plain, slow, obviously correct CPU definition
-// of the fused RGB8 -> FP32 NCHW preprocess and of the exact Top-K.
+// of the fused RGB8 -> FP32 NCHW preprocess, the exact Top-K, and the
+// detection decode + greedy NMS.
 //
 // TEST INFRASTRUCTURE. Only the tests, the smoke check and the benchmark's
 // CPU-baseline leg load this library.  It shares no code, header, table or
@@ -207,6 +208,151 @@ int oracle_topk(const float* x, int64_t rows, int64_t cols, int k,
         }
     }
     return 0;
+}
+
+}  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Detection decode and non-maximum suppression.
+//
+// What it follows: yolo.cu README ("Why is it this fast?", GPU-resident NMS,
+// and the end-to-end pipeline: DFL decode, then NMS with a bitonic sort sized
+// to the live candidate count and greedy suppression) and "Inside WarpStream
+// TRT" (next steps: detection decode and NMS).  The pages name the steps but
+// not their formulas; the readings taken:
+//  * head layout [batch][4 * R + C][A] (R DFL bins per box side, C classes,
+//    A anchors), FP32 logits;
+//  * anchors run level by level (strides given, e.g. 8, 16, 32), row-major
+//    within a level; anchor (x, y) of a level with stride s has its centre
+//    at ((x + 1/2) s, (y + 1/2) s) in input pixels;
+//  * DFL: the distance of each side (left, top, right, bottom) is the
+//    expectation sum_i i * softmax(z)_i over its R bins, in units of the
+//    stride; box = (cx - l s, cy - t s, cx + r s, cy + b s);
+//  * the class is the arg-max of the class logits (lower class on ties); an
+//    anchor is a candidate when that logit exceeds a logit threshold (the
+//    caller passes logit(conf) so the decision needs no transcendental); its
+//    score is the logistic of the logit;
+//  * greedy NMS per image, class-aware: candidates in order of logit
+//    (higher first, lower anchor on ties); a candidate is kept unless an
+//    already kept box of the same class has IoU > iou_thr with it, tested as
+//    inter > iou_thr * union in FP32 with the operation order below; at most
+//    max_det are kept.
+// ---------------------------------------------------------------------------
+
+namespace {
+
+// IoU test in FP32 (no fused operations: the file is built with
+// -ffp-contract=off).  Boxes are x1, y1, x2, y2.
+bool iou_above(const float* a, const float* b, float thr) {
+    const float iw = std::max(0.0f, std::min(a[2], b[2]) - std::max(a[0], b[0]));
+    const float ih = std::max(0.0f, std::min(a[3], b[3]) - std::max(a[1], b[1]));
+    const float inter = iw * ih;
+    const float area_a = (a[2] - a[0]) * (a[3] - a[1]);
+    const float area_b = (b[2] - b[0]) * (b[3] - b[1]);
+    const float uni = area_a + area_b - inter;
+    return inter > thr * uni;
+}
+
+}  // namespace
+
+extern "C" {
+
+// Anchor centre and stride of anchor a for an input of in_w x in_h pixels
+// and the given strides.  Returns 0, or -1 if a is out of range.
+int oracle_anchor(int64_t a, int in_w, int in_h, const int* strides, int nlevels,
+                  double* cx, double* cy, int* stride) {
+    int64_t off = 0;
+    for (int l = 0; l < nlevels; ++l) {
+        const int s = strides[l];
+        const int64_t gw = in_w / s, gh = in_h / s;
+        if (a < off + gw * gh) {
+            const int64_t k = a - off;
+            *cx = ((double)(k % gw) + 0.5) * s;
+            *cy = ((double)(k / gw) + 0.5) * s;
+            *stride = s;
+            return 0;
+        }
+        off += gw * gh;
+    }
+    return -1;
+}
+
+// Decode of one image: candidates (box, logit, score, class, anchor) for every
+// anchor whose best class logit exceeds logit_thr, in anchor order.
+// Returns the number of candidates written (at most max_cand; the true count
+// goes to *total), or -1 on invalid arguments.  DFL arithmetic in double.
+int oracle_decode(const float* head, int64_t anchors, int reg_max, int num_classes,
+                  int in_w, int in_h, const int* strides, int nlevels, float logit_thr,
+                  int max_cand, float* boxes, float* logits, float* scores, int32_t* classes,
+                  int32_t* anchor_idx, int* total) {
+    if (!head || anchors <= 0 || reg_max <= 0 || num_classes <= 0 || max_cand < 0) return -1;
+    int64_t count_levels = 0;
+    for (int l = 0; l < nlevels; ++l) count_levels += (int64_t)(in_w / strides[l]) * (in_h / strides[l]);
+    if (count_levels != anchors) return -1;
+    int n = 0, all = 0;
+    for (int64_t a = 0; a < anchors; ++a) {
+        int best = 0;
+        float bl = head[(int64_t)(4 * reg_max) * anchors + a];
+        for (int c = 1; c < num_classes; ++c) {
+            const float v = head[(int64_t)(4 * reg_max + c) * anchors + a];
+            if (v > bl) { bl = v; best = c; }
+        }
+        if (!(bl > logit_thr)) continue;
+        ++all;
+        if (n >= max_cand) continue;
+        double cx, cy;
+        int s;
+        oracle_anchor(a, in_w, in_h, strides, nlevels, &cx, &cy, &s);
+        double dist[4];
+        for (int side = 0; side < 4; ++side) {
+            double m = -1e300;
+            for (int i = 0; i < reg_max; ++i) m = std::max(m, (double)head[(int64_t)(side * reg_max + i) * anchors + a]);
+            double z = 0.0, e = 0.0;
+            for (int i = 0; i < reg_max; ++i) {
+                const double w = std::exp((double)head[(int64_t)(side * reg_max + i) * anchors + a] - m);
+                z += w;
+                e += w * i;
+            }
+            dist[side] = e / z;
+        }
+        boxes[4 * n + 0] = (float)(cx - dist[0] * s);
+        boxes[4 * n + 1] = (float)(cy - dist[1] * s);
+        boxes[4 * n + 2] = (float)(cx + dist[2] * s);
+        boxes[4 * n + 3] = (float)(cy + dist[3] * s);
+        logits[n] = bl;
+        scores[n] = (float)(1.0 / (1.0 + std::exp(-(double)bl)));
+        classes[n] = best;
+        anchor_idx[n] = (int32_t)a;
+        ++n;
+    }
+    if (total) *total = all;
+    return n;
+}
+
+// Greedy class-aware NMS of n candidates (any order).  Writes the indices
+// (into the candidate arrays) of the kept boxes, in keep order; returns how
+// many were kept (at most max_det), or -1 on invalid arguments.
+int oracle_nms(const float* boxes, const float* logits, const int32_t* classes, const int32_t* anchor_idx,
+               int n, float iou_thr, int max_det, int32_t* keep) {
+    if (n < 0 || max_det < 0 || (n > 0 && (!boxes || !logits || !classes || !anchor_idx || !keep))) return -1;
+    std::vector<int> order((size_t)n);
+    for (int i = 0; i < n; ++i) order[(size_t)i] = i;
+    std::sort(order.begin(), order.end(), [&](int a, int b) {
+        if (logits[a] > logits[b]) return true;
+        if (logits[a] < logits[b]) return false;
+        return anchor_idx[a] < anchor_idx[b];
+    });
+    int kept = 0;
+    for (int oi = 0; oi < n && kept < max_det; ++oi) {
+        const int i = order[(size_t)oi];
+        bool ok = true;
+        for (int q = 0; q < kept && ok; ++q) {
+            const int j = keep[q];
+            if (classes[j] == classes[i] && iou_above(boxes + 4 * j, boxes + 4 * i, iou_thr)) ok = false;
+        }
+        if (ok) keep[kept++] = i;
+    }
+    return kept;
 }
 
 }  // extern "C"

@@ -218,3 +218,30 @@ def make_logits(name: str, rows: int | None = None) -> np.ndarray:
     if w["logits"] == "ties":
         return logits_with_ties(seed, r, w["cols"])
     return logits_normal(seed, r, w["cols"])
+
+
+# --------------------------------------------------------------------------
+# Detection head (YOLO-style, before the DFL decode)
+# --------------------------------------------------------------------------
+
+YOLO_STRIDES = (8, 16, 32)
+
+
+def yolo_anchor_count(in_w: int, in_h: int, strides=YOLO_STRIDES) -> int:
+    return sum((in_w // s) * (in_h // s) for s in strides)
+
+
+def yolo_head(seed: int, batch: int, in_w: int = 640, in_h: int = 640, reg_max: int = 16,
+              num_classes: int = 80, dfl_sigma: float = 2.0, cls_mu: float = -8.0,
+              cls_sigma: float = 2.0, strides=YOLO_STRIDES) -> np.ndarray:
+    """Raw head output [batch, 4*reg_max + num_classes, A]: DFL bin logits
+    N(0, dfl_sigma) and class logits N(cls_mu, cls_sigma).  With the defaults
+    about 2 % of the anchors of a 640x640 input clear a 0.25 confidence, and
+    neighbouring anchors' boxes overlap, so suppression has work to do."""
+    A = yolo_anchor_count(in_w, in_h, strides)
+    ch = 4 * reg_max + num_classes
+    out = np.empty((batch, ch, A), np.float32)
+    for b in range(batch):
+        out[b, :4 * reg_max] = normal(derive_seed(seed, b, 0), 4 * reg_max * A, 0.0, dfl_sigma).reshape(4 * reg_max, A)
+        out[b, 4 * reg_max:] = normal(derive_seed(seed, b, 1), num_classes * A, cls_mu, cls_sigma).reshape(num_classes, A)
+    return out

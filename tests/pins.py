@@ -303,3 +303,138 @@ PRE_PINS = [pin_bilinear_golden, pin_letterbox_boxes, pin_axis_taps, pin_identit
             pin_constant, pin_torch_interpolate, pin_strides]
 TOPK_PINS = [pin_topk_golden, pin_topk_bruteforce, pin_topk_torch, pin_topk_invariants]
 ALL_PINS = PRE_PINS + TOPK_PINS
+
+
+# ---------------------------------------------------------------- detection
+
+def pin_anchor_geometry(o):
+    """Hand-computed anchor centres: 640x640 with strides 8, 16, 32 (80x80,
+    40x40 and 20x20 cells = 8400 anchors) and a 320x192 input."""
+    cases = [((0, 640, 640), (4.0, 4.0, 8)), ((79, 640, 640), (636.0, 4.0, 8)),
+             ((80, 640, 640), (4.0, 12.0, 8)), ((6399, 640, 640), (636.0, 636.0, 8)),
+             ((6400, 640, 640), (8.0, 8.0, 16)), ((8000, 640, 640), (16.0, 16.0, 32)),
+             ((8399, 640, 640), (624.0, 624.0, 32)), ((41, 320, 192), (12.0, 12.0, 8)),
+             ((960, 320, 192), (8.0, 8.0, 16)), ((1259, 320, 192), (304.0, 176.0, 32))]
+    for (a, w, h), want in cases:
+        assert o.anchor(a, w, h, (8, 16, 32)) == want, (a, w, h)
+    try:
+        o.anchor(8400, 640, 640, (8, 16, 32))
+    except ValueError:
+        pass
+    else:
+        raise AssertionError("anchor 8400 of 8400 accepted")
+
+
+def _head(A, R=16, C=4):
+    return np.zeros((4 * R + C, A), np.float32)
+
+
+def pin_dfl_closed_forms(o):
+    """Uniform bins decode to the middle bin (R-1)/2; a dominant bin to its
+    index; two equal dominant bins to their midpoint.  Class arg-max takes the
+    lower class on ties; the threshold is strict."""
+    R, C, strides = 16, 4, (8, 16, 32)
+    A = 8400
+    head = _head(A, R, C)
+    head[4 * R:] = -10.0
+    # anchor 0 (stride 8, centre 4,4): uniform bins -> 7.5 on every side
+    head[4 * R + 2, 0] = 1.0
+    # anchor 6400 (stride 16, centre 8,8): left bin 3, top bin 0, right bin 15, bottom bins 2 and 6
+    for side, b in ((0, 3), (1, 0), (2, 15)):
+        head[side * R + b, 6400] = 100.0
+    head[3 * R + 2, 6400] = 100.0
+    head[3 * R + 6, 6400] = 100.0
+    head[4 * R + 3, 6400] = 2.0            # ties between classes 1 and 3: class 1
+    head[4 * R + 1, 6400] = 2.0
+    # anchor 8399: logit exactly at the threshold -> not a candidate
+    head[4 * R + 0, 8399] = 0.5
+    d = o.decode(head, R, C, 640, 640, strides, 0.5)
+    assert list(d["anchors"]) == [0, 6400], d["anchors"]
+    assert np.array_equal(d["boxes"][0], np.float32([4 - 7.5 * 8, 4 - 7.5 * 8, 4 + 7.5 * 8, 4 + 7.5 * 8]))
+    assert np.allclose(d["boxes"][1], [8 - 3 * 16, 8 - 0 * 16, 8 + 15 * 16, 8 + 4 * 16], atol=1e-4)
+    assert list(d["classes"]) == [2, 1]
+    assert d["logits"][0] == 1.0 and d["logits"][1] == 2.0
+    assert abs(d["scores"][1] - 1 / (1 + math.exp(-2.0))) < 1e-7
+    assert d["total"] == 2
+
+
+def pin_dfl_torch(o):
+    """Library special case: softmax expectation with torch in float64."""
+    import torch
+    head = synth.yolo_head(4, 1, 320, 192, num_classes=6, cls_mu=0.0)[0]
+    R = 16
+    d = o.decode(head, R, 6, 320, 192, synth.YOLO_STRIDES, -1e30)
+    A = head.shape[1]
+    assert d["total"] == A
+    z = torch.from_numpy(head[:4 * R].astype(np.float64)).reshape(4, R, A)
+    dist = (torch.softmax(z, dim=1) * torch.arange(R, dtype=torch.float64)[None, :, None]).sum(1)
+    for n in range(0, A, 37):
+        cx, cy, s = o.anchor(n, 320, 192, synth.YOLO_STRIDES)
+        want = [cx - dist[0, n] * s, cy - dist[1, n] * s, cx + dist[2, n] * s, cy + dist[3, n] * s]
+        assert np.allclose(d["boxes"][n], np.array(want, np.float64), rtol=0, atol=1e-4), n
+
+
+def read_nms_cases():
+    cases, cur = [], None
+    for line in open(os.path.join(GOLDEN, "nms_hand.txt")):
+        line = line.strip()
+        if not line or line.startswith("#"):
+            continue
+        tok = line.split()
+        if tok[0] == "case":
+            cur = dict(thr=float(tok[1]), max_det=int(tok[2]), rows=[])
+            cases.append(cur)
+        elif tok[0] == "keep":
+            cur["keep"] = [int(t) for t in tok[1:]]
+        else:
+            cur["rows"].append([float(t) for t in tok])
+    return cases
+
+
+def pin_nms_golden(o):
+    for c in read_nms_cases():
+        r = np.array(c["rows"], np.float64)
+        keep = o.nms(r[:, :4], r[:, 4], r[:, 5].astype(np.int32), r[:, 6].astype(np.int32), c["thr"], c["max_det"])
+        assert [int(r[i, 6]) for i in keep] == c["keep"], (c, keep)
+
+
+def _iou_above_f32(a, b, thr):
+    f = np.float32
+    iw = max(f(0), f(min(a[2], b[2])) - f(max(a[0], b[0])))
+    ih = max(f(0), f(min(a[3], b[3])) - f(max(a[1], b[1])))
+    inter = f(iw) * f(ih)
+    ua = f(a[2] - a[0]) * f(a[3] - a[1])
+    ub = f(b[2] - b[0]) * f(b[3] - b[1])
+    return inter > f(thr) * f(f(ua + ub) - inter)
+
+
+def pin_nms_bruteforce(o):
+    """Greedy NMS returns the lexicographically first maximal conflict-free
+    set (in score order): found here by enumerating every subset."""
+    rng = np.random.default_rng(11)
+    for trial in range(40):
+        n = int(rng.integers(1, 11))
+        xy = rng.integers(0, 12, size=(n, 2)).astype(np.float32)
+        wh = rng.integers(1, 9, size=(n, 2)).astype(np.float32)
+        boxes = np.concatenate([xy, xy + wh], 1).astype(np.float32)
+        logits = rng.integers(0, 4, n).astype(np.float32)        # ties on purpose
+        classes = rng.integers(0, 2, n).astype(np.int32)
+        anchors = rng.permutation(50)[:n].astype(np.int32)
+        thr = float(rng.choice([0.1, 0.3, 0.5, 0.7]))
+        order = sorted(range(n), key=lambda i: (-logits[i], anchors[i]))
+        conflict = [[classes[i] == classes[j] and i != j and _iou_above_f32(boxes[i], boxes[j], thr)
+                     for j in range(n)] for i in range(n)]
+        best = None
+        for mask in range(1 << n):
+            chosen = [order[p] for p in range(n) if mask >> (n - 1 - p) & 1]
+            if any(conflict[a][b] for a in chosen for b in chosen):
+                continue
+            key = tuple(1 if (mask >> (n - 1 - p)) & 1 else 0 for p in range(n))
+            if best is None or key > best[0]:
+                best = (key, chosen)
+        keep = o.nms(boxes, logits, classes, anchors, thr, 100)
+        assert list(keep) == best[1], (trial, list(keep), best[1])
+
+
+DET_PINS = [pin_anchor_geometry, pin_dfl_closed_forms, pin_dfl_torch, pin_nms_golden, pin_nms_bruteforce]
+ALL_PINS = ALL_PINS + DET_PINS

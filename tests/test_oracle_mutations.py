@@ -37,6 +37,17 @@ MUTATIONS = [
      "out_val[r * k + i] = row[j];"),
     ("signed zero lost", "out_val[r * k + i] = std::isnan(row[j]) ? ninf : row[j];",
      "out_val[r * k + i] = std::isnan(row[j]) ? ninf : row[j] + 0.0f;"),
+    ("anchor centre offset", "*cx = ((double)(k % gw) + 0.5) * s;", "*cx = ((double)(k % gw)) * s;"),
+    ("box sides swapped", "boxes[4 * n + 0] = (float)(cx - dist[0] * s);",
+     "boxes[4 * n + 0] = (float)(cx - dist[2] * s);"),
+    ("DFL bin index off by one", "e += w * i;", "e += w * (i + 1);"),
+    ("class tie to higher index", "if (v > bl) { bl = v; best = c; }", "if (v >= bl) { bl = v; best = c; }"),
+    ("threshold not strict", "if (!(bl > logit_thr)) continue;", "if (!(bl >= logit_thr)) continue;"),
+    ("IoU test not strict", "return inter > thr * uni;", "return inter >= thr * uni;"),
+    ("union without the overlap", "const float uni = area_a + area_b - inter;",
+     "const float uni = area_a + area_b;"),
+    ("class-agnostic suppression", "if (classes[j] == classes[i] && iou_above(", "if (iou_above("),
+    ("NMS tie to higher anchor", "return anchor_idx[a] < anchor_idx[b];", "return anchor_idx[a] > anchor_idx[b];"),
 ]
 
 
