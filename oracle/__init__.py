@@ -60,7 +60,7 @@ def load(path: str | None = None):
     lib.oracle_decode.argtypes = [vp, i64, i32, i32, i32, i32, vp, i32, ctypes.c_float, i32,
                                   vp, vp, vp, vp, vp, ctypes.POINTER(i32)]
     lib.oracle_decode.restype = i32
-    lib.oracle_nms.argtypes = [vp, vp, vp, vp, i32, ctypes.c_float, i32, vp]
+    lib.oracle_nms.argtypes = [vp, vp, vp, vp, i32, ctypes.c_float, i32, i32, vp]
     lib.oracle_nms.restype = i32
     if path is None:
         _lib = lib
@@ -153,7 +153,7 @@ class Oracle:
         return dict(boxes=boxes[:n], logits=logits[:n], scores=scores[:n], classes=classes[:n],
                     anchors=anchors[:n], total=total.value)
 
-    def nms(self, boxes, logits, classes, anchors, iou_thr: float, max_det: int):
+    def nms(self, boxes, logits, classes, anchors, iou_thr: float, max_det: int, max_cand: int = 1 << 30):
         boxes = np.ascontiguousarray(boxes, dtype=np.float32).reshape(-1, 4)
         logits = np.ascontiguousarray(logits, dtype=np.float32)
         classes = np.ascontiguousarray(classes, dtype=np.int32)
@@ -161,7 +161,7 @@ class Oracle:
         n = boxes.shape[0]
         keep = np.empty(max(max_det, 1), np.int32)
         k = self.lib.oracle_nms(boxes.ctypes.data, logits.ctypes.data, classes.ctypes.data, anchors.ctypes.data,
-                                n, ctypes.c_float(iou_thr), max_det, keep.ctypes.data)
+                                n, ctypes.c_float(iou_thr), max_cand, max_det, keep.ctypes.data)
         if k < 0:
             raise ValueError("oracle_nms rejected its arguments")
         return keep[:k]

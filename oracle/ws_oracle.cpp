@@ -233,7 +233,8 @@ int oracle_topk(const float* x, int64_t rows, int64_t cols, int k,
 //    caller passes logit(conf) so the decision needs no transcendental); its
 //    score is the logistic of the logit;
 //  * greedy NMS per image, class-aware: candidates in order of logit
-//    (higher first, lower anchor on ties); a candidate is kept unless an
+//    (higher first, lower anchor on ties), of which only the first max_cand
+//    enter (a per-image cap, this library's reading); a candidate is kept unless an
 //    already kept box of the same class has IoU > iou_thr with it, tested as
 //    inter > iou_thr * union in FP32 with the operation order below; at most
 //    max_det are kept.
@@ -329,12 +330,15 @@ int oracle_decode(const float* head, int64_t anchors, int reg_max, int num_class
     return n;
 }
 
-// Greedy class-aware NMS of n candidates (any order).  Writes the indices
+// Greedy class-aware NMS of n candidates (any order), of which the first
+// max_cand in sorted order enter.  Writes the indices
 // (into the candidate arrays) of the kept boxes, in keep order; returns how
 // many were kept (at most max_det), or -1 on invalid arguments.
 int oracle_nms(const float* boxes, const float* logits, const int32_t* classes, const int32_t* anchor_idx,
-               int n, float iou_thr, int max_det, int32_t* keep) {
-    if (n < 0 || max_det < 0 || (n > 0 && (!boxes || !logits || !classes || !anchor_idx || !keep))) return -1;
+               int n, float iou_thr, int max_cand, int max_det, int32_t* keep) {
+    if (n < 0 || max_det < 0 || max_cand < 0 ||
+        (n > 0 && (!boxes || !logits || !classes || !anchor_idx || !keep)))
+        return -1;
     std::vector<int> order((size_t)n);
     for (int i = 0; i < n; ++i) order[(size_t)i] = i;
     std::sort(order.begin(), order.end(), [&](int a, int b) {
@@ -343,7 +347,8 @@ int oracle_nms(const float* boxes, const float* logits, const int32_t* classes, 
         return anchor_idx[a] < anchor_idx[b];
     });
     int kept = 0;
-    for (int oi = 0; oi < n && kept < max_det; ++oi) {
+    const int entering = std::min(n, max_cand);
+    for (int oi = 0; oi < entering && kept < max_det; ++oi) {
         const int i = order[(size_t)oi];
         bool ok = true;
         for (int q = 0; q < kept && ok; ++q) {

@@ -382,7 +382,8 @@ def read_nms_cases():
             continue
         tok = line.split()
         if tok[0] == "case":
-            cur = dict(thr=float(tok[1]), max_det=int(tok[2]), rows=[])
+            cur = dict(thr=float(tok[1]), max_det=int(tok[2]), max_cand=int(tok[3]) if len(tok) > 3 else 1 << 30,
+                       rows=[])
             cases.append(cur)
         elif tok[0] == "keep":
             cur["keep"] = [int(t) for t in tok[1:]]
@@ -394,7 +395,8 @@ def read_nms_cases():
 def pin_nms_golden(o):
     for c in read_nms_cases():
         r = np.array(c["rows"], np.float64)
-        keep = o.nms(r[:, :4], r[:, 4], r[:, 5].astype(np.int32), r[:, 6].astype(np.int32), c["thr"], c["max_det"])
+        keep = o.nms(r[:, :4], r[:, 4], r[:, 5].astype(np.int32), r[:, 6].astype(np.int32), c["thr"], c["max_det"],
+                     c["max_cand"])
         assert [int(r[i, 6]) for i in keep] == c["keep"], (c, keep)
 
 

@@ -48,6 +48,7 @@ MUTATIONS = [
      "const float uni = area_a + area_b;"),
     ("class-agnostic suppression", "if (classes[j] == classes[i] && iou_above(", "if (iou_above("),
     ("NMS tie to higher anchor", "return anchor_idx[a] < anchor_idx[b];", "return anchor_idx[a] > anchor_idx[b];"),
+    ("candidate cap ignored", "const int entering = std::min(n, max_cand);", "const int entering = n;"),
 ]
 
 
