@@ -211,6 +211,82 @@ ws_status ws_topk(const float* x, int64_t rows, int64_t cols, int32_t k,
 ws_status ws_topk_noalloc(const float* x, int64_t rows, int64_t cols, int32_t k,
                           float* out_val, int32_t* out_idx, cudaStream_t stream);
 
+/* ---------------------------------------------------------------- detection
+ * DFL box decode and class-aware greedy NMS of a YOLO-style head, on the GPU
+ * (yolo.cu README, "Why is it this fast?": GPU-resident NMS, a bitonic sort
+ * sized to the live candidate count, then greedy suppression, inside the
+ * graph; "Inside WarpStream TRT", next steps: detection decode and NMS).
+ * Readings where the pages give no formula:
+ *  - head: float32 [batch][4 * reg_max + num_classes][A]; anchors run level
+ *    by level (strides[]), row-major within a level; anchor (x, y) of a level
+ *    with stride s is centred at ((x + 1/2) s, (y + 1/2) s) input pixels;
+ *  - DFL: each side's distance (left, top, right, bottom) is the expectation
+ *    of the bin index under the softmax of its reg_max logits, in strides;
+ *    box = (cx - l s, cy - t s, cx + r s, cy + b s), FP32 on the GPU;
+ *  - class = arg-max of the class logits (lower class on ties); an anchor is a
+ *    candidate when that logit exceeds logit_thr (pass logit(conf)): the
+ *    decision needs no transcendental, so it is exact;
+ *  - candidates enter NMS in order of logit, higher first, lower anchor on
+ *    ties; if an image has more than max_cand, only the first max_cand do;
+ *  - greedy, class-aware: a candidate is dropped when an already kept box of
+ *    its class has IoU > iou_thr with it, tested as inter > iou_thr * union in
+ *    FP32 with each operation rounded separately; at most max_det are kept;
+ *    score = logistic(logit). */
+typedef struct ws_detect_desc {
+    int32_t in_w, in_h;           /* network input size in pixels                 */
+    int32_t nlevels;              /* feature levels, 1 .. 4                        */
+    int32_t strides[4];           /* stride of each level; in_w, in_h divisible   */
+    int32_t reg_max;              /* DFL bins per side, 1 .. 32                    */
+    int32_t num_classes;          /* 1 .. 4096                                     */
+    float   logit_thr;            /* candidate when best class logit > logit_thr  */
+    float   iou_thr;              /* drop when IoU > iou_thr (same class)         */
+    int32_t max_cand;             /* candidates entering NMS per image, 1 .. 1024 */
+    int32_t max_det;              /* detections kept per image, 1 .. max_cand     */
+} ws_detect_desc;
+
+/* A candidate box (decode output, NMS input), 32 bytes. */
+typedef struct ws_candidate {
+    float   x1, y1, x2, y2;       /* input pixels                                  */
+    float   logit;                /* best class logit                              */
+    int32_t cls, anchor, pad_;
+} ws_candidate;
+
+/* A kept detection, 32 bytes. */
+typedef struct ws_detection {
+    float   x1, y1, x2, y2;       /* input pixels                                  */
+    float   score;                /* logistic(logit)                               */
+    int32_t cls, anchor, pad_;
+} ws_detection;
+
+/* Host-only check; also reports the anchor count A of the geometry. */
+ws_status ws_detect_validate(const ws_detect_desc* desc, int32_t batch, int64_t* anchors);
+
+/* Bytes of device workspace ws_detect needs (candidates of every image plus
+ * per-image counters).  Zero it once with ws_detect_workspace_init(); every
+ * completed ws_detect leaves the counters at zero again. */
+ws_status ws_detect_workspace_bytes(const ws_detect_desc* desc, int32_t batch, size_t* bytes);
+ws_status ws_detect_workspace_init(void* workspace, size_t bytes, cudaStream_t stream);
+
+/* Decode only.  cand: device ws_candidate [batch][A] (in no particular order);
+ * count: device int32 [batch], which must be zero on entry; receives each
+ * image's number of candidates (at most A).  One kernel launch. */
+ws_status ws_detect_decode(const ws_detect_desc* desc, const float* head, int32_t batch,
+                           ws_candidate* cand, int32_t* count, cudaStream_t stream);
+
+/* NMS only.  cand / count as written by ws_detect_decode (or by the caller:
+ * any order, count[b] <= A).  out: device ws_detection [batch][max_det] in
+ * keep order; out_count: device int32 [batch].  count[b] is reset to zero.
+ * One kernel launch. */
+ws_status ws_detect_nms(const ws_detect_desc* desc, ws_candidate* cand, int32_t* count, int32_t batch,
+                        ws_detection* out, int32_t* out_count, cudaStream_t stream);
+
+/* Decode + NMS with the candidates in `workspace`.  Two kernel launches.
+ * Errors: WS_ERR_INVALID_ARGUMENT (descriptor, pointers, workspace too
+ * small), WS_ERR_CUDA (launch failed). */
+ws_status ws_detect(const ws_detect_desc* desc, const float* head, int32_t batch,
+                    ws_detection* out, int32_t* out_count, void* workspace, size_t workspace_bytes,
+                    cudaStream_t stream);
+
 /* ------------------------------------------------------------------- lanes */
 
 #define WS_INPUT_DEVICE 0   /* producer writes a device buffer                       */

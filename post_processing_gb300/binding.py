@@ -68,6 +68,22 @@ class ws_lane_timing(ctypes.Structure):
     _fields_ = [("gpu_us", _f32), ("preprocess_us", _f32), ("topk_us", _f32), ("host_us", ctypes.c_double)]
 
 
+class ws_detect_desc(ctypes.Structure):
+    _fields_ = [("in_w", _i32), ("in_h", _i32), ("nlevels", _i32), ("strides", _i32 * 4), ("reg_max", _i32),
+                ("num_classes", _i32), ("logit_thr", _f32), ("iou_thr", _f32), ("max_cand", _i32),
+                ("max_det", _i32)]
+
+
+class ws_candidate(ctypes.Structure):
+    _fields_ = [("x1", _f32), ("y1", _f32), ("x2", _f32), ("y2", _f32), ("logit", _f32), ("cls", _i32),
+                ("anchor", _i32), ("pad_", _i32)]
+
+
+class ws_detection(ctypes.Structure):
+    _fields_ = [("x1", _f32), ("y1", _f32), ("x2", _f32), ("y2", _f32), ("score", _f32), ("cls", _i32),
+                ("anchor", _i32), ("pad_", _i32)]
+
+
 # name: (restype, argtypes) -- one entry per declaration in include/ws.h
 SIGNATURES = {
     "ws_status_string": (ctypes.c_char_p, [_i32]),
@@ -81,6 +97,12 @@ SIGNATURES = {
     "ws_topk_workspace_init": (_i32, [_vp, _sz, _vp]),
     "ws_topk": (_i32, [_vp, _i64, _i64, _i32, _vp, _vp, _vp, _sz, _vp]),
     "ws_topk_noalloc": (_i32, [_vp, _i64, _i64, _i32, _vp, _vp, _vp]),
+    "ws_detect_validate": (_i32, [ctypes.POINTER(ws_detect_desc), _i32, ctypes.POINTER(_i64)]),
+    "ws_detect_workspace_bytes": (_i32, [ctypes.POINTER(ws_detect_desc), _i32, ctypes.POINTER(_sz)]),
+    "ws_detect_workspace_init": (_i32, [_vp, _sz, _vp]),
+    "ws_detect_decode": (_i32, [ctypes.POINTER(ws_detect_desc), _vp, _i32, _vp, _vp, _vp]),
+    "ws_detect_nms": (_i32, [ctypes.POINTER(ws_detect_desc), _vp, _vp, _i32, _vp, _vp, _vp]),
+    "ws_detect": (_i32, [ctypes.POINTER(ws_detect_desc), _vp, _i32, _vp, _vp, _vp, _sz, _vp]),
     "ws_lane_create": (_i32, [ctypes.POINTER(ws_lane_desc), ctypes.POINTER(_vp)]),
     "ws_lane_get_buffers": (_i32, [_vp, ctypes.POINTER(ws_lane_buffers)]),
     "ws_lane_acquire": (_i32, [_vp]),
@@ -172,6 +194,51 @@ def ws_topk(x: int, rows: int, cols: int, k: int, out_val: int, out_idx: int,
 def ws_topk_noalloc(x: int, rows: int, cols: int, k: int, out_val: int, out_idx: int,
                     stream: int = 0) -> int:
     return lib.ws_topk_noalloc(x, rows, cols, k, out_val, out_idx, stream)
+
+
+def ws_detect_validate(desc: ws_detect_desc, batch: int) -> tuple[int, int]:
+    a = _i64(0)
+    st = lib.ws_detect_validate(ctypes.byref(desc), batch, ctypes.byref(a))
+    return st, a.value
+
+
+def ws_detect_workspace_bytes(desc: ws_detect_desc, batch: int) -> tuple[int, int]:
+    n = _sz(0)
+    st = lib.ws_detect_workspace_bytes(ctypes.byref(desc), batch, ctypes.byref(n))
+    return st, n.value
+
+
+def ws_detect_workspace_init(workspace: int, nbytes: int, stream: int = 0) -> int:
+    return lib.ws_detect_workspace_init(workspace, nbytes, stream)
+
+
+def ws_detect_decode(desc: ws_detect_desc, head: int, batch: int, cand: int, count: int, stream: int = 0) -> int:
+    return lib.ws_detect_decode(ctypes.byref(desc), head, batch, cand, count, stream)
+
+
+def ws_detect_nms(desc: ws_detect_desc, cand: int, count: int, batch: int, out: int, out_count: int,
+                  stream: int = 0) -> int:
+    return lib.ws_detect_nms(ctypes.byref(desc), cand, count, batch, out, out_count, stream)
+
+
+def ws_detect(desc: ws_detect_desc, head: int, batch: int, out: int, out_count: int, workspace: int,
+              workspace_bytes: int, stream: int = 0) -> int:
+    return lib.ws_detect(ctypes.byref(desc), head, batch, out, out_count, workspace, workspace_bytes, stream)
+
+
+def detect_desc(in_w: int = 640, in_h: int = 640, strides=(8, 16, 32), reg_max: int = 16, num_classes: int = 80,
+                conf: float = 0.25, iou_thr: float = 0.45, max_cand: int = 1024, max_det: int = 300) -> ws_detect_desc:
+    """Descriptor with the confidence given as a probability (its logit is the threshold)."""
+    import math
+    d = ws_detect_desc()
+    d.in_w, d.in_h = in_w, in_h
+    d.nlevels = len(strides)
+    d.strides[:] = list(strides) + [0] * (4 - len(strides))
+    d.reg_max, d.num_classes = reg_max, num_classes
+    d.logit_thr = math.log(conf / (1.0 - conf))
+    d.iou_thr = iou_thr
+    d.max_cand, d.max_det = max_cand, max_det
+    return d
 
 
 def ws_lane_create(desc: ws_lane_desc) -> tuple[int, int | None]:

@@ -245,3 +245,27 @@ def yolo_head(seed: int, batch: int, in_w: int = 640, in_h: int = 640, reg_max: 
         out[b, :4 * reg_max] = normal(derive_seed(seed, b, 0), 4 * reg_max * A, 0.0, dfl_sigma).reshape(4 * reg_max, A)
         out[b, 4 * reg_max:] = normal(derive_seed(seed, b, 1), num_classes * A, cls_mu, cls_sigma).reshape(num_classes, A)
     return out
+
+
+def clustered_candidates(seed: int, objects: int, per_object: int, num_classes: int = 80,
+                         in_w: int = 640, in_h: int = 640, jitter: float = 0.08,
+                         logit_mu: float = 0.0, logit_sigma: float = 2.0, anchors: int = 8400) -> dict:
+    """Detection candidates the way a detector's dense head emits them: around
+    each of ``objects`` random boxes, ``per_object`` copies whose corners move
+    by N(0, jitter * side), all of the object's class; logits N(mu, sigma);
+    distinct anchor ids drawn from [0, anchors).  Returns float32 boxes
+    [n, 4] (x1, y1, x2, y2), float32 logits, int32 classes and anchors."""
+    n = objects * per_object
+    u = uniform_doubles(derive_seed(seed, 0), 4 * objects).reshape(objects, 4)
+    w = 16.0 + u[:, 2] * (in_w / 2.0)
+    h = 16.0 + u[:, 3] * (in_h / 2.0)
+    cx = u[:, 0] * in_w
+    cy = u[:, 1] * in_h
+    base = np.stack([cx - w / 2, cy - h / 2, cx + w / 2, cy + h / 2], axis=1)
+    side = np.stack([w, h, w, h], axis=1)
+    z = normal_f64(derive_seed(seed, 1), 4 * n).reshape(n, 4)
+    boxes = (np.repeat(base, per_object, axis=0) + jitter * np.repeat(side, per_object, axis=0) * z)
+    cls = (splitmix64(derive_seed(seed, 2), objects) % np.uint64(num_classes)).astype(np.int32)
+    perm = np.argsort(splitmix64(derive_seed(seed, 3), anchors), kind="stable")[:n].astype(np.int32)
+    return dict(boxes=boxes.astype(np.float32), logits=normal(derive_seed(seed, 4), n, logit_mu, logit_sigma),
+                classes=np.repeat(cls, per_object), anchors=perm)

@@ -37,7 +37,9 @@ def test_every_declared_symbol_is_exported(B):
 
 def test_struct_layout_matches_c(B, tmp_path):
     structs = {"ws_preprocess_desc": B.ws_preprocess_desc, "ws_lane_desc": B.ws_lane_desc,
-               "ws_lane_buffers": B.ws_lane_buffers, "ws_lane_timing": B.ws_lane_timing}
+               "ws_lane_buffers": B.ws_lane_buffers, "ws_lane_timing": B.ws_lane_timing,
+               "ws_detect_desc": B.ws_detect_desc, "ws_candidate": B.ws_candidate,
+               "ws_detection": B.ws_detection}
     lines = ['#include <stdio.h>', '#include <stddef.h>', '#include "ws.h"', "int main(void) {"]
     for name, cls in structs.items():
         lines.append(f'printf("{name} size %zu\\n", sizeof({name}));')
@@ -161,3 +163,22 @@ def test_product_does_not_import_the_oracle():
                 text = open(os.path.join(dirpath, f)).read()
                 assert "import oracle" not in text and "from oracle" not in text, f
                 assert "ws_oracle" not in text and "liboracle" not in text, f
+
+
+def test_detect_validation(B):
+    d = B.detect_desc()
+    st, A = B.ws_detect_validate(d, 4)
+    assert st == B.WS_OK and A == 8400
+    st, n = B.ws_detect_workspace_bytes(d, 4)
+    assert st == B.WS_OK and n >= 4 * 8400 * 32
+    for field, value in (("max_cand", 2000), ("max_det", 0), ("reg_max", 40), ("num_classes", 0),
+                         ("nlevels", 5)):
+        bad = B.detect_desc()
+        setattr(bad, field, value)
+        assert B.ws_detect_validate(bad, 1)[0] == B.WS_ERR_INVALID_ARGUMENT, field
+        assert B.ws_detect(bad, 16, 1, 16, 16, 256, 1 << 20, 0) == B.WS_ERR_INVALID_ARGUMENT
+    bad = B.detect_desc(in_w=650)            # 650 is not a multiple of 32
+    assert B.ws_detect_validate(bad, 1)[0] == B.WS_ERR_INVALID_ARGUMENT
+    assert B.ws_detect_validate(d, 0)[0] == B.WS_ERR_INVALID_ARGUMENT
+    # a workspace that is too small is refused before any launch
+    assert B.ws_detect(d, 16, 4, 16, 16, 256, n - 32, 0) == B.WS_ERR_INVALID_ARGUMENT

@@ -1,0 +1,227 @@
+"""Detection decode + NMS on the GPU against the oracle.
+
+Decode: the candidate set (anchors), classes and logits are exact (no
+transcendental decides them); boxes agree within 2e-4 pixels (the GPU's FP32
+softmax against the oracle's double one).  NMS: given the same candidates
+the kept list is exact -- the IoU test is FP32 with every operation rounded
+separately on both sides.  End to end, ws_detect equals the oracle's NMS of
+the candidates the GPU decoded.
+"""
+import numpy as np
+import pytest
+import torch
+
+import synth
+
+pytestmark = pytest.mark.gpu
+BOX_TOL = 2e-4
+
+
+@pytest.fixture(scope="module")
+def B():
+    import __graft_entry__
+    __graft_entry__.build()
+    from post_processing_gb300 import binding
+    return binding
+
+
+def stream():
+    return torch.cuda.current_stream().cuda_stream
+
+
+def unpack(rows):
+    """ws_candidate / ws_detection rows (int32 view [n, 8]) to fields."""
+    rows = np.ascontiguousarray(rows)
+    return dict(boxes=rows[:, :4].view(np.float32), f4=rows[:, 4].view(np.float32), cls=rows[:, 5].copy(),
+                anchor=rows[:, 6].copy())
+
+
+def gpu_decode(B, desc, head):
+    batch, _, A = head.shape
+    h = torch.from_numpy(head).cuda()
+    cand = torch.zeros((batch, A, 8), dtype=torch.int32, device="cuda")
+    count = torch.zeros(batch, dtype=torch.int32, device="cuda")
+    B.check(B.ws_detect_decode(desc, h.data_ptr(), batch, cand.data_ptr(), count.data_ptr(), stream()))
+    torch.cuda.synchronize()
+    c, n = cand.cpu().numpy(), count.cpu().numpy()
+    out = []
+    for b in range(batch):
+        u = unpack(c[b, :n[b]])
+        order = np.argsort(u["anchor"], kind="stable")
+        out.append({k: v[order] for k, v in u.items()})
+    return out
+
+
+def gpu_nms(B, desc, cands):
+    """cands: list per image of dicts (boxes, logits, classes, anchors), any order."""
+    batch = len(cands)
+    st, A = B.ws_detect_validate(desc, batch)      # the buffer is [batch][A], A the geometry's anchor count
+    B.check(st)
+    rows = np.zeros((batch, A, 8), np.int32)
+    count = np.zeros(batch, np.int32)
+    for b, c in enumerate(cands):
+        n = len(c["anchors"])
+        rows[b, :n, :4] = np.asarray(c["boxes"], np.float32).view(np.int32)
+        rows[b, :n, 4] = np.asarray(c["logits"], np.float32).view(np.int32)
+        rows[b, :n, 5] = c["classes"]
+        rows[b, :n, 6] = c["anchors"]
+        count[b] = n
+    cand = torch.from_numpy(rows).cuda()
+    cnt = torch.from_numpy(count).cuda()
+    out = torch.zeros((batch, desc.max_det, 8), dtype=torch.int32, device="cuda")
+    oc = torch.zeros(batch, dtype=torch.int32, device="cuda")
+    B.check(B.ws_detect_nms(desc, cand.data_ptr(), cnt.data_ptr(), batch, out.data_ptr(), oc.data_ptr(), stream()))
+    torch.cuda.synchronize()
+    assert np.all(cnt.cpu().numpy() == 0), "candidate counters are reset for the next call"
+    o, k = out.cpu().numpy(), oc.cpu().numpy()
+    return [unpack(o[b, :k[b]]) for b in range(batch)]
+
+
+def oracle_cands(oracle, desc, head_b):
+    d = oracle.decode(head_b, desc.reg_max, desc.num_classes, desc.in_w, desc.in_h,
+                      list(desc.strides)[:desc.nlevels], desc.logit_thr)
+    return dict(boxes=d["boxes"], logits=d["logits"], classes=d["classes"], anchors=d["anchors"], total=d["total"])
+
+
+def check_decode(B, oracle, desc, head):
+    got = gpu_decode(B, desc, head)
+    for b in range(head.shape[0]):
+        want = oracle_cands(oracle, desc, head[b])
+        g = got[b]
+        assert np.array_equal(g["anchor"], want["anchors"]), b
+        assert np.array_equal(g["cls"], want["classes"])
+        assert np.array_equal(g["f4"].view(np.uint32), want["logits"].view(np.uint32))
+        if len(g["anchor"]):
+            assert float(np.max(np.abs(g["boxes"] - want["boxes"]))) <= BOX_TOL
+    return got
+
+
+def test_decode_parity(B, oracle):
+    desc = B.detect_desc()
+    head = synth.yolo_head(21, 3)
+    got = check_decode(B, oracle, desc, head)
+    assert all(50 < len(g["anchor"]) < 1000 for g in got)      # a realistic candidate count
+
+
+def test_decode_small_geometry(B, oracle):
+    desc = B.detect_desc(in_w=320, in_h=192, reg_max=8, num_classes=3, conf=0.3)
+    head = synth.yolo_head(22, 2, 320, 192, reg_max=8, num_classes=3, cls_mu=-2.0)
+    check_decode(B, oracle, desc, head)
+
+
+def shuffled(c, seed):
+    p = np.random.default_rng(seed).permutation(len(c["anchors"]))
+    return {k: np.asarray(v)[p] for k, v in c.items() if k != "total"}
+
+
+def check_nms(B, oracle, desc, cands_list):
+    got = gpu_nms(B, desc, [shuffled(c, i) for i, c in enumerate(cands_list)])
+    for b, c in enumerate(cands_list):
+        keep = oracle.nms(c["boxes"], c["logits"], c["classes"], c["anchors"], desc.iou_thr, desc.max_det,
+                          desc.max_cand)
+        assert list(got[b]["anchor"]) == [int(c["anchors"][i]) for i in keep], b
+        assert np.array_equal(got[b]["boxes"].view(np.uint32), c["boxes"][keep].view(np.uint32))
+        want_score = 1.0 / (1.0 + np.exp(-c["logits"][keep].astype(np.float64)))
+        assert np.allclose(got[b]["f4"], want_score, rtol=1e-6, atol=1e-7)
+    return got
+
+
+@pytest.mark.parametrize("iou", [0.45, 0.7, 0.2])
+def test_nms_exact(B, oracle, iou):
+    desc = B.detect_desc(iou_thr=iou)
+    head = synth.yolo_head(23, 2)
+    cands = [oracle_cands(oracle, desc, head[b]) for b in range(2)]
+    got = check_nms(B, oracle, desc, cands)
+    assert all(0 < len(g["anchor"]) <= len(c["anchors"]) for g, c in zip(got, cands))
+
+
+@pytest.mark.parametrize("iou", [0.2, 0.45, 0.7])
+def test_nms_exact_clustered(B, oracle, iou):
+    # dense clusters of same-class boxes: most candidates are suppressed
+    desc = B.detect_desc(iou_thr=iou)
+    cands = [synth.clustered_candidates(50 + b, 40, 20) for b in range(3)]
+    got = check_nms(B, oracle, desc, cands)
+    assert all(len(g["anchor"]) < len(c["anchors"]) // 2 for g, c in zip(got, cands))
+
+
+def test_nms_clustered_cap_ties_and_max_det(B, oracle):
+    # 3000 candidates > max_cand (radix select), logits on a 0.25 grid (ties), max_det truncation
+    cands = [synth.clustered_candidates(60 + b, 100, 30) for b in range(2)]
+    for c in cands:
+        c["logits"] = np.round(c["logits"] * 4) / 4
+    for max_cand, max_det in ((1024, 300), (1024, 25), (257, 257), (1, 1)):
+        desc = B.detect_desc(max_cand=max_cand, max_det=max_det)
+        check_nms(B, oracle, desc, cands)
+
+
+def test_nms_caps_and_ties(B, oracle):
+    # many candidates (cap by radix select), coarse logits (ties -> lower anchor first), few detections
+    desc = B.detect_desc(conf=0.05, max_cand=200, max_det=40)
+    head = synth.yolo_head(24, 2, cls_mu=-3.0)
+    head[:, 64:] = np.round(head[:, 64:] * 2) / 2
+    cands = [oracle_cands(oracle, desc, head[b]) for b in range(2)]
+    assert all(len(c["anchors"]) > 1000 for c in cands)
+    check_nms(B, oracle, desc, cands)
+    desc.max_cand, desc.max_det = 1024, 1024
+    check_nms(B, oracle, desc, cands)
+
+
+def run_detect(B, desc, head, ws=None):
+    batch = head.shape[0]
+    st, n = B.ws_detect_workspace_bytes(desc, batch)
+    B.check(st)
+    if ws is None:
+        ws = torch.empty(n + 256, dtype=torch.uint8, device="cuda")
+    wp = ws.data_ptr() + (-ws.data_ptr()) % 256
+    out = torch.zeros((batch, desc.max_det, 8), dtype=torch.int32, device="cuda")
+    oc = torch.zeros(batch, dtype=torch.int32, device="cuda")
+    return ws, wp, n, out, oc
+
+
+def test_detect_end_to_end_and_replay(B, oracle):
+    desc = B.detect_desc()
+    heads = [synth.yolo_head(30 + i, 2) for i in range(3)]
+    ws, wp, n, out, oc = run_detect(B, desc, heads[0])
+    s = torch.cuda.Stream()
+    h = torch.empty((2,) + heads[0].shape[1:], dtype=torch.float32, device="cuda")
+    with torch.cuda.stream(s):
+        B.check(B.ws_detect_workspace_init(wp, n, s.cuda_stream))
+        g = torch.cuda.CUDAGraph()
+        for i, head in enumerate(heads):
+            h.copy_(torch.from_numpy(head))
+            if i < 2:   # plain calls, twice on one workspace
+                B.check(B.ws_detect(desc, h.data_ptr(), 2, out.data_ptr(), oc.data_ptr(), wp, n, s.cuda_stream))
+            else:       # then captured once and replayed
+                with torch.cuda.graph(g, stream=s):
+                    B.check(B.ws_detect(desc, h.data_ptr(), 2, out.data_ptr(), oc.data_ptr(), wp, n, s.cuda_stream))
+                g.replay()
+            s.synchronize()
+            dec = gpu_decode(B, desc, head)          # the GPU's own candidates
+            o, k = out.cpu().numpy(), oc.cpu().numpy()
+            for b in range(2):
+                c = dec[b]
+                keep = oracle.nms(c["boxes"], c["f4"], c["cls"], c["anchor"], desc.iou_thr, desc.max_det,
+                                  desc.max_cand)
+                got = unpack(o[b, :k[b]])
+                assert list(got["anchor"]) == [int(c["anchor"][j]) for j in keep]
+                assert np.array_equal(got["boxes"].view(np.uint32), c["boxes"][keep].view(np.uint32))
+
+
+def test_detect_no_candidates_and_all_candidates(B, oracle):
+    desc = B.detect_desc(max_cand=1024, max_det=300)
+    quiet = synth.yolo_head(40, 1, cls_mu=-20.0, cls_sigma=0.1)
+    ws, wp, n, out, oc = run_detect(B, desc, quiet)
+    B.check(B.ws_detect_workspace_init(wp, n, stream()))
+    h = torch.from_numpy(quiet).cuda()
+    B.check(B.ws_detect(desc, h.data_ptr(), 1, out.data_ptr(), oc.data_ptr(), wp, n, stream()))
+    torch.cuda.synchronize()
+    assert int(oc[0]) == 0
+    loud = synth.yolo_head(41, 1, cls_mu=5.0)        # every anchor a candidate: 8400 > max_cand
+    h = torch.from_numpy(loud).cuda()
+    B.check(B.ws_detect(desc, h.data_ptr(), 1, out.data_ptr(), oc.data_ptr(), wp, n, stream()))
+    torch.cuda.synchronize()
+    dec = gpu_decode(B, desc, loud)[0]
+    assert len(dec["anchor"]) == 8400
+    keep = oracle.nms(dec["boxes"], dec["f4"], dec["cls"], dec["anchor"], desc.iou_thr, desc.max_det, desc.max_cand)
+    got = unpack(out.cpu().numpy()[0, :int(oc[0])])
+    assert list(got["anchor"]) == [int(dec["anchor"][j]) for j in keep]

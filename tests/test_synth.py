@@ -38,3 +38,13 @@ def test_ties_are_planted():
 def test_gradient_frame_shape_and_range():
     f = synth.frames_gradient_noise(1, 1, 9, 16)
     assert f.shape == (1, 9, 48) and f.dtype == np.uint8
+
+
+def test_clustered_candidates():
+    a = synth.clustered_candidates(4, 10, 6, num_classes=5)
+    b = synth.clustered_candidates(4, 10, 6, num_classes=5)
+    assert all(np.array_equal(a[k], b[k]) for k in a)
+    assert a["boxes"].shape == (60, 4) and a["boxes"].dtype == np.float32
+    assert np.unique(a["anchors"]).size == 60 and a["anchors"].max() < 8400
+    assert all(np.unique(a["classes"][i * 6:(i + 1) * 6]).size == 1 for i in range(10))
+    assert np.all(a["boxes"][:, 2] > a["boxes"][:, 0])    # jitter small against the side
