@@ -228,12 +228,13 @@ int oracle_topk(const float* x, int64_t rows, int64_t cols, int k,
 //  * DFL: the distance of each side (left, top, right, bottom) is the
 //    expectation sum_i i * softmax(z)_i over its R bins, in units of the
 //    stride; box = (cx - l s, cy - t s, cx + r s, cy + b s);
-//  * the class is the arg-max of the class logits (lower class on ties); an
+//  * the class is the arg-max of the class logits (lower class on ties, NaN
+//    ranked as -inf and -0 equal to +0, as in the Top-K); an
 //    anchor is a candidate when that logit exceeds a logit threshold (the
 //    caller passes logit(conf) so the decision needs no transcendental); its
 //    score is the logistic of the logit;
 //  * greedy NMS per image, class-aware: candidates in order of logit
-//    (higher first, lower anchor on ties), of which only the first max_cand
+//    (higher first, the same NaN / -0 rule, lower anchor on ties), of which only the first max_cand
 //    enter (a per-image cap, this library's reading); a candidate is kept unless an
 //    already kept box of the same class has IoU > iou_thr with it, tested as
 //    inter > iou_thr * union in FP32 with the operation order below; at most
@@ -241,6 +242,8 @@ int oracle_topk(const float* x, int64_t rows, int64_t cols, int k,
 // ---------------------------------------------------------------------------
 
 namespace {
+
+float nan_as_ninf(float v) { return std::isnan(v) ? -std::numeric_limits<float>::infinity() : v; }
 
 // IoU test in FP32 (no fused operations: the file is built with
 // -ffp-contract=off).  Boxes are x1, y1, x2, y2.
@@ -292,10 +295,11 @@ int oracle_decode(const float* head, int64_t anchors, int reg_max, int num_class
     if (count_levels != anchors) return -1;
     int n = 0, all = 0;
     for (int64_t a = 0; a < anchors; ++a) {
+        // arg-max with NaN ranked as -inf (as in the Top-K), the first class on ties
         int best = 0;
-        float bl = head[(int64_t)(4 * reg_max) * anchors + a];
+        float bl = nan_as_ninf(head[(int64_t)(4 * reg_max) * anchors + a]);
         for (int c = 1; c < num_classes; ++c) {
-            const float v = head[(int64_t)(4 * reg_max + c) * anchors + a];
+            const float v = nan_as_ninf(head[(int64_t)(4 * reg_max + c) * anchors + a]);
             if (v > bl) { bl = v; best = c; }
         }
         if (!(bl > logit_thr)) continue;
@@ -341,9 +345,11 @@ int oracle_nms(const float* boxes, const float* logits, const int32_t* classes, 
         return -1;
     std::vector<int> order((size_t)n);
     for (int i = 0; i < n; ++i) order[(size_t)i] = i;
+    // higher logit first (NaN as -inf, -0 equal to +0), then the lower anchor
     std::sort(order.begin(), order.end(), [&](int a, int b) {
-        if (logits[a] > logits[b]) return true;
-        if (logits[a] < logits[b]) return false;
+        const float la = nan_as_ninf(logits[a]), lb = nan_as_ninf(logits[b]);
+        if (la > lb) return true;
+        if (la < lb) return false;
         return anchor_idx[a] < anchor_idx[b];
     });
     int kept = 0;

@@ -438,5 +438,31 @@ def pin_nms_bruteforce(o):
         assert list(keep) == best[1], (trial, list(keep), best[1])
 
 
-DET_PINS = [pin_anchor_geometry, pin_dfl_closed_forms, pin_dfl_torch, pin_nms_golden, pin_nms_bruteforce]
+def pin_nan_and_signed_zero(o):
+    """NaN class logits rank as -inf and -0 equals +0, as in the Top-K: a NaN
+    class 0 does not hide a later class; an all-NaN anchor is no candidate;
+    between -0 and +0 the lower class wins with its own bits.  In NMS a NaN
+    logit sorts after every number, and -0 / +0 tie on the lower anchor."""
+    R, C = 2, 4
+    head = _head(21, R, C)          # 32x32 input: 16 + 4 + 1 anchors
+    head[4 * R:] = -10.0
+    head[4 * R + 0, 0] = np.nan
+    head[4 * R + 2, 0] = 3.0
+    head[4 * R:, 1] = np.nan
+    head[4 * R + 1, 2] = -0.0
+    head[4 * R + 3, 2] = 0.0
+    d = o.decode(head, R, C, 32, 32, (8, 16, 32), -1.0)
+    assert list(d["anchors"]) == [0, 2] and list(d["classes"]) == [2, 1]
+    assert d["logits"][0] == 3.0 and np.signbit(d["logits"][1])
+    box = np.float32([0, 0, 4, 4])
+    # the same box four times, one class: only the first in order survives
+    for logits, anchors, first in (([np.nan, -5.0], [0, 1], 1),       # NaN last although its anchor is lower
+                                   ([0.0, -0.0], [3, 2], 1),          # -0 == +0: anchor 2 first
+                                   ([-np.inf, np.nan], [5, 4], 1)):   # NaN == -inf: anchor 4 first
+        keep = o.nms(np.stack([box, box]), np.float32(logits), np.int32([0, 0]), np.int32(anchors), 0.5, 10)
+        assert list(keep) == [first], (logits, anchors, keep)
+
+
+DET_PINS = [pin_anchor_geometry, pin_dfl_closed_forms, pin_dfl_torch, pin_nms_golden, pin_nms_bruteforce,
+            pin_nan_and_signed_zero]
 ALL_PINS = ALL_PINS + DET_PINS

@@ -49,6 +49,10 @@ MUTATIONS = [
     ("class-agnostic suppression", "if (classes[j] == classes[i] && iou_above(", "if (iou_above("),
     ("NMS tie to higher anchor", "return anchor_idx[a] < anchor_idx[b];", "return anchor_idx[a] > anchor_idx[b];"),
     ("candidate cap ignored", "const int entering = std::min(n, max_cand);", "const int entering = n;"),
+    ("NaN class logit taken raw", "float bl = nan_as_ninf(head[(int64_t)(4 * reg_max) * anchors + a]);",
+     "float bl = head[(int64_t)(4 * reg_max) * anchors + a];"),
+    ("NaN logit sorted raw", "const float la = nan_as_ninf(logits[a]), lb = nan_as_ninf(logits[b]);",
+     "const float la = logits[a], lb = logits[b];"),
 ]
 
 
