@@ -223,11 +223,13 @@ ws_status ws_topk_noalloc(const float* x, int64_t rows, int64_t cols, int32_t k,
  *  - DFL: each side's distance (left, top, right, bottom) is the expectation
  *    of the bin index under the softmax of its reg_max logits, in strides;
  *    box = (cx - l s, cy - t s, cx + r s, cy + b s), FP32 on the GPU;
- *  - class = arg-max of the class logits (lower class on ties); an anchor is a
- *    candidate when that logit exceeds logit_thr (pass logit(conf)): the
- *    decision needs no transcendental, so it is exact;
- *  - candidates enter NMS in order of logit, higher first, lower anchor on
- *    ties; if an image has more than max_cand, only the first max_cand do;
+ *  - class = arg-max of the class logits (lower class on ties, NaN ranked as
+ *    -inf, -0 equal to +0, as in the Top-K); an anchor is a candidate when
+ *    that logit exceeds logit_thr (pass logit(conf)): the decision needs no
+ *    transcendental, so it is exact;
+ *  - candidates enter NMS in order of logit (the same NaN / -0 rule), higher
+ *    first, lower anchor on ties; if an image has more than max_cand, only
+ *    the first max_cand do;
  *  - greedy, class-aware: a candidate is dropped when an already kept box of
  *    its class has IoU > iou_thr with it, tested as inter > iou_thr * union in
  *    FP32 with each operation rounded separately; at most max_det are kept;
@@ -274,13 +276,16 @@ ws_status ws_detect_decode(const ws_detect_desc* desc, const float* head, int32_
                            ws_candidate* cand, int32_t* count, cudaStream_t stream);
 
 /* NMS only.  cand / count as written by ws_detect_decode (or by the caller:
- * any order, count[b] <= A).  out: device ws_detection [batch][max_det] in
- * keep order; out_count: device int32 [batch].  count[b] is reset to zero.
- * One kernel launch. */
+ * any order, count[b] <= A, anchors distinct within an image).  out: device
+ * ws_detection [batch][max_det] in keep order; out_count: device int32
+ * [batch].  count[b] is reset to zero.  One kernel launch, programmatically
+ * dependent on the previous kernel in the stream (it waits for that
+ * kernel's results before reading cand / count). */
 ws_status ws_detect_nms(const ws_detect_desc* desc, ws_candidate* cand, int32_t* count, int32_t batch,
                         ws_detection* out, int32_t* out_count, cudaStream_t stream);
 
-/* Decode + NMS with the candidates in `workspace`.  Two kernel launches.
+/* Decode + NMS with the candidates in `workspace`.  Two kernel launches, the
+ * NMS a programmatic dependent launch of the decode.
  * Errors: WS_ERR_INVALID_ARGUMENT (descriptor, pointers, workspace too
  * small), WS_ERR_CUDA (launch failed). */
 ws_status ws_detect(const ws_detect_desc* desc, const float* head, int32_t batch,

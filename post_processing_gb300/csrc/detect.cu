@@ -8,20 +8,28 @@
 // formula are stated in include/ws.h next to ws_detect_desc.
 //
 // How:
-//  * decode: one thread per anchor.  The class logits of consecutive anchors
-//    are consecutive in memory, so the arg-max scan over the classes is
-//    coalesced; only anchors whose best logit clears the threshold (about 2 %
-//    of them) go on to the DFL softmax expectations and are appended to their
-//    image's candidate buffer.
-//  * NMS: one block per image.  If the image has more than max_cand
-//    candidates, a radix select on the 64-bit keys (logit order bits, then
-//    the complemented anchor) keeps the best max_cand.  The survivors are
-//    bitonic-sorted in shared memory, every pair's suppression test (same
-//    class, IoU > threshold) is evaluated in parallel into a bit matrix, and
-//    one warp walks the sorted list keeping a running "removed" bit set, so
-//    the greedy pass costs one step per candidate.  The IoU test is FP32 with
-//    every operation rounded separately (no fused multiply-add), so given the
-//    same boxes the decisions are exactly those of the definition.
+//  * decode: a block takes 128 consecutive anchors, 4 per lane; its 8 warps
+//    split the classes (warp g scans classes g, g + 8, ...), each load a
+//    coalesced 512-byte row segment (16 bytes a lane), and 128 threads merge
+//    the 8 partial arg-maxes.  Only
+//    anchors whose best logit clears the threshold (about 2 % of them) go on
+//    to the DFL: one thread per (candidate, side) loads that side's reg_max
+//    logits and takes the softmax expectation.  One atomic per block reserves
+//    the block's candidate slots.
+//  * NMS: one block per image, launched as a programmatic dependent of the
+//    decode so its launch overlaps the decode's tail.  If the image has more
+//    than max_cand candidates, their 64-bit keys (logit order bits, then the
+//    complemented anchor) are staged in shared memory and a radix select
+//    (warp-aggregated histograms, early exit once a digit bin closes the
+//    count) keeps the best max_cand.  The survivors are ranked by counting
+//    when there are few, else bitonic-sorted at the next power of two of the
+//    live count.  Every pair's suppression test (same class, IoU > threshold)
+//    is evaluated in parallel into a bit matrix, a thread per (row, 64-bit
+//    word), the IoU only where the classes match, and one warp walks the sorted list a 64-candidate word at a time,
+//    deciding at each step every candidate that nothing live can still
+//    suppress.  The IoU test is FP32 with every operation rounded
+//    separately (no fused multiply-add), so given the same boxes the
+//    decisions are exactly those of the definition.
 #include <algorithm>
 #include <cmath>
 
@@ -31,9 +39,14 @@ namespace ws {
 namespace {
 
 constexpr int kDecodeThreads = 256;
+constexpr int kDecodeAnchors = 128;                    // anchors per decode block (4 per lane)
+constexpr int kClassGroups = kDecodeThreads / 32;      // warps splitting the classes
 constexpr int kNmsThreads = 512;
 constexpr int kMaxCand = 1024;
 constexpr int kMaxLevels = 4;
+constexpr int kMaxRegMax = 32;
+constexpr int kStageCap = 16384;      // candidate keys staged in shared memory for the cap selection
+constexpr int kCountSortMax = 256;    // rank by counting up to this many candidates, bitonic above
 constexpr unsigned kFull = 0xffffffffu;
 
 struct DetParams {
@@ -51,68 +64,188 @@ struct DetParams {
     ws_detection* out;                // [batch][max_det]
     int* out_count;                   // [batch]
     // NMS shared-memory layout
-    int P;                            // power of two >= max_cand
-    int W;                            // 64-bit words per mask row
-    int off_idx, off_box, off_cls, off_logit, off_anchor, off_mask, off_keep, off_hist;
+    int Pcap;                         // power of two >= max_cand
+    int stage_cap;                    // candidates whose keys fit the staging area
+    int off_idx, off_box, off_cls, off_logit, off_anchor, off_keep, off_hist, off_u;
+    int u_bytes;                      // staged keys, later the suppression matrix
 };
 
+// Class logits and NMS keys: NaN ranks as -inf and -0 equals +0, as in the
+// Top-K.
+__device__ __forceinline__ float nan_as_ninf(float v) { return v != v ? -INFINITY : v; }
+
 __device__ __forceinline__ uint32_t order_bits(float f) {
-    const uint32_t b = __float_as_uint(f);
+    uint32_t b = __float_as_uint(nan_as_ninf(f));
+    if (b == 0x80000000u) b = 0u;
     return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
 }
 
-__device__ __forceinline__ unsigned long long cand_key(const ws_candidate& c) {
-    return ((unsigned long long)order_bits(c.logit) << 32) | (uint32_t)(~(uint32_t)c.anchor);
+__device__ __forceinline__ unsigned long long cand_key(const ws_candidate* c) {
+    const float4 rest = __ldcg(reinterpret_cast<const float4*>(c) + 1);   // logit, class, anchor, pad
+    return ((unsigned long long)order_bits(rest.x) << 32) | (uint32_t)(~(uint32_t)__float_as_int(rest.z));
 }
 
-__global__ void __launch_bounds__(kDecodeThreads) detect_decode_kernel(const __grid_constant__ DetParams p) {
-    const int b = blockIdx.y;
-    const long long a = (long long)blockIdx.x * blockDim.x + threadIdx.x;
-    if (a >= p.A) return;
-    const float* hb = p.head + (size_t)b * p.ch * p.A;
-    const float* cl = hb + (size_t)(4 * p.R) * p.A + a;
-    float best = __ldg(cl);
-    int bc = 0;
-    for (int c = 1; c < p.C; ++c) {
-        const float v = __ldg(cl + (size_t)c * p.A);
-        if (v > best) {
-            best = v;
-            bc = c;
-        }
-    }
-    if (!(best > p.logit_thr)) return;
+// One block: kDecodeAnchors anchors.  Thread (g, t) of warp g scans classes
+// g, g + 8, ... of anchors 4t .. 4t + 3 (one 16-byte load each when kVec).
+template <bool kVec>
+__global__ void __launch_bounds__(kDecodeThreads, 4) detect_decode_kernel(const __grid_constant__ DetParams p) {
+    __shared__ float s_v[kClassGroups][kDecodeAnchors];
+    __shared__ int s_c[kClassGroups][kDecodeAnchors];
+    __shared__ int s_off[kDecodeAnchors];     // anchor offset (in the block) of the q-th candidate
+    __shared__ float s_best[kDecodeAnchors];
+    __shared__ int s_cls[kDecodeAnchors];
+    __shared__ float s_dist[kDecodeAnchors][4];
+    __shared__ int s_wcnt[kDecodeAnchors / 32];
+    __shared__ int s_n, s_base;
 
-    int l = 0;
-    while (l + 1 < p.nlevels && a >= p.off[l + 1]) ++l;
-    const long long k = a - p.off[l];
-    const float s = (float)p.stride[l];
-    const float cx = ((float)(k % p.gw[l]) + 0.5f) * s;
-    const float cy = ((float)(k / p.gw[l]) + 0.5f) * s;
-    float dist[4];
+    const int b = blockIdx.y, tid = threadIdx.x, lane = tid & 31, g = tid >> 5;
+    const long long a0 = (long long)blockIdx.x * kDecodeAnchors;
+    const float* hb = p.head + (size_t)b * p.ch * p.A;
+    const float* cl = hb + (size_t)(4 * p.R) * p.A;
+
+    // 1. arg-max over this warp's classes for 4 anchors; NaN as -inf, the lower class on ties
+    float best[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+    int bc[4] = {g, g, g, g};
+    const long long a4 = a0 + 4 * lane;
+    if (kVec) {
+        if (a4 < p.A) {   // A % 4 == 0: all four anchors exist
+            auto take = [&](const float4 v4, int c) {
+                const float v[4] = {nan_as_ninf(v4.x), nan_as_ninf(v4.y), nan_as_ninf(v4.z), nan_as_ninf(v4.w)};
 #pragma unroll
-    for (int side = 0; side < 4; ++side) {
-        const float* z = hb + (size_t)(side * p.R) * p.A + a;
-        float m = -INFINITY;
-        for (int i = 0; i < p.R; ++i) m = fmaxf(m, __ldg(z + (size_t)i * p.A));
-        float zs = 0.f, es = 0.f;
-        for (int i = 0; i < p.R; ++i) {
-            const float w = expf(__ldg(z + (size_t)i * p.A) - m);
-            zs += w;
-            es += w * (float)i;
+                for (int e = 0; e < 4; ++e)
+                    if (v[e] > best[e]) {
+                        best[e] = v[e];
+                        bc[e] = c;
+                    }
+            };
+            const float* col = cl + a4;
+            int c = g;
+            constexpr int kU = 5;   // loads in flight per thread
+            for (; c + (kU - 1) * kClassGroups < p.C; c += kU * kClassGroups) {
+                float4 v4[kU];
+#pragma unroll
+                for (int u = 0; u < kU; ++u)
+                    v4[u] = __ldg(reinterpret_cast<const float4*>(col + (size_t)(c + u * kClassGroups) * p.A));
+#pragma unroll
+                for (int u = 0; u < kU; ++u) take(v4[u], c + u * kClassGroups);
+            }
+            for (; c < p.C; c += kClassGroups) take(__ldg(reinterpret_cast<const float4*>(col + (size_t)c * p.A)), c);
         }
-        dist[side] = es / zs;
+    } else {
+#pragma unroll 2
+        for (int c = g; c < p.C; c += kClassGroups) {
+            const float* row = cl + (size_t)c * p.A;
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                if (a4 + e < p.A) {
+                    const float v = nan_as_ninf(__ldg(row + a4 + e));
+                    if (v > best[e]) {
+                        best[e] = v;
+                        bc[e] = c;
+                    }
+                }
+            }
+        }
     }
-    ws_candidate c;
-    c.x1 = cx - dist[0] * s;
-    c.y1 = cy - dist[1] * s;
-    c.x2 = cx + dist[2] * s;
-    c.y2 = cy + dist[3] * s;
-    c.logit = best;
-    c.cls = bc;
-    c.anchor = (int32_t)a;
-    c.pad_ = 0;
-    const int slot = atomicAdd(&p.count[b], 1);
-    if (slot < p.A) p.cand[(size_t)b * p.A + slot] = c;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        s_v[g][4 * lane + e] = best[e];
+        s_c[g][4 * lane + e] = bc[e];
+    }
+    __syncthreads();
+
+    // 2. merge the warps' partial arg-maxes: thread t < kDecodeAnchors owns anchor a0 + t
+    bool is_cand = false;
+    float bt = -INFINITY;
+    int ct = 0;
+    if (tid < kDecodeAnchors) {
+        bt = s_v[0][tid];
+        ct = s_c[0][tid];
+#pragma unroll
+        for (int q = 1; q < kClassGroups; ++q) {
+            const float v = s_v[q][tid];
+            const int c = s_c[q][tid];
+            if (v > bt || (v == bt && c < ct)) {
+                bt = v;
+                ct = c;
+            }
+        }
+        is_cand = a0 + tid < p.A && bt > p.logit_thr;
+    }
+    const unsigned bal = __ballot_sync(kFull, is_cand);
+    if (tid < kDecodeAnchors && lane == 0) s_wcnt[g] = __popc(bal);
+    __syncthreads();
+    if (tid < kDecodeAnchors) {
+        int before = __popc(bal & ((1u << lane) - 1u));
+        for (int w = 0; w < g; ++w) before += s_wcnt[w];
+        if (is_cand) {
+            s_off[before] = tid;
+            s_best[before] = bt;
+            s_cls[before] = ct;
+        }
+        if (tid == 0) {
+            int n = 0;
+            for (int w = 0; w < kDecodeAnchors / 32; ++w) n += s_wcnt[w];
+            s_n = n;
+            s_base = n ? atomicAdd(&p.count[b], n) : 0;
+        }
+    }
+    __syncthreads();
+    // the NMS may start launching: what is left here is a few loads per block
+    asm volatile("griddepcontrol.launch_dependents;");
+    const int n = s_n;
+    if (n == 0) return;
+
+    // 3. DFL: the expected bin of each side's softmax, one thread per (candidate, side)
+    for (int t = tid; t < 4 * n; t += kDecodeThreads) {
+        const int q = t >> 2, side = t & 3;
+        const float* z = hb + (size_t)(side * p.R) * p.A + (a0 + s_off[q]);
+        float v[kMaxRegMax];
+#pragma unroll
+        for (int i = 0; i < kMaxRegMax; ++i) v[i] = i < p.R ? __ldg(z + (size_t)i * p.A) : -INFINITY;
+        float m = -INFINITY;
+#pragma unroll
+        for (int i = 0; i < kMaxRegMax; ++i) m = fmaxf(m, v[i]);
+        float zs = 0.f, es = 0.f;
+#pragma unroll
+        for (int i = 0; i < kMaxRegMax; ++i) {
+            if (i < p.R) {
+                const float w = expf(v[i] - m);
+                zs += w;
+                es += w * (float)i;
+            }
+        }
+        s_dist[q][side] = es / zs;
+    }
+    __syncthreads();
+
+    // 4. boxes around the anchor centres, into the reserved slots
+    for (int q = tid; q < n; q += kDecodeThreads) {
+        const long long aq = a0 + s_off[q];
+        int l = 0;
+        while (l + 1 < p.nlevels && aq >= p.off[l + 1]) ++l;
+        const long long k = aq - p.off[l];
+        const float s = (float)p.stride[l];
+        const float cx = ((float)(k % p.gw[l]) + 0.5f) * s;
+        const float cy = ((float)(k / p.gw[l]) + 0.5f) * s;
+        float4 box;
+        box.x = cx - s_dist[q][0] * s;
+        box.y = cy - s_dist[q][1] * s;
+        box.z = cx + s_dist[q][2] * s;
+        box.w = cy + s_dist[q][3] * s;
+        const int slot = s_base + q;
+        if (slot < p.A) {
+            float4* dst = reinterpret_cast<float4*>(p.cand + (size_t)b * p.A + slot);
+            dst[0] = box;
+            dst[1] = make_float4(s_best[q], __int_as_float(s_cls[q]), __int_as_float((int)aq), 0.f);
+        }
+    }
+}
+
+__device__ __forceinline__ unsigned long long or_all(unsigned long long v) {
+    const unsigned lo = __reduce_or_sync(kFull, (unsigned)v);
+    const unsigned hi = __reduce_or_sync(kFull, (unsigned)(v >> 32));
+    return ((unsigned long long)hi << 32) | lo;
 }
 
 // IoU(a, b) > thr, as inter > thr * union, every operation rounded on its own.
@@ -126,149 +259,250 @@ __device__ __forceinline__ bool iou_above(const float4 a, const float4 b, float 
     return inter > __fmul_rn(thr, uni);
 }
 
+__device__ __forceinline__ void put_sorted(const ws_candidate* cb, int from, int to,
+                                           float4* s_box, int* s_cls, float* s_logit, int* s_anchor) {
+    const float4* c = reinterpret_cast<const float4*>(cb + from);
+    const float4 box = __ldcg(c);
+    const float4 rest = __ldcg(c + 1);
+    s_box[to] = box;
+    s_logit[to] = rest.x;
+    s_cls[to] = __float_as_int(rest.y);
+    s_anchor[to] = __float_as_int(rest.z);
+}
+
 __global__ void __launch_bounds__(kNmsThreads) detect_nms_kernel(const __grid_constant__ DetParams p) {
     extern __shared__ __align__(16) unsigned char smem[];
-    unsigned long long* s_key = reinterpret_cast<unsigned long long*>(smem);   // [P]
-    int* s_idx = reinterpret_cast<int*>(smem + p.off_idx);                     // [P] candidate slot
+    unsigned long long* s_key = reinterpret_cast<unsigned long long*>(smem);   // [Pcap]
+    int* s_idx = reinterpret_cast<int*>(smem + p.off_idx);                     // [Pcap] candidate slot
     float4* s_box = reinterpret_cast<float4*>(smem + p.off_box);                // [max_cand] sorted
     int* s_cls = reinterpret_cast<int*>(smem + p.off_cls);
     float* s_logit = reinterpret_cast<float*>(smem + p.off_logit);
     int* s_anchor = reinterpret_cast<int*>(smem + p.off_anchor);
-    unsigned long long* s_mask = reinterpret_cast<unsigned long long*>(smem + p.off_mask);  // [max_cand][W]
     int* s_keep = reinterpret_cast<int*>(smem + p.off_keep);
-    uint32_t* s_hist = reinterpret_cast<uint32_t*>(smem + p.off_hist);         // [256] + 4 words
-    uint32_t* s_misc = s_hist + 256;
+    uint32_t* s_hist = reinterpret_cast<uint32_t*>(smem + p.off_hist);         // [256]
+    uint32_t* s_misc = s_hist + 256;                                            // [8]
+    unsigned char* s_u = smem + p.off_u;
 
     const int b = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    if (tid < 8) s_misc[tid] = 0;
+    // the candidates and their count come from the kernel this one may overlap
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     const ws_candidate* cb = p.cand + (size_t)b * p.A;
-    const int n = (int)min((long long)p.count[b], p.A);
+    const int n = (int)min((long long)__ldcg(p.count + b), p.A);
     const int m = min(n, p.max_cand);
-    if (tid == 0) s_misc[0] = 0;
-    for (int i = tid; i < p.P; i += kNmsThreads) s_key[i] = 0ull;   // padding sorts last
     __syncthreads();
 
-    // 1. the best m candidates' keys into shared memory
-    unsigned long long kth = 0;
-    if (n > m) {
-        // exact radix select of the m-th largest key (8 passes of 8 bits)
+    // 1. the best m candidates' keys
+    if (n <= p.max_cand) {
+        for (int i = tid; i < n; i += kNmsThreads) {
+            s_key[i] = cand_key(cb + i);
+            s_idx[i] = i;
+        }
+    } else {
+        const bool staged = n <= p.stage_cap;
+        unsigned long long* s_all = reinterpret_cast<unsigned long long*>(s_u);
+        if (staged) {
+            for (int i = tid; i < n; i += kNmsThreads) s_all[i] = cand_key(cb + i);
+            __syncthreads();
+        }
+        // exact radix select of the m-th largest key, 8 bits a pass
         unsigned long long prefix = 0, mask = 0;
         uint32_t remaining = (uint32_t)m;
+        const int iters = (n + kNmsThreads - 1) / kNmsThreads;
         for (int shift = 56; shift >= 0; shift -= 8) {
             for (int i = tid; i < 256; i += kNmsThreads) s_hist[i] = 0;
             __syncthreads();
-            for (int i = tid; i < n; i += kNmsThreads) {
-                const unsigned long long key = cand_key(cb[i]);
-                if ((key & mask) == prefix) atomicAdd(&s_hist[(key >> shift) & 255u], 1u);
+            for (int r = 0; r < iters; ++r) {
+                const int i = r * kNmsThreads + tid;
+                uint32_t d = 256u;
+                if (i < n) {
+                    const unsigned long long k = staged ? s_all[i] : cand_key(cb + i);
+                    if ((k & mask) == prefix) d = (uint32_t)(k >> shift) & 255u;
+                }
+                const unsigned peers = __match_any_sync(kFull, d);
+                if (d < 256u && lane == __ffs(peers) - 1) atomicAdd(&s_hist[d], (uint32_t)__popc(peers));
             }
             __syncthreads();
-            if (tid == 0) {
-                uint32_t acc = 0;
-                for (int d = 255; d >= 0; --d) {
-                    if (acc + s_hist[d] >= remaining) {
-                        s_misc[1] = (uint32_t)d;
-                        s_misc[2] = remaining - acc;
-                        break;
+            if (warp == 0) {
+                // lane l holds bins 255 - 8 l .. 248 - 8 l; a scan from the top finds
+                // the bin holding the remaining-th largest key
+                uint32_t h[8], sum = 0;
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    h[e] = s_hist[255 - 8 * lane - e];
+                    sum += h[e];
+                }
+                uint32_t incl = sum;
+#pragma unroll
+                for (int o = 1; o < 32; o <<= 1) {
+                    const uint32_t v = __shfl_up_sync(kFull, incl, o);
+                    if (lane >= o) incl += v;
+                }
+                uint32_t acc = incl - sum;
+                if (acc < remaining && incl >= remaining) {
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        if (acc + h[e] >= remaining) {
+                            s_misc[1] = (uint32_t)(255 - 8 * lane - e);
+                            s_misc[2] = remaining - acc;
+                            s_misc[4] = (acc + h[e] == remaining);   // the whole bin is in: done
+                            break;
+                        }
+                        acc += h[e];
                     }
-                    acc += s_hist[d];
                 }
             }
             __syncthreads();
             prefix |= (unsigned long long)s_misc[1] << shift;
             mask |= 0xffull << shift;
             remaining = s_misc[2];
+            const bool done = s_misc[4] != 0;
             __syncthreads();
+            if (done) break;
         }
-        kth = prefix;   // keys are unique (anchors are), so exactly m are >= kth
-    }
-    for (int i = tid; i < n; i += kNmsThreads) {
-        const unsigned long long key = cand_key(cb[i]);
-        if (key >= kth) {
-            const uint32_t pos = atomicAdd(&s_misc[0], 1u);
-            if (pos < (uint32_t)m) {
-                s_key[pos] = key;
-                s_idx[pos] = i;
-            }
-        }
-    }
-    __syncthreads();
-
-    // 2. bitonic sort, descending (padding keys 0 go last)
-    for (int k = 2; k <= p.P; k <<= 1) {
-        for (int j = k >> 1; j > 0; j >>= 1) {
-            for (int i = tid; i < p.P; i += kNmsThreads) {
-                const int ixj = i ^ j;
-                if (ixj > i) {
-                    const unsigned long long a = s_key[i], c = s_key[ixj];
-                    const bool desc = (i & k) == 0;
-                    if (desc ? (a < c) : (a > c)) {
-                        s_key[i] = c;
-                        s_key[ixj] = a;
-                        const int t = s_idx[i];
-                        s_idx[i] = s_idx[ixj];
-                        s_idx[ixj] = t;
-                    }
+        // keys are distinct (anchors are), so exactly m keys are >= prefix
+        for (int i = tid; i < n; i += kNmsThreads) {
+            const unsigned long long k = staged ? s_all[i] : cand_key(cb + i);
+            if (k >= prefix) {
+                const uint32_t pos = atomicAdd(&s_misc[0], 1u);
+                if (pos < (uint32_t)m) {
+                    s_key[pos] = k;
+                    s_idx[pos] = i;
                 }
             }
-            __syncthreads();
         }
     }
-
-    // 3. the sorted candidates
-    for (int q = tid; q < m; q += kNmsThreads) {
-        const ws_candidate c = cb[s_idx[q]];
-        s_box[q] = make_float4(c.x1, c.y1, c.x2, c.y2);
-        s_cls[q] = c.cls;
-        s_logit[q] = c.logit;
-        s_anchor[q] = c.anchor;
-    }
     __syncthreads();
 
-    // 4. suppression bits: word w of row i holds j = 64 w + bit, j > i
-    const int W = p.W;
-    for (int t = tid; t < m * W; t += kNmsThreads) {
-        const int i = t / W, w = t - i * W;
-        const float4 bi = s_box[i];
-        const int ci = s_cls[i];
-        unsigned long long bits = 0;
-        const int j0 = w * 64;
-        const int j1 = min(m, j0 + 64);
-        for (int j = max(j0, i + 1); j < j1; ++j)
-            if (s_cls[j] == ci && iou_above(bi, s_box[j], p.iou_thr)) bits |= 1ull << (j - j0);
-        s_mask[(size_t)i * W + w] = bits;
-    }
-    __syncthreads();
-
-    // 5. greedy walk by one warp; lane w holds removed-word w
-    if (warp == 0) {
-        unsigned long long rem = 0;
-        int nk = 0;
-        for (int i = 0; i < m && nk < p.max_det; ++i) {
-            const unsigned long long word = __shfl_sync(kFull, rem, i >> 6);
-            if (!((word >> (i & 63)) & 1ull)) {
-                if (lane == 0) s_keep[nk] = i;
-                ++nk;
-                if (lane < W) rem |= s_mask[(size_t)i * W + lane];
+    // 2. descending order: rank by counting when few, else a bitonic sort at
+    //    the next power of two of the live count
+    if (m <= kCountSortMax) {
+        for (int t = tid; t < m; t += kNmsThreads) {
+            const unsigned long long k = s_key[t];
+            int r = 0;
+#pragma unroll 4
+            for (int j = 0; j < m; ++j) r += s_key[j] > k;
+            put_sorted(cb, s_idx[t], r, s_box, s_cls, s_logit, s_anchor);
+        }
+    } else {
+        int P = 1;
+        while (P < m) P <<= 1;
+        for (int i = m + tid; i < P; i += kNmsThreads) s_key[i] = 0ull;   // padding sorts last
+        __syncthreads();
+        for (int k = 2; k <= P; k <<= 1) {
+            for (int j = k >> 1; j > 0; j >>= 1) {
+                for (int t = tid; t < (P >> 1); t += kNmsThreads) {
+                    const int i = ((t & ~(j - 1)) << 1) | (t & (j - 1));
+                    const int ixj = i + j;
+                    const unsigned long long x = s_key[i], y = s_key[ixj];
+                    const bool desc = (i & k) == 0;
+                    if (desc ? (x < y) : (x > y)) {
+                        s_key[i] = y;
+                        s_key[ixj] = x;
+                        const int tmp = s_idx[i];
+                        s_idx[i] = s_idx[ixj];
+                        s_idx[ixj] = tmp;
+                    }
+                }
+                __syncthreads();
             }
+        }
+        for (int q = tid; q < m; q += kNmsThreads) put_sorted(cb, s_idx[q], q, s_box, s_cls, s_logit, s_anchor);
+    }
+    __syncthreads();
+
+    // 3. suppression bits: row i holds bit j (j > i, same class, IoU above the
+    //    threshold) in word j / 64; words below i / 64 are never read.  A task
+    //    is one (row, word): it gathers the word's class matches four at a
+    //    time (the lanes of a warp read the same classes), then takes the IoU
+    //    only for those.  The odd row stride keeps the row-parallel stores
+    //    apart.
+    const int Wl = (m + 63) >> 6;
+    const int RS = Wl | 1;
+    unsigned long long* s_m = reinterpret_cast<unsigned long long*>(s_u);
+    {
+        const int4* s_cls4 = reinterpret_cast<const int4*>(s_cls);
+        for (int t = tid; t < m * Wl; t += kNmsThreads) {
+            const int w = t / m, i = t - w * m;
+            if (w < (i >> 6)) continue;
+            const int ci = s_cls[i];
+            const int lo = max(0, i + 1 - 64 * w), hi = min(64, m - 64 * w);   // bits (lo, hi] of interest: [lo, hi)
+            unsigned long long match = 0;
+            for (int j4 = 0; j4 < hi; j4 += 4) {
+                const int4 c = s_cls4[(64 * w + j4) >> 2];
+                const unsigned nib = (unsigned)(c.x == ci) | ((unsigned)(c.y == ci) << 1) |
+                                     ((unsigned)(c.z == ci) << 2) | ((unsigned)(c.w == ci) << 3);
+                match |= (unsigned long long)nib << j4;
+            }
+            if (hi < 64) match &= (1ull << hi) - 1ull;
+            match = lo >= 64 ? 0ull : match & ~((1ull << lo) - 1ull);
+            unsigned long long bits = 0;
+            if (match != 0ull) {
+                const float4 bi = s_box[i];
+                while (match != 0ull) {
+                    const int b = __ffsll((long long)match) - 1;
+                    match &= match - 1ull;
+                    if (iou_above(bi, s_box[64 * w + b], p.iou_thr)) bits |= 1ull << b;
+                }
+            }
+            s_m[(size_t)i * RS + w] = bits;
+        }
+    }
+    __syncthreads();
+
+    // 4. greedy walk by one warp, a 64-candidate word at a time.  A word
+    //    starts with the bits that the boxes kept so far suppress in it (each
+    //    lane ORs that word of every 32nd kept row).  Then, every live
+    //    candidate that no live candidate of the word suppresses is kept
+    //    (nothing before it that could still be kept removes it); those
+    //    remove what they suppress, and the step repeats until the word is
+    //    decided -- the greedy result, in as many steps as the longest chain
+    //    of suppressions inside the word.  Lane l holds the word's rows l and
+    //    l + 32.
+    if (warp == 0) {
+        int nk = 0;
+        for (int w = 0; w < Wl && nk < p.max_det; ++w) {
+            const int r0 = 64 * w + lane, r1 = r0 + 32;
+            const unsigned long long d0 = r0 < m ? s_m[(size_t)r0 * RS + w] : 0ull;
+            const unsigned long long d1 = r1 < m ? s_m[(size_t)r1 * RS + w] : 0ull;
+            unsigned long long mine = 0;
+            for (int q = lane; q < nk; q += 32) mine |= s_m[(size_t)s_keep[q] * RS + w];
+            unsigned long long cur = ~or_all(mine);
+            const int live = m - 64 * w;
+            if (live < 64) cur &= (1ull << live) - 1ull;
+            unsigned long long kept = 0;
+            while (cur != 0ull) {
+                mine = (((cur >> lane) & 1ull) ? d0 : 0ull) | (((cur >> (lane + 32)) & 1ull) ? d1 : 0ull);
+                const unsigned long long sure = cur & ~or_all(mine);
+                mine = (((sure >> lane) & 1ull) ? d0 : 0ull) | (((sure >> (lane + 32)) & 1ull) ? d1 : 0ull);
+                const unsigned long long gone = or_all(mine);
+                kept |= sure;
+                cur &= ~(sure | gone);
+            }
+            // kept boxes in order, at most max_det in all
+            if ((kept >> lane) & 1ull) {
+                const int pos = nk + __popcll(kept & ((1ull << lane) - 1ull));
+                if (pos < p.max_det) s_keep[pos] = r0;
+            }
+            if ((kept >> (lane + 32)) & 1ull) {
+                const int pos = nk + __popcll(kept & ((1ull << (lane + 32)) - 1ull));
+                if (pos < p.max_det) s_keep[pos] = r1;
+            }
+            __syncwarp();
+            nk = min(nk + __popcll(kept), p.max_det);
         }
         if (lane == 0) s_misc[3] = (uint32_t)nk;
     }
     __syncthreads();
 
-    // 6. detections in keep order
+    // 5. detections in keep order
     const int nk = (int)s_misc[3];
     for (int q = tid; q < nk; q += kNmsThreads) {
         const int i = s_keep[q];
-        ws_detection d;
-        const float4 bx = s_box[i];
-        d.x1 = bx.x;
-        d.y1 = bx.y;
-        d.x2 = bx.z;
-        d.y2 = bx.w;
-        d.score = 1.0f / (1.0f + expf(-s_logit[i]));
-        d.cls = s_cls[i];
-        d.anchor = s_anchor[i];
-        d.pad_ = 0;
-        p.out[(size_t)b * p.max_det + q] = d;
+        float4* dst = reinterpret_cast<float4*>(p.out + (size_t)b * p.max_det + q);
+        dst[0] = s_box[i];
+        dst[1] = make_float4(1.0f / (1.0f + expf(-s_logit[i])), __int_as_float(s_cls[i]), __int_as_float(s_anchor[i]),
+                             0.f);
     }
     if (tid == 0) {
         p.out_count[b] = nk;
@@ -315,22 +549,35 @@ ws_status fill_params(const ws_detect_desc* d, int32_t batch, DetParams& p) {
     p.iou_thr = d->iou_thr;
     p.max_cand = d->max_cand;
     p.max_det = d->max_det;
-    p.P = 1;
-    while (p.P < d->max_cand) p.P <<= 1;
-    p.W = (d->max_cand + 63) / 64;
-    size_t o = (size_t)p.P * 8;
-    p.off_idx = (int)o;        o = align16(o + (size_t)p.P * 4);
+    p.Pcap = 2;
+    while (p.Pcap < d->max_cand) p.Pcap <<= 1;
+    size_t o = (size_t)p.Pcap * 8;
+    p.off_idx = (int)o;        o = align16(o + (size_t)p.Pcap * 4);
     p.off_box = (int)o;        o = align16(o + (size_t)d->max_cand * 16);
     p.off_cls = (int)o;        o = align16(o + (size_t)d->max_cand * 4);
     p.off_logit = (int)o;      o = align16(o + (size_t)d->max_cand * 4);
     p.off_anchor = (int)o;     o = align16(o + (size_t)d->max_cand * 4);
-    p.off_mask = (int)o;       o = align16(o + (size_t)d->max_cand * p.W * 8);
     p.off_keep = (int)o;       o = align16(o + (size_t)d->max_cand * 4);
-    p.off_hist = (int)o;
+    p.off_hist = (int)o;       o = align16(o + (256 + 8) * 4);
+    p.off_u = (int)o;
+    // the suppression matrix: max_cand rows of ceil(max_cand / 64) words, the
+    // row stride made odd
+    p.u_bytes = (int)((size_t)d->max_cand * (((d->max_cand + 63) / 64) | 1) * 8);
+    p.stage_cap = 0;
     return WS_OK;
 }
 
-size_t nms_smem(const DetParams& p) { return (size_t)p.off_hist + (256 + 4) * 4; }
+// Staging room for the cap selection: as many keys as the device's shared
+// memory allows on top of the fixed layout, at most kStageCap.
+size_t nms_smem(DetParams& p, int smem_optin) {
+    p.stage_cap = 0;
+    if (p.A > p.max_cand) {
+        const long long room = ((long long)smem_optin - p.off_u) / 8;
+        p.stage_cap = (int)std::min<long long>(std::min<long long>(p.A, kStageCap), std::max(0LL, room));
+    }
+    const size_t u = std::max<size_t>((size_t)p.u_bytes, (size_t)p.stage_cap * 8);
+    return (size_t)p.off_u + u;
+}
 
 size_t det_workspace(const DetParams& p, int32_t batch) {
     return (size_t)(batch * 4 + 255) / 256 * 256 + (size_t)batch * p.A * sizeof(ws_candidate);
@@ -339,27 +586,45 @@ size_t det_workspace(const DetParams& p, int32_t batch) {
 bool g_nms_attr_set[64];
 
 ws_status launch_decode(const DetParams& p, int32_t batch, cudaStream_t stream) {
-    const dim3 grid((unsigned)((p.A + kDecodeThreads - 1) / kDecodeThreads), (unsigned)batch);
-    detect_decode_kernel<<<grid, kDecodeThreads, 0, stream>>>(p);
+    const dim3 grid((unsigned)((p.A + kDecodeAnchors - 1) / kDecodeAnchors), (unsigned)batch);
+    const bool vec = p.A % 4 == 0 && (uintptr_t)p.head % 16 == 0;
+    if (vec)
+        detect_decode_kernel<true><<<grid, kDecodeThreads, 0, stream>>>(p);
+    else
+        detect_decode_kernel<false><<<grid, kDecodeThreads, 0, stream>>>(p);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e, "decode launch");
     return WS_OK;
 }
 
-ws_status launch_nms(const DetParams& p, int32_t batch, cudaStream_t stream) {
+// The NMS is a programmatic dependent launch ("Streams, concurrency and CUDA
+// Graphs", PDL section): it may be scheduled while the decode drains and
+// waits in griddepcontrol.wait for the decode's results.
+ws_status launch_nms(DetParams p, int32_t batch, cudaStream_t stream) {
     int dev;
     const DeviceInfo* info;
     ws_status st = current_device_info(&dev, &info);
     if (st != WS_OK) return st;
-    const size_t smem = nms_smem(p);
+    const size_t smem = nms_smem(p, info->max_smem_optin);
     if (smem > (size_t)info->max_smem_optin) return fail(WS_ERR_UNSUPPORTED, "NMS needs %zu bytes of shared memory", smem);
+    if (dev < 0 || dev >= 64) return fail(WS_ERR_UNSUPPORTED, "device ordinal %d", dev);
     if (!g_nms_attr_set[dev]) {
         WS_TRY_CUDA(cudaFuncSetAttribute(detect_nms_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          info->max_smem_optin));
         g_nms_attr_set[dev] = true;
     }
-    detect_nms_kernel<<<batch, kNmsThreads, smem, stream>>>(p);
-    cudaError_t e = cudaGetLastError();
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3((unsigned)batch);
+    cfg.blockDim = dim3(kNmsThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, detect_nms_kernel, p);
+    if (e == cudaSuccess) e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e, "NMS launch");
     return WS_OK;
 }

@@ -109,6 +109,40 @@ def test_decode_small_geometry(B, oracle):
     check_decode(B, oracle, desc, head)
 
 
+def test_decode_nan_and_signed_zero(B, oracle):
+    desc = B.detect_desc(in_w=64, in_h=64, reg_max=4, num_classes=20, conf=0.3)
+    head = synth.yolo_head(25, 2, 64, 64, reg_max=4, num_classes=20, cls_mu=-2.0)
+    C0 = 16
+    rng = np.random.default_rng(3)
+    A = head.shape[2]
+    for b in range(2):
+        nan_at = rng.random((20, A)) < 0.1                 # scattered NaN class logits
+        head[b, C0:][nan_at] = np.nan
+        head[b, C0:, :5] = np.nan                           # all-NaN anchors
+        head[b, C0:, 5:9] = -3.0                            # -0 / +0 ties above the threshold
+        head[b, C0 + 7, 5:9] = -0.0
+        head[b, C0 + 2, 5:9] = 0.0
+        head[b, C0 + 0, 9] = np.nan                         # NaN in class 0 then a real winner
+        head[b, C0 + 19, 9] = 4.0
+    got = check_decode(B, oracle, desc, head)
+    for g in got:
+        assert 9 in g["anchor"] and not any(a < 5 for a in g["anchor"])
+
+
+def test_nms_nan_and_signed_zero(B, oracle):
+    desc = B.detect_desc(iou_thr=0.5)
+    c = synth.clustered_candidates(70, 30, 8)
+    lg = np.round(c["logits"])                              # many ties
+    lg[::7] = np.nan
+    lg[1::5] = np.where(lg[1::5] == 0, -0.0, lg[1::5])
+    lg[2::11] = -np.inf
+    c["logits"] = lg.astype(np.float32)
+    got = gpu_nms(B, desc, [shuffled(c, 1)])[0]
+    keep = oracle.nms(c["boxes"], c["logits"], c["classes"], c["anchors"], desc.iou_thr, desc.max_det,
+                      desc.max_cand)
+    assert list(got["anchor"]) == [int(c["anchors"][i]) for i in keep]
+
+
 def shuffled(c, seed):
     p = np.random.default_rng(seed).permutation(len(c["anchors"]))
     return {k: np.asarray(v)[p] for k, v in c.items() if k != "total"}
