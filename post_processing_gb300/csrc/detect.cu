@@ -19,13 +19,14 @@
 //  * NMS: one block per image, launched as a programmatic dependent of the
 //    decode so its launch overlaps the decode's tail.  If the image has more
 //    than max_cand candidates, their 64-bit keys (logit order bits, then the
-//    complemented anchor) are staged in shared memory and a radix select
-//    (warp-aggregated histograms, early exit once a digit bin closes the
-//    count) keeps the best max_cand.  The survivors are ranked by counting
+//    complemented anchor) are held in registers and a radix select
+//    (warp-aggregated histogram counts, early exit once a digit bin closes
+//    the count) keeps the best max_cand.  The survivors are ranked by counting
 //    when there are few, else bitonic-sorted at the next power of two of the
-//    live count.  Every pair's suppression test (same class, IoU > threshold)
+//    live count (shuffles within a warp's 64 elements, shared memory above).  Every pair's suppression test (same class, IoU > threshold)
 //    is evaluated in parallel into a bit matrix, a thread per (row, 64-bit
-//    word), the IoU only where the classes match, and one warp walks the sorted list a 64-candidate word at a time,
+//    word), the IoU only where a class-bucket table shows a match, and one
+//    warp walks the sorted list a 64-candidate word at a time,
 //    deciding at each step every candidate that nothing live can still
 //    suppress.  The IoU test is FP32 with every operation rounded
 //    separately (no fused multiply-add), so given the same boxes the
@@ -42,10 +43,12 @@ constexpr int kDecodeThreads = 256;
 constexpr int kDecodeAnchors = 128;                    // anchors per decode block (4 per lane)
 constexpr int kClassGroups = kDecodeThreads / 32;      // warps splitting the classes
 constexpr int kNmsThreads = 512;
+constexpr int kNmsWarps = kNmsThreads / 32;
 constexpr int kMaxCand = 1024;
 constexpr int kMaxLevels = 4;
 constexpr int kMaxRegMax = 32;
-constexpr int kStageCap = 16384;      // candidate keys staged in shared memory for the cap selection
+constexpr int kKeysPerThread = 32;    // candidate keys a thread holds in registers for the cap selection
+constexpr int kBuckets = 256;         // class buckets of the match table
 constexpr int kCountSortMax = 256;    // rank by counting up to this many candidates, bitonic above
 constexpr unsigned kFull = 0xffffffffu;
 
@@ -65,9 +68,9 @@ struct DetParams {
     int* out_count;                   // [batch]
     // NMS shared-memory layout
     int Pcap;                         // power of two >= max_cand
-    int stage_cap;                    // candidates whose keys fit the staging area
     int off_idx, off_box, off_cls, off_logit, off_anchor, off_keep, off_hist, off_u;
-    int u_bytes;                      // staged keys, later the suppression matrix
+    int off_tab;                      // match table, from off_u
+    int u_bytes;                      // per-warp histograms, later the suppression matrix and match table
 };
 
 // Class logits and NMS keys: NaN ranks as -inf and -0 equals +0, as in the
@@ -81,8 +84,7 @@ __device__ __forceinline__ uint32_t order_bits(float f) {
 }
 
 __device__ __forceinline__ unsigned long long cand_key(const ws_candidate* c) {
-    const float4 rest = __ldcg(reinterpret_cast<const float4*>(c) + 1);   // logit, class, anchor, pad
-    return ((unsigned long long)order_bits(rest.x) << 32) | (uint32_t)(~(uint32_t)__float_as_int(rest.z));
+    return ((unsigned long long)order_bits(c->logit) << 32) | (uint32_t)(~(uint32_t)c->anchor);
 }
 
 // One block: kDecodeAnchors anchors.  Thread (g, t) of warp g scans classes
@@ -299,28 +301,56 @@ __global__ void __launch_bounds__(kNmsThreads) detect_nms_kernel(const __grid_co
             s_idx[i] = i;
         }
     } else {
-        const bool staged = n <= p.stage_cap;
-        unsigned long long* s_all = reinterpret_cast<unsigned long long*>(s_u);
-        if (staged) {
-            for (int i = tid; i < n; i += kNmsThreads) s_all[i] = cand_key(cb + i);
-            __syncthreads();
+        // exact radix select of the m-th largest key, 8 bits a pass; up to
+        // kKeysPerThread keys a thread are held in registers, more are re-read
+        const bool in_regs = n <= kNmsThreads * kKeysPerThread;
+        const int iters = (n + kNmsThreads - 1) / kNmsThreads;
+        unsigned long long kr[kKeysPerThread];
+        if (in_regs) {
+#pragma unroll
+            for (int r = 0; r < kKeysPerThread; ++r) {
+                const int i = r * kNmsThreads + tid;
+                kr[r] = (r < iters && i < n) ? cand_key(cb + i) : 0ull;
+            }
         }
-        // exact radix select of the m-th largest key, 8 bits a pass
         unsigned long long prefix = 0, mask = 0;
         uint32_t remaining = (uint32_t)m;
-        const int iters = (n + kNmsThreads - 1) / kNmsThreads;
+        uint32_t* s_whist = reinterpret_cast<uint32_t*>(s_u) + warp * 256;   // this warp's histogram
         for (int shift = 56; shift >= 0; shift -= 8) {
-            for (int i = tid; i < 256; i += kNmsThreads) s_hist[i] = 0;
+            for (int i = tid; i < kNmsWarps * 256; i += kNmsThreads) reinterpret_cast<uint32_t*>(s_u)[i] = 0;
             __syncthreads();
-            for (int r = 0; r < iters; ++r) {
-                const int i = r * kNmsThreads + tid;
-                uint32_t d = 256u;
-                if (i < n) {
-                    const unsigned long long k = staged ? s_all[i] : cand_key(cb + i);
-                    if ((k & mask) == prefix) d = (uint32_t)(k >> shift) & 255u;
+            // Histogram counts, per warp and aggregated over it: up to three times the
+            // lanes sharing the first remaining lane's digit add once (the
+            // leading passes see only a few distinct digits), then any lanes
+            // left add one each.
+            auto count = [&](unsigned long long k, bool valid) {
+                unsigned act = __ballot_sync(kFull, valid && (k & mask) == prefix);
+                const uint32_t d = (uint32_t)(k >> shift) & 255u;
+                for (int r = 0; r < 3 && act != 0u; ++r) {
+                    const int leader = __ffs(act) - 1;
+                    const uint32_t lead = __shfl_sync(kFull, d, leader);
+                    const unsigned same = __ballot_sync(kFull, ((act >> lane) & 1u) && d == lead);
+                    if (lane == leader) atomicAdd(&s_whist[lead], (uint32_t)__popc(same));
+                    act &= ~same;
                 }
-                const unsigned peers = __match_any_sync(kFull, d);
-                if (d < 256u && lane == __ffs(peers) - 1) atomicAdd(&s_hist[d], (uint32_t)__popc(peers));
+                if ((act >> lane) & 1u) atomicAdd(&s_whist[d], 1u);
+            };
+            if (in_regs) {
+#pragma unroll
+                for (int r = 0; r < kKeysPerThread; ++r)
+                    if (r < iters) count(kr[r], r * kNmsThreads + tid < n);
+            } else {
+                for (int r = 0; r < iters; ++r) {
+                    const int i = r * kNmsThreads + tid;
+                    count(i < n ? cand_key(cb + i) : 0ull, i < n);
+                }
+            }
+            __syncthreads();
+            for (int d = tid; d < 256; d += kNmsThreads) {
+                uint32_t h = 0;
+#pragma unroll
+                for (int w = 0; w < kNmsWarps; ++w) h += reinterpret_cast<const uint32_t*>(s_u)[w * 256 + d];
+                s_hist[d] = h;
             }
             __syncthreads();
             if (warp == 0) {
@@ -361,14 +391,28 @@ __global__ void __launch_bounds__(kNmsThreads) detect_nms_kernel(const __grid_co
             if (done) break;
         }
         // keys are distinct (anchors are), so exactly m keys are >= prefix
-        for (int i = tid; i < n; i += kNmsThreads) {
-            const unsigned long long k = staged ? s_all[i] : cand_key(cb + i);
-            if (k >= prefix) {
-                const uint32_t pos = atomicAdd(&s_misc[0], 1u);
-                if (pos < (uint32_t)m) {
-                    s_key[pos] = k;
-                    s_idx[pos] = i;
-                }
+        auto place = [&](unsigned long long k, bool valid, int i) {   // called by whole warps
+            const bool in = valid && k >= prefix;
+            const unsigned bal = __ballot_sync(kFull, in);
+            uint32_t base = 0;
+            if (lane == 0 && bal) base = atomicAdd(&s_misc[0], (uint32_t)__popc(bal));
+            base = __shfl_sync(kFull, base, 0);
+            const uint32_t pos = base + (uint32_t)__popc(bal & ((1u << lane) - 1u));
+            if (in && pos < (uint32_t)m) {
+                s_key[pos] = k;
+                s_idx[pos] = i;
+            }
+        };
+        if (in_regs) {
+#pragma unroll
+            for (int r = 0; r < kKeysPerThread; ++r) {
+                const int i = r * kNmsThreads + tid;
+                if (r < iters) place(kr[r], i < n, i);
+            }
+        } else {
+            for (int r = 0; r < iters; ++r) {
+                const int i = r * kNmsThreads + tid;
+                place(i < n ? cand_key(cb + i) : 0ull, i < n, i);
             }
         }
     }
@@ -386,67 +430,123 @@ __global__ void __launch_bounds__(kNmsThreads) detect_nms_kernel(const __grid_co
         }
     } else {
         int P = 1;
-        while (P < m) P <<= 1;
+        while (P < m) P <<= 1;   // 512 or 1024
         for (int i = m + tid; i < P; i += kNmsThreads) s_key[i] = 0ull;   // padding sorts last
         __syncthreads();
+        // Warp w holds elements 64 w + lane and 64 w + 32 + lane in registers;
+        // stages with j >= 64 go through shared memory, the rest use shuffles.
+        const bool active = 64 * warp < P;
+        const int e0 = 64 * warp + lane, e1 = e0 + 32;
+        unsigned long long x0 = 0, x1 = 0;
+        int i0 = 0, i1 = 0;
+        if (active) {
+            x0 = s_key[e0];
+            i0 = s_idx[e0];
+            x1 = s_key[e1];
+            i1 = s_idx[e1];
+        }
         for (int k = 2; k <= P; k <<= 1) {
-            for (int j = k >> 1; j > 0; j >>= 1) {
-                for (int t = tid; t < (P >> 1); t += kNmsThreads) {
-                    const int i = ((t & ~(j - 1)) << 1) | (t & (j - 1));
-                    const int ixj = i + j;
-                    const unsigned long long x = s_key[i], y = s_key[ixj];
-                    const bool desc = (i & k) == 0;
-                    if (desc ? (x < y) : (x > y)) {
-                        s_key[i] = y;
-                        s_key[ixj] = x;
-                        const int tmp = s_idx[i];
-                        s_idx[i] = s_idx[ixj];
-                        s_idx[ixj] = tmp;
-                    }
+            if (k >= 128) {
+                if (active) {
+                    s_key[e0] = x0;
+                    s_idx[e0] = i0;
+                    s_key[e1] = x1;
+                    s_idx[e1] = i1;
                 }
                 __syncthreads();
+                for (int j = k >> 1; j >= 64; j >>= 1) {
+                    for (int t = tid; t < (P >> 1); t += kNmsThreads) {
+                        const int i = ((t & ~(j - 1)) << 1) | (t & (j - 1));
+                        const int ixj = i + j;
+                        const unsigned long long x = s_key[i], y = s_key[ixj];
+                        const bool desc = (i & k) == 0;
+                        if (desc ? (x < y) : (x > y)) {
+                            s_key[i] = y;
+                            s_key[ixj] = x;
+                            const int tmp = s_idx[i];
+                            s_idx[i] = s_idx[ixj];
+                            s_idx[ixj] = tmp;
+                        }
+                    }
+                    __syncthreads();
+                }
+                if (active) {
+                    x0 = s_key[e0];
+                    i0 = s_idx[e0];
+                    x1 = s_key[e1];
+                    i1 = s_idx[e1];
+                }
+            }
+            if (active) {
+                for (int j = min(k >> 1, 32); j >= 1; j >>= 1) {
+                    if (j == 32) {
+                        const bool desc = (e0 & k) == 0;
+                        if (desc ? (x0 < x1) : (x0 > x1)) {
+                            const unsigned long long tx = x0;
+                            x0 = x1;
+                            x1 = tx;
+                            const int ti = i0;
+                            i0 = i1;
+                            i1 = ti;
+                        }
+                    } else {
+                        const unsigned long long y0 = __shfl_xor_sync(kFull, x0, j), y1 = __shfl_xor_sync(kFull, x1, j);
+                        const int j0 = __shfl_xor_sync(kFull, i0, j), j1 = __shfl_xor_sync(kFull, i1, j);
+                        // the lower element of a pair keeps the larger key when the run is descending
+                        const bool hi0 = ((e0 & j) == 0) == ((e0 & k) == 0);
+                        const bool hi1 = ((e1 & j) == 0) == ((e1 & k) == 0);
+                        if (hi0 ? (y0 > x0) : (y0 < x0)) {
+                            x0 = y0;
+                            i0 = j0;
+                        }
+                        if (hi1 ? (y1 > x1) : (y1 < x1)) {
+                            x1 = y1;
+                            i1 = j1;
+                        }
+                    }
+                }
             }
         }
-        for (int q = tid; q < m; q += kNmsThreads) put_sorted(cb, s_idx[q], q, s_box, s_cls, s_logit, s_anchor);
+        if (active) {
+            if (e0 < m) put_sorted(cb, i0, e0, s_box, s_cls, s_logit, s_anchor);
+            if (e1 < m) put_sorted(cb, i1, e1, s_box, s_cls, s_logit, s_anchor);
+        }
     }
     __syncthreads();
 
     // 3. suppression bits: row i holds bit j (j > i, same class, IoU above the
-    //    threshold) in word j / 64; words below i / 64 are never read.  A task
-    //    is one (row, word): it gathers the word's class matches four at a
-    //    time (the lanes of a warp read the same classes), then takes the IoU
-    //    only for those.  The odd row stride keeps the row-parallel stores
-    //    apart.
+    //    threshold) in word j / 64; words below i / 64 are never read.  A table
+    //    holds, per word and class bucket (class mod kBuckets), the mask of the
+    //    word's candidates in that bucket, so a (row, word) task finds its
+    //    class matches with one load and takes the IoU only for those.  The
+    //    odd row stride keeps the row-parallel stores apart.
     const int Wl = (m + 63) >> 6;
     const int RS = Wl | 1;
     unsigned long long* s_m = reinterpret_cast<unsigned long long*>(s_u);
-    {
-        const int4* s_cls4 = reinterpret_cast<const int4*>(s_cls);
-        for (int t = tid; t < m * Wl; t += kNmsThreads) {
-            const int w = t / m, i = t - w * m;
-            if (w < (i >> 6)) continue;
-            const int ci = s_cls[i];
-            const int lo = max(0, i + 1 - 64 * w), hi = min(64, m - 64 * w);   // bits (lo, hi] of interest: [lo, hi)
-            unsigned long long match = 0;
-            for (int j4 = 0; j4 < hi; j4 += 4) {
-                const int4 c = s_cls4[(64 * w + j4) >> 2];
-                const unsigned nib = (unsigned)(c.x == ci) | ((unsigned)(c.y == ci) << 1) |
-                                     ((unsigned)(c.z == ci) << 2) | ((unsigned)(c.w == ci) << 3);
-                match |= (unsigned long long)nib << j4;
+    unsigned long long* s_tab = reinterpret_cast<unsigned long long*>(s_u + p.off_tab);   // [Wl][kBuckets]
+    for (int q = tid; q < Wl * kBuckets; q += kNmsThreads) s_tab[q] = 0ull;
+    __syncthreads();
+    for (int q = tid; q < m; q += kNmsThreads)
+        atomicOr(&s_tab[(q >> 6) * kBuckets + (s_cls[q] & (kBuckets - 1))], 1ull << (q & 63));
+    __syncthreads();
+    for (int t = tid; t < m * Wl; t += kNmsThreads) {
+        const int w = t / m, i = t - w * m;
+        if (w < (i >> 6)) continue;
+        const int ci = s_cls[i];
+        const int lo = i + 1 - 64 * w;   // bits lo .. 63 (the table holds no bit at or above m)
+        unsigned long long match = lo >= 64 ? 0ull : s_tab[w * kBuckets + (ci & (kBuckets - 1))];
+        if (lo > 0) match &= ~((1ull << lo) - 1ull);
+        unsigned long long bits = 0;
+        if (match != 0ull) {
+            const float4 bi = s_box[i];
+            while (match != 0ull) {
+                const int bit = __ffsll((long long)match) - 1;
+                match &= match - 1ull;
+                const int j = 64 * w + bit;
+                if (s_cls[j] == ci && iou_above(bi, s_box[j], p.iou_thr)) bits |= 1ull << bit;
             }
-            if (hi < 64) match &= (1ull << hi) - 1ull;
-            match = lo >= 64 ? 0ull : match & ~((1ull << lo) - 1ull);
-            unsigned long long bits = 0;
-            if (match != 0ull) {
-                const float4 bi = s_box[i];
-                while (match != 0ull) {
-                    const int b = __ffsll((long long)match) - 1;
-                    match &= match - 1ull;
-                    if (iou_above(bi, s_box[64 * w + b], p.iou_thr)) bits |= 1ull << b;
-                }
-            }
-            s_m[(size_t)i * RS + w] = bits;
         }
+        s_m[(size_t)i * RS + w] = bits;
     }
     __syncthreads();
 
@@ -561,23 +661,16 @@ ws_status fill_params(const ws_detect_desc* d, int32_t batch, DetParams& p) {
     p.off_hist = (int)o;       o = align16(o + (256 + 8) * 4);
     p.off_u = (int)o;
     // the suppression matrix: max_cand rows of ceil(max_cand / 64) words, the
-    // row stride made odd
-    p.u_bytes = (int)((size_t)d->max_cand * (((d->max_cand + 63) / 64) | 1) * 8);
-    p.stage_cap = 0;
+    // row stride made odd; then the class-bucket match table
+    const int W = (d->max_cand + 63) / 64;
+    p.off_tab = (int)align16((size_t)d->max_cand * (W | 1) * 8);
+    p.u_bytes = p.off_tab + W * kBuckets * 8;
+    // the cap selection's per-warp histograms share this area
+    p.u_bytes = std::max(p.u_bytes, kNmsWarps * 256 * 4);
     return WS_OK;
 }
 
-// Staging room for the cap selection: as many keys as the device's shared
-// memory allows on top of the fixed layout, at most kStageCap.
-size_t nms_smem(DetParams& p, int smem_optin) {
-    p.stage_cap = 0;
-    if (p.A > p.max_cand) {
-        const long long room = ((long long)smem_optin - p.off_u) / 8;
-        p.stage_cap = (int)std::min<long long>(std::min<long long>(p.A, kStageCap), std::max(0LL, room));
-    }
-    const size_t u = std::max<size_t>((size_t)p.u_bytes, (size_t)p.stage_cap * 8);
-    return (size_t)p.off_u + u;
-}
+size_t nms_smem(const DetParams& p) { return (size_t)p.off_u + (size_t)p.u_bytes; }
 
 size_t det_workspace(const DetParams& p, int32_t batch) {
     return (size_t)(batch * 4 + 255) / 256 * 256 + (size_t)batch * p.A * sizeof(ws_candidate);
@@ -600,12 +693,12 @@ ws_status launch_decode(const DetParams& p, int32_t batch, cudaStream_t stream) 
 // The NMS is a programmatic dependent launch ("Streams, concurrency and CUDA
 // Graphs", PDL section): it may be scheduled while the decode drains and
 // waits in griddepcontrol.wait for the decode's results.
-ws_status launch_nms(DetParams p, int32_t batch, cudaStream_t stream) {
+ws_status launch_nms(const DetParams& p, int32_t batch, cudaStream_t stream) {
     int dev;
     const DeviceInfo* info;
     ws_status st = current_device_info(&dev, &info);
     if (st != WS_OK) return st;
-    const size_t smem = nms_smem(p, info->max_smem_optin);
+    const size_t smem = nms_smem(p);
     if (smem > (size_t)info->max_smem_optin) return fail(WS_ERR_UNSUPPORTED, "NMS needs %zu bytes of shared memory", smem);
     if (dev < 0 || dev >= 64) return fail(WS_ERR_UNSUPPORTED, "device ordinal %d", dev);
     if (!g_nms_attr_set[dev]) {
