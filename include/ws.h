@@ -298,8 +298,8 @@ ws_status ws_detect(const ws_detect_desc* desc, const float* head, int32_t batch
 #define WS_INPUT_MAPPED 1   /* producer writes mapped pinned host memory; the kernel reads it in place */
 #define WS_INPUT_COPY   2   /* producer writes pinned host memory; the graph copies it to the device first */
 
-#define WS_RESULT_DEVICE 0  /* Top-K result stays in device memory                   */
-#define WS_RESULT_MAPPED 1  /* Top-K kernel writes straight into mapped pinned host memory */
+#define WS_RESULT_DEVICE 0  /* result stays in device memory                         */
+#define WS_RESULT_MAPPED 1  /* the last kernel writes straight into mapped pinned host memory */
 #define WS_RESULT_COPY   2  /* result is copied into pinned host memory at the end of the graph */
 
 #define WS_LANE_FLAG_NO_GRAPH     1u  /* replay by direct launches instead of the CUDA Graph   */
@@ -313,6 +313,9 @@ ws_status ws_detect(const ws_detect_desc* desc, const float* head, int32_t batch
                                          it in flight and the "GPU" finishes after fake_polls
                                          completion queries.  Exercises the state machine on
                                          machines without a GPU. */
+
+#define WS_POST_TOPK   0    /* post-processing: exact Top-K of the logits (rows x cols) */
+#define WS_POST_DETECT 1    /* post-processing: DFL decode + class-aware NMS of a detection head */
 
 #define WS_LANE_FREE      0
 #define WS_LANE_ACQUIRED  1
@@ -338,6 +341,15 @@ typedef struct ws_lane_desc {
     int32_t* result_idx;          /* same, int32 [rows][k]                          */
     cudaStream_t stream;          /* NULL: the lane creates a non-blocking stream   */
     int32_t  fake_polls;          /* WS_LANE_FLAG_NO_DEVICE only                    */
+    int32_t  post;                /* WS_POST_TOPK or WS_POST_DETECT                 */
+    ws_detect_desc detect;        /* WS_POST_DETECT: geometry and thresholds.  The
+                                     logits slot then holds the head, float32
+                                     [batch][4 reg_max + num_classes][A]; rows, cols
+                                     and k are ignored and result_val / result_idx
+                                     must be NULL.                                 */
+    ws_detection* detections;     /* WS_POST_DETECT result [batch][detect.max_det],
+                                     memory as result_mode says (like result_val)  */
+    int32_t* det_count;           /* WS_POST_DETECT, int32 [batch]: kept per image  */
 } ws_lane_desc;
 
 typedef struct ws_lane ws_lane;
@@ -354,6 +366,10 @@ typedef struct ws_lane_buffers {
     int32_t* result_idx_device;
     size_t   input_bytes, tensor_bytes, logits_bytes, result_bytes;
     cudaStream_t stream;
+    ws_detection* detections_host;   /* WS_POST_DETECT: host view (MAPPED, COPY) or NULL */
+    int32_t* det_count_host;
+    ws_detection* detections_device; /* where the NMS kernel writes             */
+    int32_t* det_count_device;
 } ws_lane_buffers;
 
 /* Times of one completed submit. */
@@ -361,13 +377,15 @@ typedef struct ws_lane_timing {
     float  gpu_us;         /* event before the graph launch -> event after the last stage
                               (-1 on WS_LANE_FLAG_NO_TIMING lanes) */
     float  preprocess_us;  /* STAGE_TIMING lanes: preprocess kernel alone, else -1   */
-    float  topk_us;        /* STAGE_TIMING lanes: Top-K kernel alone, else -1        */
+    float  post_us;        /* STAGE_TIMING lanes: the post-processing stage alone
+                              (Top-K, or decode + NMS), else -1                    */
     double host_us;        /* steady clock, entry of submit -> return of wait       */
 } ws_lane_timing;
 
-/* Validate, allocate or borrow every buffer, run both kernels once directly
- * (which settles any lazy set-up), capture copy-in -> preprocess -> Top-K ->
- * copy-out into one graph on the lane's stream and instantiate it.  All
+/* Validate, allocate or borrow every buffer, run the path once directly
+ * (which settles any lazy set-up), capture copy-in -> preprocess -> Top-K (or
+ * decode -> NMS) -> copy-out into one graph on the lane's stream and
+ * instantiate it.  All
  * allocation of the lane's life happens here.  Must not be called while the
  * stream is being captured.  On failure everything made so far is released.
  * Errors: WS_ERR_INVALID_ARGUMENT, WS_ERR_OUT_OF_MEMORY, WS_ERR_CUDA,

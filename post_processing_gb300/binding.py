@@ -37,6 +37,7 @@ WS_LANE_FLAG_NO_GRAPH = 1
 WS_LANE_FLAG_STAGE_TIMING = 2
 WS_LANE_FLAG_NO_TIMING = 4
 WS_LANE_FLAG_NO_DEVICE = 8
+WS_POST_TOPK, WS_POST_DETECT = 0, 1
 WS_LANE_FREE, WS_LANE_ACQUIRED, WS_LANE_IN_FLIGHT = 0, 1, 2
 
 _i32, _i64, _u32, _f32 = ctypes.c_int32, ctypes.c_int64, ctypes.c_uint32, ctypes.c_float
@@ -50,28 +51,31 @@ class ws_preprocess_desc(ctypes.Structure):
                 ("dst_type", _i32)]
 
 
+class ws_detect_desc(ctypes.Structure):
+    _fields_ = [("in_w", _i32), ("in_h", _i32), ("nlevels", _i32), ("strides", _i32 * 4), ("reg_max", _i32),
+                ("num_classes", _i32), ("logit_thr", _f32), ("iou_thr", _f32), ("max_cand", _i32),
+                ("max_det", _i32)]
+
+
 class ws_lane_desc(ctypes.Structure):
     _fields_ = [("pre", ws_preprocess_desc), ("batch", _i32), ("rows", _i64), ("cols", _i64), ("k", _i32),
                 ("input_mode", _i32), ("result_mode", _i32), ("flags", _u32), ("input", _vp),
                 ("tensor", _vp), ("logits", _vp), ("result_val", _vp), ("result_idx", _vp),
-                ("stream", _vp), ("fake_polls", _i32)]
+                ("stream", _vp), ("fake_polls", _i32), ("post", _i32), ("detect", ws_detect_desc),
+                ("detections", _vp), ("det_count", _vp)]
 
 
 class ws_lane_buffers(ctypes.Structure):
     _fields_ = [("input_host", _vp), ("input_device", _vp), ("tensor", _vp), ("logits", _vp),
                 ("result_val_host", _vp), ("result_idx_host", _vp), ("result_val_device", _vp),
                 ("result_idx_device", _vp), ("input_bytes", _sz), ("tensor_bytes", _sz),
-                ("logits_bytes", _sz), ("result_bytes", _sz), ("stream", _vp)]
+                ("logits_bytes", _sz), ("result_bytes", _sz), ("stream", _vp),
+                ("detections_host", _vp), ("det_count_host", _vp), ("detections_device", _vp),
+                ("det_count_device", _vp)]
 
 
 class ws_lane_timing(ctypes.Structure):
-    _fields_ = [("gpu_us", _f32), ("preprocess_us", _f32), ("topk_us", _f32), ("host_us", ctypes.c_double)]
-
-
-class ws_detect_desc(ctypes.Structure):
-    _fields_ = [("in_w", _i32), ("in_h", _i32), ("nlevels", _i32), ("strides", _i32 * 4), ("reg_max", _i32),
-                ("num_classes", _i32), ("logit_thr", _f32), ("iou_thr", _f32), ("max_cand", _i32),
-                ("max_det", _i32)]
+    _fields_ = [("gpu_us", _f32), ("preprocess_us", _f32), ("post_us", _f32), ("host_us", ctypes.c_double)]
 
 
 class ws_candidate(ctypes.Structure):
@@ -305,7 +309,10 @@ def lane_desc(pre: ws_preprocess_desc, batch: int, rows: int, cols: int, k: int,
               input_mode: int = WS_INPUT_DEVICE, result_mode: int = WS_RESULT_DEVICE, flags: int = 0,
               input: int | None = None, tensor: int | None = None, logits: int | None = None,
               result_val: int | None = None, result_idx: int | None = None, stream: int | None = None,
-              fake_polls: int = 0) -> ws_lane_desc:
+              fake_polls: int = 0, detect: ws_detect_desc | None = None, detections: int | None = None,
+              det_count: int | None = None) -> ws_lane_desc:
+    """A lane descriptor; with `detect` the lane post-processes a detection head
+    (rows, cols and k are then ignored)."""
     d = ws_lane_desc()
     d.pre = pre
     d.batch, d.rows, d.cols, d.k = batch, rows, cols, k
@@ -313,4 +320,7 @@ def lane_desc(pre: ws_preprocess_desc, batch: int, rows: int, cols: int, k: int,
     d.input, d.tensor, d.logits = input, tensor, logits
     d.result_val, d.result_idx, d.stream = result_val, result_idx, stream
     d.fake_polls = fake_polls
+    if detect is not None:
+        d.post, d.detect = WS_POST_DETECT, detect
+        d.detections, d.det_count = detections, det_count
     return d

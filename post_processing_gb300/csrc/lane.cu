@@ -11,7 +11,10 @@
 // (CUDA handbook, CUDA Graphs section): fixed addresses, capture once,
 // instantiate once, nothing synchronising inside the graph.  The network
 // between the two stages is not part of this library: its slot in the graph
-// is the logits buffer, which the caller fills.
+// is the logits buffer, which the caller fills.  The post-processing stage is
+// the Top-K of the logits or, for a detection lane (yolo.cu README: decode,
+// bitonic sort and greedy suppression inside the graph), the DFL decode and
+// NMS of the head held in that slot.
 #include <chrono>
 #include <cstring>
 #include <new>
@@ -34,10 +37,12 @@ struct ws_lane {
     bool own_tensor = false;
     float* logits = nullptr;
     bool own_logits = false;
-    float* rv_host = nullptr;
-    int32_t* ri_host = nullptr;
-    float* rv_dev = nullptr;
-    int32_t* ri_dev = nullptr;
+    // result slots: Top-K values / indices, or detections / per-image counts
+    void* rv_host = nullptr;
+    void* ri_host = nullptr;
+    void* rv_dev = nullptr;
+    void* ri_dev = nullptr;
+    size_t rv_bytes = 0, ri_bytes = 0;
     bool own_r_host = false, own_r_dev = false;
     void* ws = nullptr;
     size_t ws_bytes = 0;
@@ -45,7 +50,7 @@ struct ws_lane {
     size_t input_bytes = 0, tensor_bytes = 0, logits_bytes = 0, result_bytes = 0;
 
     cudaEvent_t ev_start = nullptr, ev_end = nullptr;
-    cudaEvent_t ev_pre0 = nullptr, ev_pre1 = nullptr, ev_topk1 = nullptr;
+    cudaEvent_t ev_pre0 = nullptr, ev_pre1 = nullptr, ev_post1 = nullptr;
     cudaGraph_t graph = nullptr;
     cudaGraphExec_t exec = nullptr;
     std::chrono::steady_clock::time_point t_submit;
@@ -57,12 +62,13 @@ namespace {
 bool stage_timing(const ws_lane* L) { return (L->d.flags & WS_LANE_FLAG_STAGE_TIMING) != 0; }
 bool submit_timing(const ws_lane* L) { return (L->d.flags & WS_LANE_FLAG_NO_TIMING) == 0; }
 bool use_graph(const ws_lane* L) { return (L->d.flags & WS_LANE_FLAG_NO_GRAPH) == 0; }
+bool detecting(const ws_lane* L) { return L->d.post == WS_POST_DETECT; }
 
 void release_all(ws_lane* L) {
     if (L->fake) return;
     if (L->exec) cudaGraphExecDestroy(L->exec);
     if (L->graph) cudaGraphDestroy(L->graph);
-    for (cudaEvent_t e : {L->ev_start, L->ev_end, L->ev_pre0, L->ev_pre1, L->ev_topk1})
+    for (cudaEvent_t e : {L->ev_start, L->ev_end, L->ev_pre0, L->ev_pre1, L->ev_post1})
         if (e) cudaEventDestroy(e);
     if (L->ws) cudaFree(L->ws);
     if (L->own_r_dev) {
@@ -122,13 +128,17 @@ ws_status enqueue_path(ws_lane* L, bool capturing) {
     st = ws_preprocess(&L->d.pre, static_cast<const uint8_t*>(L->in_dev), L->d.batch, L->tensor, L->stream);
     if (st != WS_OK) return st;
     if (stage_timing(L) && (st = record(L->ev_pre1, L->stream, capturing)) != WS_OK) return st;
-    st = ws_topk(L->logits, L->d.rows, L->d.cols, L->d.k, L->rv_dev, L->ri_dev, L->ws, L->ws_bytes, L->stream);
+    if (detecting(L))
+        st = ws_detect(&L->d.detect, L->logits, L->d.batch, static_cast<ws_detection*>(L->rv_dev),
+                       static_cast<int32_t*>(L->ri_dev), L->ws, L->ws_bytes, L->stream);
+    else
+        st = ws_topk(L->logits, L->d.rows, L->d.cols, L->d.k, static_cast<float*>(L->rv_dev),
+                     static_cast<int32_t*>(L->ri_dev), L->ws, L->ws_bytes, L->stream);
     if (st != WS_OK) return st;
-    if (stage_timing(L) && (st = record(L->ev_topk1, L->stream, capturing)) != WS_OK) return st;
+    if (stage_timing(L) && (st = record(L->ev_post1, L->stream, capturing)) != WS_OK) return st;
     if (L->d.result_mode == WS_RESULT_COPY) {
-        const size_t n = (size_t)L->d.rows * L->d.k;
-        WS_TRY_CUDA(cudaMemcpyAsync(L->rv_host, L->rv_dev, n * 4, cudaMemcpyDeviceToHost, L->stream));
-        WS_TRY_CUDA(cudaMemcpyAsync(L->ri_host, L->ri_dev, n * 4, cudaMemcpyDeviceToHost, L->stream));
+        WS_TRY_CUDA(cudaMemcpyAsync(L->rv_host, L->rv_dev, L->rv_bytes, cudaMemcpyDeviceToHost, L->stream));
+        WS_TRY_CUDA(cudaMemcpyAsync(L->ri_host, L->ri_dev, L->ri_bytes, cudaMemcpyDeviceToHost, L->stream));
     }
     return WS_OK;
 }
@@ -145,8 +155,21 @@ ws_status build(ws_lane* L) {
     L->input_bytes = (size_t)d.batch * (size_t)d.pre.src_frame_stride;
     const size_t elem = d.pre.dst_type == WS_DTYPE_F32 ? 4 : 2;
     L->tensor_bytes = (size_t)d.batch * 3 * d.pre.dst_h * d.pre.dst_w * elem;
-    L->logits_bytes = (size_t)d.rows * d.cols * sizeof(float);
-    L->result_bytes = (size_t)d.rows * d.k * sizeof(float);
+    void* borrowed_rv = d.result_val;
+    void* borrowed_ri = d.result_idx;
+    if (detecting(L)) {
+        int64_t A = 0;
+        if ((st = ws_detect_validate(&d.detect, d.batch, &A)) != WS_OK) return st;
+        L->logits_bytes = (size_t)d.batch * (4 * d.detect.reg_max + d.detect.num_classes) * (size_t)A * sizeof(float);
+        L->rv_bytes = (size_t)d.batch * d.detect.max_det * sizeof(ws_detection);
+        L->ri_bytes = (size_t)d.batch * sizeof(int32_t);
+        borrowed_rv = d.detections;
+        borrowed_ri = d.det_count;
+    } else {
+        L->logits_bytes = (size_t)d.rows * d.cols * sizeof(float);
+        L->rv_bytes = L->ri_bytes = (size_t)d.rows * d.k * sizeof(float);
+    }
+    L->result_bytes = L->rv_bytes;
 
     // producer slot
     switch (d.input_mode) {
@@ -198,16 +221,14 @@ ws_status build(ws_lane* L) {
     }
 
     // result slot
-    if ((d.result_val == nullptr) != (d.result_idx == nullptr))
-        return fail(WS_ERR_INVALID_ARGUMENT, "result_val and result_idx must both be given or both NULL");
     switch (d.result_mode) {
         case WS_RESULT_DEVICE:
-            if (d.result_val) {
-                L->rv_dev = d.result_val;
-                L->ri_dev = d.result_idx;
+            if (borrowed_rv) {
+                L->rv_dev = borrowed_rv;
+                L->ri_dev = borrowed_ri;
             } else {
-                if ((st = alloc_dev((void**)&L->rv_dev, L->result_bytes, "result")) != WS_OK) return st;
-                if ((st = alloc_dev((void**)&L->ri_dev, L->result_bytes, "result")) != WS_OK) {
+                if ((st = alloc_dev(&L->rv_dev, L->rv_bytes, "result")) != WS_OK) return st;
+                if ((st = alloc_dev(&L->ri_dev, L->ri_bytes, "result")) != WS_OK) {
                     cudaFree(L->rv_dev);
                     L->rv_dev = nullptr;
                     return st;
@@ -218,12 +239,12 @@ ws_status build(ws_lane* L) {
         case WS_RESULT_MAPPED:
         case WS_RESULT_COPY: {
             const unsigned flags = d.result_mode == WS_RESULT_MAPPED ? cudaHostAllocMapped : cudaHostAllocDefault;
-            if (d.result_val) {
-                L->rv_host = d.result_val;
-                L->ri_host = d.result_idx;
+            if (borrowed_rv) {
+                L->rv_host = borrowed_rv;
+                L->ri_host = borrowed_ri;
             } else {
-                if ((st = alloc_host((void**)&L->rv_host, L->result_bytes, flags, "result")) != WS_OK) return st;
-                if ((st = alloc_host((void**)&L->ri_host, L->result_bytes, flags, "result")) != WS_OK) {
+                if ((st = alloc_host(&L->rv_host, L->rv_bytes, flags, "result")) != WS_OK) return st;
+                if ((st = alloc_host(&L->ri_host, L->ri_bytes, flags, "result")) != WS_OK) {
                     cudaFreeHost(L->rv_host);
                     L->rv_host = nullptr;
                     return st;
@@ -231,11 +252,11 @@ ws_status build(ws_lane* L) {
                 L->own_r_host = true;
             }
             if (d.result_mode == WS_RESULT_MAPPED) {
-                if ((st = device_view(L->rv_host, (void**)&L->rv_dev, "result_val")) != WS_OK) return st;
-                if ((st = device_view(L->ri_host, (void**)&L->ri_dev, "result_idx")) != WS_OK) return st;
+                if ((st = device_view(L->rv_host, &L->rv_dev, "result")) != WS_OK) return st;
+                if ((st = device_view(L->ri_host, &L->ri_dev, "result")) != WS_OK) return st;
             } else {
-                if ((st = alloc_dev((void**)&L->rv_dev, L->result_bytes, "result")) != WS_OK) return st;
-                if ((st = alloc_dev((void**)&L->ri_dev, L->result_bytes, "result")) != WS_OK) {
+                if ((st = alloc_dev(&L->rv_dev, L->rv_bytes, "result")) != WS_OK) return st;
+                if ((st = alloc_dev(&L->ri_dev, L->ri_bytes, "result")) != WS_OK) {
                     cudaFree(L->rv_dev);
                     L->rv_dev = nullptr;
                     return st;
@@ -248,9 +269,13 @@ ws_status build(ws_lane* L) {
             return fail(WS_ERR_INVALID_ARGUMENT, "result mode %d", d.result_mode);
     }
 
-    L->ws_bytes = topk_workspace_size(d.rows, d.cols, d.k);
-    if (L->ws_bytes) {
-        if ((st = alloc_dev(&L->ws, L->ws_bytes, "top-k workspace")) != WS_OK) return st;
+    if (detecting(L)) {
+        if ((st = ws_detect_workspace_bytes(&d.detect, d.batch, &L->ws_bytes)) != WS_OK) return st;
+    } else {
+        L->ws_bytes = topk_workspace_size(d.rows, d.cols, d.k);
+    }
+    if (L->ws_bytes) {   // cudaMalloc's alignment covers both workspaces' 256-byte rule
+        if ((st = alloc_dev(&L->ws, L->ws_bytes, "post-processing workspace")) != WS_OK) return st;
         WS_TRY_CUDA(cudaMemsetAsync(L->ws, 0, L->ws_bytes, L->stream));
     }
 
@@ -264,7 +289,7 @@ ws_status build(ws_lane* L) {
     if (stage_timing(L)) {
         WS_TRY_CUDA(cudaEventCreate(&L->ev_pre0));
         WS_TRY_CUDA(cudaEventCreate(&L->ev_pre1));
-        WS_TRY_CUDA(cudaEventCreate(&L->ev_topk1));
+        WS_TRY_CUDA(cudaEventCreate(&L->ev_post1));
     }
 
     // Warm direct run: settles lazy module loading and kernel attributes
@@ -295,7 +320,19 @@ ws_status validate_lane(const ws_lane_desc* d) {
     if (!d) return fail(WS_ERR_INVALID_ARGUMENT, "descriptor is NULL");
     ws_status st = validate_preprocess(&d->pre, d->batch);
     if (st != WS_OK) return st;
-    if ((st = validate_topk(d->rows, d->cols, d->k)) != WS_OK) return st;
+    if (d->post == WS_POST_DETECT) {
+        if ((st = ws_detect_validate(&d->detect, d->batch, nullptr)) != WS_OK) return st;
+        if (d->result_val || d->result_idx)
+            return fail(WS_ERR_INVALID_ARGUMENT, "a detection lane takes detections / det_count, not result_val / result_idx");
+        if ((d->detections == nullptr) != (d->det_count == nullptr))
+            return fail(WS_ERR_INVALID_ARGUMENT, "detections and det_count must both be given or both NULL");
+    } else if (d->post == WS_POST_TOPK) {
+        if ((st = validate_topk(d->rows, d->cols, d->k)) != WS_OK) return st;
+        if ((d->result_val == nullptr) != (d->result_idx == nullptr))
+            return fail(WS_ERR_INVALID_ARGUMENT, "result_val and result_idx must both be given or both NULL");
+    } else {
+        return fail(WS_ERR_INVALID_ARGUMENT, "post-processing kind %d", d->post);
+    }
     if (d->input_mode < WS_INPUT_DEVICE || d->input_mode > WS_INPUT_COPY)
         return fail(WS_ERR_INVALID_ARGUMENT, "input mode %d", d->input_mode);
     if (d->result_mode < WS_RESULT_DEVICE || d->result_mode > WS_RESULT_COPY)
@@ -348,10 +385,17 @@ ws_status ws_lane_get_buffers(const ws_lane* L, ws_lane_buffers* b) {
     b->input_device = L->in_dev;
     b->tensor = L->tensor;
     b->logits = L->logits;
-    b->result_val_host = L->rv_host;
-    b->result_idx_host = L->ri_host;
-    b->result_val_device = L->rv_dev;
-    b->result_idx_device = L->ri_dev;
+    if (L->d.post == WS_POST_DETECT) {
+        b->detections_host = static_cast<ws_detection*>(L->rv_host);
+        b->det_count_host = static_cast<int32_t*>(L->ri_host);
+        b->detections_device = static_cast<ws_detection*>(L->rv_dev);
+        b->det_count_device = static_cast<int32_t*>(L->ri_dev);
+    } else {
+        b->result_val_host = static_cast<float*>(L->rv_host);
+        b->result_idx_host = static_cast<int32_t*>(L->ri_host);
+        b->result_val_device = static_cast<float*>(L->rv_dev);
+        b->result_idx_device = static_cast<int32_t*>(L->ri_dev);
+    }
     b->input_bytes = L->input_bytes;
     b->tensor_bytes = L->tensor_bytes;
     b->logits_bytes = L->logits_bytes;
@@ -436,7 +480,7 @@ ws_status ws_lane_wait(ws_lane* L, int64_t timeout_us, ws_lane_timing* timing) {
     const auto t1 = std::chrono::steady_clock::now();
     if (timing) {
         timing->host_us = std::chrono::duration<double, std::micro>(t1 - L->t_submit).count();
-        timing->gpu_us = timing->preprocess_us = timing->topk_us = -1.f;
+        timing->gpu_us = timing->preprocess_us = timing->post_us = -1.f;
         if (!L->fake) {
             float ms = 0.f;
             if (submit_timing(L) && cudaEventElapsedTime(&ms, L->ev_start, L->ev_end) == cudaSuccess)
@@ -444,8 +488,8 @@ ws_status ws_lane_wait(ws_lane* L, int64_t timeout_us, ws_lane_timing* timing) {
             if (stage_timing(L)) {
                 if (cudaEventElapsedTime(&ms, L->ev_pre0, L->ev_pre1) == cudaSuccess)
                     timing->preprocess_us = ms * 1000.f;
-                if (cudaEventElapsedTime(&ms, L->ev_pre1, L->ev_topk1) == cudaSuccess)
-                    timing->topk_us = ms * 1000.f;
+                if (cudaEventElapsedTime(&ms, L->ev_pre1, L->ev_post1) == cudaSuccess)
+                    timing->post_us = ms * 1000.f;
             }
             cudaGetLastError();
         }

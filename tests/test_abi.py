@@ -155,6 +155,22 @@ def test_lane_descriptor_rejected(B):
         assert st == B.WS_ERR_INVALID_ARGUMENT and h is None, kw
 
 
+def test_detection_lane_descriptor(B):
+    pre = B.preprocess_desc(1280, 720, 640, 640, letterbox=True, norm="scale")
+    fake = dict(flags=B.WS_LANE_FLAG_NO_DEVICE)
+    st, h = B.ws_lane_create(B.lane_desc(pre, 2, 0, 0, 0, detect=B.detect_desc(), **fake))
+    assert st == B.WS_OK and h is not None
+    assert B.ws_lane_destroy(h) == B.WS_OK
+    bad = [B.lane_desc(pre, 2, 0, 0, 0, detect=B.detect_desc(max_det=0), **fake),
+           B.lane_desc(pre, 2, 0, 0, 0, detect=B.detect_desc(), result_val=64, result_idx=64, **fake),
+           B.lane_desc(pre, 2, 0, 0, 0, detect=B.detect_desc(), detections=64, **fake)]
+    odd = B.lane_desc(pre, 1, 1, 100, 5, **fake)
+    odd.post = 7
+    for d in bad + [odd]:
+        st, h = B.ws_lane_create(d)
+        assert st == B.WS_ERR_INVALID_ARGUMENT and h is None
+
+
 def test_product_does_not_import_the_oracle():
     pkg = os.path.join(ROOT, "post_processing_gb300")
     for dirpath, _, files in os.walk(pkg):

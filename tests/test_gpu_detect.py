@@ -7,11 +7,14 @@ the kept list is exact -- the IoU test is FP32 with every operation rounded
 separately on both sides.  End to end, ws_detect equals the oracle's NMS of
 the candidates the GPU decoded.
 """
+import ctypes
+
 import numpy as np
 import pytest
 import torch
 
 import synth
+from cudart import memcpy
 
 pytestmark = pytest.mark.gpu
 BOX_TOL = 2e-4
@@ -259,3 +262,47 @@ def test_detect_no_candidates_and_all_candidates(B, oracle):
     keep = oracle.nms(dec["boxes"], dec["f4"], dec["cls"], dec["anchor"], desc.iou_thr, desc.max_det, desc.max_cand)
     got = unpack(out.cpu().numpy()[0, :int(oc[0])])
     assert list(got["anchor"]) == [int(dec["anchor"][j]) for j in keep]
+
+
+@pytest.mark.parametrize("result_mode,flags", [(0, 0), (1, 0), (2, 2), (0, 1)],
+                         ids=["device", "mapped", "copy-stage-timing", "no-graph"])
+def test_detection_lane(B, oracle, result_mode, flags):
+    """A lane whose graph is letterbox preprocess -> decode -> NMS; the head in
+    its logits slot changes between submits."""
+    from post_processing_gb300.api import Lane
+    desc = B.detect_desc()
+    pre = B.preprocess_desc(1280, 720, 640, 640, letterbox=True, norm="scale")
+    batch = 2
+    d = B.lane_desc(pre, batch, 0, 0, 0, detect=desc, result_mode=result_mode, flags=flags)
+    with Lane(d) as lane:
+        buf = lane.buffers
+        assert buf.result_val_device is None and buf.detections_device
+        n_head = buf.logits_bytes // 4
+        for rep in range(2):
+            head = synth.yolo_head(80 + rep, batch)
+            assert head.size == n_head
+            hdev = torch.from_numpy(head).cuda()
+            memcpy(buf.logits, hdev.data_ptr(), head.nbytes)
+            lane.acquire()
+            lane.submit()
+            t = lane.wait()
+            if flags & B.WS_LANE_FLAG_STAGE_TIMING:
+                assert t.preprocess_us > 0 and t.post_us > 0
+            if result_mode == B.WS_RESULT_DEVICE:
+                dets = torch.empty((batch, desc.max_det, 8), dtype=torch.int32, device="cuda")
+                cnts = torch.empty(batch, dtype=torch.int32, device="cuda")
+                memcpy(dets.data_ptr(), buf.detections_device, dets.numel() * 4)
+                memcpy(cnts.data_ptr(), buf.det_count_device, batch * 4)
+                o, k = dets.cpu().numpy(), cnts.cpu().numpy()
+            else:
+                raw = ctypes.string_at(buf.detections_host, batch * desc.max_det * 32)
+                o = np.frombuffer(raw, np.int32).reshape(batch, desc.max_det, 8)
+                k = np.frombuffer(ctypes.string_at(buf.det_count_host, batch * 4), np.int32)
+            dec = gpu_decode(B, desc, head)
+            for b in range(batch):
+                c = dec[b]
+                keep = oracle.nms(c["boxes"], c["f4"], c["cls"], c["anchor"], desc.iou_thr, desc.max_det,
+                                  desc.max_cand)
+                got = unpack(o[b, :k[b]])
+                assert list(got["anchor"]) == [int(c["anchor"][j]) for j in keep]
+                assert np.array_equal(got["boxes"].view(np.uint32), c["boxes"][keep].view(np.uint32))

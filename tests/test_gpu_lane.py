@@ -76,7 +76,7 @@ def test_lane_parity(B, oracle, name, mode):
             lane.acquire()
             lane.submit()
             t = lane.wait()
-            assert t.gpu_us > 0 and t.preprocess_us > 0 and t.topk_us > 0 and t.host_us > 0
+            assert t.gpu_us > 0 and t.preprocess_us > 0 and t.post_us > 0 and t.host_us > 0
             tensor, v, i = read_lane(B, lane, w["batch"], w["dst_h"], w["dst_w"], w["rows"], w["k"])
             want = oracle.preprocess(frames, w["src_w"], w["src_h"], w["dst_w"], w["dst_h"],
                                      letterbox=w["resize"] == "letterbox", norm=w["norm"])
