@@ -14,7 +14,9 @@ HBM-throughput configuration.  Also measured on every run:
 * the roofline of the dominant kernel (the preprocess): its average launch
   duration from CUDA events around back-to-back launches on the lanes'
   buffers, against the measured HBM copy bandwidth;
-* the CPU oracle on the host cores (a bounded sample), as a reported baseline.
+* the CPU oracle on the host cores (a bounded sample), as a reported baseline;
+* detection decode + NMS of a YOLO-style 640x640 head: batch-64 throughput,
+  the decode kernel's HBM rate, and batch-1 latency through a detection lane.
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
        [--workload NAME] [--latency-samples S] [--no-cpu-baseline]
@@ -253,6 +255,121 @@ def run_reference(args, w: dict) -> None:
     print(json.dumps(line), flush=True)
 
 
+DETECT_BATCH = 64
+DETECT_SEED = 0x57A70D00
+
+
+def detect_measurements(B, Lane, device, stream, samples: int) -> dict:
+    """Detection decode + NMS (the next-row extension of the hot path).
+
+    Workload: a YOLO-style head for a 640x640 input (strides 8/16/32, 8400
+    anchors, reg_max 16, 80 classes), DFL logits N(0, 2) and class logits
+    N(-8, 2) -- about 2 % of the anchors clear conf 0.25; IoU 0.45,
+    max_cand 1024, max_det 300.  Batch 64 for throughput and the decode
+    roofline (two heads alternate, 620 MB > L2), batch 1 through a detection
+    lane (720p letterbox -> 640 preprocess, decode, NMS) for latency."""
+    import torch
+    desc = B.detect_desc()
+    st, A = B.ws_detect_validate(desc, DETECT_BATCH)
+    B.check(st)
+    t0 = time.perf_counter()
+    head = synth.yolo_head(DETECT_SEED, DETECT_BATCH)
+    heads = [torch.from_numpy(head).to(device), torch.from_numpy(head[::-1].copy()).to(device)]
+    log(f"[bench] detection heads generated in {time.perf_counter() - t0:.1f} s")
+    st, nws = B.ws_detect_workspace_bytes(desc, DETECT_BATCH)
+    B.check(st)
+    ws = torch.zeros(nws + 256, dtype=torch.uint8, device=device)
+    wp = ws.data_ptr() + (-ws.data_ptr()) % 256
+    out = torch.zeros((DETECT_BATCH, desc.max_det, 8), dtype=torch.int32, device=device)
+    oc = torch.zeros(DETECT_BATCH, dtype=torch.int32, device=device)
+    cand = torch.zeros((DETECT_BATCH, A, 8), dtype=torch.int32, device=device)
+    cnt = torch.zeros(DETECT_BATCH, dtype=torch.int32, device=device)
+    s = stream.cuda_stream
+
+    def full(i):
+        B.check(B.ws_detect(desc, heads[i % 2].data_ptr(), DETECT_BATCH, out.data_ptr(), oc.data_ptr(), wp, nws, s))
+
+    def timed(fn, n):
+        for i in range(8):
+            fn(i)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        e0.record(stream)
+        for i in range(n):
+            fn(i)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) * 1000.0 / n
+
+    n = 500
+    detect_us = timed(full, n)
+    # the decode kernel alone, each launch between its own events; the NMS
+    # (which resets the counters) follows outside them
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+    for i in range(8):
+        B.check(B.ws_detect_decode(desc, heads[i % 2].data_ptr(), DETECT_BATCH, cand.data_ptr(), cnt.data_ptr(), s))
+        B.check(B.ws_detect_nms(desc, cand.data_ptr(), cnt.data_ptr(), DETECT_BATCH, out.data_ptr(), oc.data_ptr(), s))
+    torch.cuda.synchronize()
+    for i, (a, b) in enumerate(evs):
+        a.record(stream)
+        B.check(B.ws_detect_decode(desc, heads[i % 2].data_ptr(), DETECT_BATCH, cand.data_ptr(), cnt.data_ptr(), s))
+        b.record(stream)
+        B.check(B.ws_detect_nms(desc, cand.data_ptr(), cnt.data_ptr(), DETECT_BATCH, out.data_ptr(), oc.data_ptr(), s))
+    torch.cuda.synchronize()
+    decode_us = statistics.mean(a.elapsed_time(b) * 1000.0 for a, b in evs)
+    # candidate count of the timed heads (decode once more, read the counters)
+    with torch.cuda.stream(stream):
+        B.check(B.ws_detect_decode(desc, heads[0].data_ptr(), DETECT_BATCH, cand.data_ptr(), cnt.data_ptr(), s))
+        stream.synchronize()
+        n_cand = int(cnt.sum())
+        B.check(B.ws_detect_nms(desc, cand.data_ptr(), cnt.data_ptr(), DETECT_BATCH, out.data_ptr(), oc.data_ptr(), s))
+        stream.synchronize()
+    kept = int(oc.sum())
+    R, C = desc.reg_max, desc.num_classes
+    # class logits once, each candidate's 4 R DFL logits as the 32-byte
+    # sectors they sit in (A-strided rows: one sector each), its 32-byte record
+    alg_decode = DETECT_BATCH * C * A * 4 + n_cand * (4 * R * 32 + 32) + DETECT_BATCH * 4
+
+    # batch-1 latency through a detection lane
+    pre = B.preprocess_desc(1280, 720, 640, 640, letterbox=True, norm="scale")
+    frame = torch.from_numpy(synth.frames_uniform(DETECT_SEED, 1, 720, 1280)).to(device)
+    head1 = torch.from_numpy(head[:1].copy()).to(device)
+    lat = {}
+    warm = min(200, samples)
+    for label, flags in (("graph", 0), ("graph_no_timing", B.WS_LANE_FLAG_NO_TIMING)):
+        d = B.lane_desc(pre, 1, 0, 0, 0, input=frame.data_ptr(), logits=head1.data_ptr(), detect=desc, flags=flags)
+        with Lane(d) as lane:
+            gpu, host = [], []
+            for i in range(warm + samples):
+                lane.acquire()
+                lane.submit()
+                t = lane.wait()
+                if i >= warm:
+                    gpu.append(t.gpu_us)
+                    host.append(t.host_us)
+            lat[label] = {"host_us": percentiles(host)}
+            if not flags & B.WS_LANE_FLAG_NO_TIMING:
+                lat[label]["gpu_us"] = percentiles(gpu)
+    return {
+        "workload": "YOLO-style head 640x640 (8400 anchors, reg_max 16, 80 classes), conf 0.25, IoU 0.45, "
+                    "max_cand 1024, max_det 300; synthetic head DFL N(0,2), class N(-8,2)",
+        "batch": DETECT_BATCH,
+        "images_per_s": DETECT_BATCH / (detect_us * 1e-6),
+        "detect_us": detect_us,
+        "decode_us": decode_us,
+        "nms_us_by_difference": detect_us - decode_us,
+        "candidates_per_image": n_cand / DETECT_BATCH,
+        "kept_per_image": kept / DETECT_BATCH,
+        "decode_roofline": {"bound": "hbm", "kernels": "class scan + DFL boxes (ws_detect_decode)",
+                            "algorithmic_bytes_per_launch": alg_decode,
+                            "bytes_rule": "class plane + 32-byte sector per DFL logit of each candidate + "
+                                          "32-byte candidate record",
+                            "achieved_gbs": alg_decode / (decode_us * 1e-6) / 1e9},
+        "latency_b1_lane": dict(lat, samples=samples, warmup=warm,
+                                path="720p letterbox -> 640 preprocess, decode, NMS in one lane graph"),
+    }
+
+
 def workload_config(name: str, w: dict) -> dict:
     return {"workload": f"{w['batch']}x {w['src_w']}x{w['src_h']} RGB8 -> "
                         f"{'letterbox ' if w['resize'] == 'letterbox' else ''}{w['dst_w']}x{w['dst_h']} "
@@ -283,6 +400,7 @@ def main():
     ap.add_argument("--latency-samples", type=int, default=10000)
     ap.add_argument("--e2e-steps", type=int, default=60)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-detect", action="store_true", help="skip the detection decode + NMS measurements")
     ap.add_argument("--out-dtype", default="f32", choices=["f32", "f16", "bf16"],
                     help="element type of the NCHW tensor (the workloads specify FP32)")
     args = ap.parse_args()
@@ -432,6 +550,9 @@ def main():
             latency[label] = {"host_us": percentiles(host)}
             if flags & B.WS_LANE_FLAG_NO_TIMING == 0:
                 latency[label]["gpu_us"] = percentiles(gpu)
+    detect = None
+    if not args.no_detect:
+        detect = detect_measurements(B, Lane, device, stream, min(2000, args.latency_samples))
     clk = clocks.stop()
 
     # End to end through the lane API with host buffers: the producer writes
@@ -517,12 +638,17 @@ def main():
                          "topk_avg_launch_us": topk_avg_us,
                          "topk_gbs": alg["topk"] / (topk_avg_us * 1e-6) / 1e9},
             "latency_b1": latency,
+            "detect": detect,
             "e2e": e2e,
             "gpu_launches": 2 * args.steps,
             "clocks": clk,
             "cpu_baseline": cpu,
         }
         line["roofline"]["frac_note"] = "of measured" if peak_src == "measured" else "of fallback"
+        if detect:
+            r = detect["decode_roofline"]
+            r.update(peak=peak, unit="GB/s", frac=r["achieved_gbs"] / peak,
+                     frac_note="of measured" if peak_src == "measured" else "of fallback")
         print(json.dumps(line), flush=True)
     if world > 1:
         torch.distributed.destroy_process_group()

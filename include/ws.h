@@ -271,7 +271,8 @@ ws_status ws_detect_workspace_init(void* workspace, size_t bytes, cudaStream_t s
 
 /* Decode only.  cand: device ws_candidate [batch][A] (in no particular order);
  * count: device int32 [batch], which must be zero on entry; receives each
- * image's number of candidates (at most A).  One kernel launch. */
+ * image's number of candidates (at most A).  Two kernel launches: the class
+ * scan, then the DFL boxes of its candidates (a programmatic dependent). */
 ws_status ws_detect_decode(const ws_detect_desc* desc, const float* head, int32_t batch,
                            ws_candidate* cand, int32_t* count, cudaStream_t stream);
 
@@ -284,8 +285,9 @@ ws_status ws_detect_decode(const ws_detect_desc* desc, const float* head, int32_
 ws_status ws_detect_nms(const ws_detect_desc* desc, ws_candidate* cand, int32_t* count, int32_t batch,
                         ws_detection* out, int32_t* out_count, cudaStream_t stream);
 
-/* Decode + NMS with the candidates in `workspace`.  Two kernel launches, the
- * NMS a programmatic dependent launch of the decode.
+/* Decode + NMS with the candidates in `workspace`.  Three kernel launches
+ * (class scan, DFL boxes, NMS), each after the first a programmatic dependent
+ * launch of the one before.
  * Errors: WS_ERR_INVALID_ARGUMENT (descriptor, pointers, workspace too
  * small), WS_ERR_CUDA (launch failed). */
 ws_status ws_detect(const ws_detect_desc* desc, const float* head, int32_t batch,

@@ -8,16 +8,17 @@
 // formula are stated in include/ws.h next to ws_detect_desc.
 //
 // How:
-//  * decode: a block takes 128 consecutive anchors, 4 per lane; its 8 warps
-//    split the classes (warp g scans classes g, g + 8, ...), each load a
-//    coalesced 512-byte row segment (16 bytes a lane), and 128 threads merge
-//    the 8 partial arg-maxes.  Only
-//    anchors whose best logit clears the threshold (about 2 % of them) go on
-//    to the DFL: one thread per (candidate, side) loads that side's reg_max
-//    logits and takes the softmax expectation.  One atomic per block reserves
-//    the block's candidate slots.
+//  * decode: a class scan, one block per tile of 128 consecutive anchors
+//    (4 per lane); its 8 warps split the classes (warp g scans classes
+//    g, g + 8, ...), each load a coalesced 512-byte row segment (16 bytes a
+//    lane, 5 in flight), and 128 threads merge the 8 partial arg-maxes.  One atomic per block reserves
+//    slots for the anchors whose best logit clears the threshold (about 2 %
+//    of them).  A second kernel, a programmatic dependent of the scan, takes
+//    those candidates' DFL: four threads per candidate, one per side, load
+//    that side's reg_max logits and take the softmax expectation.  Keeping
+//    these scattered loads out of the scan keeps the scan a pure stream.
 //  * NMS: one block per image, launched as a programmatic dependent of the
-//    decode so its launch overlaps the decode's tail.  If the image has more
+//    DFL kernel so its launch overlaps the decode's tail.  If the image has more
 //    than max_cand candidates, their 64-bit keys (logit order bits, then the
 //    complemented anchor) are held in registers and a radix select
 //    (warp-aggregated histogram counts, early exit once a digit bin closes
@@ -34,6 +35,7 @@
 #include <algorithm>
 #include <cmath>
 
+
 #include "ws_internal.cuh"
 
 namespace ws {
@@ -41,6 +43,9 @@ namespace {
 
 constexpr int kDecodeThreads = 256;
 constexpr int kDecodeAnchors = 128;                    // anchors per decode block (4 per lane)
+constexpr int kDflBlocks = 8;                          // DFL blocks per image
+constexpr int kScanLoads = 5;                          // 16-byte loads in flight per lane
+constexpr int kScanBlocksPerSM = 6;                    // register budget: 6 blocks of 256 per SM
 constexpr int kClassGroups = kDecodeThreads / 32;      // warps splitting the classes
 constexpr int kNmsThreads = 512;
 constexpr int kNmsWarps = kNmsThreads / 32;
@@ -87,51 +92,112 @@ __device__ __forceinline__ unsigned long long cand_key(const ws_candidate* c) {
     return ((unsigned long long)order_bits(c->logit) << 32) | (uint32_t)(~(uint32_t)c->anchor);
 }
 
-// One block: kDecodeAnchors anchors.  Thread (g, t) of warp g scans classes
-// g, g + 8, ... of anchors 4t .. 4t + 3 (one 16-byte load each when kVec).
+// What a scan block shares while it finishes a tile.
+struct ScanShared {
+    float v[kClassGroups][kDecodeAnchors];   // per-warp arg-max values
+    int c[kClassGroups][kDecodeAnchors];     // and classes
+    int off[kDecodeAnchors];                 // anchor offset (in the tile) of the q-th candidate
+    float best[kDecodeAnchors];
+    int cls[kDecodeAnchors];
+    int wcnt[kDecodeAnchors / 32];
+    int n, base;
+};
+
+__device__ __forceinline__ void take4(float (&best)[4], int (&bc)[4], const float4 v4, int c) {
+    const float v[4] = {nan_as_ninf(v4.x), nan_as_ninf(v4.y), nan_as_ninf(v4.z), nan_as_ninf(v4.w)};
+#pragma unroll
+    for (int e = 0; e < 4; ++e)
+        if (v[e] > best[e]) {
+            best[e] = v[e];
+            bc[e] = c;
+        }
+}
+
+// Merge the 8 warps' partial arg-maxes of a tile (thread t < kDecodeAnchors
+// owns anchor a0 + t), reserve the tile's candidate slots with one atomic and
+// write their class, logit and anchor (the DFL kernel adds the boxes).
+// Called by the whole block.
+__device__ __forceinline__ void finish_tile(const DetParams& p, ScanShared& sh, int b, long long a0,
+                                            const float (&best)[4], const int (&bc)[4]) {
+    const int tid = threadIdx.x, lane = tid & 31, g = tid >> 5;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        sh.v[g][4 * lane + e] = best[e];
+        sh.c[g][4 * lane + e] = bc[e];
+    }
+    __syncthreads();
+    bool is_cand = false;
+    float bt = -INFINITY;
+    int ct = 0;
+    if (tid < kDecodeAnchors) {
+        bt = sh.v[0][tid];
+        ct = sh.c[0][tid];
+#pragma unroll
+        for (int q = 1; q < kClassGroups; ++q) {
+            const float v = sh.v[q][tid];
+            const int c = sh.c[q][tid];
+            if (v > bt || (v == bt && c < ct)) {
+                bt = v;
+                ct = c;
+            }
+        }
+        is_cand = a0 + tid < p.A && bt > p.logit_thr;
+    }
+    const unsigned bal = __ballot_sync(kFull, is_cand);
+    if (tid < kDecodeAnchors && lane == 0) sh.wcnt[g] = __popc(bal);
+    __syncthreads();
+    if (tid < kDecodeAnchors) {
+        int before = __popc(bal & ((1u << lane) - 1u));
+        for (int w = 0; w < g; ++w) before += sh.wcnt[w];
+        if (is_cand) {
+            sh.off[before] = tid;
+            sh.best[before] = bt;
+            sh.cls[before] = ct;
+        }
+        if (tid == 0) {
+            int n = 0;
+            for (int w = 0; w < kDecodeAnchors / 32; ++w) n += sh.wcnt[w];
+            sh.n = n;
+            sh.base = n ? atomicAdd(&p.count[b], n) : 0;
+        }
+    }
+    __syncthreads();
+    for (int q = tid; q < sh.n; q += kDecodeThreads) {
+        const int slot = sh.base + q;
+        if (slot < p.A) {
+            float4* dst = reinterpret_cast<float4*>(p.cand + (size_t)b * p.A + slot);
+            dst[1] = make_float4(sh.best[q], __int_as_float(sh.cls[q]), __int_as_float((int)(a0 + sh.off[q])), 0.f);
+        }
+    }
+    // the next tile writes sh only after a barrier of its own
+}
+
+// Class scan with plain loads, one tile per block.  kVec (A % 4 == 0,
+// 16-byte aligned head): a lane loads its 4 anchors' logits as one 16-byte
+// word, kLoads classes in flight; else one anchor at a time, any alignment.
 template <bool kVec>
-__global__ void __launch_bounds__(kDecodeThreads, 4) detect_decode_kernel(const __grid_constant__ DetParams p) {
-    __shared__ float s_v[kClassGroups][kDecodeAnchors];
-    __shared__ int s_c[kClassGroups][kDecodeAnchors];
-    __shared__ int s_off[kDecodeAnchors];     // anchor offset (in the block) of the q-th candidate
-    __shared__ float s_best[kDecodeAnchors];
-    __shared__ int s_cls[kDecodeAnchors];
-    __shared__ float s_dist[kDecodeAnchors][4];
-    __shared__ int s_wcnt[kDecodeAnchors / 32];
-    __shared__ int s_n, s_base;
-
-    const int b = blockIdx.y, tid = threadIdx.x, lane = tid & 31, g = tid >> 5;
+__global__ void __launch_bounds__(kDecodeThreads, kScanBlocksPerSM) detect_scan_kernel(const __grid_constant__ DetParams p) {
+    __shared__ ScanShared sh;
+    const int b = blockIdx.y, lane = threadIdx.x & 31, g = threadIdx.x >> 5;
     const long long a0 = (long long)blockIdx.x * kDecodeAnchors;
-    const float* hb = p.head + (size_t)b * p.ch * p.A;
-    const float* cl = hb + (size_t)(4 * p.R) * p.A;
-
-    // 1. arg-max over this warp's classes for 4 anchors; NaN as -inf, the lower class on ties
+    const long long a4 = a0 + 4 * lane;
+    const float* cl = p.head + (size_t)b * p.ch * p.A + (size_t)(4 * p.R) * p.A;
     float best[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
     int bc[4] = {g, g, g, g};
-    const long long a4 = a0 + 4 * lane;
     if (kVec) {
         if (a4 < p.A) {   // A % 4 == 0: all four anchors exist
-            auto take = [&](const float4 v4, int c) {
-                const float v[4] = {nan_as_ninf(v4.x), nan_as_ninf(v4.y), nan_as_ninf(v4.z), nan_as_ninf(v4.w)};
-#pragma unroll
-                for (int e = 0; e < 4; ++e)
-                    if (v[e] > best[e]) {
-                        best[e] = v[e];
-                        bc[e] = c;
-                    }
-            };
             const float* col = cl + a4;
             int c = g;
-            constexpr int kU = 5;   // loads in flight per thread
-            for (; c + (kU - 1) * kClassGroups < p.C; c += kU * kClassGroups) {
-                float4 v4[kU];
+            for (; c + (kScanLoads - 1) * kClassGroups < p.C; c += kScanLoads * kClassGroups) {
+                float4 v4[kScanLoads];
 #pragma unroll
-                for (int u = 0; u < kU; ++u)
+                for (int u = 0; u < kScanLoads; ++u)
                     v4[u] = __ldg(reinterpret_cast<const float4*>(col + (size_t)(c + u * kClassGroups) * p.A));
 #pragma unroll
-                for (int u = 0; u < kU; ++u) take(v4[u], c + u * kClassGroups);
+                for (int u = 0; u < kScanLoads; ++u) take4(best, bc, v4[u], c + u * kClassGroups);
             }
-            for (; c < p.C; c += kClassGroups) take(__ldg(reinterpret_cast<const float4*>(col + (size_t)c * p.A)), c);
+            for (; c < p.C; c += kClassGroups)
+                take4(best, bc, __ldg(reinterpret_cast<const float4*>(col + (size_t)c * p.A)), c);
         }
     } else {
 #pragma unroll 2
@@ -149,98 +215,58 @@ __global__ void __launch_bounds__(kDecodeThreads, 4) detect_decode_kernel(const 
             }
         }
     }
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-        s_v[g][4 * lane + e] = best[e];
-        s_c[g][4 * lane + e] = bc[e];
-    }
-    __syncthreads();
-
-    // 2. merge the warps' partial arg-maxes: thread t < kDecodeAnchors owns anchor a0 + t
-    bool is_cand = false;
-    float bt = -INFINITY;
-    int ct = 0;
-    if (tid < kDecodeAnchors) {
-        bt = s_v[0][tid];
-        ct = s_c[0][tid];
-#pragma unroll
-        for (int q = 1; q < kClassGroups; ++q) {
-            const float v = s_v[q][tid];
-            const int c = s_c[q][tid];
-            if (v > bt || (v == bt && c < ct)) {
-                bt = v;
-                ct = c;
-            }
-        }
-        is_cand = a0 + tid < p.A && bt > p.logit_thr;
-    }
-    const unsigned bal = __ballot_sync(kFull, is_cand);
-    if (tid < kDecodeAnchors && lane == 0) s_wcnt[g] = __popc(bal);
-    __syncthreads();
-    if (tid < kDecodeAnchors) {
-        int before = __popc(bal & ((1u << lane) - 1u));
-        for (int w = 0; w < g; ++w) before += s_wcnt[w];
-        if (is_cand) {
-            s_off[before] = tid;
-            s_best[before] = bt;
-            s_cls[before] = ct;
-        }
-        if (tid == 0) {
-            int n = 0;
-            for (int w = 0; w < kDecodeAnchors / 32; ++w) n += s_wcnt[w];
-            s_n = n;
-            s_base = n ? atomicAdd(&p.count[b], n) : 0;
-        }
-    }
-    __syncthreads();
-    // the NMS may start launching: what is left here is a few loads per block
+    finish_tile(p, sh, b, a0, best, bc);
     asm volatile("griddepcontrol.launch_dependents;");
-    const int n = s_n;
-    if (n == 0) return;
+}
 
-    // 3. DFL: the expected bin of each side's softmax, one thread per (candidate, side)
-    for (int t = tid; t < 4 * n; t += kDecodeThreads) {
+// DFL box decode of the candidates the scan found: four consecutive threads
+// take one candidate's four sides (the expected bin of each side's softmax
+// over its reg_max logits), the first of them writes the box.  A grid of
+// kDflBlocks x batch blocks strides over each image's candidates.
+__global__ void __launch_bounds__(kDecodeThreads) detect_dfl_kernel(const __grid_constant__ DetParams p) {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;");   // the NMS waits for this grid anyway
+    const int b = blockIdx.y, lane = threadIdx.x & 31;
+    const int n = (int)min((long long)p.count[b], p.A);
+    const float* hb = p.head + (size_t)b * p.ch * p.A;
+    ws_candidate* cb = p.cand + (size_t)b * p.A;
+    const int tasks = (4 * n + 31) & ~31;   // whole warps, for the shuffles
+    for (int t = blockIdx.x * kDecodeThreads + threadIdx.x; t < tasks; t += gridDim.x * kDecodeThreads) {
         const int q = t >> 2, side = t & 3;
-        const float* z = hb + (size_t)(side * p.R) * p.A + (a0 + s_off[q]);
-        float v[kMaxRegMax];
+        float dist = 0.f;
+        int a = 0;
+        if (q < n) {
+            a = cb[q].anchor;
+            const float* z = hb + (size_t)(side * p.R) * p.A + a;
+            float v[kMaxRegMax];
 #pragma unroll
-        for (int i = 0; i < kMaxRegMax; ++i) v[i] = i < p.R ? __ldg(z + (size_t)i * p.A) : -INFINITY;
-        float m = -INFINITY;
+            for (int i = 0; i < kMaxRegMax; ++i) v[i] = i < p.R ? __ldg(z + (size_t)i * p.A) : -INFINITY;
+            float m = -INFINITY;
 #pragma unroll
-        for (int i = 0; i < kMaxRegMax; ++i) m = fmaxf(m, v[i]);
-        float zs = 0.f, es = 0.f;
+            for (int i = 0; i < kMaxRegMax; ++i) m = fmaxf(m, v[i]);
+            float zs = 0.f, es = 0.f;
 #pragma unroll
-        for (int i = 0; i < kMaxRegMax; ++i) {
-            if (i < p.R) {
-                const float w = expf(v[i] - m);
-                zs += w;
-                es += w * (float)i;
+            for (int i = 0; i < kMaxRegMax; ++i) {
+                if (i < p.R) {
+                    const float w = expf(v[i] - m);
+                    zs += w;
+                    es += w * (float)i;
+                }
             }
+            dist = es / zs;
         }
-        s_dist[q][side] = es / zs;
-    }
-    __syncthreads();
-
-    // 4. boxes around the anchor centres, into the reserved slots
-    for (int q = tid; q < n; q += kDecodeThreads) {
-        const long long aq = a0 + s_off[q];
-        int l = 0;
-        while (l + 1 < p.nlevels && aq >= p.off[l + 1]) ++l;
-        const long long k = aq - p.off[l];
-        const float s = (float)p.stride[l];
-        const float cx = ((float)(k % p.gw[l]) + 0.5f) * s;
-        const float cy = ((float)(k / p.gw[l]) + 0.5f) * s;
-        float4 box;
-        box.x = cx - s_dist[q][0] * s;
-        box.y = cy - s_dist[q][1] * s;
-        box.z = cx + s_dist[q][2] * s;
-        box.w = cy + s_dist[q][3] * s;
-        const int slot = s_base + q;
-        if (slot < p.A) {
-            float4* dst = reinterpret_cast<float4*>(p.cand + (size_t)b * p.A + slot);
-            dst[0] = box;
-            dst[1] = make_float4(s_best[q], __int_as_float(s_cls[q]), __int_as_float((int)aq), 0.f);
+        const float d1 = __shfl_down_sync(kFull, dist, 1), d2 = __shfl_down_sync(kFull, dist, 2),
+                    d3 = __shfl_down_sync(kFull, dist, 3);
+        if (q < n && side == 0) {
+            int l = 0;
+            while (l + 1 < p.nlevels && a >= p.off[l + 1]) ++l;
+            const long long k = a - p.off[l];
+            const float s = (float)p.stride[l];
+            const float cx = ((float)(k % p.gw[l]) + 0.5f) * s;
+            const float cy = ((float)(k / p.gw[l]) + 0.5f) * s;
+            reinterpret_cast<float4*>(cb + q)[0] = make_float4(cx - dist * s, cy - d1 * s, cx + d2 * s, cy + d3 * s);
         }
+        (void)lane;
     }
 }
 
@@ -678,15 +704,29 @@ size_t det_workspace(const DetParams& p, int32_t batch) {
 
 bool g_nms_attr_set[64];
 
-ws_status launch_decode(const DetParams& p, int32_t batch, cudaStream_t stream) {
-    const dim3 grid((unsigned)((p.A + kDecodeAnchors - 1) / kDecodeAnchors), (unsigned)batch);
+ws_status launch_decode(DetParams p, int32_t batch, cudaStream_t stream) {
+    const int tiles = (int)((p.A + kDecodeAnchors - 1) / kDecodeAnchors);
     const bool vec = p.A % 4 == 0 && (uintptr_t)p.head % 16 == 0;
-    if (vec)
-        detect_decode_kernel<true><<<grid, kDecodeThreads, 0, stream>>>(p);
-    else
-        detect_decode_kernel<false><<<grid, kDecodeThreads, 0, stream>>>(p);
+    if (vec) {
+        detect_scan_kernel<true><<<dim3((unsigned)tiles, (unsigned)batch), kDecodeThreads, 0, stream>>>(p);
+    } else {
+        detect_scan_kernel<false><<<dim3((unsigned)tiles, (unsigned)batch), kDecodeThreads, 0, stream>>>(p);
+    }
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e, "decode launch");
+    // the DFL boxes, a programmatic dependent of the scan
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(kDflBlocks, (unsigned)batch);
+    cfg.blockDim = dim3(kDecodeThreads);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, detect_dfl_kernel, p);
+    if (e == cudaSuccess) e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(e, "DFL launch");
     return WS_OK;
 }
 
