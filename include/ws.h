@@ -315,6 +315,16 @@ ws_status ws_detect(const ws_detect_desc* desc, const float* head, int32_t batch
                                          it in flight and the "GPU" finishes after fake_polls
                                          completion queries.  Exercises the state machine on
                                          machines without a GPU. */
+#define WS_LANE_FLAG_NVTX        16u  /* NVTX ranges (domain "ws") around create, submit, wait and
+                                         rebind, for a profiler's timeline ("Inside WarpStream
+                                         TRT", next steps: NVTX instrumentation) */
+#define WS_LANE_FLAG_BUCKETS     32u  /* one graph per batch bucket 1, 2, 4, ... below batch, plus
+                                         batch itself; ws_lane_submit_n(n) replays the smallest
+                                         bucket that holds n frames ("Streams, concurrency and
+                                         CUDA Graphs", CUDA Graphs: one graph per batch-size
+                                         bucket, the real batch rounded up).  A Top-K lane needs
+                                         rows a multiple of batch (per-frame rows scale with
+                                         the bucket); a detection lane takes one head per frame. */
 
 #define WS_POST_TOPK   0    /* post-processing: exact Top-K of the logits (rows x cols) */
 #define WS_POST_DETECT 1    /* post-processing: DFL decode + class-aware NMS of a detection head */
@@ -405,6 +415,30 @@ ws_status ws_lane_acquire(ws_lane* lane);
  * then returns to ACQUIRED). */
 ws_status ws_lane_submit(ws_lane* lane);
 
+/* As ws_lane_submit, for the first n frames (1 <= n <= batch): a bucketed lane
+ * replays the smallest bucket of at least n frames (frames past n in it are
+ * processed as they are and their results are to be ignored); otherwise the
+ * whole batch is replayed.  Results for the first n frames (rows) are valid. */
+ws_status ws_lane_submit_n(ws_lane* lane, int32_t n);
+
+/* Point the lane at a new producer slot and / or logits slot without
+ * rebuilding it: input is, per input_mode, a device buffer (DEVICE), the host
+ * pointer of a mapped pinned allocation (MAPPED) or pinned host memory (COPY),
+ * with the lane's frame layout; logits is a device buffer of the lane's
+ * logits (or head) shape.  NULL keeps the current one.  The new buffers are
+ * borrowed and must outlive their use.  Each bucket's graph is re-captured
+ * and its executable graph updated in place with cudaGraphExecUpdate ("Streams,
+ * concurrency and CUDA Graphs", CUDA Graphs); only if the update is refused is
+ * it re-instantiated, which *reinstantiated (if not NULL) reports.  Buffers the
+ * lane allocated itself stay allocated until ws_lane_destroy.  This is how a
+ * producer that writes into its own device memory (a decoder's or camera's
+ * GPUDirect buffers) registers them with a lane.
+ * WS_ERR_LANE_BUSY while in flight; WS_ERR_INVALID_ARGUMENT for a MAPPED input
+ * that is not mapped pinned memory (the lane is unchanged); WS_ERR_CAPTURE if
+ * a capture or instantiation fails, after which the lane may only be
+ * destroyed. */
+ws_status ws_lane_rebind(ws_lane* lane, void* input, float* logits, int32_t* reinstantiated);
+
 /* IN_FLIGHT -> FREE once the end event has completed.  timeout_us < 0 waits
  * without limit; otherwise WS_ERR_TIMEOUT after timeout_us microseconds, with
  * the lane still IN_FLIGHT (call again).  timing may be NULL.
@@ -420,6 +454,43 @@ ws_status ws_lane_destroy(ws_lane* lane);
 
 /* WS_LANE_FREE / ACQUIRED / IN_FLIGHT, or -1 for NULL. */
 int32_t ws_lane_state(const ws_lane* lane);
+
+/* -------------------------------------------------------------- lane pool */
+
+/* N identical lanes with a producer / consumer hand-off ("Inside WarpStream
+ * TRT", lane and state-machine sections: several lanes keep the GPU busy while
+ * the host fills and drains others; a busy lane is reported, not waited on).
+ * A lane goes: free -> acquired (ws_pool_acquire; the producer fills its
+ * input / logits slots) -> submitted (ws_pool_submit) -> completed
+ * (ws_pool_complete, oldest submission first; its results are readable and it
+ * is held) -> free (ws_pool_recycle).  Any number of producer threads and one
+ * consumer thread at a time may call concurrently.  Timeouts: < 0 waits
+ * without limit, 0 does not wait. */
+typedef struct ws_pool ws_pool;
+
+/* `lanes` (1 .. 64) lanes from one descriptor; its buffer pointers must be
+ * NULL (every lane owns its buffers).  Errors as ws_lane_create. */
+ws_status ws_pool_create(const ws_lane_desc* desc, int32_t lanes, ws_pool** pool);
+
+/* Lane i of the pool (for ws_lane_get_buffers). */
+ws_status ws_pool_lane(const ws_pool* pool, int32_t i, ws_lane** lane);
+
+/* A free lane, acquired; WS_ERR_TIMEOUT if none became free in time. */
+ws_status ws_pool_acquire(ws_pool* pool, int64_t timeout_us, ws_lane** lane);
+
+/* ws_lane_submit_n on an acquired pool lane; on failure it stays acquired. */
+ws_status ws_pool_submit(ws_pool* pool, ws_lane* lane, int32_t n);
+
+/* Waits for the oldest submitted lane; *lane is it, completed and held.
+ * WS_ERR_TIMEOUT if nothing completed in time; WS_ERR_CUDA if its GPU work
+ * failed (it is still returned, held, its results undefined). */
+ws_status ws_pool_complete(ws_pool* pool, int64_t timeout_us, ws_lane** lane, ws_lane_timing* timing);
+
+/* A held (or an acquired, unsubmitted) lane back to the free list. */
+ws_status ws_pool_recycle(ws_pool* pool, ws_lane* lane);
+
+/* Destroys every lane; WS_ERR_LANE_BUSY while any is submitted. */
+ws_status ws_pool_destroy(ws_pool* pool);
 
 #ifdef __cplusplus
 }

@@ -75,8 +75,17 @@ class Lane:
     def acquire(self):
         B.check(B.ws_lane_acquire(self.handle))
 
-    def submit(self):
-        B.check(B.ws_lane_submit(self.handle))
+    def submit(self, n: int | None = None):
+        """Submit the whole batch, or the first n frames (ws_lane_submit_n)."""
+        B.check(B.ws_lane_submit(self.handle) if n is None else B.ws_lane_submit_n(self.handle, n))
+
+    def rebind(self, input: int | None = None, logits: int | None = None) -> bool:
+        """Point the lane at new slots; True if a graph was re-instantiated."""
+        st, re = B.ws_lane_rebind(self.handle, input, logits)
+        B.check(st)
+        st, self.buffers = B.ws_lane_get_buffers(self.handle)
+        B.check(st)
+        return bool(re)
 
     def wait(self, timeout_us: int = -1) -> B.ws_lane_timing:
         st, t = B.ws_lane_wait(self.handle, timeout_us)

@@ -37,6 +37,8 @@ WS_LANE_FLAG_NO_GRAPH = 1
 WS_LANE_FLAG_STAGE_TIMING = 2
 WS_LANE_FLAG_NO_TIMING = 4
 WS_LANE_FLAG_NO_DEVICE = 8
+WS_LANE_FLAG_NVTX = 16
+WS_LANE_FLAG_BUCKETS = 32
 WS_POST_TOPK, WS_POST_DETECT = 0, 1
 WS_LANE_FREE, WS_LANE_ACQUIRED, WS_LANE_IN_FLIGHT = 0, 1, 2
 
@@ -111,10 +113,19 @@ SIGNATURES = {
     "ws_lane_get_buffers": (_i32, [_vp, ctypes.POINTER(ws_lane_buffers)]),
     "ws_lane_acquire": (_i32, [_vp]),
     "ws_lane_submit": (_i32, [_vp]),
+    "ws_lane_submit_n": (_i32, [_vp, _i32]),
+    "ws_lane_rebind": (_i32, [_vp, _vp, _vp, ctypes.POINTER(_i32)]),
     "ws_lane_wait": (_i32, [_vp, _i64, ctypes.POINTER(ws_lane_timing)]),
     "ws_lane_release": (_i32, [_vp]),
     "ws_lane_destroy": (_i32, [_vp]),
     "ws_lane_state": (_i32, [_vp]),
+    "ws_pool_create": (_i32, [ctypes.POINTER(ws_lane_desc), _i32, ctypes.POINTER(_vp)]),
+    "ws_pool_lane": (_i32, [_vp, _i32, ctypes.POINTER(_vp)]),
+    "ws_pool_acquire": (_i32, [_vp, _i64, ctypes.POINTER(_vp)]),
+    "ws_pool_submit": (_i32, [_vp, _vp, _i32]),
+    "ws_pool_complete": (_i32, [_vp, _i64, ctypes.POINTER(_vp), ctypes.POINTER(ws_lane_timing)]),
+    "ws_pool_recycle": (_i32, [_vp, _vp]),
+    "ws_pool_destroy": (_i32, [_vp]),
 }
 
 
@@ -265,6 +276,17 @@ def ws_lane_submit(lane: int) -> int:
     return lib.ws_lane_submit(lane)
 
 
+def ws_lane_submit_n(lane: int, n: int) -> int:
+    return lib.ws_lane_submit_n(lane, n)
+
+
+def ws_lane_rebind(lane: int, input: int | None = None, logits: int | None = None) -> tuple[int, int]:
+    """(status, 1 if an executable graph had to be re-instantiated else 0)."""
+    r = _i32(0)
+    st = lib.ws_lane_rebind(lane, input, logits, ctypes.byref(r))
+    return st, r.value
+
+
 def ws_lane_wait(lane: int, timeout_us: int = -1) -> tuple[int, ws_lane_timing]:
     t = ws_lane_timing()
     st = lib.ws_lane_wait(lane, timeout_us, ctypes.byref(t))
@@ -324,3 +346,40 @@ def lane_desc(pre: ws_preprocess_desc, batch: int, rows: int, cols: int, k: int,
         d.post, d.detect = WS_POST_DETECT, detect
         d.detections, d.det_count = detections, det_count
     return d
+
+
+def ws_pool_create(desc: ws_lane_desc, lanes: int) -> tuple[int, int | None]:
+    h = _vp()
+    st = lib.ws_pool_create(ctypes.byref(desc), lanes, ctypes.byref(h))
+    return st, h.value
+
+
+def ws_pool_lane(pool: int, i: int) -> tuple[int, int | None]:
+    h = _vp()
+    st = lib.ws_pool_lane(pool, i, ctypes.byref(h))
+    return st, h.value
+
+
+def ws_pool_acquire(pool: int, timeout_us: int = -1) -> tuple[int, int | None]:
+    h = _vp()
+    st = lib.ws_pool_acquire(pool, timeout_us, ctypes.byref(h))
+    return st, h.value
+
+
+def ws_pool_submit(pool: int, lane: int, n: int) -> int:
+    return lib.ws_pool_submit(pool, lane, n)
+
+
+def ws_pool_complete(pool: int, timeout_us: int = -1) -> tuple[int, int | None, ws_lane_timing]:
+    h = _vp()
+    t = ws_lane_timing()
+    st = lib.ws_pool_complete(pool, timeout_us, ctypes.byref(h), ctypes.byref(t))
+    return st, h.value, t
+
+
+def ws_pool_recycle(pool: int, lane: int) -> int:
+    return lib.ws_pool_recycle(pool, lane)
+
+
+def ws_pool_destroy(pool: int) -> int:
+    return lib.ws_pool_destroy(pool)

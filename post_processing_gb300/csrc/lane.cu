@@ -19,7 +19,11 @@
 #include <cstring>
 #include <new>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include "ws_internal.cuh"
+
+constexpr int kMaxBuckets = 17;   // batch sizes 1, 2, 4, ..., 2^15 and the lane's own
 
 struct ws_lane {
     ws_lane_desc d{};
@@ -32,11 +36,14 @@ struct ws_lane {
 
     void* in_host = nullptr;       // MAPPED / COPY: host view
     void* in_dev = nullptr;        // what the preprocess reads
-    bool own_in_host = false, own_in_dev = false;
+    // what the lane allocated itself (freed at destroy); in_host, in_dev and
+    // logits are the current bindings, which ws_lane_rebind may change
+    void* owned_in_host = nullptr;
+    void* owned_in_dev = nullptr;
     void* tensor = nullptr;
     bool own_tensor = false;
     float* logits = nullptr;
-    bool own_logits = false;
+    float* owned_logits = nullptr;
     // result slots: Top-K values / indices, or detections / per-image counts
     void* rv_host = nullptr;
     void* ri_host = nullptr;
@@ -44,15 +51,22 @@ struct ws_lane {
     void* ri_dev = nullptr;
     size_t rv_bytes = 0, ri_bytes = 0;
     bool own_r_host = false, own_r_dev = false;
-    void* ws = nullptr;
-    size_t ws_bytes = 0;
+    // one post-processing workspace per bucket: a call with a smaller batch
+    // lays its workspace out differently, and each layout must keep its own
+    // counters at zero between calls
+    void* ws[kMaxBuckets] = {};
+    size_t ws_bytes[kMaxBuckets] = {};
 
     size_t input_bytes = 0, tensor_bytes = 0, logits_bytes = 0, result_bytes = 0;
 
     cudaEvent_t ev_start = nullptr, ev_end = nullptr;
     cudaEvent_t ev_pre0 = nullptr, ev_pre1 = nullptr, ev_post1 = nullptr;
-    cudaGraph_t graph = nullptr;
-    cudaGraphExec_t exec = nullptr;
+    // batch buckets: bucket i replays bucket_batch[i] frames (the last is the
+    // lane's batch); one captured graph and one executable graph per bucket
+    int nbuckets = 1;
+    int bucket_batch[kMaxBuckets] = {};
+    cudaGraph_t graph[kMaxBuckets] = {};
+    cudaGraphExec_t exec[kMaxBuckets] = {};
     std::chrono::steady_clock::time_point t_submit;
 };
 
@@ -64,13 +78,44 @@ bool submit_timing(const ws_lane* L) { return (L->d.flags & WS_LANE_FLAG_NO_TIMI
 bool use_graph(const ws_lane* L) { return (L->d.flags & WS_LANE_FLAG_NO_GRAPH) == 0; }
 bool detecting(const ws_lane* L) { return L->d.post == WS_POST_DETECT; }
 
+// NVTX ranges in the "ws" domain (WS_LANE_FLAG_NVTX): host-side spans of the
+// lane calls, visible to a profiler that is attached; a no-op otherwise.
+nvtxDomainHandle_t nvtx_domain() {
+    static nvtxDomainHandle_t d = nvtxDomainCreateA("ws");
+    return d;
+}
+
+struct NvtxRange {
+    bool on;
+    NvtxRange(const ws_lane* L, const char* name) : on(L && (L->d.flags & WS_LANE_FLAG_NVTX)) {
+        if (!on) return;
+        nvtxEventAttributes_t a{};
+        a.version = NVTX_VERSION;
+        a.size = NVTX_EVENT_ATTRIB_STRUCT_SIZE;
+        a.messageType = NVTX_MESSAGE_TYPE_ASCII;
+        a.message.ascii = name;
+        nvtxDomainRangePushEx(nvtx_domain(), &a);
+    }
+    ~NvtxRange() {
+        if (on) nvtxDomainRangePop(nvtx_domain());
+    }
+};
+
+// Rows of the logits a bucket of nb frames post-processes: per-frame rows
+// scale with the batch; a lane that is not bucketed always takes all rows.
+int64_t bucket_rows(const ws_lane* L, int nb) {
+    return nb == L->d.batch ? L->d.rows : L->d.rows / L->d.batch * nb;
+}
+
 void release_all(ws_lane* L) {
     if (L->fake) return;
-    if (L->exec) cudaGraphExecDestroy(L->exec);
-    if (L->graph) cudaGraphDestroy(L->graph);
+    for (int i = 0; i < kMaxBuckets; ++i) {
+        if (L->exec[i]) cudaGraphExecDestroy(L->exec[i]);
+        if (L->graph[i]) cudaGraphDestroy(L->graph[i]);
+        if (L->ws[i]) cudaFree(L->ws[i]);
+    }
     for (cudaEvent_t e : {L->ev_start, L->ev_end, L->ev_pre0, L->ev_pre1, L->ev_post1})
         if (e) cudaEventDestroy(e);
-    if (L->ws) cudaFree(L->ws);
     if (L->own_r_dev) {
         cudaFree(L->rv_dev);
         cudaFree(L->ri_dev);
@@ -79,10 +124,10 @@ void release_all(ws_lane* L) {
         cudaFreeHost(L->rv_host);
         cudaFreeHost(L->ri_host);
     }
-    if (L->own_logits) cudaFree(L->logits);
+    if (L->owned_logits) cudaFree(L->owned_logits);
     if (L->own_tensor) cudaFree(L->tensor);
-    if (L->own_in_dev) cudaFree(L->in_dev);
-    if (L->own_in_host) cudaFreeHost(L->in_host);
+    if (L->owned_in_dev) cudaFree(L->owned_in_dev);
+    if (L->owned_in_host) cudaFreeHost(L->owned_in_host);
     if (L->own_stream) cudaStreamDestroy(L->stream);
 }
 
@@ -118,28 +163,63 @@ ws_status record(cudaEvent_t ev, cudaStream_t s, bool capturing) {
     return WS_OK;
 }
 
-// The lane's whole path, enqueued on its stream: captured once into the
-// graph, and also used directly for the warm-up and NO_GRAPH lanes.
-ws_status enqueue_path(ws_lane* L, bool capturing) {
+// The lane's whole path for bucket bi (its first bucket_batch[bi] frames),
+// enqueued on its stream: captured once into the bucket's graph, and also
+// used directly for the warm-up and NO_GRAPH lanes.
+ws_status enqueue_path(ws_lane* L, bool capturing, int bi) {
     ws_status st;
+    const int nb = L->bucket_batch[bi];
+    const int64_t rows = bucket_rows(L, nb);
     if (L->d.input_mode == WS_INPUT_COPY)
-        WS_TRY_CUDA(cudaMemcpyAsync(L->in_dev, L->in_host, L->input_bytes, cudaMemcpyHostToDevice, L->stream));
+        WS_TRY_CUDA(cudaMemcpyAsync(L->in_dev, L->in_host, L->input_bytes / L->d.batch * nb, cudaMemcpyHostToDevice,
+                                    L->stream));
     if (stage_timing(L) && (st = record(L->ev_pre0, L->stream, capturing)) != WS_OK) return st;
-    st = ws_preprocess(&L->d.pre, static_cast<const uint8_t*>(L->in_dev), L->d.batch, L->tensor, L->stream);
+    st = ws_preprocess(&L->d.pre, static_cast<const uint8_t*>(L->in_dev), nb, L->tensor, L->stream);
     if (st != WS_OK) return st;
     if (stage_timing(L) && (st = record(L->ev_pre1, L->stream, capturing)) != WS_OK) return st;
-    if (detecting(L))
-        st = ws_detect(&L->d.detect, L->logits, L->d.batch, static_cast<ws_detection*>(L->rv_dev),
-                       static_cast<int32_t*>(L->ri_dev), L->ws, L->ws_bytes, L->stream);
-    else
-        st = ws_topk(L->logits, L->d.rows, L->d.cols, L->d.k, static_cast<float*>(L->rv_dev),
-                     static_cast<int32_t*>(L->ri_dev), L->ws, L->ws_bytes, L->stream);
+    size_t rv = L->rv_bytes, ri = L->ri_bytes;
+    if (detecting(L)) {
+        st = ws_detect(&L->d.detect, L->logits, nb, static_cast<ws_detection*>(L->rv_dev),
+                       static_cast<int32_t*>(L->ri_dev), L->ws[bi], L->ws_bytes[bi], L->stream);
+        rv = rv / L->d.batch * nb;
+        ri = ri / L->d.batch * nb;
+    } else {
+        st = ws_topk(L->logits, rows, L->d.cols, L->d.k, static_cast<float*>(L->rv_dev),
+                     static_cast<int32_t*>(L->ri_dev), L->ws[bi], L->ws_bytes[bi], L->stream);
+        rv = ri = (size_t)rows * L->d.k * sizeof(float);
+    }
     if (st != WS_OK) return st;
     if (stage_timing(L) && (st = record(L->ev_post1, L->stream, capturing)) != WS_OK) return st;
     if (L->d.result_mode == WS_RESULT_COPY) {
-        WS_TRY_CUDA(cudaMemcpyAsync(L->rv_host, L->rv_dev, L->rv_bytes, cudaMemcpyDeviceToHost, L->stream));
-        WS_TRY_CUDA(cudaMemcpyAsync(L->ri_host, L->ri_dev, L->ri_bytes, cudaMemcpyDeviceToHost, L->stream));
+        WS_TRY_CUDA(cudaMemcpyAsync(L->rv_host, L->rv_dev, rv, cudaMemcpyDeviceToHost, L->stream));
+        WS_TRY_CUDA(cudaMemcpyAsync(L->ri_host, L->ri_dev, ri, cudaMemcpyDeviceToHost, L->stream));
     }
+    return WS_OK;
+}
+
+// Capture bucket bi's path into a new graph (its buffers as bound now).
+ws_status capture_bucket(ws_lane* L, int bi, cudaGraph_t* out) {
+    *out = nullptr;
+    cudaError_t e = cudaStreamBeginCapture(L->stream, cudaStreamCaptureModeThreadLocal);
+    if (e != cudaSuccess) return fail(WS_ERR_CAPTURE, "begin capture: %s", cudaGetErrorName(e));
+    ws_status st = enqueue_path(L, true, bi);
+    cudaGraph_t g = nullptr;
+    e = cudaStreamEndCapture(L->stream, &g);
+    if (st != WS_OK) {
+        if (g) cudaGraphDestroy(g);
+        return st;
+    }
+    if (e != cudaSuccess) return fail(WS_ERR_CAPTURE, "end capture: %s", cudaGetErrorName(e));
+    *out = g;
+    return WS_OK;
+}
+
+ws_status instantiate_bucket(ws_lane* L, int bi) {
+    cudaError_t e = cudaGraphInstantiateWithFlags(&L->exec[bi], L->graph[bi], 0);
+    if (e != cudaSuccess) return fail(WS_ERR_CAPTURE, "instantiate: %s", cudaGetErrorName(e));
+    // Upload once so the first submit pays no first-launch set-up.
+    e = cudaGraphUpload(L->exec[bi], L->stream);
+    if (e != cudaSuccess) return fail(WS_ERR_CAPTURE, "upload: %s", cudaGetErrorName(e));
     return WS_OK;
 }
 
@@ -178,7 +258,7 @@ ws_status build(ws_lane* L) {
                 L->in_dev = d.input;
             } else {
                 if ((st = alloc_dev(&L->in_dev, L->input_bytes, "input")) != WS_OK) return st;
-                L->own_in_dev = true;
+                L->owned_in_dev = L->in_dev;
             }
             break;
         case WS_INPUT_MAPPED:
@@ -187,7 +267,7 @@ ws_status build(ws_lane* L) {
             } else {
                 if ((st = alloc_host(&L->in_host, L->input_bytes, cudaHostAllocMapped, "input")) != WS_OK)
                     return st;
-                L->own_in_host = true;
+                L->owned_in_host = L->in_host;
             }
             if ((st = device_view(L->in_host, &L->in_dev, "input")) != WS_OK) return st;
             break;
@@ -197,10 +277,10 @@ ws_status build(ws_lane* L) {
             } else {
                 if ((st = alloc_host(&L->in_host, L->input_bytes, cudaHostAllocDefault, "input")) != WS_OK)
                     return st;
-                L->own_in_host = true;
+                L->owned_in_host = L->in_host;
             }
             if ((st = alloc_dev(&L->in_dev, L->input_bytes, "input copy")) != WS_OK) return st;
-            L->own_in_dev = true;
+            L->owned_in_dev = L->in_dev;
             break;
         default:
             return fail(WS_ERR_INVALID_ARGUMENT, "input mode %d", d.input_mode);
@@ -216,7 +296,7 @@ ws_status build(ws_lane* L) {
         L->logits = d.logits;
     } else {
         if ((st = alloc_dev((void**)&L->logits, L->logits_bytes, "logits")) != WS_OK) return st;
-        L->own_logits = true;
+        L->owned_logits = L->logits;
         WS_TRY_CUDA(cudaMemsetAsync(L->logits, 0, L->logits_bytes, L->stream));
     }
 
@@ -269,14 +349,22 @@ ws_status build(ws_lane* L) {
             return fail(WS_ERR_INVALID_ARGUMENT, "result mode %d", d.result_mode);
     }
 
-    if (detecting(L)) {
-        if ((st = ws_detect_workspace_bytes(&d.detect, d.batch, &L->ws_bytes)) != WS_OK) return st;
-    } else {
-        L->ws_bytes = topk_workspace_size(d.rows, d.cols, d.k);
-    }
-    if (L->ws_bytes) {   // cudaMalloc's alignment covers both workspaces' 256-byte rule
-        if ((st = alloc_dev(&L->ws, L->ws_bytes, "post-processing workspace")) != WS_OK) return st;
-        WS_TRY_CUDA(cudaMemsetAsync(L->ws, 0, L->ws_bytes, L->stream));
+    // batch buckets
+    L->nbuckets = 0;
+    if (d.flags & WS_LANE_FLAG_BUCKETS)
+        for (int nb = 1; nb < d.batch && L->nbuckets < kMaxBuckets - 1; nb *= 2) L->bucket_batch[L->nbuckets++] = nb;
+    L->bucket_batch[L->nbuckets++] = d.batch;
+    for (int bi = 0; bi < L->nbuckets; ++bi) {
+        const int nb = L->bucket_batch[bi];
+        if (detecting(L)) {
+            if ((st = ws_detect_workspace_bytes(&d.detect, nb, &L->ws_bytes[bi])) != WS_OK) return st;
+        } else {
+            L->ws_bytes[bi] = topk_workspace_size(bucket_rows(L, nb), d.cols, d.k);
+        }
+        if (L->ws_bytes[bi]) {   // cudaMalloc's alignment covers both workspaces' 256-byte rule
+            if ((st = alloc_dev(&L->ws[bi], L->ws_bytes[bi], "post-processing workspace")) != WS_OK) return st;
+            WS_TRY_CUDA(cudaMemsetAsync(L->ws[bi], 0, L->ws_bytes[bi], L->stream));
+        }
     }
 
     if (submit_timing(L)) {
@@ -292,25 +380,17 @@ ws_status build(ws_lane* L) {
         WS_TRY_CUDA(cudaEventCreate(&L->ev_post1));
     }
 
-    // Warm direct run: settles lazy module loading and kernel attributes
+    // Warm direct runs: settle lazy module loading and kernel attributes
     // before anything is captured.
-    if ((st = enqueue_path(L, false)) != WS_OK) return st;
+    for (int bi = 0; bi < L->nbuckets; ++bi)
+        if ((st = enqueue_path(L, false, bi)) != WS_OK) return st;
     WS_TRY_CUDA(cudaStreamSynchronize(L->stream));
 
     if (use_graph(L)) {
-        cudaError_t e = cudaStreamBeginCapture(L->stream, cudaStreamCaptureModeThreadLocal);
-        if (e != cudaSuccess) return fail(WS_ERR_CAPTURE, "begin capture: %s", cudaGetErrorName(e));
-        st = enqueue_path(L, true);
-        cudaGraph_t g = nullptr;
-        e = cudaStreamEndCapture(L->stream, &g);
-        L->graph = g;
-        if (st != WS_OK) return st;
-        if (e != cudaSuccess) return fail(WS_ERR_CAPTURE, "end capture: %s", cudaGetErrorName(e));
-        e = cudaGraphInstantiateWithFlags(&L->exec, L->graph, 0);
-        if (e != cudaSuccess) return fail(WS_ERR_CAPTURE, "instantiate: %s", cudaGetErrorName(e));
-        // Upload once so the first submit pays no first-launch set-up.
-        e = cudaGraphUpload(L->exec, L->stream);
-        if (e != cudaSuccess) return fail(WS_ERR_CAPTURE, "upload: %s", cudaGetErrorName(e));
+        for (int bi = 0; bi < L->nbuckets; ++bi) {
+            if ((st = capture_bucket(L, bi, &L->graph[bi])) != WS_OK) return st;
+            if ((st = instantiate_bucket(L, bi)) != WS_OK) return st;
+        }
         WS_TRY_CUDA(cudaStreamSynchronize(L->stream));
     }
     return WS_OK;
@@ -337,11 +417,14 @@ ws_status validate_lane(const ws_lane_desc* d) {
         return fail(WS_ERR_INVALID_ARGUMENT, "input mode %d", d->input_mode);
     if (d->result_mode < WS_RESULT_DEVICE || d->result_mode > WS_RESULT_COPY)
         return fail(WS_ERR_INVALID_ARGUMENT, "result mode %d", d->result_mode);
-    const uint32_t known =
-        WS_LANE_FLAG_NO_GRAPH | WS_LANE_FLAG_STAGE_TIMING | WS_LANE_FLAG_NO_TIMING | WS_LANE_FLAG_NO_DEVICE;
+    const uint32_t known = WS_LANE_FLAG_NO_GRAPH | WS_LANE_FLAG_STAGE_TIMING | WS_LANE_FLAG_NO_TIMING |
+                           WS_LANE_FLAG_NO_DEVICE | WS_LANE_FLAG_NVTX | WS_LANE_FLAG_BUCKETS;
     if (d->flags & ~known) return fail(WS_ERR_INVALID_ARGUMENT, "unknown flags 0x%x", d->flags & ~known);
     if ((d->flags & WS_LANE_FLAG_NO_DEVICE) && d->fake_polls < 0)
         return fail(WS_ERR_INVALID_ARGUMENT, "fake_polls %d < 0", d->fake_polls);
+    if ((d->flags & WS_LANE_FLAG_BUCKETS) && d->post == WS_POST_TOPK && d->rows % d->batch != 0)
+        return fail(WS_ERR_INVALID_ARGUMENT, "bucketed Top-K lane needs rows (%lld) a multiple of batch (%d)",
+                    (long long)d->rows, d->batch);
     return WS_OK;
 }
 
@@ -360,6 +443,7 @@ ws_status ws_lane_create(const ws_lane_desc* desc, ws_lane** out) {
     ws_lane* L = new (std::nothrow) ws_lane();
     if (!L) return fail(WS_ERR_OUT_OF_MEMORY, "lane object");
     L->d = *desc;
+    NvtxRange r(L, "ws_lane_create");
     if (desc->flags & WS_LANE_FLAG_NO_DEVICE) {
         L->fake = true;
         *out = L;
@@ -413,28 +497,32 @@ ws_status ws_lane_acquire(ws_lane* L) {
     return WS_OK;
 }
 
-ws_status ws_lane_submit(ws_lane* L) {
+ws_status ws_lane_submit_n(ws_lane* L, int32_t n) {
     using namespace ws;
     clear_error();
     if (!L) return fail(WS_ERR_INVALID_ARGUMENT, "lane is NULL");
+    NvtxRange r(L, "ws_lane_submit");
     if (L->state != WS_LANE_ACQUIRED)
         return fail(WS_ERR_LANE_STATE, "submit needs an acquired lane (state %d)", L->state);
+    if (n < 1 || n > L->d.batch) return fail(WS_ERR_INVALID_ARGUMENT, "%d frames for a lane of %d", n, L->d.batch);
     L->t_submit = std::chrono::steady_clock::now();
     if (L->fake) {
         L->fake_left = L->d.fake_polls;
         L->state = WS_LANE_IN_FLIGHT;
         return WS_OK;
     }
+    int bi = 0;   // the smallest bucket that holds n frames
+    while (L->bucket_batch[bi] < n) ++bi;
     cudaError_t e = cudaSuccess;
     if (submit_timing(L)) {
         e = cudaEventRecord(L->ev_start, L->stream);
         if (e != cudaSuccess) return cuda_fail(e, "record start event");
     }
     if (use_graph(L)) {
-        e = cudaGraphLaunch(L->exec, L->stream);
+        e = cudaGraphLaunch(L->exec[bi], L->stream);
         if (e != cudaSuccess) return cuda_fail(e, "graph launch");
     } else {
-        ws_status st = enqueue_path(L, false);
+        ws_status st = enqueue_path(L, false, bi);
         if (st != WS_OK) return st;
     }
     e = cudaEventRecord(L->ev_end, L->stream);
@@ -443,10 +531,74 @@ ws_status ws_lane_submit(ws_lane* L) {
     return WS_OK;
 }
 
+ws_status ws_lane_submit(ws_lane* L) {
+    if (!L) {
+        ws::clear_error();
+        return ws::fail(WS_ERR_INVALID_ARGUMENT, "lane is NULL");
+    }
+    return ws_lane_submit_n(L, L->d.batch);
+}
+
+ws_status ws_lane_rebind(ws_lane* L, void* input, float* logits, int32_t* reinstantiated) {
+    using namespace ws;
+    clear_error();
+    if (reinstantiated) *reinstantiated = 0;
+    if (!L) return fail(WS_ERR_INVALID_ARGUMENT, "lane is NULL");
+    NvtxRange r(L, "ws_lane_rebind");
+    if (L->state == WS_LANE_IN_FLIGHT) return fail(WS_ERR_LANE_BUSY, "lane is in flight; wait first");
+    if (!input && !logits) return WS_OK;
+    if (L->fake) {
+        if (input) L->d.input = input;
+        if (logits) L->d.logits = logits;
+        return WS_OK;
+    }
+    // the new slot addresses; the old ones stay valid if anything fails
+    void* in_host = L->in_host;
+    void* in_dev = L->in_dev;
+    if (input) {
+        switch (L->d.input_mode) {
+            case WS_INPUT_DEVICE: in_dev = input; break;
+            case WS_INPUT_MAPPED: {
+                in_host = input;
+                ws_status st = device_view(input, &in_dev, "input");
+                if (st != WS_OK) return st;
+                break;
+            }
+            default: in_host = input; break;   // COPY: the graph's copy source
+        }
+    }
+    L->in_host = in_host;
+    L->in_dev = in_dev;
+    if (logits) L->logits = logits;
+    if (!use_graph(L)) return WS_OK;
+    // Re-capture each bucket with the new addresses and update its executable
+    // graph in place ("Streams, concurrency and CUDA Graphs", CUDA Graphs:
+    // cudaGraphExecUpdate instead of re-instantiation); re-instantiate only if
+    // the update is refused.
+    for (int bi = 0; bi < L->nbuckets; ++bi) {
+        cudaGraph_t g = nullptr;
+        ws_status st = capture_bucket(L, bi, &g);
+        if (st != WS_OK) return st;
+        cudaGraphExecUpdateResultInfo info;
+        cudaError_t e = cudaGraphExecUpdate(L->exec[bi], g, &info);
+        cudaGraphDestroy(L->graph[bi]);
+        L->graph[bi] = g;
+        if (e != cudaSuccess) {
+            cudaGetLastError();
+            cudaGraphExecDestroy(L->exec[bi]);
+            L->exec[bi] = nullptr;
+            if ((st = instantiate_bucket(L, bi)) != WS_OK) return st;
+            if (reinstantiated) *reinstantiated = 1;
+        }
+    }
+    return WS_OK;
+}
+
 ws_status ws_lane_wait(ws_lane* L, int64_t timeout_us, ws_lane_timing* timing) {
     using namespace ws;
     clear_error();
     if (!L) return fail(WS_ERR_INVALID_ARGUMENT, "lane is NULL");
+    NvtxRange r(L, "ws_lane_wait");
     if (L->state != WS_LANE_IN_FLIGHT) return fail(WS_ERR_LANE_STATE, "wait needs a lane in flight");
     const auto t0 = std::chrono::steady_clock::now();
     if (!L->fake && timeout_us < 0) {
