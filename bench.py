@@ -16,7 +16,9 @@ HBM-throughput configuration.  Also measured on every run:
   buffers, against the measured HBM copy bandwidth;
 * the CPU oracle on the host cores (a bounded sample), as a reported baseline;
 * detection decode + NMS of a YOLO-style 640x640 head: batch-64 throughput,
-  the decode kernel's HBM rate, and batch-1 latency through a detection lane.
+  the decode kernel's HBM rate, and batch-1 latency through a detection lane;
+* lane graph variants: re-binding cost (cudaGraphExecUpdate), a bucketed
+  lane's 1-frame replay, and batch-1 frames/s through a pool of 1, 2, 4 lanes.
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
        [--workload NAME] [--latency-samples S] [--no-cpu-baseline]
@@ -370,6 +372,80 @@ def detect_measurements(B, Lane, device, stream, samples: int) -> dict:
     }
 
 
+def lane_measurements(B, Lane, device, samples: int) -> dict:
+    """Graph variants and the lane pool on the batch-1 1080p -> 224 + Top-5
+    workload: the cost of re-binding a lane's producer slot (cudaGraphExecUpdate
+    instead of re-instantiation), a 1-frame submit on a bucketed 64-frame lane,
+    and frames/s through a pool of 1, 2 and 4 lanes, each on its own stream."""
+    import torch
+    lw = synth.WORKLOADS[LATENCY_WORKLOAD]
+    frames = torch.from_numpy(synth.make_frames(LATENCY_WORKLOAD)).to(device)
+    frames2 = frames.clone()
+    logits = torch.from_numpy(synth.make_logits(LATENCY_WORKLOAD)).to(device)
+    pre = B.preprocess_desc(lw["src_w"], lw["src_h"], lw["dst_w"], lw["dst_h"], norm=lw["norm"])
+    out = {"workload": LATENCY_WORKLOAD}
+    d = B.lane_desc(pre, 1, 1, lw["cols"], lw["k"], input=frames.data_ptr(), logits=logits.data_ptr())
+    with Lane(d) as lane:
+        times, reinst = [], 0
+        for i in range(200):
+            t0 = time.perf_counter()
+            reinst += lane.rebind(input=(frames2 if i % 2 else frames).data_ptr())
+            times.append((time.perf_counter() - t0) * 1e6)
+            lane.acquire(); lane.submit(); lane.wait()
+        out["rebind_host_us"] = percentiles(times[10:])
+        out["rebind_reinstantiated"] = reinst
+    # a 64-frame bucketed lane replaying its 1-frame bucket
+    w64 = synth.WORKLOADS[DEFAULT_WORKLOAD]
+    src64 = torch.zeros((64, lw["src_h"], 3 * lw["src_w"]), dtype=torch.uint8, device=device)
+    src64[0].copy_(frames[0])
+    lg64 = torch.from_numpy(synth.logits_normal(0x57A7D64, 64, lw["cols"])).to(device)
+    d = B.lane_desc(pre, 64, 64, lw["cols"], w64["k"], input=src64.data_ptr(), logits=lg64.data_ptr(),
+                    flags=B.WS_LANE_FLAG_BUCKETS)
+    with Lane(d) as lane:
+        for n in (1, 64):
+            gpu = []
+            for i in range(min(samples, 1000) + 50):
+                lane.acquire(); lane.submit(n); t = lane.wait()
+                if i >= 50:
+                    gpu.append(t.gpu_us)
+            out[f"bucketed_b64_lane_submit_n{n}_gpu_us"] = percentiles(gpu)
+    # lane pool: batch-1 jobs, producer and consumer on this thread
+    d = B.lane_desc(pre, 1, 1, lw["cols"], lw["k"], flags=B.WS_LANE_FLAG_NO_TIMING)
+    pool = {}
+    for nl in (1, 2, 4):
+        st, P = B.ws_pool_create(d, nl)
+        B.check(st)
+        try:
+            jobs = max(400, min(2 * samples, 8000))
+
+            def run(n):
+                # bursts: every lane submitted (each on its own stream), then
+                # all completed, so the lanes' graphs can overlap on the GPU
+                done = 0
+                while done < n:
+                    burst = []
+                    for _ in range(nl):
+                        st, L = B.ws_pool_acquire(P, 0)
+                        B.check(st)
+                        B.check(B.ws_pool_submit(P, L, 1))
+                        burst.append(L)
+                    for _ in burst:
+                        st, L, _ = B.ws_pool_complete(P, -1)
+                        B.check(st)
+                        B.check(B.ws_pool_recycle(P, L))
+                    done += nl
+
+            run(100)
+            t0 = time.perf_counter()
+            run(jobs)
+            dt = time.perf_counter() - t0
+            pool[f"lanes_{nl}"] = {"frames_per_s": (jobs // nl * nl) / dt, "jobs": jobs // nl * nl}
+        finally:
+            B.check(B.ws_pool_destroy(P))
+    out["pool_b1"] = pool
+    return out
+
+
 def workload_config(name: str, w: dict) -> dict:
     return {"workload": f"{w['batch']}x {w['src_w']}x{w['src_h']} RGB8 -> "
                         f"{'letterbox ' if w['resize'] == 'letterbox' else ''}{w['dst_w']}x{w['dst_h']} "
@@ -553,6 +629,7 @@ def main():
     detect = None
     if not args.no_detect:
         detect = detect_measurements(B, Lane, device, stream, min(2000, args.latency_samples))
+    lanes_extra = lane_measurements(B, Lane, device, args.latency_samples)
     clk = clocks.stop()
 
     # End to end through the lane API with host buffers: the producer writes
@@ -639,6 +716,7 @@ def main():
                          "topk_gbs": alg["topk"] / (topk_avg_us * 1e-6) / 1e9},
             "latency_b1": latency,
             "detect": detect,
+            "lanes": lanes_extra,
             "e2e": e2e,
             "gpu_launches": 2 * args.steps,
             "clocks": clk,
