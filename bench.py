@@ -5,7 +5,11 @@ frames into the FP32 NCHW tensor, then the row-wise exact Top-K of the
 logits (the network between them is out of scope; its output slot is a
 fixed logits buffer).  Default workload: 64 independent 1920x1080 RGB8
 frames -> 224x224 mean/std, Top-32 of [64, 1000] logits, the batched
-HBM-throughput configuration.  Also measured on every run:
+HBM-throughput configuration.  The headline replays three lanes in
+rotation, each on its own stream (one lane's preprocess overlaps the
+previous lane's Top-K, as lanes run in a deployment); the same three lanes
+on one shared stream, every step serialised, are reported beside it.  Also
+measured on every run:
 
 * batch-1 graph-replay latency (p50 / p99 / max, GPU events and host steady
   clock, graph and no-graph) on one 1920x1080 frame -> 224x224, Top-5 of 1000;
@@ -525,44 +529,68 @@ def main():
     out_bytes = 4 if args.out_dtype == "f32" else 2
     pre = B.preprocess_desc(w["src_w"], w["src_h"], w["dst_w"], w["dst_h"],
                             letterbox=w["resize"] == "letterbox", norm=w["norm"], dst_type=dst_type)
-    lanes, keep = [], []
-    for _ in range(LANES):
-        src = frames_dev.clone()
-        lg = logits_dev.clone()
-        keep += [src, lg]
-        # throughput lanes: only a completion event per submit (no timing pair)
-        d = B.lane_desc(pre, w["batch"], w["rows"], w["cols"], w["k"], input=src.data_ptr(), logits=lg.data_ptr(),
-                        stream=stream.cuda_stream, flags=B.WS_LANE_FLAG_NO_TIMING)
-        lanes.append(Lane(d))
+    # Two sets of throughput lanes, only a completion event per submit (no
+    # timing pair): each lane of the first set on its own stream, as lanes run
+    # in a deployment (a lane's preprocess overlaps the previous lane's Top-K;
+    # within a lane the order copy-in -> preprocess -> Top-K is unchanged) --
+    # the headline; the second set sharing one stream, every step serialised
+    # behind the previous one.
+    lanes, lanes_1s, keep = [], [], []
+    for one_stream in (False, True):
+        for _ in range(LANES):
+            src = frames_dev.clone()
+            lg = logits_dev.clone()
+            keep += [src, lg]
+            d = B.lane_desc(pre, w["batch"], w["rows"], w["cols"], w["k"], input=src.data_ptr(), logits=lg.data_ptr(),
+                            stream=stream.cuda_stream if one_stream else None, flags=B.WS_LANE_FLAG_NO_TIMING)
+            (lanes_1s if one_stream else lanes).append(Lane(d))
     torch.cuda.synchronize()
     alg = algorithmic_bytes(w, out_bytes)
     touched_per_rotation = LANES * alg["total"]
 
-    def run_steps(n):
+    def run_steps(ls, n):
+        """Round-robin submits; returns the lanes still in flight."""
         inflight = []
-        for s in range(n):
-            lane = lanes[s % LANES]
+        for s_ in range(n):
+            lane = ls[s_ % LANES]
             if lane.state == B.WS_LANE_IN_FLIGHT:
                 lane.wait()
                 inflight.remove(lane)
             lane.acquire()
             lane.submit()
             inflight.append(lane)
+        return inflight
+
+    def timed_steps(ls, n):
+        """Device time of n steps: a start event on `stream`, which every lane
+        stream waits on, and an end event after `stream` has waited on every
+        lane stream's last work."""
+        lane_streams = [torch.cuda.ExternalStream(lane.buffers.stream) for lane in ls]
+        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        ev0.record(stream)
+        for ls_ in lane_streams:
+            ls_.wait_event(ev0)
+        inflight = run_steps(ls, n)
+        for ls_ in lane_streams:
+            e = torch.cuda.Event()
+            e.record(ls_)
+            stream.wait_event(e)
+        ev1.record(stream)
         for lane in inflight:
             lane.wait()
+        torch.cuda.synchronize()
+        return ev0.elapsed_time(ev1) / 1000.0
 
-    run_steps(args.warmup)
+    for ls in (lanes, lanes_1s):
+        for lane in run_steps(ls, args.warmup):
+            lane.wait()
     torch.cuda.synchronize()
     if world > 1:
         torch.distributed.barrier()
     clocks.start()
-    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    torch.cuda.synchronize()
-    ev0.record(stream)
-    run_steps(args.steps)
-    ev1.record(stream)
-    torch.cuda.synchronize()
-    elapsed_s = ev0.elapsed_time(ev1) / 1000.0
+    elapsed_s = timed_steps(lanes, args.steps)
+    elapsed_1s = timed_steps(lanes_1s, args.steps)
     if world > 1:
         torch.distributed.barrier()
 
@@ -571,7 +599,7 @@ def main():
     # L2), launched back to back through the C ABI and bracketed by CUDA
     # events, right after the timed region.
     kernel_launches = min(args.steps, 2000)
-    bufs = [lane.buffers for lane in lanes]
+    bufs = [lane.buffers for lane in lanes_1s]
     st_ws = [B.ws_topk_workspace_bytes(w["rows"], w["cols"], w["k"])[1] for _ in lanes]
     topk_ws = [torch.zeros(max(n, 1), dtype=torch.uint8, device=device) for n in st_ws]
 
@@ -677,10 +705,11 @@ def main():
         for lane in e_lanes:
             lane.close()
 
-    for lane in lanes:
+    for lane in lanes + lanes_1s:
         lane.close()
 
     value, t_max = whole_job_rate(w["batch"] * args.steps, elapsed_s, world, device)
+    value_1s, t_max_1s = whole_job_rate(w["batch"] * args.steps, elapsed_1s, world, device)
     peaks_path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(peaks_path):
         peak, peak_src = float(json.load(open(peaks_path))["hbm_gbs"]), "measured"
@@ -704,8 +733,12 @@ def main():
                               f"(> {touched_per_rotation / l2:.1f}x the {l2 / 2 ** 20:.0f} MiB L2): inputs larger "
                                 "than L2",
                            parallelism=f"replicas x{world}", graph=True,
+                           lanes=f"{LANES} lanes, each on its own stream, replayed in rotation",
                            algorithmic_bytes_per_step=alg["total"]),
             "hbm_gbs_step": alg["total"] * args.steps * world / t_max / 1e9,
+            "serialized_one_stream": {"value": value_1s, "ms_per_step": 1000.0 * t_max_1s / args.steps,
+                                      "hbm_gbs_step": alg["total"] * args.steps * world / t_max_1s / 1e9,
+                                      "lanes": f"{LANES} lanes sharing one stream: each step after the previous"},
             "roofline": {"bound": "hbm", "kernel": "pre_ring_kernel", "achieved": achieved, "peak": peak,
                          "unit": "GB/s", "frac": achieved / peak, "peak_source": peak_src,
                          "traffic": traffic, "algorithmic_bytes_per_launch": alg["preprocess"],
