@@ -627,33 +627,42 @@ def main():
     pre_avg_us = time_kernel(launch_pre, kernel_launches)
     topk_avg_us = time_kernel(launch_topk, kernel_launches)
 
-    # batch-1 latency: one lane, submit -> wait, graph and direct launches
-    lw = synth.WORKLOADS[LATENCY_WORKLOAD]
-    lframes = torch.from_numpy(synth.make_frames(LATENCY_WORKLOAD)).to(device)
-    llogits = torch.from_numpy(synth.make_logits(LATENCY_WORKLOAD)).to(device)
-    lpre = B.preprocess_desc(lw["src_w"], lw["src_h"], lw["dst_w"], lw["dst_h"], norm=lw["norm"])
-    latency = {"workload": workload_config(LATENCY_WORKLOAD, lw)["workload"], "samples": args.latency_samples,
-               "warmup": min(1000, args.latency_samples), "input": "device-resident"}
+    # batch-1 latency: one lane, submit -> wait, graph and direct launches.
     # "graph": the page's measurement, timing events just before the graph
     # launch and after the Top-K (GPU interval) plus the host steady clock;
     # "graph_no_timing": the same replay with only a completion event (host
     # clock); "no_graph": direct launches with the timing events.
-    for label, flags in (("graph", 0), ("graph_no_timing", B.WS_LANE_FLAG_NO_TIMING),
-                         ("no_graph", B.WS_LANE_FLAG_NO_GRAPH)):
-        d = B.lane_desc(lpre, 1, 1, lw["cols"], lw["k"], input=lframes.data_ptr(), logits=llogits.data_ptr(),
-                        flags=flags)
-        with Lane(d) as lane:
-            gpu, host = [], []
-            for i in range(latency["warmup"] + args.latency_samples):
-                lane.acquire()
-                lane.submit()
-                t = lane.wait()
-                if i >= latency["warmup"]:
-                    gpu.append(t.gpu_us)
-                    host.append(t.host_us)
-            latency[label] = {"host_us": percentiles(host)}
-            if flags & B.WS_LANE_FLAG_NO_TIMING == 0:
-                latency[label]["gpu_us"] = percentiles(gpu)
+    def latency_of(name, samples):
+        lw = synth.WORKLOADS[name]
+        lframes = torch.from_numpy(synth.make_frames(name)).to(device)
+        llogits = torch.from_numpy(synth.make_logits(name)).to(device)
+        lpre = B.preprocess_desc(lw["src_w"], lw["src_h"], lw["dst_w"], lw["dst_h"],
+                                 letterbox=lw["resize"] == "letterbox", norm=lw["norm"])
+        out = {"workload": workload_config(name, lw)["workload"], "samples": samples,
+               "warmup": min(1000, samples), "input": "device-resident"}
+        for label, flags in (("graph", 0), ("graph_no_timing", B.WS_LANE_FLAG_NO_TIMING),
+                             ("no_graph", B.WS_LANE_FLAG_NO_GRAPH)):
+            d = B.lane_desc(lpre, 1, lw["rows"], lw["cols"], lw["k"], input=lframes.data_ptr(),
+                            logits=llogits.data_ptr(), flags=flags)
+            with Lane(d) as lane:
+                gpu, host = [], []
+                for i in range(out["warmup"] + samples):
+                    lane.acquire()
+                    lane.submit()
+                    t = lane.wait()
+                    if i >= out["warmup"]:
+                        gpu.append(t.gpu_us)
+                        host.append(t.host_us)
+                out[label] = {"host_us": percentiles(host)}
+                if flags & B.WS_LANE_FLAG_NO_TIMING == 0:
+                    out[label]["gpu_us"] = percentiles(gpu)
+        return out
+
+    latency = latency_of(LATENCY_WORKLOAD, args.latency_samples)
+    # the other two batch-1 configurations: 224x224 identity + Top-5 of 1000,
+    # and 1280x720 letterboxed to 640x640 + Top-32 of one 672,000-entry row
+    latency_other = {name: latency_of(name, args.latency_samples)
+                     for name in ("b1_224_identity", "b1_720p_letterbox_640")}
     detect = None
     if not args.no_detect:
         detect = detect_measurements(B, Lane, device, stream, min(2000, args.latency_samples))
@@ -748,6 +757,7 @@ def main():
                          "topk_avg_launch_us": topk_avg_us,
                          "topk_gbs": alg["topk"] / (topk_avg_us * 1e-6) / 1e9},
             "latency_b1": latency,
+            "latency_b1_other": latency_other,
             "detect": detect,
             "lanes": lanes_extra,
             "e2e": e2e,
