@@ -631,7 +631,9 @@ def main():
     # "graph": the page's measurement, timing events just before the graph
     # launch and after the Top-K (GPU interval) plus the host steady clock;
     # "graph_no_timing": the same replay with only a completion event (host
-    # clock); "no_graph": direct launches with the timing events.
+    # clock); "no_graph": direct launches with the timing events;
+    # "graph_no_pdl": the graph with the Top-K as an ordinary launch instead
+    # of a programmatic dependent launch (what PDL saves).
     def latency_of(name, samples):
         lw = synth.WORKLOADS[name]
         lframes = torch.from_numpy(synth.make_frames(name)).to(device)
@@ -641,7 +643,7 @@ def main():
         out = {"workload": workload_config(name, lw)["workload"], "samples": samples,
                "warmup": min(1000, samples), "input": "device-resident"}
         for label, flags in (("graph", 0), ("graph_no_timing", B.WS_LANE_FLAG_NO_TIMING),
-                             ("no_graph", B.WS_LANE_FLAG_NO_GRAPH)):
+                             ("no_graph", B.WS_LANE_FLAG_NO_GRAPH), ("graph_no_pdl", B.WS_LANE_FLAG_NO_PDL)):
             d = B.lane_desc(lpre, 1, lw["rows"], lw["cols"], lw["k"], input=lframes.data_ptr(),
                             logits=llogits.data_ptr(), flags=flags)
             with Lane(d) as lane:

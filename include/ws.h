@@ -325,6 +325,10 @@ ws_status ws_detect(const ws_detect_desc* desc, const float* head, int32_t batch
                                          bucket, the real batch rounded up).  A Top-K lane needs
                                          rows a multiple of batch (per-frame rows scale with
                                          the bucket); a detection lane takes one head per frame. */
+#define WS_LANE_FLAG_NO_PDL      64u  /* launch the lane's Top-K / DFL / NMS kernels as ordinary
+                                         stream-ordered launches instead of programmatic
+                                         dependent launches (to measure what PDL saves:
+                                         "Streams, concurrency and CUDA Graphs", PDL section) */
 
 #define WS_POST_TOPK   0    /* post-processing: exact Top-K of the logits (rows x cols) */
 #define WS_POST_DETECT 1    /* post-processing: DFL decode + class-aware NMS of a detection head */

@@ -39,6 +39,7 @@ WS_LANE_FLAG_NO_TIMING = 4
 WS_LANE_FLAG_NO_DEVICE = 8
 WS_LANE_FLAG_NVTX = 16
 WS_LANE_FLAG_BUCKETS = 32
+WS_LANE_FLAG_NO_PDL = 64
 WS_POST_TOPK, WS_POST_DETECT = 0, 1
 WS_LANE_FREE, WS_LANE_ACQUIRED, WS_LANE_IN_FLIGHT = 0, 1, 2
 

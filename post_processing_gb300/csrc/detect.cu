@@ -723,7 +723,7 @@ ws_status launch_decode(DetParams p, int32_t batch, cudaStream_t stream) {
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = pdl_enabled() ? 1 : 0;
     e = cudaLaunchKernelEx(&cfg, detect_dfl_kernel, p);
     if (e == cudaSuccess) e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e, "DFL launch");
@@ -755,7 +755,7 @@ ws_status launch_nms(const DetParams& p, int32_t batch, cudaStream_t stream) {
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = pdl_enabled() ? 1 : 0;
     cudaError_t e = cudaLaunchKernelEx(&cfg, detect_nms_kernel, p);
     if (e == cudaSuccess) e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e, "NMS launch");

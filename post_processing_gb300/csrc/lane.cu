@@ -168,6 +168,7 @@ ws_status record(cudaEvent_t ev, cudaStream_t s, bool capturing) {
 // used directly for the warm-up and NO_GRAPH lanes.
 ws_status enqueue_path(ws_lane* L, bool capturing, int bi) {
     ws_status st;
+    const NoPdlScope no_pdl((L->d.flags & WS_LANE_FLAG_NO_PDL) != 0);
     const int nb = L->bucket_batch[bi];
     const int64_t rows = bucket_rows(L, nb);
     if (L->d.input_mode == WS_INPUT_COPY)
@@ -418,7 +419,8 @@ ws_status validate_lane(const ws_lane_desc* d) {
     if (d->result_mode < WS_RESULT_DEVICE || d->result_mode > WS_RESULT_COPY)
         return fail(WS_ERR_INVALID_ARGUMENT, "result mode %d", d->result_mode);
     const uint32_t known = WS_LANE_FLAG_NO_GRAPH | WS_LANE_FLAG_STAGE_TIMING | WS_LANE_FLAG_NO_TIMING |
-                           WS_LANE_FLAG_NO_DEVICE | WS_LANE_FLAG_NVTX | WS_LANE_FLAG_BUCKETS;
+                           WS_LANE_FLAG_NO_DEVICE | WS_LANE_FLAG_NVTX | WS_LANE_FLAG_BUCKETS |
+                           WS_LANE_FLAG_NO_PDL;
     if (d->flags & ~known) return fail(WS_ERR_INVALID_ARGUMENT, "unknown flags 0x%x", d->flags & ~known);
     if ((d->flags & WS_LANE_FLAG_NO_DEVICE) && d->fake_polls < 0)
         return fail(WS_ERR_INVALID_ARGUMENT, "fake_polls %d < 0", d->fake_polls);

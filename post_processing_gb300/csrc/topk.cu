@@ -613,7 +613,7 @@ ws_status ws_topk(const float* x, int64_t rows, int64_t cols, int32_t k, float* 
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = pdl_enabled() ? 1 : 0;
     cudaError_t e = vec ? cudaLaunchKernelEx(&cfg, topk_kernel<true>, p) : cudaLaunchKernelEx(&cfg, topk_kernel<false>, p);
     if (e != cudaSuccess) return cuda_fail(e, "top-k launch");
     e = cudaGetLastError();

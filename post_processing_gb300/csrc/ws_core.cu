@@ -60,6 +60,18 @@ ws_status current_device_info(int* device, const DeviceInfo** info) {
     return WS_OK;
 }
 
+namespace {
+thread_local bool t_no_pdl = false;
+}
+
+bool pdl_enabled() { return !t_no_pdl; }
+
+NoPdlScope::NoPdlScope(bool active) : prev(t_no_pdl) {
+    if (active) t_no_pdl = true;
+}
+
+NoPdlScope::~NoPdlScope() { t_no_pdl = prev; }
+
 uint32_t* device_error_word() {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;

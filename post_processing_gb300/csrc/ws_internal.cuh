@@ -46,4 +46,14 @@ enum : uint32_t {
 // parameter (no relocatable device code, so they cannot name it directly).
 uint32_t* device_error_word();
 
+// Programmatic dependent launch of the stream-ordered kernels (Top-K, DFL,
+// NMS): on unless the calling thread is inside a NoPdlScope (a lane with
+// WS_LANE_FLAG_NO_PDL enqueuing or capturing its path).
+bool pdl_enabled();
+struct NoPdlScope {
+    bool prev;
+    explicit NoPdlScope(bool active);
+    ~NoPdlScope();
+};
+
 }  // namespace ws

@@ -54,7 +54,7 @@ def read_lane(B, lane, batch, dh, dw, rows, k):
     return t, v, i
 
 
-MODES = [(0, 0, 0), (0, 0, 1), (1, 1, 0), (2, 2, 0), (2, 1, 2), (1, 2, 1)]   # input, result, flags
+MODES = [(0, 0, 0), (0, 0, 1), (1, 1, 0), (2, 2, 0), (2, 1, 2), (1, 2, 1), (0, 2, 64)]   # input, result, flags
 
 
 @pytest.mark.parametrize("name", ["b1_1080p_to_224", "b1_720p_letterbox_640", "b8_4k_to_512"])
