@@ -319,3 +319,39 @@ def test_detection_lane(B, oracle, result_mode, flags):
                 got = unpack(o[b, :k[b]])
                 assert list(got["anchor"]) == [int(c["anchor"][j]) for j in keep]
                 assert np.array_equal(got["boxes"].view(np.uint32), c["boxes"][keep].view(np.uint32))
+
+
+@pytest.mark.parametrize("geom", [
+    dict(in_w=40, in_h=24, strides=(8,), reg_max=4, num_classes=3),          # A = 15: scalar scan
+    dict(in_w=64, in_h=64, strides=(8, 16, 32, 64), reg_max=1, num_classes=1),  # one bin, one class, 4 levels
+    dict(in_w=96, in_h=32, strides=(32,), reg_max=32, num_classes=130),      # widest DFL, many classes
+], ids=["A15-scalar", "R1-C1-L4", "R32-C130"])
+def test_decode_edge_geometries(B, oracle, geom):
+    strides = geom.pop("strides")
+    desc = B.detect_desc(strides=strides, conf=0.2, **geom)
+    desc.nlevels = len(strides)
+    head = synth.yolo_head(90, 3, geom["in_w"], geom["in_h"], reg_max=geom["reg_max"],
+                           num_classes=geom["num_classes"], cls_mu=-1.0, strides=strides)
+    got = check_decode(B, oracle, desc, head)
+    assert sum(len(g["anchor"]) for g in got) > 0
+
+
+def test_decode_misaligned_head(B, oracle):
+    """A head that is not 16-byte aligned takes the scalar scan."""
+    desc = B.detect_desc()
+    head = synth.yolo_head(91, 2)
+    buf = torch.empty(head.size + 1, dtype=torch.float32, device="cuda")
+    buf[1:].copy_(torch.from_numpy(head.reshape(-1)))
+    batch, A = 2, head.shape[2]
+    cand = torch.zeros((batch, A, 8), dtype=torch.int32, device="cuda")
+    count = torch.zeros(batch, dtype=torch.int32, device="cuda")
+    B.check(B.ws_detect_decode(desc, buf.data_ptr() + 4, batch, cand.data_ptr(), count.data_ptr(), stream()))
+    torch.cuda.synchronize()
+    c, n = cand.cpu().numpy(), count.cpu().numpy()
+    for b in range(batch):
+        u = unpack(c[b, :n[b]])
+        order = np.argsort(u["anchor"], kind="stable")
+        want = oracle_cands(oracle, desc, head[b])
+        assert np.array_equal(u["anchor"][order], want["anchors"])
+        assert np.array_equal(u["f4"][order].view(np.uint32), want["logits"].view(np.uint32))
+        assert float(np.max(np.abs(u["boxes"][order] - want["boxes"]))) <= box_tol(desc)
