@@ -62,6 +62,101 @@ def topk(x: torch.Tensor, k: int, out_val: torch.Tensor | None = None, out_idx: 
     return out_val, out_idx
 
 
+def detect_workspace(desc: B.ws_detect_desc, batch: int, device="cuda", stream=None) -> torch.Tensor:
+    """A zeroed, 256-byte aligned workspace for ws_detect of this geometry and batch."""
+    st, n = B.ws_detect_workspace_bytes(desc, batch)
+    B.check(st)
+    ws = torch.empty(n + 256, dtype=torch.uint8, device=device)
+    off = (-ws.data_ptr()) % 256
+    ws = ws[off:off + n]
+    B.check(B.ws_detect_workspace_init(ws.data_ptr(), n, _stream(stream)))
+    return ws
+
+
+def detect(head: torch.Tensor, desc: B.ws_detect_desc, workspace: torch.Tensor | None = None,
+           out: torch.Tensor | None = None, out_count: torch.Tensor | None = None, stream=None):
+    """ws_detect on a float32 CUDA head [batch, 4*reg_max + num_classes, A].
+
+    Returns (detections, counts): detections is the raw int32 [batch, max_det,
+    8] buffer of ws_detection records and counts the int32 [batch] kept per
+    image; detection_fields() gives named views of it."""
+    if head.dtype != torch.float32 or not head.is_cuda or not head.is_contiguous() or head.dim() != 3:
+        raise TypeError("head must be a contiguous float32 CUDA tensor [batch, channels, anchors]")
+    batch = head.shape[0]
+    if workspace is None:
+        workspace = detect_workspace(desc, batch, head.device, stream)
+    if out is None:
+        out = torch.empty((batch, desc.max_det, 8), dtype=torch.int32, device=head.device)
+    if out_count is None:
+        out_count = torch.empty(batch, dtype=torch.int32, device=head.device)
+    B.check(B.ws_detect(desc, head.data_ptr(), batch, out.data_ptr(), out_count.data_ptr(), workspace.data_ptr(),
+                        workspace.numel(), _stream(stream)))
+    return out, out_count
+
+
+def detection_fields(detections: torch.Tensor) -> dict:
+    """Named views of a [..., 8] int32 ws_detection buffer: boxes (x1, y1, x2,
+    y2) and score as float32, class and anchor as int32."""
+    f = detections.view(torch.float32)
+    return {"boxes": f[..., 0:4], "score": f[..., 4], "cls": detections[..., 5], "anchor": detections[..., 6]}
+
+
+class Pool:
+    """ws_pool_*: N identical lanes with a producer / consumer hand-off;
+    destroyed by close() or `with`.  Lanes are returned as raw handles."""
+
+    def __init__(self, desc: B.ws_lane_desc, lanes: int):
+        st, h = B.ws_pool_create(desc, lanes)
+        B.check(st)
+        self.handle = h
+        self.size = lanes
+        self._batch = desc.batch
+
+    def lane(self, i: int) -> int:
+        st, h = B.ws_pool_lane(self.handle, i)
+        B.check(st)
+        return h
+
+    def buffers(self, lane: int) -> B.ws_lane_buffers:
+        st, b = B.ws_lane_get_buffers(lane)
+        B.check(st)
+        return b
+
+    def acquire(self, timeout_us: int = -1) -> int | None:
+        """A free lane, or None if none became free in time (back-pressure)."""
+        st, h = B.ws_pool_acquire(self.handle, timeout_us)
+        if st == B.WS_ERR_TIMEOUT:
+            return None
+        B.check(st)
+        return h
+
+    def submit(self, lane: int, n: int | None = None):
+        """Submit the lane's whole batch, or its first n frames."""
+        B.check(B.ws_pool_submit(self.handle, lane, self._batch if n is None else n))
+
+    def complete(self, timeout_us: int = -1):
+        """(lane, timing) of the oldest submission, or (None, None) on timeout."""
+        st, h, t = B.ws_pool_complete(self.handle, timeout_us)
+        if st == B.WS_ERR_TIMEOUT:
+            return None, None
+        B.check(st)
+        return h, t
+
+    def recycle(self, lane: int):
+        B.check(B.ws_pool_recycle(self.handle, lane))
+
+    def close(self):
+        if self.handle is not None:
+            B.check(B.ws_pool_destroy(self.handle))
+            self.handle = None
+
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *exc):
+        self.close()
+
+
 class Lane:
     """One fixed-shape lane (ws_lane_*); destroyed by close() or `with`."""
 

@@ -355,3 +355,19 @@ def test_decode_misaligned_head(B, oracle):
         assert np.array_equal(u["anchor"][order], want["anchors"])
         assert np.array_equal(u["f4"][order].view(np.uint32), want["logits"].view(np.uint32))
         assert float(np.max(np.abs(u["boxes"][order] - want["boxes"]))) <= box_tol(desc)
+
+
+def test_python_detect_wrapper(B, oracle):
+    from post_processing_gb300 import detect, detection_fields
+    desc = B.detect_desc()
+    head = synth.yolo_head(95, 2)
+    out, cnt = detect(torch.from_numpy(head).cuda(), desc)
+    torch.cuda.synchronize()
+    f = detection_fields(out)
+    dec = gpu_decode(B, desc, head)
+    for b in range(2):
+        keep = oracle.nms(dec[b]["boxes"], dec[b]["f4"], dec[b]["cls"], dec[b]["anchor"], desc.iou_thr,
+                          desc.max_det, desc.max_cand)
+        k = int(cnt[b])
+        assert f["anchor"][b, :k].cpu().tolist() == [int(dec[b]["anchor"][j]) for j in keep]
+        assert np.array_equal(f["boxes"][b, :k].cpu().numpy(), dec[b]["boxes"][keep])

@@ -130,3 +130,17 @@ def test_submit_n_and_rebind_host_logic(B):
     d = fake_desc(B, flags=B.WS_LANE_FLAG_BUCKETS)
     d.rows = 6
     assert B.ws_lane_create(d)[0] == B.WS_ERR_INVALID_ARGUMENT
+
+
+def test_python_pool_wrapper(B):
+    from post_processing_gb300 import Pool
+    with Pool(fake_desc(B, polls=1), 2) as pool:
+        a, b = pool.acquire(0), pool.acquire(0)
+        assert a and b and pool.acquire(0) is None                 # back-pressure
+        pool.submit(a)
+        pool.submit(b, 1)
+        assert pool.complete()[0] == a and pool.complete()[0] == b
+        assert pool.complete(0) == (None, None)
+        pool.recycle(a)
+        pool.recycle(b)
+        assert pool.lane(0) in (a, b)
