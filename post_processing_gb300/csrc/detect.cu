@@ -42,7 +42,9 @@ namespace ws {
 namespace {
 
 constexpr int kDecodeThreads = 256;
-constexpr int kDecodeAnchors = 128;                    // anchors per decode block (4 per lane)
+constexpr int kLaneVec = 1;                            // 16-byte words per lane per class row
+constexpr int kDecodeAnchors = 128 * kLaneVec;         // anchors per scan tile (4 kLaneVec per lane)
+constexpr int kLaneAnchors = 4 * kLaneVec;
 constexpr int kDflBlocks = 8;                          // DFL blocks per image
 constexpr int kScanLoads = 5;                          // 16-byte loads in flight per lane
 constexpr int kScanBlocksPerSM = 6;                    // register budget: 6 blocks of 256 per SM
@@ -103,13 +105,18 @@ struct ScanShared {
     int n, base;
 };
 
-__device__ __forceinline__ void take4(float (&best)[4], int (&bc)[4], const float4 v4, int c) {
+// Anchor e of a lane: a0 + 128 (e / 4) + 4 lane + e % 4, so that a warp's
+// loads of one class row are whole 512-byte segments.
+__device__ __forceinline__ int lane_anchor(int lane, int e) { return 128 * (e >> 2) + 4 * lane + (e & 3); }
+
+__device__ __forceinline__ void take4(float (&best)[kLaneAnchors], int (&bc)[kLaneAnchors], int h, const float4 v4,
+                                      int c) {
     const float v[4] = {nan_as_ninf(v4.x), nan_as_ninf(v4.y), nan_as_ninf(v4.z), nan_as_ninf(v4.w)};
 #pragma unroll
     for (int e = 0; e < 4; ++e)
-        if (v[e] > best[e]) {
-            best[e] = v[e];
-            bc[e] = c;
+        if (v[e] > best[4 * h + e]) {
+            best[4 * h + e] = v[e];
+            bc[4 * h + e] = c;
         }
 }
 
@@ -118,12 +125,12 @@ __device__ __forceinline__ void take4(float (&best)[4], int (&bc)[4], const floa
 // write their class, logit and anchor (the DFL kernel adds the boxes).
 // Called by the whole block.
 __device__ __forceinline__ void finish_tile(const DetParams& p, ScanShared& sh, int b, long long a0,
-                                            const float (&best)[4], const int (&bc)[4]) {
+                                            const float (&best)[kLaneAnchors], const int (&bc)[kLaneAnchors]) {
     const int tid = threadIdx.x, lane = tid & 31, g = tid >> 5;
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-        sh.v[g][4 * lane + e] = best[e];
-        sh.c[g][4 * lane + e] = bc[e];
+    for (int e = 0; e < kLaneAnchors; ++e) {
+        sh.v[g][lane_anchor(lane, e)] = best[e];
+        sh.c[g][lane_anchor(lane, e)] = bc[e];
     }
     __syncthreads();
     bool is_cand = false;
@@ -173,40 +180,54 @@ __device__ __forceinline__ void finish_tile(const DetParams& p, ScanShared& sh, 
 }
 
 // Class scan with plain loads, one tile per block.  kVec (A % 4 == 0,
-// 16-byte aligned head): a lane loads its 4 anchors' logits as one 16-byte
-// word, kLoads classes in flight; else one anchor at a time, any alignment.
+// 16-byte aligned head): a lane loads its anchors' logits as 16-byte words,
+// kScanLoads classes in flight; else one anchor at a time, any alignment.
 template <bool kVec>
 __global__ void __launch_bounds__(kDecodeThreads, kScanBlocksPerSM) detect_scan_kernel(const __grid_constant__ DetParams p) {
     __shared__ ScanShared sh;
     const int b = blockIdx.y, lane = threadIdx.x & 31, g = threadIdx.x >> 5;
     const long long a0 = (long long)blockIdx.x * kDecodeAnchors;
-    const long long a4 = a0 + 4 * lane;
     const float* cl = p.head + (size_t)b * p.ch * p.A + (size_t)(4 * p.R) * p.A;
-    float best[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-    int bc[4] = {g, g, g, g};
-    if (kVec) {
-        if (a4 < p.A) {   // A % 4 == 0: all four anchors exist
-            const float* col = cl + a4;
-            int c = g;
-            for (; c + (kScanLoads - 1) * kClassGroups < p.C; c += kScanLoads * kClassGroups) {
-                float4 v4[kScanLoads];
+    float best[kLaneAnchors];
+    int bc[kLaneAnchors];
 #pragma unroll
-                for (int u = 0; u < kScanLoads; ++u)
-                    v4[u] = __ldg(reinterpret_cast<const float4*>(col + (size_t)(c + u * kClassGroups) * p.A));
+    for (int e = 0; e < kLaneAnchors; ++e) {
+        best[e] = -INFINITY;
+        bc[e] = g;
+    }
+    if (kVec) {   // A % 4 == 0: a word's four anchors all exist or none does
+        bool live[kLaneVec];
 #pragma unroll
-                for (int u = 0; u < kScanLoads; ++u) take4(best, bc, v4[u], c + u * kClassGroups);
-            }
-            for (; c < p.C; c += kClassGroups)
-                take4(best, bc, __ldg(reinterpret_cast<const float4*>(col + (size_t)c * p.A)), c);
+        for (int h = 0; h < kLaneVec; ++h) live[h] = a0 + lane_anchor(lane, 4 * h) < p.A;
+        const float* col = cl + a0 + 4 * lane;
+        auto load = [&](int c, int h) -> float4 {
+            return live[h] ? __ldg(reinterpret_cast<const float4*>(col + (size_t)c * p.A + 128 * h))
+                           : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+        };
+        int c = g;
+        for (; c + (kScanLoads - 1) * kClassGroups < p.C; c += kScanLoads * kClassGroups) {
+            float4 v4[kScanLoads][kLaneVec];
+#pragma unroll
+            for (int u = 0; u < kScanLoads; ++u)
+#pragma unroll
+                for (int h = 0; h < kLaneVec; ++h) v4[u][h] = load(c + u * kClassGroups, h);
+#pragma unroll
+            for (int u = 0; u < kScanLoads; ++u)
+#pragma unroll
+                for (int h = 0; h < kLaneVec; ++h) take4(best, bc, h, v4[u][h], c + u * kClassGroups);
         }
+        for (; c < p.C; c += kClassGroups)
+#pragma unroll
+            for (int h = 0; h < kLaneVec; ++h) take4(best, bc, h, load(c, h), c);
     } else {
 #pragma unroll 2
         for (int c = g; c < p.C; c += kClassGroups) {
             const float* row = cl + (size_t)c * p.A;
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                if (a4 + e < p.A) {
-                    const float v = nan_as_ninf(__ldg(row + a4 + e));
+            for (int e = 0; e < kLaneAnchors; ++e) {
+                const long long a = a0 + lane_anchor(lane, e);
+                if (a < p.A) {
+                    const float v = nan_as_ninf(__ldg(row + a));
                     if (v > best[e]) {
                         best[e] = v;
                         bc[e] = c;
