@@ -83,6 +83,13 @@ int32_t ws_version(void);
  * flags synchronously; clears them when clear != 0.  *flags == 0 means none. */
 ws_status ws_device_error(uint32_t* flags, int32_t clear);
 
+/* Diagnostic of that path: launches one thread that arms an mbarrier for 16
+ * bytes no copy will deliver and waits for it at most limit_us (1 .. 1e6)
+ * microseconds; when the wait runs out it sets the timeout bit in the device
+ * error word and returns, as a kernel whose bulk copy never landed does.
+ * Asynchronous on `stream`; read the result with ws_device_error. */
+ws_status ws_selftest_wait_timeout(uint32_t limit_us, cudaStream_t stream);
+
 /* -------------------------------------------------------------- preprocess */
 
 #define WS_RESIZE_STRETCH   0  /* bilinear resize of the whole frame to dst_w x dst_h   */

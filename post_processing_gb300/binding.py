@@ -97,6 +97,7 @@ SIGNATURES = {
     "ws_last_error": (ctypes.c_char_p, []),
     "ws_version": (_i32, []),
     "ws_device_error": (_i32, [ctypes.POINTER(_u32), _i32]),
+    "ws_selftest_wait_timeout": (_i32, [_u32, _vp]),
     "ws_preprocess_validate": (_i32, [ctypes.POINTER(ws_preprocess_desc), _i32]),
     "ws_preprocess": (_i32, [ctypes.POINTER(ws_preprocess_desc), _vp, _i32, _vp, _vp]),
     "ws_topk_validate": (_i32, [_i64, _i64, _i32]),
@@ -178,6 +179,10 @@ def ws_device_error(clear: bool = False) -> tuple[int, int]:
     flags = _u32(0)
     st = lib.ws_device_error(ctypes.byref(flags), int(clear))
     return st, flags.value
+
+
+def ws_selftest_wait_timeout(limit_us: int, stream: int = 0) -> int:
+    return lib.ws_selftest_wait_timeout(limit_us, stream)
 
 
 def ws_preprocess_validate(desc: ws_preprocess_desc, batch: int) -> int:

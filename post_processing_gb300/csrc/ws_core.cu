@@ -5,6 +5,7 @@
 #include <string>
 
 #include "ws_internal.cuh"
+#include "ws_ptx.cuh"
 
 // Error bits raised by kernels whose bounded waits ran out; one copy per
 // device, zero at module load.
@@ -99,9 +100,41 @@ const char* ws_status_string(ws_status s) {
     }
 }
 
+}  // extern "C"
+
+namespace ws {
+
+// An mbarrier armed for 16 bytes that no copy will deliver: the bounded wait
+// runs out, the kernel records the timeout in the device error word and
+// returns -- the path every kernel takes when a bulk copy never lands.
+__global__ void selftest_wait_kernel(uint32_t* err, unsigned long long limit_ns) {
+    __shared__ __align__(8) uint64_t bar;
+    if (threadIdx.x != 0) return;
+    mbar_init(&bar, 1);
+    fence_mbar_init();
+    mbar_arrive_expect_tx(&bar, 16u);
+    if (!mbar_wait_bounded(&bar, 0, limit_ns)) atomicOr(err, kDevErrBulkCopyTimeout);
+}
+
+}  // namespace ws
+
+extern "C" {
+
 const char* ws_last_error(void) { return ws::t_error.c_str(); }
 
 int32_t ws_version(void) { return 100; }  // 0.1.0
+
+ws_status ws_selftest_wait_timeout(uint32_t limit_us, cudaStream_t stream) {
+    ws::clear_error();
+    if (limit_us < 1 || limit_us > 1000000) return ws::fail(WS_ERR_INVALID_ARGUMENT, "limit %u us outside 1..1e6", limit_us);
+    int dev;
+    const ws::DeviceInfo* info;
+    ws_status st = ws::current_device_info(&dev, &info);
+    if (st != WS_OK) return st;
+    ws::selftest_wait_kernel<<<1, 32, 0, stream>>>(ws::device_error_word(), 1000ull * limit_us);
+    WS_TRY_CUDA(cudaGetLastError());
+    return WS_OK;
+}
 
 ws_status ws_device_error(uint32_t* flags, int32_t clear) {
     ws::clear_error();
