@@ -671,20 +671,20 @@ def main():
     lanes_extra = lane_measurements(B, Lane, device, args.latency_samples)
     clk = clocks.stop()
 
-    # End to end through the lane API with host buffers: the producer writes
-    # the frames into the lane's mapped pinned input slot, the preprocess
-    # reads the rows it needs in place across the host link, and the Top-K
-    # writes the K pairs straight into mapped pinned host memory (the
-    # producer / result path of the WarpStream write-up).  Two lanes, each on
-    # its own stream.
-    e2e = None
-    if args.e2e_steps > 0:
+    # End to end through the lane API with host buffers, two lanes each on its
+    # own stream, host clock.  "e2e": the producer writes the frames into the
+    # lane's mapped pinned input slot, the preprocess reads the rows it needs
+    # in place across the host link, and the Top-K writes the K pairs straight
+    # into mapped pinned host memory (the producer / result path of the
+    # WarpStream write-up).  "e2e_copy_in": the other input topology the page
+    # says to measure -- the graph first copies the whole frames from pinned
+    # host memory into a fixed device slot, and copies the K pairs back.
+    def end_to_end(input_mode, result_mode):
         import ctypes
         e_lanes = []
         for _ in range(2):
-            d = B.lane_desc(pre, w["batch"], w["rows"], w["cols"], w["k"], input_mode=B.WS_INPUT_MAPPED,
-                            result_mode=B.WS_RESULT_MAPPED, logits=logits_dev.data_ptr(),
-                            flags=B.WS_LANE_FLAG_NO_TIMING)
+            d = B.lane_desc(pre, w["batch"], w["rows"], w["cols"], w["k"], input_mode=input_mode,
+                            result_mode=result_mode, logits=logits_dev.data_ptr(), flags=B.WS_LANE_FLAG_NO_TIMING)
             lane = Lane(d)
             buf = (ctypes.c_char * frames.nbytes).from_address(lane.buffers.input_host)
             np.frombuffer(buf, dtype=np.uint8)[:] = frames.reshape(-1)
@@ -695,8 +695,8 @@ def main():
         if world > 1:
             torch.distributed.barrier()
         t0 = time.perf_counter()
-        for s in range(args.e2e_steps):
-            lane = e_lanes[s % 2]
+        for s_ in range(args.e2e_steps):
+            lane = e_lanes[s_ % 2]
             if lane.state == B.WS_LANE_IN_FLIGHT:
                 lane.wait()
             lane.acquire()
@@ -705,16 +705,28 @@ def main():
             if lane.state == B.WS_LANE_IN_FLIGHT:
                 lane.wait()
         e_dt = time.perf_counter() - t0
-        e_rate, _ = whole_job_rate(w["batch"] * args.e2e_steps, e_dt, world, device)
-        e2e = {"value": e_rate, "unit": "frames/s", "h2d_bytes_per_step": int(alg["source"]),
+        for lane in e_lanes:
+            lane.close()
+        rate, _ = whole_job_rate(w["batch"] * args.e2e_steps, e_dt, world, device)
+        return rate, e_dt
+
+    e2e = e2e_copy = None
+    if args.e2e_steps > 0:
+        rate, dt = end_to_end(B.WS_INPUT_MAPPED, B.WS_RESULT_MAPPED)
+        e2e = {"value": rate, "unit": "frames/s", "h2d_bytes_per_step": int(alg["source"]),
                "d2h_bytes_per_step": int(w["rows"] * w["k"] * 8),
                "path": "ws_lane_submit/wait on host buffers: input_mode=MAPPED (frames written by the host "
                        "into mapped pinned memory; the kernel reads the needed rows, h2d_bytes_per_step, "
                        "in place), result_mode=MAPPED (the K pairs written into pinned host memory); "
                        "2 lanes on their own streams; host clock",
-               "frames_bytes_per_step": int(frames.nbytes)}
-        for lane in e_lanes:
-            lane.close()
+               "frames_bytes_per_step": int(frames.nbytes),
+               "link_gbs": alg["source"] * args.e2e_steps / dt / 1e9}
+        rate, dt = end_to_end(B.WS_INPUT_COPY, B.WS_RESULT_COPY)
+        e2e_copy = {"value": rate, "unit": "frames/s", "h2d_bytes_per_step": int(frames.nbytes),
+                    "d2h_bytes_per_step": int(w["rows"] * w["k"] * 8),
+                    "path": "input_mode=COPY (cudaMemcpyAsync of the whole frames into a fixed device slot "
+                            "inside the graph), result_mode=COPY; 2 lanes on their own streams; host clock",
+                    "link_gbs": frames.nbytes * args.e2e_steps / dt / 1e9}
 
     for lane in lanes + lanes_1s:
         lane.close()
@@ -763,6 +775,7 @@ def main():
             "detect": detect,
             "lanes": lanes_extra,
             "e2e": e2e,
+            "e2e_copy_in": e2e_copy,
             "gpu_launches": 2 * args.steps,
             "clocks": clk,
             "cpu_baseline": cpu,
