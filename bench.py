@@ -60,8 +60,8 @@ LANES = 3
 # unchanged.  Filled from the committed ncu summary under profiles/.
 NCU_TRAFFIC = {
     "b64_1080p_to_224": {
-        "bytes": 185_219_840,
-        "source_sha": "0888480da5c29cfdd447a74bc1232489025e72fb0f0924f48333c0bb8efadbe5",
+        "bytes": 186_236_672,
+        "source_sha": "73ad60ab8c3f726265642910b71974e9f58f782c3bd0f38fa6f625ad56fa4fa8",
     },
 }
 

@@ -144,13 +144,25 @@ ws_status ws_preprocess_validate(const ws_preprocess_desc* desc, int32_t batch);
  *        src[b * src_frame_stride + j * src_row_stride + 3 * i + c].
  *   dst: device, [batch][3][dst_h][dst_w] (NCHW, contiguous) of the element
  *        type desc->dst_type (float32, half or bfloat16).
- * One kernel launch on `stream`.  Any alignment is accepted; a 16-byte
- * aligned src, row stride and frame stride select the staged bulk-copy
- * kernel, anything else a per-pixel kernel with the same results.
+ * One kernel launch on `stream`, a programmatic dependent of the kernel
+ * before it (it reads and writes nothing until that kernel has finished).
+ * Any alignment is accepted.  Outputs above 2^19 pixels (batch x dst_w x
+ * dst_h) with a 16-byte aligned src, row stride and frame stride take the
+ * staged bulk-copy kernel; smaller outputs, or other alignments, a
+ * per-pixel kernel with the same results (see ws_preprocess_path).
  * Errors: WS_ERR_INVALID_ARGUMENT (NULL pointer, batch < 1, bad descriptor),
  * WS_ERR_CUDA (launch failed). */
 ws_status ws_preprocess(const ws_preprocess_desc* desc, const uint8_t* src, int32_t batch,
                         void* dst, cudaStream_t stream);
+
+#define WS_PRE_PATH_AUTO   0  /* as ws_preprocess                                        */
+#define WS_PRE_PATH_STAGED 1  /* the staged bulk-copy kernel whenever the alignment allows */
+#define WS_PRE_PATH_DIRECT 2  /* the per-pixel kernel                                     */
+
+/* ws_preprocess with the kernel chosen by `path` (the results are the same;
+ * for measurement and tests).  WS_ERR_INVALID_ARGUMENT for an unknown path. */
+ws_status ws_preprocess_path(const ws_preprocess_desc* desc, const uint8_t* src, int32_t batch,
+                             void* dst, int32_t path, cudaStream_t stream);
 
 /* ------------------------------------------------------------------- top-k */
 

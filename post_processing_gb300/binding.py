@@ -31,6 +31,7 @@ WS_RESIZE_STRETCH, WS_RESIZE_LETTERBOX = 0, 1
 WS_NORM_MEAN_STD, WS_NORM_SCALE = 0, 1
 WS_ORDER_RGB, WS_ORDER_BGR = 0, 1
 WS_DTYPE_F32, WS_DTYPE_F16, WS_DTYPE_BF16 = 0, 1, 2
+WS_PRE_PATH_AUTO, WS_PRE_PATH_STAGED, WS_PRE_PATH_DIRECT = 0, 1, 2
 WS_INPUT_DEVICE, WS_INPUT_MAPPED, WS_INPUT_COPY = 0, 1, 2
 WS_RESULT_DEVICE, WS_RESULT_MAPPED, WS_RESULT_COPY = 0, 1, 2
 WS_LANE_FLAG_NO_GRAPH = 1
@@ -100,6 +101,7 @@ SIGNATURES = {
     "ws_selftest_wait_timeout": (_i32, [_u32, _vp]),
     "ws_preprocess_validate": (_i32, [ctypes.POINTER(ws_preprocess_desc), _i32]),
     "ws_preprocess": (_i32, [ctypes.POINTER(ws_preprocess_desc), _vp, _i32, _vp, _vp]),
+    "ws_preprocess_path": (_i32, [ctypes.POINTER(ws_preprocess_desc), _vp, _i32, _vp, _i32, _vp]),
     "ws_topk_validate": (_i32, [_i64, _i64, _i32]),
     "ws_topk_workspace_bytes": (_i32, [_i64, _i64, _i32, ctypes.POINTER(_sz)]),
     "ws_topk_workspace_init": (_i32, [_vp, _sz, _vp]),
@@ -191,6 +193,10 @@ def ws_preprocess_validate(desc: ws_preprocess_desc, batch: int) -> int:
 
 def ws_preprocess(desc: ws_preprocess_desc, src: int, batch: int, dst: int, stream: int = 0) -> int:
     return lib.ws_preprocess(ctypes.byref(desc), src, batch, dst, stream)
+
+
+def ws_preprocess_path(desc: ws_preprocess_desc, src: int, batch: int, dst: int, path: int, stream: int = 0) -> int:
+    return lib.ws_preprocess_path(ctypes.byref(desc), src, batch, dst, path, stream)
 
 
 def ws_topk_validate(rows: int, cols: int, k: int) -> int:

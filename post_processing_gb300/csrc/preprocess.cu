@@ -50,6 +50,11 @@ constexpr int kMaxBand = 8;            // output rows per unit
 constexpr int kMaxStages = 8;
 constexpr int kMaxThreads = 512;
 constexpr int kMaxTableCols = 8192;
+// AUTO: outputs of at most this many pixels (batch x dst_w x dst_h) take the
+// direct kernel.  Batch-1..32 lane graphs on GB300 put the crossover between
+// 8 x 224x224 (401K px: direct 13.6 us, staged 15.8) and 12 x 224x224 (602K:
+// direct 16.6, staged 15.8).
+constexpr long long kDirectMaxPixels = 1LL << 19;
 constexpr unsigned kFull = 0xffffffffu;
 
 struct StagePlan {
@@ -254,8 +259,11 @@ __global__ void __launch_bounds__(kMaxThreads) pre_ring_kernel(const __grid_cons
     unsigned char* slots = smem + p.off_slots;
 
     // Let a programmatic dependent (the Top-K) be launched now; it waits for
-    // this grid's completion before it reads anything.
+    // this grid's completion before it reads anything.  This grid is itself
+    // a programmatic dependent of the previous kernel on the stream: nothing
+    // global is read or written before that kernel has finished.
     asm volatile("griddepcontrol.launch_dependents;");
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     const int tid = threadIdx.x;
     const long long G = gridDim.x;
     const long long first = blockIdx.x;
@@ -311,6 +319,7 @@ __global__ void __launch_bounds__(kMaxThreads) pre_ring_kernel(const __grid_cons
 template <typename OutT>
 __global__ void __launch_bounds__(256) pre_direct_kernel(const __grid_constant__ PreParams p, long long total) {
     asm volatile("griddepcontrol.launch_dependents;");
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     const size_t plane = (size_t)p.dh * p.dw;
     for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < total;
          i += (long long)gridDim.x * blockDim.x) {
@@ -419,6 +428,26 @@ PreTuning default_tuning(const PreParams& p, int batch, const DeviceInfo& info) 
 
 bool g_ring_attr_set[64][3][2];
 
+// A launch as a programmatic dependent of the previous kernel on the stream
+// ("Streams, concurrency and CUDA Graphs", PDL section), unless the caller is
+// inside a NoPdlScope.
+template <typename Kernel, typename... Args>
+ws_status pdl_launch(Kernel kernel, dim3 grid, dim3 block, size_t smem, cudaStream_t stream, Args... args) {
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl_enabled() ? 1 : 0;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, args...);
+    if (e != cudaSuccess) return cuda_fail(e, "preprocess launch");
+    return WS_OK;
+}
+
 template <typename OutT, bool kVec>
 ws_status launch_ring(const PreParams& p, int dev, const DeviceInfo& info, unsigned blocks, int threads, size_t smem,
                       int type_slot, cudaStream_t stream) {
@@ -427,9 +456,10 @@ ws_status launch_ring(const PreParams& p, int dev, const DeviceInfo& info, unsig
                                          info.max_smem_optin));
         g_ring_attr_set[dev][type_slot][kVec] = true;
     }
-    pre_ring_kernel<OutT, kVec><<<blocks, threads, smem, stream>>>(p);
-    return WS_OK;
+    return pdl_launch(pre_ring_kernel<OutT, kVec>, dim3(blocks), dim3(threads), smem, stream, p);
 }
+
+bool g_direct_attr_set[64][3];
 
 template <typename OutT>
 ws_status launch_any(const PreParams& p, bool ring, bool vec, int dev, const DeviceInfo& info, unsigned blocks,
@@ -437,8 +467,18 @@ ws_status launch_any(const PreParams& p, bool ring, bool vec, int dev, const Dev
     if (ring)
         return vec ? launch_ring<OutT, true>(p, dev, info, blocks, threads, smem, type_slot, stream)
                    : launch_ring<OutT, false>(p, dev, info, blocks, threads, smem, type_slot, stream);
-    pre_direct_kernel<OutT><<<blocks, 256, 0, stream>>>(p, total);
-    return WS_OK;
+    // The direct kernel needs no shared memory, but the kernels that follow it
+    // (Top-K stages a 32 KB chunk, NMS far more) do.  Left to its default, an
+    // SM runs it with the largest L1 and must drain and re-partition before
+    // the next kernel's blocks fit: measured as ~2 us added to a batch-1
+    // 640x640 letterbox + Top-5 over 672K graph.  Asking for the shared-heavy
+    // split keeps one partition across the sequence at no cost to this kernel.
+    if (!g_direct_attr_set[dev][type_slot]) {
+        WS_TRY_CUDA(cudaFuncSetAttribute(pre_direct_kernel<OutT>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                         (int)cudaSharedmemCarveoutMaxShared));
+        g_direct_attr_set[dev][type_slot] = true;
+    }
+    return pdl_launch(pre_direct_kernel<OutT>, dim3(blocks), dim3(256), 0, stream, p, total);
 }
 
 }  // namespace
@@ -484,7 +524,7 @@ ws_status validate_preprocess(const ws_preprocess_desc* d, int32_t batch) {
 
 // Launch with an explicit ring tuning (NULL = the default policy).
 ws_status preprocess_launch(const ws_preprocess_desc* d, const uint8_t* src, int32_t batch, void* dst,
-                            cudaStream_t stream, const PreTuning* tuning) {
+                            cudaStream_t stream, const PreTuning* tuning, int32_t path) {
     ws_status st = validate_preprocess(d, batch);
     if (st != WS_OK) return st;
     if (!src || !dst) return fail(WS_ERR_INVALID_ARGUMENT, "src or dst is NULL");
@@ -521,7 +561,12 @@ ws_status preprocess_launch(const ws_preprocess_desc* d, const uint8_t* src, int
                          (batch == 1 || d->src_frame_stride % 16 == 0);
     PreTuning t = tuning ? *tuning : default_tuning(p, batch, *info);
     const size_t smem = ring_layout(p, t);
-    const bool ring_ok = aligned && d->dst_w <= kMaxTableCols && t.band >= 1 && t.band <= kMaxBand &&
+    // The staged ring needs 16-byte aligned rows and pays a fixed set-up per
+    // block (barriers, plan, column table, a copy round trip): small outputs
+    // (a single 224x224 frame) finish sooner one thread per pixel.
+    const bool small = (long long)batch * d->dst_w * d->dst_h <= kDirectMaxPixels;
+    const bool want_ring = path == WS_PRE_PATH_STAGED || (path == WS_PRE_PATH_AUTO && !small);
+    const bool ring_ok = want_ring && aligned && d->dst_w <= kMaxTableCols && t.band >= 1 && t.band <= kMaxBand &&
                          t.stages >= 1 && t.stages <= kMaxStages && t.threads >= 32 &&
                          t.threads <= kMaxThreads && smem <= (size_t)info->max_smem_optin;
     bool vec = false;
@@ -564,7 +609,15 @@ ws_status ws_preprocess_validate(const ws_preprocess_desc* desc, int32_t batch) 
 ws_status ws_preprocess(const ws_preprocess_desc* d, const uint8_t* src, int32_t batch, void* dst,
                         cudaStream_t stream) {
     ws::clear_error();
-    return ws::preprocess_launch(d, src, batch, dst, stream, nullptr);
+    return ws::preprocess_launch(d, src, batch, dst, stream, nullptr, WS_PRE_PATH_AUTO);
+}
+
+ws_status ws_preprocess_path(const ws_preprocess_desc* d, const uint8_t* src, int32_t batch, void* dst,
+                             int32_t path, cudaStream_t stream) {
+    ws::clear_error();
+    if (path < WS_PRE_PATH_AUTO || path > WS_PRE_PATH_DIRECT)
+        return ws::fail(WS_ERR_INVALID_ARGUMENT, "preprocess path %d", path);
+    return ws::preprocess_launch(d, src, batch, dst, stream, nullptr, path);
 }
 
 }  // extern "C"

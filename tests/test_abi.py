@@ -155,6 +155,12 @@ def test_lane_descriptor_rejected(B):
         assert st == B.WS_ERR_INVALID_ARGUMENT and h is None, kw
 
 
+def test_preprocess_path_rejected(B):
+    d = B.preprocess_desc(64, 48, 32, 32)
+    assert B.ws_preprocess_path(d, 4096, 1, 8192, 3, 0) == B.WS_ERR_INVALID_ARGUMENT
+    assert B.ws_preprocess_path(d, 4096, 1, 8192, -1, 0) == B.WS_ERR_INVALID_ARGUMENT
+
+
 def test_detection_lane_descriptor(B):
     pre = B.preprocess_desc(1280, 720, 640, 640, letterbox=True, norm="scale")
     fake = dict(flags=B.WS_LANE_FLAG_NO_DEVICE)

@@ -25,7 +25,7 @@ def B():
 
 
 def run_gpu(B, frames, sw, sh, dw, dh, *, letterbox=False, norm="mean_std", row_stride=None,
-            frame_stride=None, offset=0, pad_value=114):
+            frame_stride=None, offset=0, pad_value=114, path=0):
     """frames: uint8 [B, H, stride] laid out with the given strides."""
     batch = frames.shape[0]
     rs = 3 * sw if row_stride is None else row_stride
@@ -38,10 +38,13 @@ def run_gpu(B, frames, sw, sh, dw, dh, *, letterbox=False, norm="mean_std", row_
     out = torch.full((batch, 3, dh, dw), float("nan"), dtype=torch.float32, device="cuda")
     d = B.preprocess_desc(sw, sh, dw, dh, letterbox=letterbox, norm=norm, row_stride=rs,
                           frame_stride=fs, pad_value=pad_value)
-    B.check(B.ws_preprocess(d, dev.data_ptr() + offset, batch, out.data_ptr(),
-                            torch.cuda.current_stream().cuda_stream))
+    B.check(B.ws_preprocess_path(d, dev.data_ptr() + offset, batch, out.data_ptr(), path,
+                                 torch.cuda.current_stream().cuda_stream))
     torch.cuda.synchronize()
     return out.cpu().numpy()
+
+
+PATHS = [0, 1, 2]   # WS_PRE_PATH_AUTO, _STAGED (the bulk-copy ring whenever aligned), _DIRECT
 
 
 def compare(got, want):
@@ -52,12 +55,14 @@ def compare(got, want):
     return err
 
 
+@pytest.mark.parametrize("path", PATHS, ids=["auto", "staged", "direct"])
 @pytest.mark.parametrize("name", list(synth.WORKLOADS))
-def test_workload_parity(B, oracle, name):
+def test_workload_parity(B, oracle, name, path):
     w = synth.WORKLOADS[name]
     frames = synth.make_frames(name)
     lb = w["resize"] == "letterbox"
-    got = run_gpu(B, frames, w["src_w"], w["src_h"], w["dst_w"], w["dst_h"], letterbox=lb, norm=w["norm"])
+    got = run_gpu(B, frames, w["src_w"], w["src_h"], w["dst_w"], w["dst_h"], letterbox=lb, norm=w["norm"],
+                  path=path)
     want = oracle.preprocess(frames, w["src_w"], w["src_h"], w["dst_w"], w["dst_h"], letterbox=lb,
                              norm=w["norm"])
     compare(got, want)
@@ -86,14 +91,15 @@ ODD = [
 ]
 
 
+@pytest.mark.parametrize("path", [1, 2], ids=["staged", "direct"])
 @pytest.mark.parametrize("case", ODD, ids=[f"{c[0]}x{c[1]}-{c[2]}x{c[3]}-lb{int(c[4])}-o{c[8]}" for c in ODD])
-def test_odd_shapes(B, oracle, case):
+def test_odd_shapes(B, oracle, case, path):
     sw, sh, dw, dh, lb, norm, er, ef, off, batch = case
     rs = 3 * sw + er
     fs = rs * sh + ef
     frames = synth.frames_uniform(sw * 7 + sh, batch, sh, sw, row_stride=rs)
     got = run_gpu(B, frames, sw, sh, dw, dh, letterbox=lb, norm=norm, row_stride=rs, frame_stride=fs,
-                  offset=off)
+                  offset=off, path=path)
     buf = np.zeros((batch, fs), np.uint8)
     buf[:, :rs * sh] = frames.reshape(batch, -1)
     want = oracle.preprocess(buf, sw, sh, dw, dh, letterbox=lb, norm=norm, row_stride=rs, frame_stride=fs)
@@ -124,7 +130,7 @@ def test_no_device_error_raised(B):
 # ---- precision- and format-specialised outputs ------------------------------
 
 def run_gpu_typed(B, frames, sw, sh, dw, dh, dst_type, channel_order=0, letterbox=False, norm="mean_std",
-                  offset=0):
+                  offset=0, path=1):
     batch = frames.shape[0]
     flat = np.zeros(offset + frames.size + 64, np.uint8)
     flat[offset:offset + frames.size] = frames.reshape(-1)
@@ -133,8 +139,8 @@ def run_gpu_typed(B, frames, sw, sh, dw, dh, dst_type, channel_order=0, letterbo
     out = torch.full((batch, 3, dh, dw), float("nan"), dtype=tdt, device="cuda")
     d = B.preprocess_desc(sw, sh, dw, dh, letterbox=letterbox, norm=norm, channel_order=channel_order,
                           dst_type=dst_type)
-    B.check(B.ws_preprocess(d, dev.data_ptr() + offset, batch, out.data_ptr(),
-                            torch.cuda.current_stream().cuda_stream))
+    B.check(B.ws_preprocess_path(d, dev.data_ptr() + offset, batch, out.data_ptr(), path,
+                                 torch.cuda.current_stream().cuda_stream))
     torch.cuda.synchronize()
     return out.cpu()
 
@@ -158,9 +164,10 @@ def ulp_of(x, dst_type, B):
 SHAPES_TYPED = [("b64_1080p_to_224", 8), ("b1_720p_letterbox_640", 1), ("b8_4k_to_512", 2), (None, 2)]
 
 
+@pytest.mark.parametrize("path", [1, 2], ids=["staged", "direct"])
 @pytest.mark.parametrize("dst", ["f16", "bf16"])
 @pytest.mark.parametrize("name,batch", SHAPES_TYPED, ids=[str(s[0]) for s in SHAPES_TYPED])
-def test_half_outputs(B, oracle, dst, name, batch):
+def test_half_outputs(B, oracle, dst, name, batch, path):
     """Half outputs equal the FP32 oracle rounded to the format, except where
     the two FP32 values (within 1e-5 of each other) straddle a rounding
     boundary: there an element may differ by one unit in the last place, plus
@@ -174,7 +181,7 @@ def test_half_outputs(B, oracle, dst, name, batch):
         sw, sh, dw, dh, lb, norm, off = (w["src_w"], w["src_h"], w["dst_w"], w["dst_h"],
                                           w["resize"] == "letterbox", w["norm"], 0)
         frames = synth.make_frames(name, batch=batch)
-    got = run_gpu_typed(B, frames, sw, sh, dw, dh, dst_type, letterbox=lb, norm=norm, offset=off)
+    got = run_gpu_typed(B, frames, sw, sh, dw, dh, dst_type, letterbox=lb, norm=norm, offset=off, path=path)
     want32 = oracle.preprocess(frames, sw, sh, dw, dh, letterbox=lb, norm=norm)
     want = rounded(want32, dst_type, B)
     diff = (got.float() - want.float()).abs()
