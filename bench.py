@@ -108,8 +108,9 @@ def algorithmic_bytes(w: dict, out_bytes: int = 4) -> dict:
     src = src_sectors * 32 * w["batch"]
     dst = w["batch"] * 3 * w["dst_w"] * w["dst_h"] * out_bytes
     topk = w["rows"] * w["cols"] * 4 + w["rows"] * w["k"] * 8
+    full = w["batch"] * 3 * w["src_w"] * w["src_h"] + dst     # every source byte read: a sanity bound
     return {"preprocess": int(src + dst), "source": int(src), "tensor": int(dst), "topk": int(topk),
-            "total": int(src + dst + topk)}
+            "total": int(src + dst + topk), "full_frame_preprocess": int(full)}
 
 
 # ----------------------------------------------------------------- clocks
@@ -203,6 +204,25 @@ def whole_job_rate(units_per_rank: float, seconds_per_rank: float, world: int, d
 
 # ----------------------------------------------------------------- oracle baseline
 
+def host_cpu() -> str:
+    """The host CPU as /proc/cpuinfo names it (x86: model name; Arm: the
+    implementer and part codes), or the platform string."""
+    import platform
+    fields = {}
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                k, _, v = line.partition(":")
+                fields.setdefault(k.strip(), v.strip())
+    except OSError:
+        pass
+    if fields.get("model name"):
+        return fields["model name"]
+    if fields.get("CPU implementer"):
+        return f"{platform.machine()} implementer {fields['CPU implementer']} part {fields.get('CPU part', '?')}"
+    return platform.processor() or platform.machine()
+
+
 def cpu_baseline(w: dict, frames: np.ndarray, logits: np.ndarray, budget_s: float = 10.0) -> dict:
     """The oracle as it stands, single-threaded, repeated over a bounded sample."""
     import oracle as oracle_pkg
@@ -221,7 +241,7 @@ def cpu_baseline(w: dict, frames: np.ndarray, logits: np.ndarray, budget_s: floa
         if time.perf_counter() - t0 >= budget_s:
             break
     dt = time.perf_counter() - t0
-    return {"value": done / dt, "unit": "frames/s", "cores": 1, "kind": "oracle",
+    return {"value": done / dt, "unit": "frames/s", "cores": 1, "kind": "oracle", "cpu_model": host_cpu(),
             "sample": f"{done} frames of the workload (preprocess of the frame + Top-{w['k']} of its "
                       f"{w['cols']}-logit row), single-threaded C++ oracle, {dt:.1f} s"}
 
@@ -253,7 +273,7 @@ def cpu_baseline_all_cores(w: dict, frames: np.ndarray, logits: np.ndarray, budg
         t.join()
     dt = time.perf_counter() - t0
     done = sum(counts)
-    return {"value": done / dt, "unit": "frames/s", "cores": cores, "kind": "oracle",
+    return {"value": done / dt, "unit": "frames/s", "cores": cores, "kind": "oracle", "cpu_model": host_cpu(),
             "sample": f"{done} frames on {cores} threads (one per host core), {dt:.1f} s"}
 
 
@@ -284,7 +304,7 @@ def run_reference(args, w: dict) -> None:
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000 * dt / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "data": "synthetic", "config": workload_config(args.workload, w),
-        "cpu_baseline": {"value": value, "unit": "frames/s", "cores": 1, "kind": "oracle",
+        "cpu_baseline": {"value": value, "unit": "frames/s", "cores": 1, "kind": "oracle", "cpu_model": host_cpu(),
                          "sample": "one frame of the workload per step (its preprocess + the Top-K of its "
                                    "logit row), single-threaded C++ oracle"},
         "e2e": {"value": value, "unit": "frames/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -797,6 +817,7 @@ def main():
             "roofline": {"bound": "hbm", "kernel": "pre_ring_kernel", "achieved": achieved, "peak": peak,
                          "unit": "GB/s", "frac": achieved / peak, "peak_source": peak_src,
                          "traffic": traffic, "algorithmic_bytes_per_launch": alg["preprocess"],
+                         "full_frame_bytes_per_launch": alg["full_frame_preprocess"],
                          "avg_launch_us": pre_avg_us, "launches_timed": kernel_launches,
                          "timing": "CUDA events on the launching stream around back-to-back launches "
                                    "on the lanes' rotating buffers, after the timed region",

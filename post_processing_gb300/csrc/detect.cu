@@ -185,6 +185,7 @@ __device__ __forceinline__ void finish_tile(const DetParams& p, ScanShared& sh, 
 template <bool kVec>
 __global__ void __launch_bounds__(kDecodeThreads, kScanBlocksPerSM) detect_scan_kernel(const __grid_constant__ DetParams p) {
     __shared__ ScanShared sh;
+    asm volatile("griddepcontrol.wait;" ::: "memory");   // the head and the counters are the previous kernels'
     const int b = blockIdx.y, lane = threadIdx.x & 31, g = threadIdx.x >> 5;
     const long long a0 = (long long)blockIdx.x * kDecodeAnchors;
     const float* cl = p.head + (size_t)b * p.ch * p.A + (size_t)(4 * p.R) * p.A;
@@ -728,25 +729,13 @@ bool g_nms_attr_set[64];
 ws_status launch_decode(DetParams p, int32_t batch, cudaStream_t stream) {
     const int tiles = (int)((p.A + kDecodeAnchors - 1) / kDecodeAnchors);
     const bool vec = p.A % 4 == 0 && (uintptr_t)p.head % 16 == 0;
-    if (vec) {
-        detect_scan_kernel<true><<<dim3((unsigned)tiles, (unsigned)batch), kDecodeThreads, 0, stream>>>(p);
-    } else {
-        detect_scan_kernel<false><<<dim3((unsigned)tiles, (unsigned)batch), kDecodeThreads, 0, stream>>>(p);
-    }
-    cudaError_t e = cudaGetLastError();
+    // the scan, a programmatic dependent of whatever wrote the head; then the
+    // DFL boxes, a programmatic dependent of the scan
+    const dim3 scan_grid((unsigned)tiles, (unsigned)batch);
+    cudaError_t e = vec ? launch_pdl(detect_scan_kernel<true>, scan_grid, dim3(kDecodeThreads), 0, stream, p)
+                        : launch_pdl(detect_scan_kernel<false>, scan_grid, dim3(kDecodeThreads), 0, stream, p);
     if (e != cudaSuccess) return cuda_fail(e, "decode launch");
-    // the DFL boxes, a programmatic dependent of the scan
-    cudaLaunchConfig_t cfg{};
-    cfg.gridDim = dim3(kDflBlocks, (unsigned)batch);
-    cfg.blockDim = dim3(kDecodeThreads);
-    cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = pdl_enabled() ? 1 : 0;
-    e = cudaLaunchKernelEx(&cfg, detect_dfl_kernel, p);
-    if (e == cudaSuccess) e = cudaGetLastError();
+    e = launch_pdl(detect_dfl_kernel, dim3(kDflBlocks, (unsigned)batch), dim3(kDecodeThreads), 0, stream, p);
     if (e != cudaSuccess) return cuda_fail(e, "DFL launch");
     return WS_OK;
 }
@@ -767,18 +756,7 @@ ws_status launch_nms(const DetParams& p, int32_t batch, cudaStream_t stream) {
                                          info->max_smem_optin));
         g_nms_attr_set[dev] = true;
     }
-    cudaLaunchConfig_t cfg{};
-    cfg.gridDim = dim3((unsigned)batch);
-    cfg.blockDim = dim3(kNmsThreads);
-    cfg.dynamicSmemBytes = smem;
-    cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = pdl_enabled() ? 1 : 0;
-    cudaError_t e = cudaLaunchKernelEx(&cfg, detect_nms_kernel, p);
-    if (e == cudaSuccess) e = cudaGetLastError();
+    const cudaError_t e = launch_pdl(detect_nms_kernel, dim3((unsigned)batch), dim3(kNmsThreads), smem, stream, p);
     if (e != cudaSuccess) return cuda_fail(e, "NMS launch");
     return WS_OK;
 }

@@ -428,22 +428,11 @@ PreTuning default_tuning(const PreParams& p, int batch, const DeviceInfo& info) 
 
 bool g_ring_attr_set[64][3][2];
 
-// A launch as a programmatic dependent of the previous kernel on the stream
-// ("Streams, concurrency and CUDA Graphs", PDL section), unless the caller is
-// inside a NoPdlScope.
+// Both preprocess kernels launch as programmatic dependents of the kernel
+// before them and wait in griddepcontrol.wait before their first read.
 template <typename Kernel, typename... Args>
 ws_status pdl_launch(Kernel kernel, dim3 grid, dim3 block, size_t smem, cudaStream_t stream, Args... args) {
-    cudaLaunchConfig_t cfg{};
-    cfg.gridDim = grid;
-    cfg.blockDim = block;
-    cfg.dynamicSmemBytes = smem;
-    cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = pdl_enabled() ? 1 : 0;
-    cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, args...);
+    cudaError_t e = launch_pdl(kernel, grid, block, smem, stream, args...);
     if (e != cudaSuccess) return cuda_fail(e, "preprocess launch");
     return WS_OK;
 }

@@ -603,20 +603,10 @@ ws_status ws_topk(const float* x, int64_t rows, int64_t cols, int32_t k, float* 
         g_topk_attr_set[dev] = true;
     }
     p.err = device_error_word();
-    cudaLaunchConfig_t cfg{};
-    cfg.gridDim = dim3((unsigned)blocks);
-    cfg.blockDim = dim3(kThreads);
     // the staged chunk only needs the row's length when the row is short
-    cfg.dynamicSmemBytes = (size_t)kSharedBytes + (size_t)(p.chunk + 3) / 4 * 16;
-    cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = pdl_enabled() ? 1 : 0;
-    cudaError_t e = vec ? cudaLaunchKernelEx(&cfg, topk_kernel<true>, p) : cudaLaunchKernelEx(&cfg, topk_kernel<false>, p);
-    if (e != cudaSuccess) return cuda_fail(e, "top-k launch");
-    e = cudaGetLastError();
+    const size_t smem = (size_t)kSharedBytes + (size_t)(p.chunk + 3) / 4 * 16;
+    const cudaError_t e = vec ? launch_pdl(topk_kernel<true>, dim3((unsigned)blocks), dim3(kThreads), smem, stream, p)
+                              : launch_pdl(topk_kernel<false>, dim3((unsigned)blocks), dim3(kThreads), smem, stream, p);
     if (e != cudaSuccess) return cuda_fail(e, "top-k launch");
     return WS_OK;
 }

@@ -46,14 +46,34 @@ enum : uint32_t {
 // parameter (no relocatable device code, so they cannot name it directly).
 uint32_t* device_error_word();
 
-// Programmatic dependent launch of the stream-ordered kernels (Top-K, DFL,
-// NMS): on unless the calling thread is inside a NoPdlScope (a lane with
-// WS_LANE_FLAG_NO_PDL enqueuing or capturing its path).
+// Programmatic dependent launch of the stream-ordered kernels (preprocess,
+// Top-K, class scan, DFL, NMS): on unless the calling thread is inside a
+// NoPdlScope (a lane with WS_LANE_FLAG_NO_PDL enqueuing or capturing its path).
 bool pdl_enabled();
 struct NoPdlScope {
     bool prev;
     explicit NoPdlScope(bool active);
     ~NoPdlScope();
 };
+
+// Launches `kernel` as a programmatic dependent of the previous kernel on the
+// stream ("Streams, concurrency and CUDA Graphs", PDL section) when
+// pdl_enabled(), else as an ordinary launch.  Every kernel launched this way
+// executes griddepcontrol.wait before its first global-memory access.
+template <typename Kernel, typename... Args>
+cudaError_t launch_pdl(Kernel kernel, dim3 grid, dim3 block, size_t smem, cudaStream_t stream, Args... args) {
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl_enabled() ? 1 : 0;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, args...);
+    return e == cudaSuccess ? cudaGetLastError() : e;
+}
 
 }  // namespace ws
