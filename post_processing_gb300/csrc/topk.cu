@@ -30,6 +30,8 @@
 // so the workspace is ready for the next call or graph replay) merges the
 // chunks' keys with the same threshold / rank steps, taking as threshold the
 // largest K-th key over chunks.
+// Many short rows take a second kernel with one warp per row and no block
+// barrier (topk_warp_kernel, further down); use_warp_kernel() picks it.
 #include <algorithm>
 #include <cmath>
 #include <mutex>
@@ -487,6 +489,254 @@ __global__ void __launch_bounds__(kThreads, 4) topk_kernel(const __grid_constant
     if (tid == 0) p.tickets[row] = 0u;   // ready for the next call / replay
 }
 
+// ---------------------------------------------------------------------------
+// Many short rows (at most kWarpMaxCols entries; see use_warp_kernel): one
+// warp per row, no block-wide barrier.  The row sits in the warp's registers (V values per lane); the
+// selection is the same threshold / candidates / rank scheme as above, with
+// warp-wide steps only:
+//  1. delegates: the maximum of each 4-value group (NaN and padding count as
+//     -inf); V / 4 per lane.
+//  2. threshold t: a value with at least K delegates >= t, found by
+//     bisection between the smallest and the largest delegate, counting with
+//     redux.sync.  Those delegates are K distinct elements >= t, so every
+//     element of the row's Top-K is >= t.
+//  3. the elements >= t (typically K plus a few) go to the warp's slice of
+//     shared memory as 64-bit keys, each lane's slots from a warp scan.
+//  4. each candidate's rank is the number of candidates with a larger key.
+// Without K delegates above -inf, every element is a candidate.  If more than
+// kWarpCap elements are candidates (a constant row, many NaN), an exact
+// selection replaces steps 2-4: the K-th largest value is built bit by bit
+// from warp counts, the elements above it are taken, and the ties at it are
+// taken in index order, lowest first.
+// ---------------------------------------------------------------------------
+constexpr int kWarpMaxCols = 2048;
+constexpr int kWarpCap = 256;          // candidate keys per warp in shared memory
+constexpr int kWarpSlots = kWarpCap;
+constexpr int kWarpRounds = 4;         // threshold search rounds (3 pivots each: 4x narrower)
+
+struct TopkWarpParams {
+    const float* x;
+    long long rows;
+    int cols;
+    int k;
+    float* out_val;
+    int* out_idx;
+};
+
+// Element index of a lane's i-th register: 16-byte loads put 4 consecutive
+// elements in each lane (a warp covers 128 per load); scalar loads 1 (32).
+template <bool kVec>
+__device__ __forceinline__ int warp_elem(int i, int lane) {
+    return kVec ? 128 * (i >> 2) + 4 * lane + (i & 3) : 32 * i + lane;
+}
+
+__device__ __forceinline__ uint32_t warp_scan_excl(uint32_t v, uint32_t& total) {
+    const int lane = threadIdx.x & 31;
+    uint32_t incl = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t y = __shfl_up_sync(kFull, incl, o);
+        if (lane >= o) incl += y;
+    }
+    total = __shfl_sync(kFull, incl, 31);
+    return incl - v;
+}
+
+template <int V, bool kVec>
+__global__ void __launch_bounds__(128) topk_warp_kernel(const __grid_constant__ TopkWarpParams p) {
+    extern __shared__ __align__(16) unsigned long long wsm[];   // [warps][kWarpSlots]
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    const long long row = (long long)blockIdx.x * (blockDim.x >> 5) + w;
+    if (row >= p.rows) return;
+    unsigned long long* cand = wsm + w * kWarpSlots;
+    const int n = p.cols, k = p.k;
+    const float* xr = p.x + row * (long long)n;
+    const float qnan = __int_as_float(0x7fffffff);
+
+    float v[V];
+    if (kVec) {
+#pragma unroll
+        for (int j = 0; j < V / 4; ++j) {
+            const int e = 128 * j + 4 * lane;   // n % 4 == 0: a group is whole or absent
+            const float4 f = e < n ? __ldg(reinterpret_cast<const float4*>(xr + e)) : make_float4(qnan, qnan, qnan, qnan);
+            v[4 * j] = f.x;
+            v[4 * j + 1] = f.y;
+            v[4 * j + 2] = f.z;
+            v[4 * j + 3] = f.w;
+        }
+    } else {
+#pragma unroll
+        for (int i = 0; i < V; ++i) {
+            const int e = 32 * i + lane;
+            v[i] = e < n ? __ldg(xr + e) : qnan;
+        }
+    }
+
+    // 1-2. delegates and the bisected threshold
+    constexpr int G = V / 4;
+    float d[G];
+    uint32_t nvalid = 0, dmin = 0xffffffffu, dmax = 0u;
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+        d[g] = fmaxf(fmaxf(fmaxf(-INFINITY, v[4 * g]), fmaxf(v[4 * g + 1], v[4 * g + 2])), v[4 * g + 3]);
+        const uint32_t ob = order_bits(d[g]);
+        const bool valid = d[g] > -INFINITY;
+        nvalid += valid ? 1u : 0u;
+        dmin = min(dmin, valid ? ob : 0xffffffffu);
+        dmax = max(dmax, ob);
+    }
+    nvalid = __reduce_add_sync(kFull, nvalid);
+    bool by_value = nvalid >= (uint32_t)k;
+    float t = -INFINITY;
+    if (by_value) {
+        dmin = __reduce_min_sync(kFull, dmin);
+        dmax = __reduce_max_sync(kFull, dmax);
+        auto value_of = [](uint32_t u) { return __uint_as_float((u & 0x80000000u) ? (u & 0x7fffffffu) : ~u); };
+        float lo = value_of(dmin);                  // count(d >= lo) = nvalid >= K
+        float hi = fminf(value_of(dmax), 3.402823466e38f);
+        // Only lo must keep at least K delegates at or above it; hi only
+        // narrows the search.  Each round counts three pivots at once (their
+        // warp sums are independent, so their latencies overlap).
+        for (int r = 0; r < kWarpRounds; ++r) {
+            const float q1 = 0.75f * lo + 0.25f * hi, q2 = 0.5f * lo + 0.5f * hi, q3 = 0.25f * lo + 0.75f * hi;
+            if (!(q2 > lo && q2 < hi)) break;
+            uint32_t c1 = 0, c2 = 0, c3 = 0;
+#pragma unroll
+            for (int g = 0; g < G; ++g) {
+                c1 += d[g] >= q1 ? 1u : 0u;
+                c2 += d[g] >= q2 ? 1u : 0u;
+                c3 += d[g] >= q3 ? 1u : 0u;
+            }
+            c1 = __reduce_add_sync(kFull, c1);
+            c2 = __reduce_add_sync(kFull, c2);
+            c3 = __reduce_add_sync(kFull, c3);
+            const uint32_t kk = (uint32_t)k;
+            // counts fall as the pivot rises: take the highest pivot that keeps K
+            const float nlo = c3 >= kk ? q3 : c2 >= kk ? q2 : c1 >= kk ? q1 : lo;
+            const float nhi = c1 < kk ? q1 : c2 < kk ? q2 : c3 < kk ? q3 : hi;
+            lo = fmaxf(lo, nlo);
+            hi = nhi;
+        }
+        t = lo;
+    }
+
+    // 3. candidates: elements >= t (every present element without a threshold)
+    unsigned long long taken = 0;   // bit i: register i is a candidate
+#pragma unroll
+    for (int i = 0; i < V; ++i) {
+        const bool take = by_value ? v[i] >= t : warp_elem<kVec>(i, lane) < n;
+        taken |= (unsigned long long)(take ? 1u : 0u) << i;
+    }
+    uint32_t total;
+    uint32_t pos = warp_scan_excl((uint32_t)__popcll(taken), total);
+    if (total <= (uint32_t)kWarpCap) {
+        // A lane visits only its own candidates (usually none or one) and
+        // re-reads each by index from the cached row.
+        for (; taken; taken &= taken - 1) {
+            const int e = warp_elem<kVec>(__ffsll(taken) - 1, lane);
+            cand[pos++] = make_key(order_bits(__ldg(xr + e)), (uint32_t)e);
+        }
+    } else {
+        // Exact selection.  ob[i]: order bits, 0 for padding (below every
+        // element, NaN included, which maps to -inf).
+        uint32_t ob[V];
+#pragma unroll
+        for (int i = 0; i < V; ++i) ob[i] = warp_elem<kVec>(i, lane) < n ? order_bits(v[i]) : 0u;
+        uint32_t T = 0;   // the K-th largest order bits: the largest T with count(ob >= T) >= K
+        for (int b = 31; b >= 0; --b) {
+            const uint32_t c_try = T | (1u << b);
+            uint32_t c = 0;
+#pragma unroll
+            for (int i = 0; i < V; ++i) c += ob[i] >= c_try ? 1u : 0u;
+            if (__reduce_add_sync(kFull, c) >= (uint32_t)k) T = c_try;
+        }
+        uint32_t gt = 0;
+#pragma unroll
+        for (int i = 0; i < V; ++i) gt += ob[i] > T ? 1u : 0u;
+        uint32_t ngt;
+        pos = warp_scan_excl(gt, ngt);   // ngt < K
+#pragma unroll
+        for (int i = 0; i < V; ++i)
+            if (ob[i] > T) cand[pos++] = make_key(ob[i], (uint32_t)warp_elem<kVec>(i, lane));
+        // ties at T, lowest indices first: registers in index order, a tile
+        // (one register group across the warp) at a time
+        const uint32_t need = (uint32_t)k - ngt;
+        uint32_t ties = 0;                   // ties taken so far (warp-uniform)
+        constexpr int kPer = kVec ? 4 : 1;   // registers of one lane in a tile
+#pragma unroll
+        for (int j = 0; j < V / kPer; ++j) {
+            if (ties < need) {
+                uint32_t eq = 0;
+#pragma unroll
+                for (int c = 0; c < kPer; ++c) eq += ob[kPer * j + c] == T ? 1u : 0u;
+                uint32_t tile_total;
+                uint32_t slot = ngt + ties + warp_scan_excl(eq, tile_total);
+#pragma unroll
+                for (int c = 0; c < kPer; ++c) {
+                    const int i = kPer * j + c;
+                    if (ob[i] == T && slot < (uint32_t)k)
+                        cand[slot++] = make_key(T, (uint32_t)warp_elem<kVec>(i, lane));
+                }
+                ties += tile_total;
+            }
+        }
+        total = (uint32_t)k;
+    }
+    __syncwarp();
+
+    // 4. rank and emit: each lane ranks two candidates per pass over the list
+    for (uint32_t base = 0; base < total; base += 64) {
+        const uint32_t i0 = base + lane, i1 = base + 32 + lane;
+        const unsigned long long a = i0 < total ? cand[i0] : ~0ull;
+        const unsigned long long b = i1 < total ? cand[i1] : ~0ull;
+        int ra = 0, rb = 0;
+#pragma unroll 4
+        for (uint32_t j = 0; j < total; ++j) {
+            const unsigned long long c = cand[j];
+            ra += c > a ? 1 : 0;
+            rb += c > b ? 1 : 0;
+        }
+        if (i0 < total && ra < k) {
+            p.out_val[row * k + ra] = key_value(a, xr);
+            p.out_idx[row * k + ra] = (int)key_index(a);
+        }
+        if (i1 < total && rb < k) {
+            p.out_val[row * k + rb] = key_value(b, xr);
+            p.out_idx[row * k + rb] = (int)key_index(b);
+        }
+    }
+}
+
+// The one-warp-per-row kernel has fewer steps per row but a longer serial
+// chain per warp than the block kernel.  Measured on GB300 (back-to-back
+// launches): it wins from about two rows per SM (608 x 1000: 4.1 against
+// 5.1 us; 4096 x 1000: 8.8 against 24.0 us) and on rows of at most 512
+// entries (304 x 256: 3.2 against 5.5 us); with fewer, longer rows the block
+// kernel's wider fan-out is faster (64 x 1000: 3.3 against 4.0 us).
+bool use_warp_kernel(int64_t rows, int64_t cols, int sm_count) {
+    return cols <= kWarpMaxCols && (cols <= 512 || rows >= 2LL * sm_count);
+}
+
+template <int V>
+cudaError_t launch_warp_v(const TopkWarpParams& p, bool vec, int warps, cudaStream_t stream) {
+    const long long blocks = (p.rows + warps - 1) / warps;
+    const size_t smem = (size_t)warps * kWarpSlots * sizeof(unsigned long long);
+    return vec ? launch_pdl(topk_warp_kernel<V, true>, dim3((unsigned)blocks), dim3(32 * warps), smem, stream, p)
+               : launch_pdl(topk_warp_kernel<V, false>, dim3((unsigned)blocks), dim3(32 * warps), smem, stream, p);
+}
+
+// Rows of at most kWarpMaxCols entries: one warp per row, the row in
+// V = 8 .. 64 registers per lane.
+cudaError_t launch_topk_warp(const TopkWarpParams& p, bool vec, int sm_count, cudaStream_t stream) {
+    // one warp per block while the rows alone do not fill the SMs, four after
+    const int warps = p.rows <= sm_count ? 1 : 4;
+    if (p.cols <= 256) return launch_warp_v<8>(p, vec, warps, stream);
+    if (p.cols <= 512) return launch_warp_v<16>(p, vec, warps, stream);
+    if (p.cols <= 1024) return launch_warp_v<32>(p, vec, warps, stream);
+    return launch_warp_v<64>(p, vec, warps, stream);
+}
+
 size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
 bool g_topk_attr_set[64];
@@ -572,14 +822,23 @@ ws_status ws_topk(const float* x, int64_t rows, int64_t cols, int32_t k, float* 
     if (need > 0 && (uintptr_t)workspace % 256 != 0)
         return fail(WS_ERR_INVALID_ARGUMENT, "workspace must be 256-byte aligned");
 
-    TopkParams p{};
-    p.x = x;
-    p.cols = cols;
-    p.k = k;
     int dev;
     const DeviceInfo* info;
     st = current_device_info(&dev, &info);
     if (st != WS_OK) return st;
+    const bool vec = (cols % 4 == 0) && ((uintptr_t)x % 16 == 0);
+    if (use_warp_kernel(rows, cols, info->sm_count)) {
+        if ((rows + 3) / 4 > 2147483647LL) return fail(WS_ERR_UNSUPPORTED, "too many rows");
+        const TopkWarpParams wp{x, rows, (int)cols, k, out_val, out_idx};
+        const cudaError_t e = launch_topk_warp(wp, vec, info->sm_count, stream);
+        if (e != cudaSuccess) return cuda_fail(e, "top-k launch");
+        return WS_OK;
+    }
+
+    TopkParams p{};
+    p.x = x;
+    p.cols = cols;
+    p.k = k;
     p.nchunks = blocks_per_row(rows, cols, info->sm_count);
     p.chunk = chunk_len(cols, p.nchunks);
     p.nchunks = (int)((cols + p.chunk - 1) / p.chunk);
@@ -592,7 +851,6 @@ ws_status ws_topk(const float* x, int64_t rows, int64_t cols, int32_t k, float* 
     }
     const long long blocks = rows * p.nchunks;
     if (blocks > 2147483647LL) return fail(WS_ERR_UNSUPPORTED, "too many blocks");
-    const bool vec = (cols % 4 == 0) && ((uintptr_t)x % 16 == 0);
     // Programmatic dependent launch ("Streams, concurrency and CUDA Graphs",
     // PDL section): the grid may be launched while the previous kernel on the
     // stream is still running and waits in griddepcontrol.wait, which hides

@@ -148,3 +148,76 @@ def test_torch_sort_agrees(B):
     t = torch.from_numpy(np.where(np.isnan(x), -np.inf, x)) + 0.0
     sv, si = torch.sort(t, dim=1, descending=True, stable=True)
     assert np.array_equal(i, si[:, :32].numpy().astype(np.int32))
+
+
+# Rows of at most 2048 entries take the one-warp-per-row kernel when there
+# are at least two rows per SM, or when the rows hold at most 512 entries
+# (8, 16, 32 or 64 values per lane); the block kernel takes the rest.  The
+# cases below are sized so that they reach the kernel they name: lengths at
+# each register-count boundary, aligned and misaligned (16-byte vs scalar
+# loads), row counts on both sides of the choice, and rows built to reach the
+# warp kernel's exact fallback (more than 256 elements at or above its
+# threshold).
+def warp_rows(cols):
+    """A row count that puts rows of this length on the warp kernel."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    return 3 if cols <= 512 else 2 * sms + 3
+
+
+@pytest.mark.parametrize("cols", [4, 8, 255, 256, 257, 511, 512, 513, 1023, 1024, 1025, 2044, 2047, 2048])
+@pytest.mark.parametrize("offset", [0, 1])
+def test_warp_rows_lengths(B, oracle, cols, offset):
+    for k in (1, 4, 32):
+        if k > cols:
+            continue
+        x = synth.logits_with_ties(cols * 7 + k + offset, warp_rows(cols), cols, frac=0.2)
+        assert_exact(gpu_topk(B, x, k, offset=offset), oracle.topk(x, k))
+
+
+def test_warp_rows_counts(B, oracle):
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    for rows in (1, 2 * sms - 1, 2 * sms, 2 * sms + 1, 4 * sms + 5):
+        x = synth.logits_with_ties(rows + 3, rows, 1000)
+        assert_exact(gpu_topk(B, x, 32), oracle.topk(x, 32))
+    for rows in (1, 5, 64):
+        x = synth.logits_with_ties(rows + 4, rows, 300)
+        assert_exact(gpu_topk(B, x, 8), oracle.topk(x, 8))
+
+
+def warp_fallback_rows(cols, rng):
+    rows = []
+    r = rng.standard_normal(cols).astype(np.float32)          # 300 copies of the maximum
+    r[rng.choice(cols, min(cols, 300), replace=False)] = 9.0
+    rows.append(r)
+    r = np.full(cols, np.nan, np.float32)                      # too few delegates above -inf
+    r[rng.choice(cols, 6, replace=False)] = rng.standard_normal(6)
+    rows.append(r)
+    r = np.full(cols, -np.inf, np.float32); r[::3] = np.nan    # -inf and NaN only
+    rows.append(r)
+    r = np.full(cols, np.inf, np.float32)                      # +inf everywhere
+    rows.append(r)
+    r = rng.standard_normal(cols).astype(np.float32)
+    r[rng.choice(cols, min(cols, 40), replace=False)] = np.inf # +inf delegates, search capped
+    rows.append(r)
+    r = (rng.integers(0, 2, cols) * 2 - 1).astype(np.float32)  # two values: half the row ties
+    rows.append(r)
+    r = np.ldexp(np.ones(cols, np.float32), rng.integers(-120, 120, cols)).astype(np.float32)
+    rows.append(r)                                             # values over 70 binades
+    z = np.zeros(cols, np.float32); z[1::2] = -0.0; z[5] = -1e-30
+    rows.append(z)
+    r = rng.standard_normal(cols).astype(np.float32)          # a plain row between them
+    rows.append(r)
+    return np.stack(rows)
+
+
+@pytest.mark.parametrize("cols", [40, 300, 1000, 2048])
+@pytest.mark.parametrize("k", [1, 7, 32])
+@pytest.mark.parametrize("offset", [0, 1])
+def test_warp_rows_fallback(B, oracle, cols, k, offset):
+    rng = np.random.default_rng(cols * k + offset)
+    base = warp_fallback_rows(cols, rng)
+    reps = -(-warp_rows(cols) // len(base))
+    x = np.concatenate([base] + [warp_fallback_rows(cols, rng) for _ in range(reps - 1)])
+    got = gpu_topk(B, x, k, offset=offset)
+    assert_exact(got, oracle.topk(x, k))
+    check_topk_invariants(x, got[0], got[1], k)
