@@ -32,6 +32,7 @@ Rank 0 prints one JSON line on stdout; everything else goes to stderr.
 from __future__ import annotations
 
 import argparse
+import ctypes
 import hashlib
 import json
 import os
@@ -68,6 +69,27 @@ NCU_TRAFFIC = {
 
 def log(*a):
     print(*a, file=sys.stderr, flush=True)
+
+
+CUDA_LIMIT_MAX_L2_FETCH_GRANULARITY = 5   # cudaLimitMaxL2FetchGranularity
+
+
+def _cudart():
+    """The CUDA runtime torch has loaded (dlopen returns that copy), or None."""
+    import glob
+    import torch
+    names = ["libcudart.so.13", "libcudart.so"]
+    names += glob.glob(os.path.join(os.path.dirname(torch.__file__), "..", "nvidia", "*", "lib", "libcudart.so*"))
+    names += glob.glob("/usr/local/cuda/lib64/libcudart.so*")
+    for n in names:
+        try:
+            lib = ctypes.CDLL(n)
+        except OSError:
+            continue
+        lib.cudaDeviceGetLimit.argtypes = [ctypes.POINTER(ctypes.c_size_t), ctypes.c_int]
+        lib.cudaDeviceSetLimit.argtypes = [ctypes.c_int, ctypes.c_size_t]
+        return lib
+    return None
 
 
 # ----------------------------------------------------------------- geometry
@@ -374,6 +396,29 @@ def detect_measurements(B, Lane, device, stream, samples: int) -> dict:
         B.check(B.ws_detect_nms(desc, cand.data_ptr(), cnt.data_ptr(), DETECT_BATCH, out.data_ptr(), oc.data_ptr(), s))
     torch.cuda.synchronize()
     decode_us = statistics.mean(a.elapsed_time(b) * 1000.0 for a, b in evs)
+
+    def decode_mean():
+        torch.cuda.synchronize()
+        for i, (a, b) in enumerate(evs):
+            a.record(stream)
+            B.check(B.ws_detect_decode(desc, heads[i % 2].data_ptr(), DETECT_BATCH, cand.data_ptr(), cnt.data_ptr(), s))
+            b.record(stream)
+            B.check(B.ws_detect_nms(desc, cand.data_ptr(), cnt.data_ptr(), DETECT_BATCH, out.data_ptr(), oc.data_ptr(), s))
+        torch.cuda.synchronize()
+        return statistics.mean(a.elapsed_time(b) * 1000.0 for a, b in evs)
+
+    # Deployment option: the context's L2 fetch granularity at 32 bytes makes
+    # each isolated 4-byte DFL read fetch one sector instead of two.  The
+    # library never sets this context-wide limit; it is set here for this one
+    # measurement and put back.
+    decode_us_fetch32 = None
+    rt = _cudart()
+    if rt is not None:
+        prev = ctypes.c_size_t(0)
+        if rt.cudaDeviceGetLimit(ctypes.byref(prev), CUDA_LIMIT_MAX_L2_FETCH_GRANULARITY) == 0:
+            if rt.cudaDeviceSetLimit(CUDA_LIMIT_MAX_L2_FETCH_GRANULARITY, ctypes.c_size_t(32)) == 0:
+                decode_us_fetch32 = decode_mean()
+            rt.cudaDeviceSetLimit(CUDA_LIMIT_MAX_L2_FETCH_GRANULARITY, prev)
     # candidate count of the timed heads (decode once more, read the counters)
     with torch.cuda.stream(stream):
         B.check(B.ws_detect_decode(desc, heads[0].data_ptr(), DETECT_BATCH, cand.data_ptr(), cnt.data_ptr(), s))
@@ -417,11 +462,15 @@ def detect_measurements(B, Lane, device, stream, samples: int) -> dict:
         "nms_us_by_difference": detect_us - decode_us,
         "candidates_per_image": n_cand / DETECT_BATCH,
         "kept_per_image": kept / DETECT_BATCH,
-        "decode_roofline": {"bound": "hbm", "kernels": "class scan + DFL boxes (ws_detect_decode)",
+        "decode_roofline": {"bound": "hbm", "kernels": "class scan + DFL boxes in one kernel (ws_detect_decode)",
                             "algorithmic_bytes_per_launch": alg_decode,
                             "bytes_rule": "class plane + 32-byte sector per DFL logit of each candidate + "
                                           "32-byte candidate record",
                             "achieved_gbs": alg_decode / (decode_us * 1e-6) / 1e9},
+        "decode_l2_fetch_32": None if decode_us_fetch32 is None else {
+            "decode_us": decode_us_fetch32, "achieved_gbs": alg_decode / (decode_us_fetch32 * 1e-6) / 1e9,
+            "setting": "cudaLimitMaxL2FetchGranularity = 32 bytes for this measurement only (a context-wide "
+                       "limit the library does not set)"},
         "latency_b1_lane": dict(lat, samples=samples, warmup=warm,
                                 path="720p letterbox -> 640 preprocess, decode, NMS in one lane graph"),
     }
@@ -839,6 +888,9 @@ def main():
             r = detect["decode_roofline"]
             r.update(peak=peak, unit="GB/s", frac=r["achieved_gbs"] / peak,
                      frac_note="of measured" if peak_src == "measured" else "of fallback")
+            if detect.get("decode_l2_fetch_32"):
+                r32 = detect["decode_l2_fetch_32"]
+                r32.update(frac=r32["achieved_gbs"] / peak)
         print(json.dumps(line), flush=True)
     if world > 1:
         torch.distributed.destroy_process_group()

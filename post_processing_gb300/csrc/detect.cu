@@ -8,17 +8,17 @@
 // formula are stated in include/ws.h next to ws_detect_desc.
 //
 // How:
-//  * decode: a class scan, one block per tile of 128 consecutive anchors
-//    (4 per lane); its 8 warps split the classes (warp g scans classes
-//    g, g + 8, ...), each load a coalesced 512-byte row segment (16 bytes a
-//    lane, 5 in flight), and 128 threads merge the 8 partial arg-maxes.  One atomic per block reserves
-//    slots for the anchors whose best logit clears the threshold (about 2 %
-//    of them).  A second kernel, a programmatic dependent of the scan, takes
-//    those candidates' DFL: four threads per candidate, one per side, load
-//    that side's reg_max logits and take the softmax expectation.  Keeping
-//    these scattered loads out of the scan keeps the scan a pure stream.
+//  * decode: one warp per tile of 128 consecutive anchors (4 per lane).  The
+//    warp scans every class row of its tile with coalesced 512-byte row
+//    segments (16 bytes a lane, 8 rows in flight), so the arg-max needs no
+//    merge across warps and no block barrier.  One atomic reserves slots for
+//    the anchors whose best logit clears the threshold (about 2 % of them),
+//    and the same warp then takes their DFL: four lanes per candidate, one
+//    per side, load that side's reg_max logits and take the softmax
+//    expectation.  All tiles stream at once; a warp's scattered DFL loads
+//    overlap the other warps' class rows.
 //  * NMS: one block per image, launched as a programmatic dependent of the
-//    DFL kernel so its launch overlaps the decode's tail.  If the image has more
+//    decode kernel so its launch overlaps the decode's tail.  If the image has more
 //    than max_cand candidates, their 64-bit keys (logit order bits, then the
 //    complemented anchor) are held in registers and a radix select
 //    (warp-aggregated histogram counts, early exit once a digit bin closes
@@ -41,14 +41,10 @@
 namespace ws {
 namespace {
 
-constexpr int kDecodeThreads = 256;
-constexpr int kLaneVec = 1;                            // 16-byte words per lane per class row
-constexpr int kDecodeAnchors = 128 * kLaneVec;         // anchors per scan tile (4 kLaneVec per lane)
-constexpr int kLaneAnchors = 4 * kLaneVec;
-constexpr int kDflBlocks = 8;                          // DFL blocks per image
-constexpr int kScanLoads = 5;                          // 16-byte loads in flight per lane
-constexpr int kScanBlocksPerSM = 6;                    // register budget: 6 blocks of 256 per SM
-constexpr int kClassGroups = kDecodeThreads / 32;      // warps splitting the classes
+constexpr int kDecodeAnchors = 128;                    // anchors per decode tile: 4 per lane
+constexpr int kLaneAnchors = 4;
+constexpr int kWarpScanWarps = 4;                      // warps (tiles) per decode block
+constexpr int kWarpScanLoads = 8;                      // class rows in flight per lane
 constexpr int kNmsThreads = 512;
 constexpr int kNmsWarps = kNmsThreads / 32;
 constexpr int kMaxCand = 1024;
@@ -94,139 +90,66 @@ __device__ __forceinline__ unsigned long long cand_key(const ws_candidate* c) {
     return ((unsigned long long)order_bits(c->logit) << 32) | (uint32_t)(~(uint32_t)c->anchor);
 }
 
-// What a scan block shares while it finishes a tile.
-struct ScanShared {
-    float v[kClassGroups][kDecodeAnchors];   // per-warp arg-max values
-    int c[kClassGroups][kDecodeAnchors];     // and classes
-    int off[kDecodeAnchors];                 // anchor offset (in the tile) of the q-th candidate
-    float best[kDecodeAnchors];
-    int cls[kDecodeAnchors];
-    int wcnt[kDecodeAnchors / 32];
-    int n, base;
-};
-
-// Anchor e of a lane: a0 + 128 (e / 4) + 4 lane + e % 4, so that a warp's
-// loads of one class row are whole 512-byte segments.
-__device__ __forceinline__ int lane_anchor(int lane, int e) { return 128 * (e >> 2) + 4 * lane + (e & 3); }
-
-__device__ __forceinline__ void take4(float (&best)[kLaneAnchors], int (&bc)[kLaneAnchors], int h, const float4 v4,
-                                      int c) {
+// Running arg-max of a lane's four anchors over one class row (NaN counts
+// as -inf; a strictly larger logit replaces, so the lower class keeps a tie).
+__device__ __forceinline__ void take4(float (&best)[kLaneAnchors], int (&bc)[kLaneAnchors], const float4 v4, int c) {
     const float v[4] = {nan_as_ninf(v4.x), nan_as_ninf(v4.y), nan_as_ninf(v4.z), nan_as_ninf(v4.w)};
 #pragma unroll
     for (int e = 0; e < 4; ++e)
-        if (v[e] > best[4 * h + e]) {
-            best[4 * h + e] = v[e];
-            bc[4 * h + e] = c;
+        if (v[e] > best[e]) {
+            best[e] = v[e];
+            bc[e] = c;
         }
 }
 
-// Merge the 8 warps' partial arg-maxes of a tile (thread t < kDecodeAnchors
-// owns anchor a0 + t), reserve the tile's candidate slots with one atomic and
-// write their class, logit and anchor (the DFL kernel adds the boxes).
-// Called by the whole block.
-__device__ __forceinline__ void finish_tile(const DetParams& p, ScanShared& sh, int b, long long a0,
-                                            const float (&best)[kLaneAnchors], const int (&bc)[kLaneAnchors]) {
-    const int tid = threadIdx.x, lane = tid & 31, g = tid >> 5;
-#pragma unroll
-    for (int e = 0; e < kLaneAnchors; ++e) {
-        sh.v[g][lane_anchor(lane, e)] = best[e];
-        sh.c[g][lane_anchor(lane, e)] = bc[e];
-    }
-    __syncthreads();
-    bool is_cand = false;
-    float bt = -INFINITY;
-    int ct = 0;
-    if (tid < kDecodeAnchors) {
-        bt = sh.v[0][tid];
-        ct = sh.c[0][tid];
-#pragma unroll
-        for (int q = 1; q < kClassGroups; ++q) {
-            const float v = sh.v[q][tid];
-            const int c = sh.c[q][tid];
-            if (v > bt || (v == bt && c < ct)) {
-                bt = v;
-                ct = c;
-            }
-        }
-        is_cand = a0 + tid < p.A && bt > p.logit_thr;
-    }
-    const unsigned bal = __ballot_sync(kFull, is_cand);
-    if (tid < kDecodeAnchors && lane == 0) sh.wcnt[g] = __popc(bal);
-    __syncthreads();
-    if (tid < kDecodeAnchors) {
-        int before = __popc(bal & ((1u << lane) - 1u));
-        for (int w = 0; w < g; ++w) before += sh.wcnt[w];
-        if (is_cand) {
-            sh.off[before] = tid;
-            sh.best[before] = bt;
-            sh.cls[before] = ct;
-        }
-        if (tid == 0) {
-            int n = 0;
-            for (int w = 0; w < kDecodeAnchors / 32; ++w) n += sh.wcnt[w];
-            sh.n = n;
-            sh.base = n ? atomicAdd(&p.count[b], n) : 0;
-        }
-    }
-    __syncthreads();
-    for (int q = tid; q < sh.n; q += kDecodeThreads) {
-        const int slot = sh.base + q;
-        if (slot < p.A) {
-            float4* dst = reinterpret_cast<float4*>(p.cand + (size_t)b * p.A + slot);
-            dst[1] = make_float4(sh.best[q], __int_as_float(sh.cls[q]), __int_as_float((int)(a0 + sh.off[q])), 0.f);
-        }
-    }
-    // the next tile writes sh only after a barrier of its own
-}
-
-// Class scan with plain loads, one tile per block.  kVec (A % 4 == 0,
-// 16-byte aligned head): a lane loads its anchors' logits as 16-byte words,
-// kScanLoads classes in flight; else one anchor at a time, any alignment.
+// Decode with one warp per 128-anchor tile: the warp scans every class row of
+// its tile (lane l holds anchors 4l .. 4l + 3, one 16-byte word per class
+// row, kWarpScanLoads rows in flight), so the arg-max needs no merge across
+// warps and no block barrier; the warp then reserves its candidates' slots
+// with one atomic and decodes their DFL boxes itself, four lanes per
+// candidate (one per side).  Every tile streams at once, and the scattered
+// DFL loads of a warp overlap other warps' class rows.
 template <bool kVec>
-__global__ void __launch_bounds__(kDecodeThreads, kScanBlocksPerSM) detect_scan_kernel(const __grid_constant__ DetParams p) {
-    __shared__ ScanShared sh;
+__global__ void __launch_bounds__(32 * kWarpScanWarps) detect_decode_warp_kernel(const __grid_constant__ DetParams p) {
+    __shared__ int s_loc[kWarpScanWarps][kDecodeAnchors];   // tile offset of each local candidate
     asm volatile("griddepcontrol.wait;" ::: "memory");   // the head and the counters are the previous kernels'
-    const int b = blockIdx.y, lane = threadIdx.x & 31, g = threadIdx.x >> 5;
-    const long long a0 = (long long)blockIdx.x * kDecodeAnchors;
-    const float* cl = p.head + (size_t)b * p.ch * p.A + (size_t)(4 * p.R) * p.A;
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5, b = blockIdx.y;
+    const long long a0 = ((long long)blockIdx.x * kWarpScanWarps + w) * kDecodeAnchors;
+    if (a0 >= p.A) return;   // whole warp
+    const float* hb = p.head + (size_t)b * p.ch * p.A;
+    const float* cl = hb + (size_t)(4 * p.R) * p.A;
     float best[kLaneAnchors];
     int bc[kLaneAnchors];
 #pragma unroll
     for (int e = 0; e < kLaneAnchors; ++e) {
         best[e] = -INFINITY;
-        bc[e] = g;
+        bc[e] = 0;
     }
+    // Classes in increasing order with a strict comparison: the lower class
+    // keeps a tie.
     if (kVec) {   // A % 4 == 0: a word's four anchors all exist or none does
-        bool live[kLaneVec];
-#pragma unroll
-        for (int h = 0; h < kLaneVec; ++h) live[h] = a0 + lane_anchor(lane, 4 * h) < p.A;
+        const bool live = a0 + 4 * lane < p.A;
         const float* col = cl + a0 + 4 * lane;
-        auto load = [&](int c, int h) -> float4 {
-            return live[h] ? __ldg(reinterpret_cast<const float4*>(col + (size_t)c * p.A + 128 * h))
-                           : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+        auto load = [&](int c) -> float4 {
+            return live ? __ldg(reinterpret_cast<const float4*>(col + (size_t)c * p.A))
+                        : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
         };
-        int c = g;
-        for (; c + (kScanLoads - 1) * kClassGroups < p.C; c += kScanLoads * kClassGroups) {
-            float4 v4[kScanLoads][kLaneVec];
+        int c = 0;
+        for (; c + kWarpScanLoads <= p.C; c += kWarpScanLoads) {
+            float4 v4[kWarpScanLoads];
 #pragma unroll
-            for (int u = 0; u < kScanLoads; ++u)
+            for (int u = 0; u < kWarpScanLoads; ++u) v4[u] = load(c + u);
 #pragma unroll
-                for (int h = 0; h < kLaneVec; ++h) v4[u][h] = load(c + u * kClassGroups, h);
-#pragma unroll
-            for (int u = 0; u < kScanLoads; ++u)
-#pragma unroll
-                for (int h = 0; h < kLaneVec; ++h) take4(best, bc, h, v4[u][h], c + u * kClassGroups);
+            for (int u = 0; u < kWarpScanLoads; ++u) take4(best, bc, v4[u], c + u);
         }
-        for (; c < p.C; c += kClassGroups)
-#pragma unroll
-            for (int h = 0; h < kLaneVec; ++h) take4(best, bc, h, load(c, h), c);
+        for (; c < p.C; ++c) take4(best, bc, load(c), c);
     } else {
 #pragma unroll 2
-        for (int c = g; c < p.C; c += kClassGroups) {
+        for (int c = 0; c < p.C; ++c) {
             const float* row = cl + (size_t)c * p.A;
 #pragma unroll
             for (int e = 0; e < kLaneAnchors; ++e) {
-                const long long a = a0 + lane_anchor(lane, e);
+                const long long a = a0 + 4 * lane + e;
                 if (a < p.A) {
                     const float v = nan_as_ninf(__ldg(row + a));
                     if (v > best[e]) {
@@ -237,59 +160,77 @@ __global__ void __launch_bounds__(kDecodeThreads, kScanBlocksPerSM) detect_scan_
             }
         }
     }
-    finish_tile(p, sh, b, a0, best, bc);
-    asm volatile("griddepcontrol.launch_dependents;");
-}
 
-// DFL box decode of the candidates the scan found: four consecutive threads
-// take one candidate's four sides (the expected bin of each side's softmax
-// over its reg_max logits), the first of them writes the box.  A grid of
-// kDflBlocks x batch blocks strides over each image's candidates.
-__global__ void __launch_bounds__(kDecodeThreads) detect_dfl_kernel(const __grid_constant__ DetParams p) {
-    asm volatile("griddepcontrol.wait;" ::: "memory");
-    asm volatile("griddepcontrol.launch_dependents;");   // the NMS waits for this grid anyway
-    const int b = blockIdx.y, lane = threadIdx.x & 31;
-    const int n = (int)min((long long)p.count[b], p.A);
-    const float* hb = p.head + (size_t)b * p.ch * p.A;
+    // candidates: one ballot per anchor position, slots from one atomic
+    const unsigned lt = (1u << lane) - 1u;
+    unsigned m[kLaneAnchors];
+    int total = 0;
+#pragma unroll
+    for (int e = 0; e < kLaneAnchors; ++e) {
+        m[e] = __ballot_sync(kFull, a0 + 4 * lane + e < p.A && best[e] > p.logit_thr);
+        total += __popc(m[e]);
+    }
+    if (total == 0) {
+        asm volatile("griddepcontrol.launch_dependents;");
+        return;
+    }
+    int base = 0;
+    if (lane == 0) base = atomicAdd(&p.count[b], total);
+    base = __shfl_sync(kFull, base, 0);
     ws_candidate* cb = p.cand + (size_t)b * p.A;
-    const int tasks = (4 * n + 31) & ~31;   // whole warps, for the shuffles
-    for (int t = blockIdx.x * kDecodeThreads + threadIdx.x; t < tasks; t += gridDim.x * kDecodeThreads) {
-        const int q = t >> 2, side = t & 3;
+    int before = 0;
+#pragma unroll
+    for (int e = 0; e < kLaneAnchors; ++e) {
+        if ((m[e] >> lane) & 1u) {
+            const int q = before + __popc(m[e] & lt);
+            s_loc[w][q] = 4 * lane + e;
+            const int slot = base + q;
+            if (slot < p.A)
+                reinterpret_cast<float4*>(cb + slot)[1] =
+                    make_float4(best[e], __int_as_float(bc[e]), __int_as_float((int)(a0 + 4 * lane + e)), 0.f);
+        }
+        before += __popc(m[e]);
+    }
+    __syncwarp();
+
+    // DFL boxes: lane 4q + side takes side `side` of local candidate q
+    for (int t0 = 0; t0 < 4 * total; t0 += 32) {
+        const int t = t0 + lane, q = t >> 2, side = t & 3;
         float dist = 0.f;
-        int a = 0;
-        if (q < n) {
-            a = cb[q].anchor;
+        long long a = 0;
+        if (q < total) {
+            a = a0 + s_loc[w][q];
             const float* z = hb + (size_t)(side * p.R) * p.A + a;
             float v[kMaxRegMax];
 #pragma unroll
             for (int i = 0; i < kMaxRegMax; ++i) v[i] = i < p.R ? __ldg(z + (size_t)i * p.A) : -INFINITY;
-            float m = -INFINITY;
+            float mx = -INFINITY;
 #pragma unroll
-            for (int i = 0; i < kMaxRegMax; ++i) m = fmaxf(m, v[i]);
+            for (int i = 0; i < kMaxRegMax; ++i) mx = fmaxf(mx, v[i]);
             float zs = 0.f, es = 0.f;
 #pragma unroll
             for (int i = 0; i < kMaxRegMax; ++i) {
                 if (i < p.R) {
-                    const float w = expf(v[i] - m);
-                    zs += w;
-                    es += w * (float)i;
+                    const float wgt = expf(v[i] - mx);
+                    zs += wgt;
+                    es += wgt * (float)i;
                 }
             }
             dist = es / zs;
         }
         const float d1 = __shfl_down_sync(kFull, dist, 1), d2 = __shfl_down_sync(kFull, dist, 2),
                     d3 = __shfl_down_sync(kFull, dist, 3);
-        if (q < n && side == 0) {
+        if (q < total && side == 0 && base + q < p.A) {
             int l = 0;
             while (l + 1 < p.nlevels && a >= p.off[l + 1]) ++l;
             const long long k = a - p.off[l];
             const float s = (float)p.stride[l];
             const float cx = ((float)(k % p.gw[l]) + 0.5f) * s;
             const float cy = ((float)(k / p.gw[l]) + 0.5f) * s;
-            reinterpret_cast<float4*>(cb + q)[0] = make_float4(cx - dist * s, cy - d1 * s, cx + d2 * s, cy + d3 * s);
+            reinterpret_cast<float4*>(cb + base + q)[0] = make_float4(cx - dist * s, cy - d1 * s, cx + d2 * s, cy + d3 * s);
         }
-        (void)lane;
     }
+    asm volatile("griddepcontrol.launch_dependents;");
 }
 
 __device__ __forceinline__ unsigned long long or_all(unsigned long long v) {
@@ -729,14 +670,12 @@ bool g_nms_attr_set[64];
 ws_status launch_decode(DetParams p, int32_t batch, cudaStream_t stream) {
     const int tiles = (int)((p.A + kDecodeAnchors - 1) / kDecodeAnchors);
     const bool vec = p.A % 4 == 0 && (uintptr_t)p.head % 16 == 0;
-    // the scan, a programmatic dependent of whatever wrote the head; then the
-    // DFL boxes, a programmatic dependent of the scan
-    const dim3 scan_grid((unsigned)tiles, (unsigned)batch);
-    cudaError_t e = vec ? launch_pdl(detect_scan_kernel<true>, scan_grid, dim3(kDecodeThreads), 0, stream, p)
-                        : launch_pdl(detect_scan_kernel<false>, scan_grid, dim3(kDecodeThreads), 0, stream, p);
+    // one kernel, a programmatic dependent of whatever wrote the head
+    const dim3 grid((unsigned)((tiles + kWarpScanWarps - 1) / kWarpScanWarps), (unsigned)batch);
+    const cudaError_t e =
+        vec ? launch_pdl(detect_decode_warp_kernel<true>, grid, dim3(32 * kWarpScanWarps), 0, stream, p)
+            : launch_pdl(detect_decode_warp_kernel<false>, grid, dim3(32 * kWarpScanWarps), 0, stream, p);
     if (e != cudaSuccess) return cuda_fail(e, "decode launch");
-    e = launch_pdl(detect_dfl_kernel, dim3(kDflBlocks, (unsigned)batch), dim3(kDecodeThreads), 0, stream, p);
-    if (e != cudaSuccess) return cuda_fail(e, "DFL launch");
     return WS_OK;
 }
 
