@@ -761,6 +761,32 @@ def main():
         return out
 
     latency = latency_of(LATENCY_WORKLOAD, args.latency_samples)
+
+    # The fixed cost of a replay: the same two timing events around a graph
+    # that holds one 1-element fill kernel (no work of this library).
+    def graph_floor(samples):
+        fs = torch.cuda.Stream()
+        buf = torch.zeros(1, device=device)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(fs):
+            buf.fill_(1.0)
+            fs.synchronize()
+            with torch.cuda.graph(g, stream=fs):
+                buf.fill_(2.0)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            vals = []
+            warm = min(1000, samples)
+            for i in range(warm + samples):
+                e0.record(fs)
+                g.replay()
+                e1.record(fs)
+                e1.synchronize()
+                if i >= warm:
+                    vals.append(e0.elapsed_time(e1) * 1000.0)
+        return percentiles(vals)
+
+    latency["graph_floor"] = {"gpu_us": graph_floor(args.latency_samples),
+                              "what": "the same timing events around a graph holding one 1-element fill kernel"}
     # the other two batch-1 configurations: 224x224 identity + Top-5 of 1000,
     # and 1280x720 letterboxed to 640x640 + Top-32 of one 672,000-entry row
     latency_other = {name: latency_of(name, args.latency_samples)
