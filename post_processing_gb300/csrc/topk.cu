@@ -25,11 +25,12 @@
 //  If more than 2048 elements pass the threshold (adversarial inputs, e.g. a
 //  constant row), an exact radix select on the 64-bit keys (8 passes of 8
 //  bits, warp-aggregated shared histograms) finds the K-th key instead.
-// Rows longer than one chunk: every chunk writes its K keys to a workspace;
-// the last block of the row to finish (an atomic ticket, reset by that block
-// so the workspace is ready for the next call or graph replay) merges the
-// chunks' keys with the same threshold / rank steps, taking as threshold the
-// largest K-th key over chunks.
+// Rows longer than one chunk: every chunk writes its K keys, sorted, to a
+// workspace; the last block of the row to finish (an atomic ticket, reset by
+// that block so the workspace is ready for the next call or graph replay)
+// merges the sorted lists: with bitonic merges in registers, except between
+// 49 and 96 chunks, where the threshold / rank steps are faster (the
+// threshold is the K-th largest of the lists' first keys).
 // Many short rows take a second kernel with one warp per row and no block
 // barrier (topk_warp_kernel, further down); use_warp_kernel() picks it.
 #include <algorithm>
@@ -48,9 +49,9 @@ constexpr int kVpt = 32;                       // values per thread
 constexpr int kChunk = kThreads * kVpt;        // 8192 elements per block
 constexpr int kCap = 2048;                     // shared candidate capacity
 constexpr int kMaxK = 32;
-constexpr int kMergeBatch = 8;                 // keys each merging thread loads at once
 constexpr int kMergeRegs = 12;                 // chunk lists per warp held in registers (<= 96 chunks)
 constexpr int kMergeChunks = 8 * kMergeRegs;   // blocks per row the one-round-trip merge handles
+constexpr int kBitonicChunks = 48;             // up to here the lists are merged bitonically
 constexpr int kMinChunk = 2048;                // shortest chunk a long row is cut into
 constexpr unsigned kFull = 0xffffffffu;
 
@@ -91,17 +92,25 @@ __device__ __forceinline__ uint32_t key_index(unsigned long long key) {
     return ~(uint32_t)(key & 0xffffffffull);
 }
 
-__device__ __forceinline__ unsigned long long warp_max_u64(unsigned long long v) {
+// Top 32 of two 32-key lists, each sorted descending across the warp (lane
+// 0 largest): the lane-wise maximum of one list and the other reversed is a
+// bitonic sequence holding the 32 largest keys, and five half-cleaner
+// stages sort it descending.
+__device__ __forceinline__ unsigned long long merge_top32(unsigned long long a, unsigned long long b) {
+    const int lane = threadIdx.x & 31;
+    const unsigned long long br = __shfl_sync(kFull, b, 31 - lane);
+    unsigned long long c = a > br ? a : br;
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-        const unsigned long long w = __shfl_xor_sync(kFull, v, o);
-        v = w > v ? w : v;
+    for (int j = 16; j >= 1; j >>= 1) {
+        const unsigned long long o = __shfl_xor_sync(kFull, c, j);
+        c = (lane & j) == 0 ? (c > o ? c : o) : (c < o ? c : o);
     }
-    return v;
+    return c;
 }
 
 struct __align__(16) Shared {
     unsigned long long cand[kCap + kThreads];   // candidates, then one spare slot per thread
+    unsigned long long wlist[kWarps][32];       // merge: each warp's top-K list
     unsigned long long red[kWarps];
     uint32_t hist[256];
     uint32_t warp_t[kWarps];
@@ -393,13 +402,61 @@ __global__ void __launch_bounds__(kThreads, 4) topk_kernel(const __grid_constant
 
     const unsigned long long* all = p.keys + row * p.nchunks * k;
     const int total = p.nchunks * k;
+    if (p.nchunks <= kBitonicChunks || p.nchunks > kMergeChunks) {
+        // Warp w folds the lists of chunks w, w + 8, ... (lane i holding the
+        // i-th key of each; 0 past a list's K keys, and every real key is
+        // larger than 0) with bitonic merges in registers, a batch of
+        // kLists lists at a time with the next batch's loads in flight; warp
+        // 0 then folds the eight warps' lists.  The result is the row's
+        // Top-K in rank order: no threshold, no ranking, one block barrier.
+        constexpr int kLists = kBitonicChunks / kWarps;   // per warp and batch
+        auto load_batch = [&](int c0, unsigned long long (&kb)[kLists]) {
+#pragma unroll
+            for (int r = 0; r < kLists; ++r) {
+                const int c = c0 + r * kWarps;
+                kb[r] = (c < p.nchunks && lane < k) ? __ldcg(all + (long long)c * k + lane) : 0ull;
+            }
+        };
+        unsigned long long cur[kLists], nxt[kLists];
+        load_batch(warp, cur);
+        unsigned long long acc = 0ull;
+        for (int c0 = warp; c0 < p.nchunks; c0 += kWarps * kLists) {
+            const int cn = c0 + kWarps * kLists;
+            if (cn < p.nchunks) load_batch(cn, nxt);
+#pragma unroll
+            for (int step = 1; step < kLists; step *= 2)
+#pragma unroll
+                for (int r = 0; r + step < kLists; r += 2 * step)
+                    if (c0 + (r + step) * kWarps < p.nchunks) cur[r] = merge_top32(cur[r], cur[r + step]);
+            acc = c0 == warp ? cur[0] : merge_top32(acc, cur[0]);
+#pragma unroll
+            for (int r = 0; r < kLists; ++r) cur[r] = nxt[r];
+        }
+        s.wlist[warp][lane] = acc;
+        __syncthreads();
+        if (warp != 0) return;
+        unsigned long long w8[kWarps];
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w) w8[w] = s.wlist[w][lane];
+#pragma unroll
+        for (int step = 1; step < kWarps; step *= 2)
+#pragma unroll
+            for (int r = 0; r + step < kWarps; r += 2 * step)
+                if (r + step < p.nchunks) w8[r] = merge_top32(w8[r], w8[r + step]);
+        if (lane < k) {
+            p.out_val[row * k + lane] = key_value(w8[0], xr);
+            p.out_idx[row * k + lane] = (int)key_index(w8[0]);
+        }
+        if (lane == 0) p.tickets[row] = 0u;   // ready for the next call / replay
+        return;
+    }
     // Threshold from the sorted chunk lists: the first m = ceil(K / chunks)
     // keys of every chunk hold at least K keys, so the K-th largest of that
     // union has at least K keys at or above it, and every key of the row's
     // Top-K is at or above it.  It is found by counting, like the ranks.
     const int m = (k + p.nchunks - 1) / p.nchunks;
     const int U = m * p.nchunks;
-    if (p.nchunks <= kWarps * kMergeRegs && U <= kCap) {
+    {   // 48 < chunks <= 96: U <= 96
         // One round trip: warp w holds the lists of chunks w, w + 8, ... in
         // registers, lane i the i-th key of each.  As the lists are sorted,
         // the keys at or above the threshold are a prefix of each list.
@@ -436,38 +493,6 @@ __global__ void __launch_bounds__(kThreads, 4) topk_kernel(const __grid_constant
             }
         }
         if (tid == 0) s.cnt = (uint32_t)all_total;
-    } else {
-        // very many chunks: the largest K-th key over chunks (always valid),
-        // keys gathered from global memory in batches
-        unsigned long long tm = 0;
-        for (int c0m = 0; c0m < p.nchunks; c0m += kThreads * kMergeBatch) {
-            unsigned long long v[kMergeBatch];
-#pragma unroll
-            for (int j = 0; j < kMergeBatch; ++j)
-                v[j] = __ldcg(all + (long long)min(c0m + j * kThreads + tid, p.nchunks - 1) * k + (k - 1));
-#pragma unroll
-            for (int j = 0; j < kMergeBatch; ++j) tm = v[j] > tm ? v[j] : tm;
-        }
-        tm = warp_max_u64(tm);
-        if (lane == 0) s.red[warp] = tm;
-        if (tid == 0) s.cnt = 0;
-        __syncthreads();
-        unsigned long long t64 = 0;
-#pragma unroll
-        for (int w = 0; w < kWarps; ++w) t64 = s.red[w] > t64 ? s.red[w] : t64;
-        if (t64 == 0) t64 = 1;
-        for (int i0 = 0; i0 < total; i0 += kThreads * kMergeBatch) {
-            unsigned long long v[kMergeBatch];
-#pragma unroll
-            for (int j = 0; j < kMergeBatch; ++j) v[j] = __ldcg(all + min(i0 + j * kThreads + tid, total - 1));
-#pragma unroll
-            for (int j = 0; j < kMergeBatch; ++j) {
-                if (i0 + j * kThreads + tid < total && v[j] >= t64) {
-                    const uint32_t pos = atomicAdd(&s.cnt, 1u);
-                    if (pos < kCap) s.cand[pos] = v[j];
-                }
-            }
-        }
     }
     __syncthreads();
     cnt = s.cnt;

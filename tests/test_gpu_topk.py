@@ -221,3 +221,25 @@ def test_warp_rows_fallback(B, oracle, cols, k, offset):
     got = gpu_topk(B, x, k, offset=offset)
     assert_exact(got, oracle.topk(x, k))
     check_topk_invariants(x, got[0], got[1], k)
+
+
+# Long rows: the last block of a row merges the chunks' sorted lists with
+# bitonic merges up to 48 chunks, with a threshold from the lists' first keys
+# up to 96, and with the largest K-th key as threshold beyond.  Chunk counts
+# on a 152-SM GB300: [64,131072] 16, [4,65536] 32, [2,100000] 49, [1,150000]
+# 74, [1,672000] 96, [1,1000000] 123, [2,2000000] 245.
+@pytest.mark.parametrize("rows,cols", [(64, 131072), (4, 65536), (2, 100000), (1, 150000), (1, 672000),
+                                       (1, 1_000_000), (2, 2_000_000)])
+@pytest.mark.parametrize("k", [1, 5, 32])
+def test_long_row_merge_paths(B, oracle, rows, cols, k):
+    x = synth.logits_with_ties(rows * 7 + cols + k, rows, cols, frac=0.05)
+    rng = np.random.default_rng(cols + k)
+    # ties at the top spread over many chunks, NaN and -0 sprinkled in
+    top = x.max(axis=1, keepdims=True)
+    for r in range(rows):
+        x[r, rng.choice(cols, 40, replace=False)] = top[r, 0]
+        x[r, rng.choice(cols, 100, replace=False)] = np.nan
+        x[r, rng.choice(cols, 10, replace=False)] = -0.0
+    got = gpu_topk(B, x, k)
+    assert_exact(got, oracle.topk(x, k))
+    check_topk_invariants(x, got[0], got[1], k)
