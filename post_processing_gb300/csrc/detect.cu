@@ -45,6 +45,8 @@ constexpr int kDecodeAnchors = 128;                    // anchors per decode til
 constexpr int kLaneAnchors = 4;
 constexpr int kWarpScanWarps = 4;                      // warps (tiles) per decode block
 constexpr int kWarpScanLoads = 8;                      // class rows in flight per lane
+constexpr int kDecodeSplit = 4;                        // warps per tile when tiles are few
+constexpr long long kDecodeSplitTiles = 1100;          // up to this many tiles in all (16 640x640 heads)
 constexpr int kNmsThreads = 512;
 constexpr int kNmsWarps = kNmsThreads / 32;
 constexpr int kMaxCand = 1024;
@@ -109,13 +111,25 @@ __device__ __forceinline__ void take4(float (&best)[kLaneAnchors], int (&bc)[kLa
 // with one atomic and decodes their DFL boxes itself, four lanes per
 // candidate (one per side).  Every tile streams at once, and the scattered
 // DFL loads of a warp overlap other warps' class rows.
-template <bool kVec>
-__global__ void __launch_bounds__(32 * kWarpScanWarps) detect_decode_warp_kernel(const __grid_constant__ DetParams p) {
-    __shared__ int s_loc[kWarpScanWarps][kDecodeAnchors];   // tile offset of each local candidate
+// kSplit > 1 (few tiles, e.g. one image): a block of kSplit warps takes one
+// tile, each warp a contiguous range of classes, and warp 0 merges their
+// arg-maxes (value, then the lower class) through shared memory before it
+// goes on alone.  A warp's chain of dependent class-row loads is then
+// kSplit times shorter.
+template <bool kVec, int kSplit>
+__global__ void __launch_bounds__(32 * (kSplit == 1 ? kWarpScanWarps : kSplit))
+    detect_decode_warp_kernel(const __grid_constant__ DetParams p) {
+    constexpr int kTilesPerBlock = kSplit == 1 ? kWarpScanWarps : 1;
+    __shared__ int s_loc[kTilesPerBlock][kDecodeAnchors];   // tile offset of each local candidate
+    __shared__ float s_v[kSplit][kDecodeAnchors];          // per-warp arg-max values (kSplit > 1)
+    __shared__ int s_c[kSplit][kDecodeAnchors];            // and classes
     asm volatile("griddepcontrol.wait;" ::: "memory");   // the head and the counters are the previous kernels'
     const int lane = threadIdx.x & 31, w = threadIdx.x >> 5, b = blockIdx.y;
-    const long long a0 = ((long long)blockIdx.x * kWarpScanWarps + w) * kDecodeAnchors;
-    if (a0 >= p.A) return;   // whole warp
+    const int tw = kSplit == 1 ? w : 0;                     // this warp's tile in the block
+    const long long a0 = ((long long)blockIdx.x * kTilesPerBlock + tw) * kDecodeAnchors;
+    if (a0 >= p.A) return;   // whole warp (whole block when kSplit > 1)
+    const int cbeg = kSplit == 1 ? 0 : p.C * w / kSplit;
+    const int cend = kSplit == 1 ? p.C : p.C * (w + 1) / kSplit;
     const float* hb = p.head + (size_t)b * p.ch * p.A;
     const float* cl = hb + (size_t)(4 * p.R) * p.A;
     float best[kLaneAnchors];
@@ -134,18 +148,18 @@ __global__ void __launch_bounds__(32 * kWarpScanWarps) detect_decode_warp_kernel
             return live ? __ldg(reinterpret_cast<const float4*>(col + (size_t)c * p.A))
                         : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
         };
-        int c = 0;
-        for (; c + kWarpScanLoads <= p.C; c += kWarpScanLoads) {
+        int c = cbeg;
+        for (; c + kWarpScanLoads <= cend; c += kWarpScanLoads) {
             float4 v4[kWarpScanLoads];
 #pragma unroll
             for (int u = 0; u < kWarpScanLoads; ++u) v4[u] = load(c + u);
 #pragma unroll
             for (int u = 0; u < kWarpScanLoads; ++u) take4(best, bc, v4[u], c + u);
         }
-        for (; c < p.C; ++c) take4(best, bc, load(c), c);
+        for (; c < cend; ++c) take4(best, bc, load(c), c);
     } else {
 #pragma unroll 2
-        for (int c = 0; c < p.C; ++c) {
+        for (int c = cbeg; c < cend; ++c) {
             const float* row = cl + (size_t)c * p.A;
 #pragma unroll
             for (int e = 0; e < kLaneAnchors; ++e) {
@@ -156,6 +170,30 @@ __global__ void __launch_bounds__(32 * kWarpScanWarps) detect_decode_warp_kernel
                         best[e] = v;
                         bc[e] = c;
                     }
+                }
+            }
+        }
+    }
+
+    if (kSplit > 1) {
+        // An all -inf range reports class 0, which is the arg-max exactly
+        // when every class of the anchor is -inf.
+#pragma unroll
+        for (int e = 0; e < kLaneAnchors; ++e) {
+            s_v[w][4 * lane + e] = best[e];
+            s_c[w][4 * lane + e] = bc[e];
+        }
+        __syncthreads();
+        if (w != 0) return;
+#pragma unroll
+        for (int e = 0; e < kLaneAnchors; ++e) {
+#pragma unroll
+            for (int q = 1; q < kSplit; ++q) {
+                const float v = s_v[q][4 * lane + e];
+                const int c = s_c[q][4 * lane + e];
+                if (v > best[e] || (v == best[e] && c < bc[e])) {
+                    best[e] = v;
+                    bc[e] = c;
                 }
             }
         }
@@ -183,7 +221,7 @@ __global__ void __launch_bounds__(32 * kWarpScanWarps) detect_decode_warp_kernel
     for (int e = 0; e < kLaneAnchors; ++e) {
         if ((m[e] >> lane) & 1u) {
             const int q = before + __popc(m[e] & lt);
-            s_loc[w][q] = 4 * lane + e;
+            s_loc[tw][q] = 4 * lane + e;
             const int slot = base + q;
             if (slot < p.A)
                 reinterpret_cast<float4*>(cb + slot)[1] =
@@ -199,7 +237,7 @@ __global__ void __launch_bounds__(32 * kWarpScanWarps) detect_decode_warp_kernel
         float dist = 0.f;
         long long a = 0;
         if (q < total) {
-            a = a0 + s_loc[w][q];
+            a = a0 + s_loc[tw][q];
             const float* z = hb + (size_t)(side * p.R) * p.A + a;
             float v[kMaxRegMax];
 #pragma unroll
@@ -667,14 +705,23 @@ size_t det_workspace(const DetParams& p, int32_t batch) {
 
 bool g_nms_attr_set[64];
 
+// Few tiles in all: split each tile's classes over kDecodeSplit warps.
+bool decode_split(int tiles, int32_t batch) { return (long long)tiles * batch <= kDecodeSplitTiles; }
+
 ws_status launch_decode(DetParams p, int32_t batch, cudaStream_t stream) {
     const int tiles = (int)((p.A + kDecodeAnchors - 1) / kDecodeAnchors);
     const bool vec = p.A % 4 == 0 && (uintptr_t)p.head % 16 == 0;
     // one kernel, a programmatic dependent of whatever wrote the head
-    const dim3 grid((unsigned)((tiles + kWarpScanWarps - 1) / kWarpScanWarps), (unsigned)batch);
-    const cudaError_t e =
-        vec ? launch_pdl(detect_decode_warp_kernel<true>, grid, dim3(32 * kWarpScanWarps), 0, stream, p)
-            : launch_pdl(detect_decode_warp_kernel<false>, grid, dim3(32 * kWarpScanWarps), 0, stream, p);
+    cudaError_t e;
+    if (decode_split(tiles, batch)) {
+        const dim3 grid((unsigned)tiles, (unsigned)batch);
+        e = vec ? launch_pdl(detect_decode_warp_kernel<true, kDecodeSplit>, grid, dim3(32 * kDecodeSplit), 0, stream, p)
+                : launch_pdl(detect_decode_warp_kernel<false, kDecodeSplit>, grid, dim3(32 * kDecodeSplit), 0, stream, p);
+    } else {
+        const dim3 grid((unsigned)((tiles + kWarpScanWarps - 1) / kWarpScanWarps), (unsigned)batch);
+        e = vec ? launch_pdl(detect_decode_warp_kernel<true, 1>, grid, dim3(32 * kWarpScanWarps), 0, stream, p)
+                : launch_pdl(detect_decode_warp_kernel<false, 1>, grid, dim3(32 * kWarpScanWarps), 0, stream, p);
+    }
     if (e != cudaSuccess) return cuda_fail(e, "decode launch");
     return WS_OK;
 }

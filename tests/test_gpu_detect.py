@@ -119,6 +119,27 @@ def test_decode_parity(B, oracle):
     assert all(50 < len(g["anchor"]) < 1000 for g in got)      # a realistic candidate count
 
 
+@pytest.mark.parametrize("batch", [16, 17])
+def test_decode_split_and_whole_tile_kernels(B, oracle, batch):
+    """Up to 1100 tiles in all, four warps split each 128-anchor tile's classes
+    and merge; above, one warp scans a whole tile.  A 640x640 head has 66
+    tiles: 16 heads take the first form, 17 the second."""
+    desc = B.detect_desc()
+    head = synth.yolo_head(31, batch)
+    got = check_decode(B, oracle, desc, head)
+    assert all(50 < len(g["anchor"]) < 1000 for g in got)
+
+
+def test_decode_whole_tile_kernel_scalar(B, oracle):
+    """One 15-anchor tile an image (scalar loads) for 1101 images: the
+    whole-tile form's scalar scan."""
+    desc = B.detect_desc(in_w=40, in_h=24, strides=(8,), reg_max=4, num_classes=3, conf=0.2)
+    desc.nlevels = 1
+    head = synth.yolo_head(92, 1101, 40, 24, reg_max=4, num_classes=3, cls_mu=-1.0, strides=(8,))
+    got = check_decode(B, oracle, desc, head)
+    assert sum(len(g["anchor"]) for g in got) > 1000
+
+
 def test_decode_small_geometry(B, oracle):
     desc = B.detect_desc(in_w=320, in_h=192, reg_max=8, num_classes=3, conf=0.3)
     head = synth.yolo_head(22, 2, 320, 192, reg_max=8, num_classes=3, cls_mu=-2.0)
