@@ -321,8 +321,43 @@ __global__ void __launch_bounds__(kNmsThreads) detect_nms_kernel(const __grid_co
     const int m = min(n, p.max_cand);
     __syncthreads();
 
+    const int Wl = (m + 63) >> 6;
+    const int RS = Wl | 1;
+    unsigned long long* s_m = reinterpret_cast<unsigned long long*>(s_u);
+    unsigned long long* s_tab = reinterpret_cast<unsigned long long*>(s_u + p.off_tab);   // [Wl][kBuckets]
+    // Few candidates (the usual case): each thread reads its candidate's
+    // 32-byte record once and keeps it in registers; its rank by counting
+    // then places the record and sets its class-table bit directly.
+    const bool fast = n <= p.max_cand && n <= kCountSortMax;
+    if (fast) {
+        float4 box = make_float4(0.f, 0.f, 0.f, 0.f), rest = box;
+        unsigned long long key = 0ull;
+        if (tid < n) {
+            const float4* c = reinterpret_cast<const float4*>(cb + tid);
+            box = __ldcg(c);
+            rest = __ldcg(c + 1);
+            key = ((unsigned long long)order_bits(rest.x) << 32) | (uint32_t)(~(uint32_t)__float_as_int(rest.z));
+            s_key[tid] = key;
+        }
+        // the histograms of the cap selection are not used on this path, so
+        // the match table can be cleared now
+        for (int q = tid; q < Wl * kBuckets; q += kNmsThreads) s_tab[q] = 0ull;
+        __syncthreads();
+        if (tid < n) {
+            int r = 0;
+#pragma unroll 4
+            for (int j = 0; j < n; ++j) r += s_key[j] > key;
+            s_box[r] = box;
+            s_logit[r] = rest.x;
+            s_cls[r] = __float_as_int(rest.y);
+            s_anchor[r] = __float_as_int(rest.z);
+            atomicOr(&s_tab[(r >> 6) * kBuckets + (__float_as_int(rest.y) & (kBuckets - 1))], 1ull << (r & 63));
+        }
+    }
+
     // 1. the best m candidates' keys
-    if (n <= p.max_cand) {
+    if (fast) {
+    } else if (n <= p.max_cand) {
         for (int i = tid; i < n; i += kNmsThreads) {
             s_key[i] = cand_key(cb + i);
             s_idx[i] = i;
@@ -443,11 +478,12 @@ __global__ void __launch_bounds__(kNmsThreads) detect_nms_kernel(const __grid_co
             }
         }
     }
-    __syncthreads();
+    if (!fast) __syncthreads();
 
     // 2. descending order: rank by counting when few, else a bitonic sort at
     //    the next power of two of the live count
-    if (m <= kCountSortMax) {
+    if (fast) {
+    } else if (m <= kCountSortMax) {
         for (int t = tid; t < m; t += kNmsThreads) {
             const unsigned long long k = s_key[t];
             int r = 0;
@@ -547,15 +583,13 @@ __global__ void __launch_bounds__(kNmsThreads) detect_nms_kernel(const __grid_co
     //    word's candidates in that bucket, so a (row, word) task finds its
     //    class matches with one load and takes the IoU only for those.  The
     //    odd row stride keeps the row-parallel stores apart.
-    const int Wl = (m + 63) >> 6;
-    const int RS = Wl | 1;
-    unsigned long long* s_m = reinterpret_cast<unsigned long long*>(s_u);
-    unsigned long long* s_tab = reinterpret_cast<unsigned long long*>(s_u + p.off_tab);   // [Wl][kBuckets]
-    for (int q = tid; q < Wl * kBuckets; q += kNmsThreads) s_tab[q] = 0ull;
-    __syncthreads();
-    for (int q = tid; q < m; q += kNmsThreads)
-        atomicOr(&s_tab[(q >> 6) * kBuckets + (s_cls[q] & (kBuckets - 1))], 1ull << (q & 63));
-    __syncthreads();
+    if (!fast) {
+        for (int q = tid; q < Wl * kBuckets; q += kNmsThreads) s_tab[q] = 0ull;
+        __syncthreads();
+        for (int q = tid; q < m; q += kNmsThreads)
+            atomicOr(&s_tab[(q >> 6) * kBuckets + (s_cls[q] & (kBuckets - 1))], 1ull << (q & 63));
+        __syncthreads();
+    }
     for (int t = tid; t < m * Wl; t += kNmsThreads) {
         const int w = t / m, i = t - w * m;
         if (w < (i >> 6)) continue;
