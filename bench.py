@@ -53,7 +53,8 @@ METRIC = "frames/s + HBM GB/s (% of roofline); p50/p99 batch-1 graph-replay late
 DEFAULT_WORKLOAD = "b64_1080p_to_224"
 LATENCY_WORKLOAD = "b1_1080p_to_224"
 FALLBACK_HBM_GBS = 6800.0
-LANES = 3
+LANES = 3          # throughput lanes at least; more for small workloads (see n_lanes)
+MAX_LANES = 64
 
 # DRAM traffic of the preprocess kernel per launch from one ncu
 # capture (dram__bytes_read.sum + dram__bytes_write.sum), keyed by the SHA-256
@@ -635,9 +636,13 @@ def main():
     # within a lane the order copy-in -> preprocess -> Top-K is unchanged) --
     # the headline; the second set sharing one stream, every step serialised
     # behind the previous one.
+    # Enough lanes that one rotation touches about three times the L2 (three
+    # for the batched workloads, up to MAX_LANES for the batch-1 ones).
+    alg = algorithmic_bytes(w, out_bytes)
+    n_lanes = max(LANES, min(MAX_LANES, -(-3 * l2 // max(1, int(alg["total"])))))
     lanes, lanes_1s, keep = [], [], []
     for one_stream in (False, True):
-        for _ in range(LANES):
+        for _ in range(n_lanes):
             src = frames_dev.clone()
             lg = logits_dev.clone()
             keep += [src, lg]
@@ -645,14 +650,13 @@ def main():
                             stream=stream.cuda_stream if one_stream else None, flags=B.WS_LANE_FLAG_NO_TIMING)
             (lanes_1s if one_stream else lanes).append(Lane(d))
     torch.cuda.synchronize()
-    alg = algorithmic_bytes(w, out_bytes)
-    touched_per_rotation = LANES * alg["total"]
+    touched_per_rotation = n_lanes * alg["total"]
 
     def run_steps(ls, n):
         """Round-robin submits; returns the lanes still in flight."""
         inflight = []
         for s_ in range(n):
-            lane = ls[s_ % LANES]
+            lane = ls[s_ % len(ls)]
             if lane.state == B.WS_LANE_IN_FLIGHT:
                 lane.wait()
                 inflight.remove(lane)
@@ -716,11 +720,11 @@ def main():
         return e0.elapsed_time(e1) * 1000.0 / n
 
     def launch_pre(i):
-        b = bufs[i % LANES]
+        b = bufs[i % len(bufs)]
         B.check(B.ws_preprocess(pre, b.input_device, w["batch"], b.tensor, stream.cuda_stream))
 
     def launch_topk(i):
-        b, ws_t, n = bufs[i % LANES], topk_ws[i % LANES], st_ws[i % LANES]
+        b, ws_t, n = bufs[i % len(bufs)], topk_ws[i % len(bufs)], st_ws[i % len(bufs)]
         B.check(B.ws_topk(b.logits, w["rows"], w["cols"], w["k"], b.result_val_device, b.result_idx_device,
                           ws_t.data_ptr() if n else None, n, stream.cuda_stream))
 
@@ -879,16 +883,17 @@ def main():
             "warmup": args.warmup, "ms_per_step": 1000.0 * t_max / args.steps, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
             "config": dict(workload_config(args.workload, w), out_dtype=args.out_dtype,
-                           l2=f"{LANES} lanes rotate, {touched_per_rotation / 1e6:.0f} MB touched per rotation "
-                              f"(> {touched_per_rotation / l2:.1f}x the {l2 / 2 ** 20:.0f} MiB L2): inputs larger "
-                                "than L2",
+                           l2=f"{n_lanes} lanes rotate, {touched_per_rotation / 1e6:.0f} MB touched per rotation "
+                              f"({touched_per_rotation / l2:.1f}x the {l2 / 2 ** 20:.0f} MiB L2): inputs "
+                              + ("larger than L2" if touched_per_rotation > l2 else
+                                 "SMALLER than L2 (this workload's rate is L2-resident)"),
                            parallelism=f"replicas x{world}", graph=True,
-                           lanes=f"{LANES} lanes, each on its own stream, replayed in rotation",
+                           lanes=f"{n_lanes} lanes, each on its own stream, replayed in rotation",
                            algorithmic_bytes_per_step=alg["total"]),
             "hbm_gbs_step": alg["total"] * args.steps * world / t_max / 1e9,
             "serialized_one_stream": {"value": value_1s, "ms_per_step": 1000.0 * t_max_1s / args.steps,
                                       "hbm_gbs_step": alg["total"] * args.steps * world / t_max_1s / 1e9,
-                                      "lanes": f"{LANES} lanes sharing one stream: each step after the previous"},
+                                      "lanes": f"{n_lanes} lanes sharing one stream: each step after the previous"},
             "roofline": {"bound": "hbm", "kernel": "pre_ring_kernel", "achieved": achieved, "peak": peak,
                          "unit": "GB/s", "frac": achieved / peak, "peak_source": peak_src,
                          "traffic": traffic, "algorithmic_bytes_per_launch": alg["preprocess"],
