@@ -13,8 +13,9 @@
 // order is total and the Top-K set is unique: results are bit-exact.
 //
 // One block per (row, chunk of up to 8192 elements):
-//  1. Coalesced 16-byte loads; each thread keeps its 32 order-mapped values in
-//     registers and their maximum (a "delegate").
+//  1. The chunk is staged in shared memory (one bulk copy when the row is
+//     16-byte aligned, else coalesced loads); each thread keeps the maxima of
+//     its 4-element groups in registers, and their maximum (a "delegate").
 //  2. Threshold without sorting: each warp finds the ceil(K/8)-th largest of
 //     its 32 delegates with warp max-reductions; t = the minimum over warps.
 //     Every warp then owns ceil(K/8) distinct elements >= t, so at least K
