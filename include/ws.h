@@ -147,16 +147,20 @@ ws_status ws_preprocess_validate(const ws_preprocess_desc* desc, int32_t batch);
  * One kernel launch on `stream`, a programmatic dependent of the kernel
  * before it (it reads and writes nothing until that kernel has finished).
  * Any alignment is accepted.  Outputs above 2^19 pixels (batch x dst_w x
- * dst_h) with a 16-byte aligned src, row stride and frame stride take the
- * staged bulk-copy kernel; smaller outputs, or other alignments, a
- * per-pixel kernel with the same results (see ws_preprocess_path).
+ * dst_h, dst_w at most 8192) take the staged bulk-copy kernel, smaller
+ * outputs a per-pixel kernel with the same results (see
+ * ws_preprocess_path).  The staged kernel copies each needed source row as
+ * its 16-byte window (from the 16-byte boundary at or below the row's first
+ * byte to the one at or above its last): with a base or stride that is not a
+ * multiple of 16 it reads up to 15 bytes before and after a row, always
+ * inside 16-byte blocks that hold bytes of the row, and never uses them.
  * Errors: WS_ERR_INVALID_ARGUMENT (NULL pointer, batch < 1, bad descriptor),
  * WS_ERR_CUDA (launch failed). */
 ws_status ws_preprocess(const ws_preprocess_desc* desc, const uint8_t* src, int32_t batch,
                         void* dst, cudaStream_t stream);
 
 #define WS_PRE_PATH_AUTO   0  /* as ws_preprocess                                        */
-#define WS_PRE_PATH_STAGED 1  /* the staged bulk-copy kernel whenever the alignment allows */
+#define WS_PRE_PATH_STAGED 1  /* the staged bulk-copy kernel (dst_w at most 8192)          */
 #define WS_PRE_PATH_DIRECT 2  /* the per-pixel kernel                                     */
 
 /* ws_preprocess with the kernel chosen by `path` (the results are the same;

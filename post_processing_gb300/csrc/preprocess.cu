@@ -8,12 +8,13 @@
 // its channel plane of the NCHW tensor.  Nothing else is materialised.
 //
 // How (GB300 design, not the page's one-thread-per-pixel gather):
-//  * Ring kernel (16-byte aligned rows), persistent.  The work is cut into
+//  * Ring kernel, persistent.  The work is cut into
 //    units of (frame, band of output rows); each resident block walks its
 //    share of units.  Warp 0 plans a unit (one lane per output row works out
 //    its two source rows and weight) and pulls each needed source row, whole,
-//    into a stage of a shared-memory ring with one bulk copy (cp.async.bulk),
-//    completion counted on the stage's mbarrier.  While the block computes
+//    into a stage of a shared-memory ring with one bulk copy (cp.async.bulk)
+//    of its 16-byte window, completion counted on the stage's mbarrier; any
+//    base and stride work.  While the block computes
 //    unit i from its stage, the copies of the next units are already in
 //    flight, so HBM sees a steady stream instead of load-then-compute bursts.
 //    On a 4-9x downscale the taps of a row touch every 32-byte sector, so
@@ -21,8 +22,9 @@
 //    column tap table (byte offsets and weights) is built once per block.
 //    Each thread produces four consecutive x of one output row and writes one
 //    16-byte store per channel plane: the NCHW planes are written coalesced.
-//  * Direct kernel (any alignment): one thread per output pixel with plain
-//    byte loads; same arithmetic, same results.
+//  * Direct kernel: one thread per output pixel with plain byte loads; same
+//    arithmetic, same results.  Small outputs, where the ring's per-block
+//    set-up is not amortised.
 //
 // Arithmetic (the reading where the pages are silent): half-pixel centres as
 // the exact rational ((2x+1) S - D) / (2D); floor gives the lower neighbour,
@@ -50,6 +52,8 @@ constexpr int kMaxBand = 8;            // output rows per unit
 constexpr int kMaxStages = 8;
 constexpr int kMaxThreads = 512;
 constexpr int kMaxTableCols = 8192;
+// Threads of the ring kernel an SM holds by registers (about 64 a thread).
+constexpr int kRingThreadsPerSM = 65536 / 64;
 // AUTO: outputs of at most this many pixels (batch x dst_w x dst_h) take the
 // direct kernel.  Batch-1..32 lane graphs on GB300 put the crossover between
 // 8 x 224x224 (401K px: direct 13.6 us, staged 15.8) and 12 x 224x224 (602K:
@@ -76,8 +80,7 @@ struct PreParams {
     // ring kernel
     int band;                 // output rows per unit
     int stages;               // ring depth
-    int slot_bytes;           // shared bytes per staged source row (multiple of 16)
-    int bulk_bytes;           // leading bytes of a row moved by the bulk copy (multiple of 16)
+    int slot_bytes;           // shared bytes per staged source row (multiple of 16; room for its 16-byte window)
     int row_bytes;            // 3 * sw
     int stage_bytes;          // 2 * band * slot_bytes
     int off_plan, off_cols, off_slots;
@@ -134,6 +137,12 @@ __device__ __forceinline__ void store4(OutT* dst, float a, float b, float c, flo
 
 // Warp 0: plan unit `u` into stage `s` and start its copies.  Lane r handles
 // output row r of the unit; its rows go to slots 2r and 2r+1 of the stage.
+// Each row is copied as its 16-byte window: from the 16-byte boundary at or
+// below the row's first byte to the one at or above its end, so that any base
+// and any stride work.  The extra bytes (at most 15 on each side) lie in the
+// same 16-byte blocks as bytes of the row, hence in pages the row itself
+// occupies; they are copied and never used.  The plan records where in the
+// slot the row starts.
 __device__ void issue_unit(const PreParams& p, long long u, uint64_t* bar, StagePlan* plan,
                            unsigned char* stage) {
     const int lane = threadIdx.x & 31;
@@ -141,8 +150,9 @@ __device__ void issue_unit(const PreParams& p, long long u, uint64_t* bar, Stage
     const int y0 = (int)(u - (long long)frame * p.nbands) * p.band;
     const int nrows = min(p.band, p.dh - y0);
     const uint8_t* fr = p.src + (long long)frame * p.frame_stride;
-    int ja = -1, jb = -1;
-    uint32_t bytes = 0;
+    const uint8_t* wa = nullptr;
+    const uint8_t* wb = nullptr;
+    uint32_t na = 0, nb = 0;
     if (lane < nrows) {
         const int y = y0 + lane;
         int a = -1, b = -1;
@@ -150,13 +160,17 @@ __device__ void issue_unit(const PreParams& p, long long u, uint64_t* bar, Stage
         if (y >= p.top && y < p.top + p.nh) {
             int j0, j1;
             axis_taps(y - p.top, p.sh, p.nh, j0, j1, wy);
-            a = 2 * lane * p.slot_bytes;
-            ja = j0;
-            bytes += p.bulk_bytes;
+            const uint8_t* ra = fr + (long long)j0 * p.row_stride;
+            const int oa = (int)((uintptr_t)ra & 15u);
+            wa = ra - oa;
+            na = (uint32_t)((oa + p.row_bytes + 15) & ~15);
+            a = 2 * lane * p.slot_bytes + oa;
             if (wy != 0.f && j1 != j0) {   // a zero weight needs no second row (v = t exactly)
-                b = a + p.slot_bytes;
-                jb = j1;
-                bytes += p.bulk_bytes;
+                const uint8_t* rb = fr + (long long)j1 * p.row_stride;
+                const int ob = (int)((uintptr_t)rb & 15u);
+                wb = rb - ob;
+                nb = (uint32_t)((ob + p.row_bytes + 15) & ~15);
+                b = (2 * lane + 1) * p.slot_bytes + ob;
             } else {
                 b = a;
             }
@@ -170,23 +184,15 @@ __device__ void issue_unit(const PreParams& p, long long u, uint64_t* bar, Stage
         plan->y0 = y0;
         plan->nrows = nrows;
     }
+    uint32_t bytes = na + nb;
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) bytes += __shfl_xor_sync(kFull, bytes, o);
     // The expected bytes are registered (with the one arrival) before any copy
     // can complete; a band of padding rows completes the phase at once.
     if (lane == 0) mbar_arrive_expect_tx(bar, bytes);
     __syncwarp();
-    if (p.bulk_bytes > 0) {
-        if (ja >= 0) bulk_g2s(stage + 2 * lane * p.slot_bytes, fr + (long long)ja * p.row_stride, p.bulk_bytes, bar);
-        if (jb >= 0)
-            bulk_g2s(stage + (2 * lane + 1) * p.slot_bytes, fr + (long long)jb * p.row_stride, p.bulk_bytes, bar);
-    }
-    // Ragged row ends (< 16 bytes) by plain loads; consumers see them after
-    // the block barriers that separate issue from use.
-    for (int t = p.bulk_bytes; t < p.row_bytes; ++t) {
-        if (ja >= 0) stage[2 * lane * p.slot_bytes + t] = fr[(long long)ja * p.row_stride + t];
-        if (jb >= 0) stage[(2 * lane + 1) * p.slot_bytes + t] = fr[(long long)jb * p.row_stride + t];
-    }
+    if (na) bulk_g2s(stage + 2 * lane * p.slot_bytes, wa, na, bar);
+    if (nb) bulk_g2s(stage + (2 * lane + 1) * p.slot_bytes, wb, nb, bar);
 }
 
 template <typename OutT, bool kVecStore>
@@ -390,39 +396,60 @@ size_t ring_layout(PreParams& p, const PreTuning& t) {
     return (size_t)p.off_slots + (size_t)t.stages * p.stage_bytes;
 }
 
-// Default tuning (from a sweep of rows per unit, ring depth and blocks per SM
-// on GB300, 64 x 1080p -> 224 and 8 x 4K -> 512): three resident blocks per
-// SM, each a ring of ~70 KB, so that with one stage being computed the others
-// keep >= ~64 KB of source rows in flight per SM (HBM bandwidth x loaded
-// latency); about 128 threads of 4-column items per unit; single-frame work
-// spread thin for latency.
+// Default tuning, from sweeps on GB300 of blocks per SM, output rows per unit
+// and ring depth over ten geometries (1080p, 720p, 1366x768, 640x480,
+// 320x240 and 4K sources; 224 to 640 wide outputs).  What decides is the
+// output per source byte, r = dst_w / (6 src_w): with little output per byte
+// (strong downscales) the kernel is HBM-bound and needs only enough copies in
+// flight, with more it is bound by its per-pixel work and needs more warps to
+// hide that work's latency.  The best setting had about 800 r warps per SM
+// (8 .. 32), blocks of about 128 threads while r < 0.025 and about 256
+// above, and a ring of two stages.  For example (batch, source -> output:
+// blocks per SM x rows per unit x stages, us): 64, 1080p -> 224: 4 x 2 x 2,
+// 33.7; 8, 4K -> 512: 4 x 1 x 2, 20.7; 64, 1280x720 -> 224: 3 x 4 x 2, 26.7
+// (the earlier fixed 3 blocks of 128 threads and a 3-stage ring: 35.7);
+// 256, 640x480 -> 224: 4 x 4 x 2, 74.9 (185.3); 16, 1080p -> 640:
+// 6 x 1 x 2, 36.9 (62.2).  Single-frame work is spread thin for latency.
 PreTuning default_tuning(const PreParams& p, int batch, const DeviceInfo& info) {
     const int groups = (p.dw + 3) / 4;
     const size_t fixed = align16(8 * kMaxStages) + sizeof(StagePlan) * kMaxStages + align16(12 * (size_t)p.dw) + 64;
-    PreTuning t{};
-    for (int bps = 3; bps >= 1; --bps) {
-        const size_t budget =
-            std::min<size_t>((size_t)info.smem_per_sm / bps - 1024, (size_t)info.max_smem_optin);
-        int band = std::max(1, std::min(kMaxBand, 128 / std::max(groups, 1)));
-        // keep at least ~2 units per resident block when the batch is large enough
-        const long long slots_total = (long long)info.sm_count * bps;
-        while (band > 1 && (long long)batch * ((p.dh + band - 1) / band) < 2 * slots_total) band /= 2;
-        int stages = 0;
-        for (;;) {
-            const size_t stage = 2ull * band * p.slot_bytes;
-            stages = (int)std::min<size_t>(kMaxStages, (budget > fixed ? budget - fixed : 0) / stage);
-            if (stages >= 2 || band == 1) break;
-            band /= 2;
+    const double r = (double)p.dw / (6.0 * (double)p.sw);
+    const int warps_per_sm = std::max(8, std::min(32, (int)std::lround(800.0 * r)));
+    const int target_threads = r < 0.025 ? 128 : 256;
+    auto threads_for = [&](int band) { return std::min(kMaxThreads, std::max(64, (band * groups + 31) / 32 * 32)); };
+    int band0 = std::max(1, std::min(kMaxBand, target_threads / std::max(groups, 1)));
+    while (band0 > 1 && band0 * groups > kMaxThreads) --band0;
+    for (int band = band0; band >= 1; band = band > 1 ? band / 2 : 0) {
+        const int threads = threads_for(band);
+        int want = std::max(1, std::min(8, (int)std::lround((double)warps_per_sm / (threads / 32))));
+        want = std::min(want, kRingThreadsPerSM / threads);
+        for (int bps = want; bps >= 1; --bps) {
+            const size_t budget =
+                std::min<size_t>((size_t)info.smem_per_sm / bps - 1024, (size_t)info.max_smem_optin);
+            int b = band;
+            // keep at least ~2 units per resident block when the batch is large enough
+            const long long slots_total = (long long)info.sm_count * bps;
+            while (b > 1 && (long long)batch * ((p.dh + b - 1) / b) < 2 * slots_total) b /= 2;
+            const size_t stage = 2ull * b * p.slot_bytes;
+            if (budget < fixed + 2 * stage) continue;
+            PreTuning t{};
+            t.band = b;
+            t.stages = 2;
+            t.blocks_per_sm = bps;
+            t.threads = threads_for(b);
+            // blocks that get a single unit (small batches) are latency-bound:
+            // more threads build the column table and issue the loads sooner
+            if ((long long)batch * ((p.dh + b - 1) / b) <= slots_total) t.threads = std::max(t.threads, 128);
+            return t;
         }
-        t.blocks_per_sm = bps;
-        t.band = band;
-        t.stages = std::max(1, std::min(stages, 3));
-        t.threads = std::min(kMaxThreads, std::max(64, (band * groups + 31) / 32 * 32));
-        // blocks that get a single unit (small batches) are latency-bound:
-        // more threads build the column table and issue the loads sooner
-        if ((long long)batch * ((p.dh + band - 1) / band) <= slots_total) t.threads = std::max(t.threads, 128);
-        if (stages >= 2) break;   // else: very wide rows, fewer blocks with more memory each
     }
+    // very wide rows: one block per SM with a single stage when even two do not fit
+    PreTuning t{};
+    t.band = 1;
+    t.blocks_per_sm = 1;
+    t.threads = threads_for(1);
+    const size_t budget = std::min<size_t>((size_t)info.smem_per_sm - 1024, (size_t)info.max_smem_optin);
+    t.stages = budget >= fixed + 4ull * p.slot_bytes ? 2 : 1;
     return t;
 }
 
@@ -445,6 +472,12 @@ ws_status launch_ring(const PreParams& p, int dev, const DeviceInfo& info, unsig
                                          info.max_smem_optin));
         g_ring_attr_set[dev][type_slot][kVec] = true;
     }
+    // The kernel is persistent: a grid larger than what is resident would run
+    // a second, mostly idle wave.  Clamp it to the resident blocks.
+    int resident = 0;
+    WS_TRY_CUDA(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&resident, pre_ring_kernel<OutT, kVec>, threads, smem));
+    if (resident < 1) return fail(WS_ERR_UNSUPPORTED, "preprocess: no ring block fits an SM (%zu bytes)", smem);
+    blocks = std::min<unsigned>(blocks, (unsigned)resident * (unsigned)info.sm_count);
     return pdl_launch(pre_ring_kernel<OutT, kVec>, dim3(blocks), dim3(threads), smem, stream, p);
 }
 
@@ -542,20 +575,20 @@ ws_status preprocess_launch(const ws_preprocess_desc* d, const uint8_t* src, int
     for (int c = 0; c < 3; ++c) p.cmap[c] = d->channel_order == WS_ORDER_BGR ? 2 - c : c;
     p.dst = dst;
     p.row_bytes = 3 * d->src_w;
-    p.slot_bytes = (int)align16(p.row_bytes);
-    p.bulk_bytes = p.row_bytes / 16 * 16;
-    p.err = device_error_word();
-
+    // A row's 16-byte window is align16(row_bytes) long when every row starts
+    // on a 16-byte boundary, and up to 16 bytes longer otherwise.
     const bool aligned = ((uintptr_t)src % 16 == 0) && (d->src_row_stride % 16 == 0) &&
                          (batch == 1 || d->src_frame_stride % 16 == 0);
+    p.slot_bytes = (int)align16(p.row_bytes) + (aligned ? 0 : 16);
+    p.err = device_error_word();
     PreTuning t = tuning ? *tuning : default_tuning(p, batch, *info);
     const size_t smem = ring_layout(p, t);
-    // The staged ring needs 16-byte aligned rows and pays a fixed set-up per
-    // block (barriers, plan, column table, a copy round trip): small outputs
-    // (a single 224x224 frame) finish sooner one thread per pixel.
+    // The staged ring pays a fixed set-up per block (barriers, plan, column
+    // table, a copy round trip): small outputs (a single 224x224 frame)
+    // finish sooner one thread per pixel.
     const bool small = (long long)batch * d->dst_w * d->dst_h <= kDirectMaxPixels;
     const bool want_ring = path == WS_PRE_PATH_STAGED || (path == WS_PRE_PATH_AUTO && !small);
-    const bool ring_ok = want_ring && aligned && d->dst_w <= kMaxTableCols && t.band >= 1 && t.band <= kMaxBand &&
+    const bool ring_ok = want_ring && d->dst_w <= kMaxTableCols && t.band >= 1 && t.band <= kMaxBand &&
                          t.stages >= 1 && t.stages <= kMaxStages && t.threads >= 32 &&
                          t.threads <= kMaxThreads && smem <= (size_t)info->max_smem_optin;
     bool vec = false;

@@ -3,7 +3,8 @@
 Inputs are the seeded synthetic workloads (the five inference
 configurations at full size) and small odd shapes that span several blocks
 and ragged tails: widths that are not multiples of 4 or 16, padded row and
-frame strides, misaligned base pointers (per-pixel kernel), upscales,
+frame strides, misaligned base pointers and strides that are not multiples
+of 16 (the staged kernel copies each row's 16-byte window), upscales,
 letterbox in both orientations, 1x1 frames.
 """
 import numpy as np
@@ -44,7 +45,7 @@ def run_gpu(B, frames, sw, sh, dw, dh, *, letterbox=False, norm="mean_std", row_
     return out.cpu().numpy()
 
 
-PATHS = [0, 1, 2]   # WS_PRE_PATH_AUTO, _STAGED (the bulk-copy ring whenever aligned), _DIRECT
+PATHS = [0, 1, 2]   # WS_PRE_PATH_AUTO, _STAGED (the bulk-copy ring), _DIRECT
 
 
 def compare(got, want):
@@ -80,13 +81,16 @@ ODD = [
     (96, 64, 64, 64, True, "scale", 0, 0, 0, 2),             # letterbox, rows padded
     (64, 96, 67, 64, True, "mean_std", 0, 0, 0, 2),          # letterbox, columns padded, odd split
     (1000, 999, 640, 640, True, "scale", 0, 0, 0, 1),
-    (200, 120, 64, 48, False, "mean_std", 16, 32, 0, 3),     # padded, aligned strides (staged)
-    (200, 120, 64, 48, False, "mean_std", 5, 7, 0, 3),       # unaligned strides (per-pixel)
-    (200, 120, 64, 48, False, "mean_std", 0, 0, 3, 2),       # misaligned base (per-pixel)
+    (200, 120, 64, 48, False, "mean_std", 16, 32, 0, 3),     # padded, aligned strides
+    (200, 120, 64, 48, False, "mean_std", 5, 7, 0, 3),       # unaligned row and frame strides
+    (200, 120, 64, 48, False, "mean_std", 0, 0, 3, 2),       # misaligned base
     (1920, 1080, 224, 224, False, "mean_std", 0, 0, 1, 1),   # config shape, misaligned base
+    (1920, 1080, 224, 224, False, "mean_std", 1, 0, 3, 3),   # config shape, stride 5761, base + 3
+    (1366, 768, 224, 224, False, "mean_std", 0, 0, 0, 3),    # 4098-byte rows: every row start differs mod 16
+    (1280, 720, 640, 640, True, "scale", 7, 5, 9, 2),        # letterbox, everything unaligned
     (4000, 3, 512, 7, False, "mean_std", 0, 0, 0, 1),        # 12000-byte rows, 2 rows
-    (21, 700, 8, 300, False, "scale", 0, 0, 0, 2),            # 63-byte rows: bulk part 48 + tail 15
-    (2, 50000, 3, 60000, False, "scale", 10, 0, 0, 1),       # tall: 64-bit y taps, tail-only rows
+    (21, 700, 8, 300, False, "scale", 0, 0, 0, 2),            # 63-byte rows: 64-byte windows
+    (2, 50000, 3, 60000, False, "scale", 10, 0, 0, 1),       # tall: 64-bit y taps, 6-byte rows
     (40000, 2, 30000, 1, False, "mean_std", 0, 0, 0, 1),     # wide: per-pixel kernel, 64-bit x taps
 ]
 
