@@ -146,7 +146,7 @@ ws_status ws_preprocess_validate(const ws_preprocess_desc* desc, int32_t batch);
  *        type desc->dst_type (float32, half or bfloat16).
  * One kernel launch on `stream`, a programmatic dependent of the kernel
  * before it (it reads and writes nothing until that kernel has finished).
- * Any alignment is accepted.  Outputs above 2^19 pixels (batch x dst_w x
+ * Any alignment is accepted.  Outputs above 460,000 pixels (batch x dst_w x
  * dst_h, dst_w at most 8192) take the staged bulk-copy kernel, smaller
  * outputs a per-pixel kernel with the same results (see
  * ws_preprocess_path).  The staged kernel copies each needed source row as

@@ -55,10 +55,11 @@ constexpr int kMaxTableCols = 8192;
 // Threads of the ring kernel an SM holds by registers (about 64 a thread).
 constexpr int kRingThreadsPerSM = 65536 / 64;
 // AUTO: outputs of at most this many pixels (batch x dst_w x dst_h) take the
-// direct kernel.  Batch-1..32 lane graphs on GB300 put the crossover between
-// 8 x 224x224 (401K px: direct 13.6 us, staged 15.8) and 12 x 224x224 (602K:
-// direct 16.6, staged 15.8).
-constexpr long long kDirectMaxPixels = 1LL << 19;
+// direct kernel.  One-launch graphs on GB300 (events around the replay) put
+// the crossover between 409,600 px (one 640x640 letterbox: 9.2 us either
+// way; 8 x 224x224 from 1080p, 401K px: direct 11.3, staged 12.6) and
+// 524,288 px (2 x 4K -> 512x512: direct 13.0, staged 11.2).
+constexpr long long kDirectMaxPixels = 460000;
 constexpr unsigned kFull = 0xffffffffu;
 
 struct StagePlan {
