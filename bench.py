@@ -63,7 +63,7 @@ MAX_LANES = 64
 NCU_TRAFFIC = {
     "b64_1080p_to_224": {
         "bytes": 186_313_472,
-        "source_sha": "6cb2d7dce8c44baa0ac0cfc65ae0185daa9c7020309c7b4e20c2df56a8a3cb90",
+        "source_sha": "38b3dfeb53d2eb7a5c0dd66e64a5619cab0d5ff5122ac7facd64f94b8a01347a",
     },
 }
 
