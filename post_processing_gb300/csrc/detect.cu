@@ -788,7 +788,7 @@ extern "C" {
 
 ws_status ws_detect_validate(const ws_detect_desc* desc, int32_t batch, int64_t* anchors) {
     ws::clear_error();
-    ws::DetParams p;
+    ws::DetParams p{};
     ws_status st = ws::fill_params(desc, batch, p);
     if (st == WS_OK && anchors) *anchors = p.A;
     return st;
@@ -797,7 +797,7 @@ ws_status ws_detect_validate(const ws_detect_desc* desc, int32_t batch, int64_t*
 ws_status ws_detect_workspace_bytes(const ws_detect_desc* desc, int32_t batch, size_t* bytes) {
     ws::clear_error();
     if (!bytes) return ws::fail(WS_ERR_INVALID_ARGUMENT, "bytes is NULL");
-    ws::DetParams p;
+    ws::DetParams p{};
     ws_status st = ws::fill_params(desc, batch, p);
     if (st != WS_OK) return st;
     *bytes = ws::det_workspace(p, batch);
@@ -815,7 +815,7 @@ ws_status ws_detect_workspace_init(void* workspace, size_t bytes, cudaStream_t s
 ws_status ws_detect_decode(const ws_detect_desc* desc, const float* head, int32_t batch, ws_candidate* cand,
                            int32_t* count, cudaStream_t stream) {
     ws::clear_error();
-    ws::DetParams p;
+    ws::DetParams p{};
     ws_status st = ws::fill_params(desc, batch, p);
     if (st != WS_OK) return st;
     if (!head || !cand || !count) return ws::fail(WS_ERR_INVALID_ARGUMENT, "head, cand or count is NULL");
@@ -828,7 +828,7 @@ ws_status ws_detect_decode(const ws_detect_desc* desc, const float* head, int32_
 ws_status ws_detect_nms(const ws_detect_desc* desc, ws_candidate* cand, int32_t* count, int32_t batch,
                         ws_detection* out, int32_t* out_count, cudaStream_t stream) {
     ws::clear_error();
-    ws::DetParams p;
+    ws::DetParams p{};
     ws_status st = ws::fill_params(desc, batch, p);
     if (st != WS_OK) return st;
     if (!cand || !count || !out || !out_count)
@@ -843,7 +843,7 @@ ws_status ws_detect_nms(const ws_detect_desc* desc, ws_candidate* cand, int32_t*
 ws_status ws_detect(const ws_detect_desc* desc, const float* head, int32_t batch, ws_detection* out,
                     int32_t* out_count, void* workspace, size_t workspace_bytes, cudaStream_t stream) {
     ws::clear_error();
-    ws::DetParams p;
+    ws::DetParams p{};
     ws_status st = ws::fill_params(desc, batch, p);
     if (st != WS_OK) return st;
     if (!head || !out || !out_count) return ws::fail(WS_ERR_INVALID_ARGUMENT, "head, out or out_count is NULL");
