@@ -196,10 +196,15 @@ __device__ void issue_unit(const PreParams& p, long long u, uint64_t* bar, Stage
     if (nb) bulk_g2s(stage + (2 * lane + 1) * p.slot_bytes, wb, nb, bar);
 }
 
+// Column taps: the byte offset of the left tap in a staged row, with kTapSame
+// set when the right tap is the same pixel (clamped at an edge; otherwise it
+// is the next pixel, 3 bytes on), and the weight's bits: one 8-byte entry
+// per output column, one shared load per pixel instead of three.
+constexpr int kTapSame = 1 << 30;
+
 template <typename OutT, bool kVecStore>
 __device__ __forceinline__ void compute_unit(const PreParams& p, const StagePlan& plan, const unsigned char* stage,
-                                             const int* s_off0, const int* s_off1, const float* s_wx,
-                                             const float (&padn)[3]) {
+                                             const int2* s_tap, const float (&padn)[3]) {
     const int groups = (p.dw + 3) >> 2;
     const int items = plan.nrows * groups;
     const size_t plane = (size_t)p.dh * p.dw;
@@ -223,8 +228,11 @@ __device__ __forceinline__ void compute_unit(const PreParams& p, const StagePlan
             for (int q = 0; q < 4; ++q) {
                 const int x = x0 + q;
                 if (x < p.dw && x >= p.left && x < p.left + p.nw) {
-                    const int o0 = s_off0[x], o1 = s_off1[x];
-                    const float wx = s_wx[x];
+                    const int2 tap = s_tap[x];
+                    const bool same = (tap.x & kTapSame) != 0;
+                    const int o0 = tap.x & ~kTapSame;
+                    const float wx = __int_as_float(tap.y);
+                    const int o1 = same ? o0 : o0 + 3;
 #pragma unroll
                     for (int c = 0; c < 3; ++c) {
                         const int sc = p.cmap[c];
@@ -260,9 +268,7 @@ __global__ void __launch_bounds__(kMaxThreads) pre_ring_kernel(const __grid_cons
     extern __shared__ __align__(128) unsigned char smem[];
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem);                    // [stages]
     StagePlan* plans = reinterpret_cast<StagePlan*>(smem + p.off_plan);   // [stages]
-    int* s_off0 = reinterpret_cast<int*>(smem + p.off_cols);              // [dw] byte offset of the left tap
-    int* s_off1 = s_off0 + p.dw;                                          // [dw] byte offset of the right tap
-    float* s_wx = reinterpret_cast<float*>(s_off1 + p.dw);                // [dw]
+    int2* s_tap = reinterpret_cast<int2*>(smem + p.off_cols);             // [dw] left-tap offset | same, weight
     unsigned char* slots = smem + p.off_slots;
 
     // Let a programmatic dependent (the Top-K) be launched now; it waits for
@@ -291,9 +297,7 @@ __global__ void __launch_bounds__(kMaxThreads) pre_ring_kernel(const __grid_cons
         int i0 = 0, i1 = 0;
         float wx = 0.f;
         if (x >= p.left && x < p.left + p.nw) axis_taps(x - p.left, p.sw, p.nw, i0, i1, wx);
-        s_off0[x] = 3 * i0;
-        s_off1[x] = 3 * i1;
-        s_wx[x] = wx;
+        s_tap[x] = make_int2(3 * i0 | (i1 == i0 ? kTapSame : 0), __float_as_int(wx));
     }
     float padn[3];
 #pragma unroll
@@ -305,7 +309,7 @@ __global__ void __launch_bounds__(kMaxThreads) pre_ring_kernel(const __grid_cons
         const uint32_t parity = (uint32_t)(i / p.stages) & 1u;
         const bool ok = mbar_wait_bounded(&bars[s], parity, kWaitLimitNs);
         if (ok)
-            compute_unit<OutT, kVecStore>(p, plans[s], slots + (size_t)s * p.stage_bytes, s_off0, s_off1, s_wx, padn);
+            compute_unit<OutT, kVecStore>(p, plans[s], slots + (size_t)s * p.stage_bytes, s_tap, padn);
         // Everyone is done with stage s (and agrees on whether a copy hung).
         if (__syncthreads_or(!ok)) {
             if (tid == 0) {
@@ -393,7 +397,7 @@ size_t ring_layout(PreParams& p, const PreTuning& t) {
     p.stage_bytes = 2 * t.band * p.slot_bytes;
     p.off_plan = (int)align16(8 * kMaxStages);
     p.off_cols = (int)align16(p.off_plan + sizeof(StagePlan) * kMaxStages);
-    p.off_slots = (int)align16(p.off_cols + 12 * (size_t)p.dw);
+    p.off_slots = (int)align16(p.off_cols + 8 * (size_t)p.dw);
     return (size_t)p.off_slots + (size_t)t.stages * p.stage_bytes;
 }
 
@@ -413,7 +417,7 @@ size_t ring_layout(PreParams& p, const PreTuning& t) {
 // 6 x 1 x 2, 36.9 (62.2).  Single-frame work is spread thin for latency.
 PreTuning default_tuning(const PreParams& p, int batch, const DeviceInfo& info) {
     const int groups = (p.dw + 3) / 4;
-    const size_t fixed = align16(8 * kMaxStages) + sizeof(StagePlan) * kMaxStages + align16(12 * (size_t)p.dw) + 64;
+    const size_t fixed = align16(8 * kMaxStages) + sizeof(StagePlan) * kMaxStages + align16(8 * (size_t)p.dw) + 64;
     const double r = (double)p.dw / (6.0 * (double)p.sw);
     const int warps_per_sm = std::max(8, std::min(32, (int)std::lround(800.0 * r)));
     const int target_threads = r < 0.025 ? 128 : 256;
