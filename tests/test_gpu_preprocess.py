@@ -92,6 +92,9 @@ ODD = [
     (21, 700, 8, 300, False, "scale", 0, 0, 0, 2),            # 63-byte rows: 64-byte windows
     (2, 50000, 3, 60000, False, "scale", 10, 0, 0, 1),       # tall: 64-bit y taps, 6-byte rows
     (40000, 2, 30000, 1, False, "mean_std", 0, 0, 0, 1),     # wide: per-pixel kernel, 64-bit x taps
+    (20000, 6, 4000, 5, False, "mean_std", 0, 0, 0, 2),      # 60 KB rows: a one-stage ring
+    (20000, 6, 4000, 5, False, "scale", 7, 3, 5, 2),         # the same, nothing aligned
+    (40000, 4, 1000, 3, False, "mean_std", 0, 0, 0, 1),      # 120 KB rows: no ring fits, per-pixel kernel
 ]
 
 
