@@ -57,9 +57,9 @@ LANES = 3          # throughput lanes at least; more for small workloads (see n_
 MAX_LANES = 64
 
 # DRAM traffic of the preprocess kernel per launch from one ncu
-# capture (dram__bytes_read.sum + dram__bytes_write.sum), keyed by the SHA-256
-# of the kernel source it was taken on; reported only while that source is
-# unchanged.  Filled from the committed ncu summary under profiles/.
+# capture (dram__bytes_read.sum + dram__bytes_write.sum) of the FP32-output
+# workload, keyed by the SHA-256 of the kernel source it was taken on;
+# reported only for that output type and while that source is unchanged.  Filled from the committed ncu summary under profiles/.
 NCU_TRAFFIC = {
     "b64_1080p_to_224": {
         "bytes": 186_106_368,
@@ -870,7 +870,7 @@ def main():
         peak, peak_src = FALLBACK_HBM_GBS, "fallback"
     achieved = alg["preprocess"] / (pre_avg_us * 1e-6) / 1e9
     sha = source_sha(os.path.join(ROOT, "post_processing_gb300", "csrc", "preprocess.cu"))
-    traffic = NCU_TRAFFIC.get(args.workload)
+    traffic = NCU_TRAFFIC.get(args.workload) if args.out_dtype == "f32" else None   # captured on FP32 output
     traffic = traffic["bytes"] if traffic and traffic.get("source_sha") == sha else None
 
     if rank == 0:
