@@ -59,7 +59,8 @@ MAX_LANES = 64
 # DRAM traffic of the preprocess kernel per launch from one ncu
 # capture (dram__bytes_read.sum + dram__bytes_write.sum) of the FP32-output
 # workload, keyed by the SHA-256 of the kernel source it was taken on;
-# reported only for that output type and while that source is unchanged.  Filled from the committed ncu summary under profiles/.
+# reported only for that output type and while that source is unchanged.
+# Filled from the committed ncu summary under profiles/.
 NCU_TRAFFIC = {
     "b64_1080p_to_224": {
         "bytes": 186_106_368,
