@@ -51,7 +51,7 @@ constexpr int kChunk = kThreads * kVpt;        // 8192 elements per block
 constexpr int kCap = 2048;                     // shared candidate capacity
 constexpr int kMaxK = 32;
 constexpr int kMergeRegs = 12;                 // chunk lists per warp held in registers (<= 96 chunks)
-constexpr int kMergeChunks = 8 * kMergeRegs;   // blocks per row the one-round-trip merge handles
+constexpr int kMergeChunks = kWarps * kMergeRegs;   // blocks per row the one-round-trip merge handles
 constexpr int kBitonicChunks = 48;             // up to here the lists are merged bitonically
 constexpr int kMinChunk = 2048;                // shortest chunk a long row is cut into
 constexpr unsigned kFull = 0xffffffffu;
