@@ -216,3 +216,71 @@ def test_pool_on_the_gpu(B, oracle):
             done += 1
     finally:
         assert B.ws_pool_destroy(P) == B.WS_OK
+
+
+def test_pool_threads_on_the_gpu(B, oracle):
+    """Two producer threads and one consumer thread share a pool of four lanes
+    on the GPU: 40 jobs with distinct frames and logits, every completed lane
+    holds its own job's result.  The lane-to-job record is written before the
+    submit, so the consumer always finds it."""
+    import threading
+    batch, cols, k = 1, 100, 5
+    pre = B.preprocess_desc(64, 48, 32, 32)
+    d = B.lane_desc(pre, batch, batch, cols, k, flags=B.WS_LANE_FLAG_NO_TIMING)
+    st, P = B.ws_pool_create(d, 4)
+    B.check(st)
+    jobs = [(synth.frames_uniform(700 + j, 1, 48, 64), synth.logits_with_ties(800 + j, 1, cols)) for j in range(40)]
+    want = [(oracle.preprocess(fr, 64, 48, 32, 32), oracle.topk(lg, k)) for fr, lg in jobs]
+    pending, lock, errors = {}, threading.Lock(), []
+
+    def producer(js):
+        try:
+            for j in js:
+                st, L = B.ws_pool_acquire(P, 5_000_000)
+                B.check(st)
+                st, buf = B.ws_lane_get_buffers(L)
+                B.check(st)
+                fr, lg = jobs[j]
+                memcpy(buf.input_device, fr.ctypes.data, fr.nbytes)
+                memcpy(buf.logits, lg.ctypes.data, lg.nbytes)
+                with lock:
+                    pending[L] = j
+                B.check(B.ws_pool_submit(P, L, 1))
+        except Exception as e:   # reported by the main thread
+            errors.append(e)
+
+    def consumer(n):
+        try:
+            for _ in range(n):
+                st, L, _ = B.ws_pool_complete(P, 5_000_000)
+                B.check(st)
+                with lock:
+                    j = pending.pop(L)
+                st, buf = B.ws_lane_get_buffers(L)
+                B.check(st)
+                t = np.empty((1, 3, 32, 32), np.float32)
+                memcpy(t.ctypes.data, buf.tensor, t.nbytes)
+                v = np.empty((1, k), np.float32)
+                idx = np.empty((1, k), np.int32)
+                memcpy(v.ctypes.data, buf.result_val_device, v.nbytes)
+                memcpy(idx.ctypes.data, buf.result_idx_device, idx.nbytes)
+                assert np.max(np.abs(t - want[j][0])) <= 1e-5, j
+                assert np.array_equal(idx, want[j][1][1]), j
+                assert np.array_equal(v.view(np.uint32), want[j][1][0].view(np.uint32)), j
+                B.check(B.ws_pool_recycle(P, L))
+        except Exception as e:
+            errors.append(e)
+
+    try:
+        threads = [threading.Thread(target=producer, args=(range(0, 40, 2),)),
+                   threading.Thread(target=producer, args=(range(1, 40, 2),)),
+                   threading.Thread(target=consumer, args=(40,))]
+        for t in threads:
+            t.start()
+        for t in threads:
+            t.join(timeout=120)
+        assert not any(t.is_alive() for t in threads), "a pool thread did not finish"
+        assert not errors, errors
+        assert not pending
+    finally:
+        assert B.ws_pool_destroy(P) == B.WS_OK
