@@ -442,8 +442,9 @@ ws_status ws_lane_get_buffers(const ws_lane* lane, ws_lane_buffers* buffers);
 /* FREE -> ACQUIRED; WS_ERR_LANE_BUSY if the lane is acquired or in flight. */
 ws_status ws_lane_acquire(ws_lane* lane);
 
-/* ACQUIRED -> IN_FLIGHT: record the start event, launch the graph (or the
- * direct launches), record the end event.  No allocation, no synchronisation.
+/* ACQUIRED -> IN_FLIGHT: record the start event (timing lanes) and launch
+ * the graph (or the direct launches), whose last step records the end event.
+ * No allocation, no synchronisation.
  * WS_ERR_LANE_STATE unless acquired; WS_ERR_CUDA if a launch fails (the lane
  * then returns to ACQUIRED). */
 ws_status ws_lane_submit(ws_lane* lane);

@@ -195,7 +195,9 @@ ws_status enqueue_path(ws_lane* L, bool capturing, int bi) {
         WS_TRY_CUDA(cudaMemcpyAsync(L->rv_host, L->rv_dev, rv, cudaMemcpyDeviceToHost, L->stream));
         WS_TRY_CUDA(cudaMemcpyAsync(L->ri_host, L->ri_dev, ri, cudaMemcpyDeviceToHost, L->stream));
     }
-    return WS_OK;
+    // The completion event is part of the path (an event-record node in a
+    // captured graph), so a submit is a single graph launch.
+    return record(L->ev_end, L->stream, capturing);
 }
 
 // Capture bucket bi's path into a new graph (its buffers as bound now).
@@ -527,8 +529,6 @@ ws_status ws_lane_submit_n(ws_lane* L, int32_t n) {
         ws_status st = enqueue_path(L, false, bi);
         if (st != WS_OK) return st;
     }
-    e = cudaEventRecord(L->ev_end, L->stream);
-    if (e != cudaSuccess) return cuda_fail(e, "record end event");
     L->state = WS_LANE_IN_FLIGHT;
     return WS_OK;
 }
