@@ -64,7 +64,7 @@ MAX_LANES = 64
 NCU_TRAFFIC = {
     "b64_1080p_to_224": {
         "bytes": 186_106_368,
-        "source_sha": "caed5e01a69a20564f45d8c240425d3d818f99fd007e1ecd1095fc95b2295a89",
+        "source_sha": "9cca8d83a1b65414634c257685b1256b9dbf66086563187ddacec092e849a3dd",
     },
 }
 

@@ -33,6 +33,7 @@
 //    separately (no fused multiply-add), so given the same boxes the
 //    decisions are exactly those of the definition.
 #include <algorithm>
+#include <atomic>
 #include <cmath>
 
 
@@ -737,7 +738,7 @@ size_t det_workspace(const DetParams& p, int32_t batch) {
     return (size_t)(batch * 4 + 255) / 256 * 256 + (size_t)batch * p.A * sizeof(ws_candidate);
 }
 
-bool g_nms_attr_set[64];
+std::atomic<bool> g_nms_attr_set[64];
 
 // Few tiles in all: split each tile's classes over kDecodeSplit warps.
 bool decode_split(int tiles, int32_t batch) { return (long long)tiles * batch <= kDecodeSplitTiles; }
@@ -771,10 +772,10 @@ ws_status launch_nms(const DetParams& p, int32_t batch, cudaStream_t stream) {
     const size_t smem = nms_smem(p);
     if (smem > (size_t)info->max_smem_optin) return fail(WS_ERR_UNSUPPORTED, "NMS needs %zu bytes of shared memory", smem);
     if (dev < 0 || dev >= 64) return fail(WS_ERR_UNSUPPORTED, "device ordinal %d", dev);
-    if (!g_nms_attr_set[dev]) {
+    if (!g_nms_attr_set[dev].load(std::memory_order_acquire)) {
         WS_TRY_CUDA(cudaFuncSetAttribute(detect_nms_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          info->max_smem_optin));
-        g_nms_attr_set[dev] = true;
+        g_nms_attr_set[dev].store(true, std::memory_order_release);
     }
     const cudaError_t e = launch_pdl(detect_nms_kernel, dim3((unsigned)batch), dim3(kNmsThreads), smem, stream, p);
     if (e != cudaSuccess) return cuda_fail(e, "NMS launch");

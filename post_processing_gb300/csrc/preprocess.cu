@@ -31,6 +31,7 @@
 // the remainder over 2D (one correctly rounded division) the weight; both
 // neighbours clamped to [0, S-1]; three FP32 lerps; out = (v - M_c) * R_c.
 #include <algorithm>
+#include <atomic>
 #include <cmath>
 
 #include <cuda_bf16.h>
@@ -458,7 +459,7 @@ PreTuning default_tuning(const PreParams& p, int batch, const DeviceInfo& info) 
     return t;
 }
 
-bool g_ring_attr_set[64][3][2];
+std::atomic<bool> g_ring_attr_set[64][3][2];
 
 // Both preprocess kernels launch as programmatic dependents of the kernel
 // before them and wait in griddepcontrol.wait before their first read.
@@ -472,10 +473,10 @@ ws_status pdl_launch(Kernel kernel, dim3 grid, dim3 block, size_t smem, cudaStre
 template <typename OutT, bool kVec>
 ws_status launch_ring(const PreParams& p, int dev, const DeviceInfo& info, unsigned blocks, int threads, size_t smem,
                       int type_slot, cudaStream_t stream) {
-    if (!g_ring_attr_set[dev][type_slot][kVec]) {
+    if (!g_ring_attr_set[dev][type_slot][kVec].load(std::memory_order_acquire)) {
         WS_TRY_CUDA(cudaFuncSetAttribute(pre_ring_kernel<OutT, kVec>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          info.max_smem_optin));
-        g_ring_attr_set[dev][type_slot][kVec] = true;
+        g_ring_attr_set[dev][type_slot][kVec].store(true, std::memory_order_release);
     }
     // The kernel is persistent: a grid larger than what is resident would run
     // a second, mostly idle wave.  Clamp it to the resident blocks.
@@ -486,7 +487,7 @@ ws_status launch_ring(const PreParams& p, int dev, const DeviceInfo& info, unsig
     return pdl_launch(pre_ring_kernel<OutT, kVec>, dim3(blocks), dim3(threads), smem, stream, p);
 }
 
-bool g_direct_attr_set[64][3];
+std::atomic<bool> g_direct_attr_set[64][3];
 
 template <typename OutT>
 ws_status launch_any(const PreParams& p, bool ring, bool vec, int dev, const DeviceInfo& info, unsigned blocks,
@@ -500,10 +501,10 @@ ws_status launch_any(const PreParams& p, bool ring, bool vec, int dev, const Dev
     // the next kernel's blocks fit: measured as ~2 us added to a batch-1
     // 640x640 letterbox + Top-5 over 672K graph.  Asking for the shared-heavy
     // split keeps one partition across the sequence at no cost to this kernel.
-    if (!g_direct_attr_set[dev][type_slot]) {
+    if (!g_direct_attr_set[dev][type_slot].load(std::memory_order_acquire)) {
         WS_TRY_CUDA(cudaFuncSetAttribute(pre_direct_kernel<OutT>, cudaFuncAttributePreferredSharedMemoryCarveout,
                                          (int)cudaSharedmemCarveoutMaxShared));
-        g_direct_attr_set[dev][type_slot] = true;
+        g_direct_attr_set[dev][type_slot].store(true, std::memory_order_release);
     }
     return pdl_launch(pre_direct_kernel<OutT>, dim3(blocks), dim3(256), 0, stream, p, total);
 }

@@ -35,6 +35,7 @@
 // Many short rows take a second kernel with one warp per row and no block
 // barrier (topk_warp_kernel, further down); use_warp_kernel() picks it.
 #include <algorithm>
+#include <atomic>
 #include <cmath>
 #include <mutex>
 
@@ -766,7 +767,7 @@ cudaError_t launch_topk_warp(const TopkWarpParams& p, bool vec, int sm_count, cu
 
 size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
-bool g_topk_attr_set[64];
+std::atomic<bool> g_topk_attr_set[64];
 
 }  // namespace
 
@@ -882,10 +883,10 @@ ws_status ws_topk(const float* x, int64_t rows, int64_t cols, int32_t k, float* 
     // PDL section): the grid may be launched while the previous kernel on the
     // stream is still running and waits in griddepcontrol.wait, which hides
     // the launch gap between the preprocess and the Top-K.
-    if (!g_topk_attr_set[dev]) {
+    if (!g_topk_attr_set[dev].load(std::memory_order_acquire)) {
         WS_TRY_CUDA(cudaFuncSetAttribute(topk_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kDynSmem));
         WS_TRY_CUDA(cudaFuncSetAttribute(topk_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kDynSmem));
-        g_topk_attr_set[dev] = true;
+        g_topk_attr_set[dev].store(true, std::memory_order_release);
     }
     p.err = device_error_word();
     // the staged chunk only needs the row's length when the row is short
