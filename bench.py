@@ -66,6 +66,10 @@ NCU_TRAFFIC = {
         "bytes": 186_106_368,
         "source_sha": "9cca8d83a1b65414634c257685b1256b9dbf66086563187ddacec092e849a3dd",
     },
+    "b8_4k_to_512": {
+        "bytes": 99_771_904,
+        "source_sha": "9cca8d83a1b65414634c257685b1256b9dbf66086563187ddacec092e849a3dd",
+    },
 }
 
 
