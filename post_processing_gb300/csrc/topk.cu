@@ -782,16 +782,19 @@ ws_status validate_topk(int64_t rows, int64_t cols, int32_t k) {
 }
 
 // Blocks per row.  Rows up to kChunk elements take one block.  Longer rows
-// take 8192-element blocks, except that when that leaves a launch short of
-// one full wave (4 blocks on every SM) the rows are cut finer, down to
-// kMinChunk elements and at most kMergeChunks blocks per row, so that the
-// wave is full and even.
+// take 8192-element blocks, except that when that leaves SMs without a block
+// the rows are cut finer, down to kMinChunk elements and at most
+// kMergeChunks blocks per row, until there is about one block per SM.  More
+// blocks per SM measured slower on GB300: a block's phases are chains of
+// short steps and block barriers, and blocks sharing an SM slow each other's
+// chains about as much as they shorten them (e.g. [16,131072]: one block per
+// SM, 16 chunks, 7.6 us; four per SM, 38 chunks, 9.5 us).
 int blocks_per_row(int64_t rows, int64_t cols, int sm_count) {
     const long long base = (cols + kChunk - 1) / kChunk;
     if (base <= 1) return 1;
     const long long cap = std::max<long long>(base, std::min<long long>((cols + kMinChunk - 1) / kMinChunk,
                                                                         kMergeChunks));
-    const long long want = (long long)sm_count * 4 / std::max<int64_t>(rows, 1);
+    const long long want = (long long)sm_count / std::max<int64_t>(rows, 1);
     return (int)std::min<long long>(cap, std::max<long long>(base, want));
 }
 
