@@ -55,6 +55,7 @@ constexpr int kMergeRegs = 12;                 // chunk lists per warp held in r
 constexpr int kMergeChunks = kWarps * kMergeRegs;   // blocks per row the one-round-trip merge handles
 constexpr int kBitonicChunks = 48;             // up to here the lists are merged bitonically
 constexpr int kMinChunk = 2048;                // shortest chunk a long row is cut into
+constexpr int kCutChunks = 16;                 // most blocks per row when a row is cut finer than 8192
 constexpr unsigned kFull = 0xffffffffu;
 
 struct TopkParams {
@@ -781,19 +782,27 @@ ws_status validate_topk(int64_t rows, int64_t cols, int32_t k) {
     return WS_OK;
 }
 
+// Most blocks a row of `cols` elements is cut into: 8192-element blocks, or
+// up to kCutChunks blocks of at least kMinChunk elements.
+long long max_blocks_per_row(int64_t cols) {
+    const long long base = (cols + kChunk - 1) / kChunk;
+    return std::max<long long>(base, std::min<long long>((cols + kMinChunk - 1) / kMinChunk, kCutChunks));
+}
+
 // Blocks per row.  Rows up to kChunk elements take one block.  Longer rows
 // take 8192-element blocks, except that when that leaves SMs without a block
-// the rows are cut finer, down to kMinChunk elements and at most
-// kMergeChunks blocks per row, until there is about one block per SM.  More
-// blocks per SM measured slower on GB300: a block's phases are chains of
+// the rows are cut finer, down to kMinChunk elements and at most kCutChunks
+// blocks per row, until there is about one block per SM.  Both limits were
+// measured on GB300.  More blocks per SM: a block's phases are chains of
 // short steps and block barriers, and blocks sharing an SM slow each other's
-// chains about as much as they shorten them (e.g. [16,131072]: one block per
-// SM, 16 chunks, 7.6 us; four per SM, 38 chunks, 9.5 us).
+// chains about as much as they shorten them ([16,131072]: one block per SM,
+// 16 chunks, 7.6 us; four per SM, 38 chunks, 9.5 us).  More blocks per row:
+// the last block has more lists to merge ([2,100000]: 16 chunks 6.5 us, 49
+// chunks 7.3 us; [4,65536]: 16 chunks 6.5 us, 32 chunks 6.8 us).
 int blocks_per_row(int64_t rows, int64_t cols, int sm_count) {
     const long long base = (cols + kChunk - 1) / kChunk;
     if (base <= 1) return 1;
-    const long long cap = std::max<long long>(base, std::min<long long>((cols + kMinChunk - 1) / kMinChunk,
-                                                                        kMergeChunks));
+    const long long cap = max_blocks_per_row(cols);
     const long long want = (long long)sm_count / std::max<int64_t>(rows, 1);
     return (int)std::min<long long>(cap, std::max<long long>(base, want));
 }
@@ -809,8 +818,7 @@ size_t topk_workspace_size(int64_t rows, int64_t cols, int32_t k) {
     // depends on (rows, cols, k) only.
     const long long base = (cols + kChunk - 1) / kChunk;
     if (base <= 1) return 0;
-    const long long nchunks =
-        std::max<long long>(base, std::min<long long>((cols + kMinChunk - 1) / kMinChunk, kMergeChunks));
+    const long long nchunks = max_blocks_per_row(cols);
     return round_up((size_t)rows * 4, 256) + (size_t)rows * nchunks * k * 8;
 }
 

@@ -226,10 +226,11 @@ def test_warp_rows_fallback(B, oracle, cols, k, offset):
 # Long rows: the last block of a row merges the chunks' sorted lists with
 # bitonic merges up to 48 chunks, with a threshold from the lists' first keys
 # from 49 to 96, and with bitonic merges in batches beyond.  Chunk counts on
-# a 152-SM GB300: [64,131072] 16, [4,65536] 32, [2,100000] 49, [1,150000] 74,
-# [1,672000] 96, [1,1000000] 123, [2,2000000] 245.
-@pytest.mark.parametrize("rows,cols", [(64, 131072), (4, 65536), (2, 100000), (1, 150000), (1, 672000),
-                                       (1, 1_000_000), (2, 2_000_000)])
+# a 152-SM GB300: [64,131072] 16, [4,65536] 16, [2,100000] 16, [1,150000] 19,
+# [1,393217] 49, [1,672000] 83, [1,786432] 96, [1,786433] 97, [1,1000000]
+# 123, [2,2000000] 245.
+@pytest.mark.parametrize("rows,cols", [(64, 131072), (4, 65536), (2, 100000), (1, 150000), (1, 393217),
+                                       (1, 672000), (1, 786432), (1, 786433), (1, 1_000_000), (2, 2_000_000)])
 @pytest.mark.parametrize("k", [1, 5, 32])
 def test_long_row_merge_paths(B, oracle, rows, cols, k):
     x = synth.logits_with_ties(rows * 7 + cols + k, rows, cols, frac=0.05)
