@@ -53,7 +53,7 @@ METRIC = "frames/s + HBM GB/s (% of roofline); p50/p99 batch-1 graph-replay late
 DEFAULT_WORKLOAD = "b64_1080p_to_224"
 LATENCY_WORKLOAD = "b1_1080p_to_224"
 FALLBACK_HBM_GBS = 6800.0
-LANES = 3          # throughput lanes at least; more for small workloads (see n_lanes)
+LANES = 4          # throughput lanes at least; more for small workloads (see n_lanes)
 MAX_LANES = 64
 
 # DRAM traffic of the preprocess kernel per launch from one ncu
@@ -641,8 +641,11 @@ def main():
     # within a lane the order copy-in -> preprocess -> Top-K is unchanged) --
     # the headline; the second set sharing one stream, every step serialised
     # behind the previous one.
-    # Enough lanes that one rotation touches about three times the L2 (three
-    # for the batched workloads, up to MAX_LANES for the batch-1 ones).
+    # Enough lanes that one rotation touches about three times the L2, and at
+    # least four: while the host waits for a lane and submits it again, three
+    # others keep the GPU busy (on the 4K workload a third lane left gaps:
+    # 24.2 us per step with three lanes, 21.5 with four or six; the 64-frame
+    # step is 28.5 us with three, four or six).
     alg = algorithmic_bytes(w, out_bytes)
     n_lanes = max(LANES, min(MAX_LANES, -(-3 * l2 // max(1, int(alg["total"])))))
     lanes, lanes_1s, keep = [], [], []
