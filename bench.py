@@ -5,16 +5,18 @@ frames into the FP32 NCHW tensor, then the row-wise exact Top-K of the
 logits (the network between them is out of scope; its output slot is a
 fixed logits buffer).  Default workload: 64 independent 1920x1080 RGB8
 frames -> 224x224 mean/std, Top-32 of [64, 1000] logits, the batched
-HBM-throughput configuration.  The headline replays three lanes in
+HBM-throughput configuration.  The headline replays four lanes in
 rotation, each on its own stream (one lane's preprocess overlaps the
-previous lane's Top-K, as lanes run in a deployment); the same three lanes
-on one shared stream, every step serialised, are reported beside it.  Also
-measured on every run:
+previous lane's Top-K, as lanes run in a deployment); the same lanes on one
+shared stream, every step serialised, are reported beside it.  Also measured
+on every run:
 
 * batch-1 graph-replay latency (p50 / p99 / max, GPU events and host steady
   clock, graph and no-graph) on one 1920x1080 frame -> 224x224, Top-5 of 1000;
-* end-to-end throughput through the lane API with host buffers: the graph
-  copies the frames from pinned host memory and the result back;
+* end-to-end throughput through the lane API with host buffers: the frames
+  sit in mapped pinned host memory, which the preprocess reads in place, and
+  the K pairs are written to pinned host memory (a second figure copies the
+  whole frames in with a copy node of the graph);
 * the roofline of the dominant kernel (the preprocess): its average launch
   duration from CUDA events around back-to-back launches on the lanes'
   buffers, against the measured HBM copy bandwidth;
