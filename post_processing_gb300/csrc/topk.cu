@@ -473,10 +473,12 @@ __global__ void __launch_bounds__(kThreads, 4) topk_kernel(const __grid_constant
             if (c >= p.nchunks || lane >= k) key[r] = 0ull;
             else if (lane < m) s.cand[c * m + lane] = key[r];
         }
-        if (tid == 0) s.red[0] = ~0ull;
         __syncthreads();
-        // min of the top K = the K-th largest
-        rank_and_emit(s.cand, (uint32_t)U, k, [&](int, unsigned long long kv) { atomicMin(&s.red[0], kv); });
+        // The U first keys are real keys, hence unique: exactly one of them
+        // has rank K - 1, and it is the K-th largest.
+        rank_and_emit(s.cand, (uint32_t)U, k, [&](int rank, unsigned long long kv) {
+            if (rank == k - 1) s.red[0] = kv;
+        });
         __syncthreads();
         unsigned long long t64 = s.red[0];
         if (t64 == 0) t64 = 1;   // padding keys (0) never pass
