@@ -103,6 +103,20 @@ def test_special_rows(B, oracle, cols, k):
     check_topk_invariants(x, got[0], got[1], k)
 
 
+# The same adversarial rows at the lengths of the long-row merge paths (19
+# chunk lists: bitonic; 49 and 83: threshold from the lists' first keys; 97:
+# bitonic in batches).  In a constant or all-NaN row that threshold keeps the
+# whole lists of the K - 1 lowest chunks and the first key of the next one:
+# 993 survivors at K = 32, ranked in the merging block.
+@pytest.mark.parametrize("cols", [150000, 393217, 672000, 786433])
+@pytest.mark.parametrize("k", [1, 32])
+def test_special_long_rows(B, oracle, cols, k):
+    x = special_rows(cols, np.random.default_rng(3 * cols + k))
+    got = gpu_topk(B, x, k)
+    assert_exact(got, oracle.topk(x, k))
+    check_topk_invariants(x, got[0], got[1], k)
+
+
 def test_misaligned_pointer_scalar_path(B, oracle):
     x = synth.logits_normal(5, 4, 10001)
     assert_exact(gpu_topk(B, x, 32, offset=1), oracle.topk(x, 32))
