@@ -574,6 +574,14 @@ def percentiles(xs):
             "mean": float(a.mean())}
 
 
+def preprocess_kernel_name(w: dict) -> str:
+    """The kernel ws_preprocess launches for a workload: outputs of at most
+    460,000 pixels (batch x dst_w x dst_h) take the per-pixel kernel, larger
+    ones (dst_w at most 8192) the staged ring kernel."""
+    small = w["batch"] * w["dst_w"] * w["dst_h"] <= 460_000
+    return "pre_direct_kernel" if small or w["dst_w"] > 8192 else "pre_ring_kernel"
+
+
 def source_sha(path: str) -> str:
     return hashlib.sha256(open(path, "rb").read()).hexdigest()
 
@@ -904,7 +912,7 @@ def main():
             "serialized_one_stream": {"value": value_1s, "ms_per_step": 1000.0 * t_max_1s / args.steps,
                                       "hbm_gbs_step": alg["total"] * args.steps * world / t_max_1s / 1e9,
                                       "lanes": f"{n_lanes} lanes sharing one stream: each step after the previous"},
-            "roofline": {"bound": "hbm", "kernel": "pre_ring_kernel", "achieved": achieved, "peak": peak,
+            "roofline": {"bound": "hbm", "kernel": preprocess_kernel_name(w), "achieved": achieved, "peak": peak,
                          "unit": "GB/s", "frac": achieved / peak, "peak_source": peak_src,
                          "traffic": traffic, "algorithmic_bytes_per_launch": alg["preprocess"],
                          "full_frame_bytes_per_launch": alg["full_frame_preprocess"],
