@@ -582,6 +582,150 @@ def preprocess_kernel_name(w: dict) -> str:
     return "pre_direct_kernel" if small or w["dst_w"] > 8192 else "pre_ring_kernel"
 
 
+ROOFLINE_LAUNCHES = 1000
+
+
+def kernel_times(B, torch, stream, pre, w: dict, bufs, n: int, device) -> tuple[float, float]:
+    """Average launch time (us) of the preprocess and of the Top-K over n
+    back-to-back launches each, through the C ABI on `stream`, rotating over
+    the lanes' buffers; CUDA events on that stream around the n launches."""
+    st_ws = [B.ws_topk_workspace_bytes(w["rows"], w["cols"], w["k"])[1] for _ in bufs]
+    topk_ws = [torch.zeros(max(m, 1), dtype=torch.uint8, device=device) for m in st_ws]
+
+    def time_kernel(launch):
+        for i in range(8):
+            launch(i)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        e0.record(stream)
+        for i in range(n):
+            launch(i)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) * 1000.0 / n
+
+    def launch_pre(i):
+        b = bufs[i % len(bufs)]
+        B.check(B.ws_preprocess(pre, b.input_device, w["batch"], b.tensor, stream.cuda_stream))
+
+    def launch_topk(i):
+        b, ws_t, m = bufs[i % len(bufs)], topk_ws[i % len(bufs)], st_ws[i % len(bufs)]
+        B.check(B.ws_topk(b.logits, w["rows"], w["cols"], w["k"], b.result_val_device, b.result_idx_device,
+                          ws_t.data_ptr() if m else None, m, stream.cuda_stream))
+
+    return time_kernel(launch_pre), time_kernel(launch_topk)
+
+
+def make_lanes(B, Lane, torch, w: dict, pre, frames_dev, logits_dev, n_lanes: int, stream):
+    """n_lanes throughput lanes without timing events, each with its own copy
+    of the inputs: on their own streams (stream None) or sharing `stream`."""
+    lanes, keep = [], []
+    for _ in range(n_lanes):
+        src = frames_dev.clone()
+        lg = logits_dev.clone()
+        keep += [src, lg]
+        d = B.lane_desc(pre, w["batch"], w["rows"], w["cols"], w["k"], input=src.data_ptr(), logits=lg.data_ptr(),
+                        stream=stream, flags=B.WS_LANE_FLAG_NO_TIMING)
+        lanes.append(Lane(d))
+    return lanes, keep
+
+
+def run_steps(B, ls, n):
+    """Round-robin submits over lanes `ls`; returns the lanes still in flight."""
+    inflight = []
+    for s_ in range(n):
+        lane = ls[s_ % len(ls)]
+        if lane.state == B.WS_LANE_IN_FLIGHT:
+            lane.wait()
+            inflight.remove(lane)
+        lane.acquire()
+        lane.submit()
+        inflight.append(lane)
+    return inflight
+
+
+def timed_steps(B, torch, stream, ls, n):
+    """Device time (s) of n steps: a start event on `stream`, which every lane
+    stream waits on, and an end event after `stream` has waited on every lane
+    stream's last work."""
+    lane_streams = [torch.cuda.ExternalStream(lane.buffers.stream) for lane in ls]
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    ev0.record(stream)
+    for ls_ in lane_streams:
+        ls_.wait_event(ev0)
+    inflight = run_steps(B, ls, n)
+    for ls_ in lane_streams:
+        e = torch.cuda.Event()
+        e.record(ls_)
+        stream.wait_event(e)
+    ev1.record(stream)
+    for lane in inflight:
+        lane.wait()
+    torch.cuda.synchronize()
+    return ev0.elapsed_time(ev1) / 1000.0
+
+
+C5_WORKLOAD = "b8_4k_to_512"
+
+
+def c5_record(B, Lane, torch, device, stream, peak: float, steps: int = 400) -> dict:
+    """The second batched configuration (8 x 4K -> 512 + Top-32 of
+    [32,131072] with 5 % ties): frames/s with four lanes on their own streams
+    and with the same lanes' steps serialised on one stream, the step's
+    algorithmic bytes per second, each kernel's average launch time and the
+    roofline fraction of both against the measured copy bandwidth."""
+    w = synth.WORKLOADS[C5_WORKLOAD]
+    frames_dev = torch.from_numpy(synth.make_frames(C5_WORKLOAD)).to(device)
+    logits_dev = torch.from_numpy(synth.make_logits(C5_WORKLOAD)).to(device)
+    pre = B.preprocess_desc(w["src_w"], w["src_h"], w["dst_w"], w["dst_h"], norm=w["norm"])
+    alg = algorithmic_bytes(w)
+    own, keep = make_lanes(B, Lane, torch, w, pre, frames_dev, logits_dev, LANES, None)
+    one, keep1 = make_lanes(B, Lane, torch, w, pre, frames_dev, logits_dev, LANES, stream.cuda_stream)
+    try:
+        for ls in (own, one):
+            for lane in run_steps(B, ls, 20):
+                lane.wait()
+        t_own = timed_steps(B, torch, stream, own, steps)
+        t_one = timed_steps(B, torch, stream, one, steps)
+        pre_us, topk_us = kernel_times(B, torch, stream, pre, w, [lane.buffers for lane in one], ROOFLINE_LAUNCHES,
+                                       device)
+    finally:
+        for lane in own + one:
+            lane.close()
+    step_own, step_one = t_own / steps, t_one / steps
+    return {
+        "workload": C5_WORKLOAD, "steps": steps,
+        "frames_per_s": w["batch"] / step_own, "us_per_step": 1e6 * step_own,
+        "step_frac": alg["total"] / step_own / 1e9 / peak,
+        "one_stream_frames_per_s": w["batch"] / step_one, "one_stream_us_per_step": 1e6 * step_one,
+        "one_stream_step_frac": alg["total"] / step_one / 1e9 / peak,
+        "preprocess_us": pre_us, "preprocess_frac": alg["preprocess"] / (pre_us * 1e-6) / 1e9 / peak,
+        "topk_us": topk_us, "topk_frac": alg["topk"] / (topk_us * 1e-6) / 1e9 / peak,
+        "algorithmic_bytes_per_step": alg["total"], "peak_gbs": peak,
+        "lanes": f"{LANES} lanes on their own streams; one_stream: {LANES} lanes sharing one stream",
+    }
+
+
+def latency_summary(latency: dict, other: dict) -> dict:
+    """p50 / p99 (us) of each batch-1 configuration, compact: GPU interval
+    and host clock of the timed graph replay, host clock of the graph replay
+    without timing events, GPU interval and host clock of direct launches."""
+    out = {}
+    for rec in [latency] + list(other.values()):
+        name = next(n for n, v in synth.WORKLOADS.items() if workload_config(n, v)["workload"] == rec["workload"])
+
+        def pp(d):
+            return [round(d["p50"], 2), round(d["p99"], 2)]
+        out[name] = {"graph_gpu": pp(rec["graph"]["gpu_us"]), "graph_host": pp(rec["graph"]["host_us"]),
+                     "graph_no_timing_host": pp(rec["graph_no_timing"]["host_us"]),
+                     "no_graph_gpu": pp(rec["no_graph"]["gpu_us"]), "no_graph_host": pp(rec["no_graph"]["host_us"])}
+    out["replay_floor_gpu"] = [round(latency["graph_floor"]["gpu_us"]["p50"], 2),
+                               round(latency["graph_floor"]["gpu_us"]["p99"], 2)]
+    out["fields"] = "[p50, p99] us; samples per entry as in latency_b1"
+    return out
+
+
 def source_sha(path: str) -> str:
     return hashlib.sha256(open(path, "rb").read()).hexdigest()
 
@@ -597,6 +741,7 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=60)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-detect", action="store_true", help="skip the detection decode + NMS measurements")
+    ap.add_argument("--no-c5", action="store_true", help="skip the compact 8 x 4K -> 512 record")
     ap.add_argument("--out-dtype", default="f32", choices=["f32", "f16", "bf16"],
                     help="element type of the NCHW tensor (the workloads specify FP32)")
     args = ap.parse_args()
@@ -658,96 +803,31 @@ def main():
     # step is 28.5 us with three, four or six).
     alg = algorithmic_bytes(w, out_bytes)
     n_lanes = max(LANES, min(MAX_LANES, -(-3 * l2 // max(1, int(alg["total"])))))
-    lanes, lanes_1s, keep = [], [], []
-    for one_stream in (False, True):
-        for _ in range(n_lanes):
-            src = frames_dev.clone()
-            lg = logits_dev.clone()
-            keep += [src, lg]
-            d = B.lane_desc(pre, w["batch"], w["rows"], w["cols"], w["k"], input=src.data_ptr(), logits=lg.data_ptr(),
-                            stream=stream.cuda_stream if one_stream else None, flags=B.WS_LANE_FLAG_NO_TIMING)
-            (lanes_1s if one_stream else lanes).append(Lane(d))
+    lanes, keep = make_lanes(B, Lane, torch, w, pre, frames_dev, logits_dev, n_lanes, None)
+    lanes_1s, keep1 = make_lanes(B, Lane, torch, w, pre, frames_dev, logits_dev, n_lanes, stream.cuda_stream)
     torch.cuda.synchronize()
     touched_per_rotation = n_lanes * alg["total"]
 
-    def run_steps(ls, n):
-        """Round-robin submits; returns the lanes still in flight."""
-        inflight = []
-        for s_ in range(n):
-            lane = ls[s_ % len(ls)]
-            if lane.state == B.WS_LANE_IN_FLIGHT:
-                lane.wait()
-                inflight.remove(lane)
-            lane.acquire()
-            lane.submit()
-            inflight.append(lane)
-        return inflight
-
-    def timed_steps(ls, n):
-        """Device time of n steps: a start event on `stream`, which every lane
-        stream waits on, and an end event after `stream` has waited on every
-        lane stream's last work."""
-        lane_streams = [torch.cuda.ExternalStream(lane.buffers.stream) for lane in ls]
-        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        torch.cuda.synchronize()
-        ev0.record(stream)
-        for ls_ in lane_streams:
-            ls_.wait_event(ev0)
-        inflight = run_steps(ls, n)
-        for ls_ in lane_streams:
-            e = torch.cuda.Event()
-            e.record(ls_)
-            stream.wait_event(e)
-        ev1.record(stream)
-        for lane in inflight:
-            lane.wait()
-        torch.cuda.synchronize()
-        return ev0.elapsed_time(ev1) / 1000.0
-
     for ls in (lanes, lanes_1s):
-        for lane in run_steps(ls, args.warmup):
+        for lane in run_steps(B, ls, args.warmup):
             lane.wait()
     torch.cuda.synchronize()
     if world > 1:
         torch.distributed.barrier()
     clocks.start()
-    elapsed_s = timed_steps(lanes, args.steps)
-    elapsed_1s = timed_steps(lanes_1s, args.steps)
+    elapsed_s = timed_steps(B, torch, stream, lanes, args.steps)
+    elapsed_1s = timed_steps(B, torch, stream, lanes_1s, args.steps)
     if world > 1:
         torch.distributed.barrier()
 
     # Per-kernel durations for the roofline: the same kernels on the same
     # stream and the lanes' own buffers (rotating, so inputs stay larger than
     # L2), launched back to back through the C ABI and bracketed by CUDA
-    # events, right after the timed region.
-    kernel_launches = min(args.steps, 2000)
-    bufs = [lane.buffers for lane in lanes_1s]
-    st_ws = [B.ws_topk_workspace_bytes(w["rows"], w["cols"], w["k"])[1] for _ in lanes]
-    topk_ws = [torch.zeros(max(n, 1), dtype=torch.uint8, device=device) for n in st_ws]
-
-    def time_kernel(launch, n):
-        for i in range(8):
-            launch(i)
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        torch.cuda.synchronize()
-        e0.record(stream)
-        for i in range(n):
-            launch(i)
-        e1.record(stream)
-        torch.cuda.synchronize()
-        return e0.elapsed_time(e1) * 1000.0 / n
-
-    def launch_pre(i):
-        b = bufs[i % len(bufs)]
-        B.check(B.ws_preprocess(pre, b.input_device, w["batch"], b.tensor, stream.cuda_stream))
-
-    def launch_topk(i):
-        b, ws_t, n = bufs[i % len(bufs)], topk_ws[i % len(bufs)], st_ws[i % len(bufs)]
-        B.check(B.ws_topk(b.logits, w["rows"], w["cols"], w["k"], b.result_val_device, b.result_idx_device,
-                          ws_t.data_ptr() if n else None, n, stream.cuda_stream))
-
-    pre_avg_us = time_kernel(launch_pre, kernel_launches)
-    topk_avg_us = time_kernel(launch_topk, kernel_launches)
+    # events, right after the timed region; a fixed number of launches,
+    # whatever --steps is.
+    kernel_launches = ROOFLINE_LAUNCHES
+    pre_avg_us, topk_avg_us = kernel_times(B, torch, stream, pre, w, [lane.buffers for lane in lanes_1s],
+                                           kernel_launches, device)
 
     # batch-1 latency: one lane, submit -> wait, graph and direct launches.
     # "graph": the page's measurement, timing events just before the graph
@@ -817,6 +897,12 @@ def main():
     if not args.no_detect:
         detect = detect_measurements(B, Lane, device, stream, min(2000, args.latency_samples))
     lanes_extra = lane_measurements(B, Lane, device, args.latency_samples)
+    peaks_path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(peaks_path):
+        peak, peak_src = float(json.load(open(peaks_path))["hbm_gbs"]), "measured"
+    else:
+        peak, peak_src = FALLBACK_HBM_GBS, "fallback"
+    c5 = None if args.no_c5 else c5_record(B, Lane, torch, device, stream, peak)
     clk = clocks.stop()
 
     # End to end through the lane API with host buffers, two lanes each on its
@@ -881,11 +967,6 @@ def main():
 
     value, t_max = whole_job_rate(w["batch"] * args.steps, elapsed_s, world, device)
     value_1s, t_max_1s = whole_job_rate(w["batch"] * args.steps, elapsed_1s, world, device)
-    peaks_path = os.path.join(ROOT, "MEASURED_PEAKS.json")
-    if os.path.exists(peaks_path):
-        peak, peak_src = float(json.load(open(peaks_path))["hbm_gbs"]), "measured"
-    else:
-        peak, peak_src = FALLBACK_HBM_GBS, "fallback"
     achieved = alg["preprocess"] / (pre_avg_us * 1e-6) / 1e9
     sha = source_sha(os.path.join(ROOT, "post_processing_gb300", "csrc", "preprocess.cu"))
     traffic = NCU_TRAFFIC.get(args.workload) if args.out_dtype == "f32" else None   # captured on FP32 output
@@ -932,6 +1013,10 @@ def main():
             "cpu_baseline": cpu,
             "cpu_baseline_all_cores": cpu_all,
         }
+        # compact records last, so that a tail of the line shows them
+        if c5 is not None:
+            line["c5"] = {k_: (round(v_, 4) if isinstance(v_, float) else v_) for k_, v_ in c5.items()}
+        line["latency_b1_summary"] = latency_summary(latency, latency_other)
         line["roofline"]["frac_note"] = "of measured" if peak_src == "measured" else "of fallback"
         if detect:
             r = detect["decode_roofline"]

@@ -90,6 +90,31 @@ ws_status ws_device_error(uint32_t* flags, int32_t clear);
  * Asynchronous on `stream`; read the result with ws_device_error. */
 ws_status ws_selftest_wait_timeout(uint32_t limit_us, cudaStream_t stream);
 
+/* Host-side fault injection for the cleanup paths of ws_lane_create,
+ * ws_lane_rebind and ws_pool_create (a test hook; the pages' lane section asks
+ * that failures be explicit, never a silent leak or a half-built lane).  Each
+ * internal call of those paths that can fail (a stream, event, device or
+ * pinned allocation, a memset, a graph capture, instantiation, upload or
+ * update) first passes a fault point.  After this call, fault points number
+ * nth, nth + 1, ..., nth + count - 1 counted from now (1-based, over all
+ * threads) fail without calling CUDA, with the status the real failure would
+ * give: WS_ERR_OUT_OF_MEMORY for an allocation, WS_ERR_CAPTURE for a graph
+ * step, WS_ERR_CUDA otherwise.  An end of capture is the one exception: the
+ * real call is made, so the stream leaves capture mode, and its graph is then
+ * discarded.  nth <= 0 or count == 0 disarms it.  Nothing runs on the GPU. */
+ws_status ws_debug_inject_failure(int32_t nth, int32_t count);
+
+/* CUDA resources the library holds now, and the fault points reached since
+ * the last ws_debug_inject_failure (for leak checks after a failure). */
+typedef struct ws_debug_counters {
+    int64_t device_allocs;        /* cudaMalloc blocks                              */
+    int64_t host_allocs;          /* cudaHostAlloc blocks                           */
+    int64_t graphs, graph_execs;  /* captured and executable graphs                 */
+    int64_t events, streams;
+    int64_t fault_points;         /* fault points reached since the last arming     */
+} ws_debug_counters;
+ws_status ws_debug_get_counters(ws_debug_counters* counters);
+
 /* -------------------------------------------------------------- preprocess */
 
 #define WS_RESIZE_STRETCH   0  /* bilinear resize of the whole frame to dst_w x dst_h   */
@@ -467,18 +492,37 @@ ws_status ws_lane_submit_n(ws_lane* lane, int32_t n);
  * lane allocated itself stay allocated until ws_lane_destroy.  This is how a
  * producer that writes into its own device memory (a decoder's or camera's
  * GPUDirect buffers) registers them with a lane.
+ * All or nothing: every bucket is re-captured before any executable graph
+ * changes, and a failure after some graphs were updated puts those back, so
+ * on an error the lane keeps its previous buffers and graphs.
  * WS_ERR_LANE_BUSY while in flight; WS_ERR_INVALID_ARGUMENT for a MAPPED input
- * that is not mapped pinned memory (the lane is unchanged); WS_ERR_CAPTURE if
- * a capture or instantiation fails, after which the lane may only be
+ * that is not mapped pinned memory; WS_ERR_CAPTURE if a capture,
+ * instantiation or update fails (the lane is unchanged and usable).  Only if
+ * putting the previous graphs back fails as well is the lane marked broken:
+ * later submits and rebinds return WS_ERR_CAPTURE and it may only be
  * destroyed. */
 ws_status ws_lane_rebind(ws_lane* lane, void* input, float* logits, int32_t* reinstantiated);
 
 /* IN_FLIGHT -> FREE once the end event has completed.  timeout_us < 0 waits
  * without limit; otherwise WS_ERR_TIMEOUT after timeout_us microseconds, with
  * the lane still IN_FLIGHT (call again).  timing may be NULL.
- * WS_ERR_LANE_STATE unless in flight; WS_ERR_CUDA if the GPU work failed
- * (the lane is then FREE, its results undefined). */
+ * Every lane has its own error word (4 bytes of mapped pinned memory) that its
+ * kernels set when a bounded wait on a bulk copy runs out ("Inside WarpStream
+ * TRT", lane section: failures are explicit); wait reads it once the work has
+ * completed, with no extra synchronisation.
+ * WS_ERR_LANE_STATE unless in flight; WS_ERR_CUDA if the GPU work failed;
+ * WS_ERR_DEVICE if one of the lane's kernels gave up a bounded wait (the
+ * message names the error bits; the word is cleared, so the next submit
+ * starts clean).  After either error the lane is FREE and this submit's
+ * results are undefined. */
 ws_status ws_lane_wait(ws_lane* lane, int64_t timeout_us, ws_lane_timing* timing);
+
+/* Diagnostic of the lane's error path: enqueues on the lane's stream the
+ * bounded wait that nothing completes (as ws_selftest_wait_timeout, 1 .. 1e6
+ * microseconds), reporting into this lane's error word, so that the wait of
+ * the next submit returns WS_ERR_DEVICE.  The lane must not be in flight
+ * (WS_ERR_LANE_BUSY) nor host-only (WS_ERR_UNSUPPORTED). */
+ws_status ws_lane_selftest_wait_timeout(ws_lane* lane, uint32_t limit_us);
 
 /* ACQUIRED -> FREE without a submit; WS_ERR_LANE_STATE otherwise. */
 ws_status ws_lane_release(ws_lane* lane);
@@ -516,8 +560,9 @@ ws_status ws_pool_acquire(ws_pool* pool, int64_t timeout_us, ws_lane** lane);
 ws_status ws_pool_submit(ws_pool* pool, ws_lane* lane, int32_t n);
 
 /* Waits for the oldest submitted lane; *lane is it, completed and held.
- * WS_ERR_TIMEOUT if nothing completed in time; WS_ERR_CUDA if its GPU work
- * failed (it is still returned, held, its results undefined). */
+ * WS_ERR_TIMEOUT if nothing completed in time; WS_ERR_CUDA or WS_ERR_DEVICE
+ * (as ws_lane_wait) if its GPU work failed (it is still returned, held, its
+ * results undefined). */
 ws_status ws_pool_complete(ws_pool* pool, int64_t timeout_us, ws_lane** lane, ws_lane_timing* timing);
 
 /* A held (or an acquired, unsubmitted) lane back to the free list. */

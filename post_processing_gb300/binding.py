@@ -78,6 +78,11 @@ class ws_lane_buffers(ctypes.Structure):
                 ("det_count_device", _vp)]
 
 
+class ws_debug_counters(ctypes.Structure):
+    _fields_ = [("device_allocs", _i64), ("host_allocs", _i64), ("graphs", _i64), ("graph_execs", _i64),
+                ("events", _i64), ("streams", _i64), ("fault_points", _i64)]
+
+
 class ws_lane_timing(ctypes.Structure):
     _fields_ = [("gpu_us", _f32), ("preprocess_us", _f32), ("post_us", _f32), ("host_us", ctypes.c_double)]
 
@@ -99,6 +104,8 @@ SIGNATURES = {
     "ws_version": (_i32, []),
     "ws_device_error": (_i32, [ctypes.POINTER(_u32), _i32]),
     "ws_selftest_wait_timeout": (_i32, [_u32, _vp]),
+    "ws_debug_inject_failure": (_i32, [_i32, _i32]),
+    "ws_debug_get_counters": (_i32, [ctypes.POINTER(ws_debug_counters)]),
     "ws_preprocess_validate": (_i32, [ctypes.POINTER(ws_preprocess_desc), _i32]),
     "ws_preprocess": (_i32, [ctypes.POINTER(ws_preprocess_desc), _vp, _i32, _vp, _vp]),
     "ws_preprocess_path": (_i32, [ctypes.POINTER(ws_preprocess_desc), _vp, _i32, _vp, _i32, _vp]),
@@ -120,6 +127,7 @@ SIGNATURES = {
     "ws_lane_submit_n": (_i32, [_vp, _i32]),
     "ws_lane_rebind": (_i32, [_vp, _vp, _vp, ctypes.POINTER(_i32)]),
     "ws_lane_wait": (_i32, [_vp, _i64, ctypes.POINTER(ws_lane_timing)]),
+    "ws_lane_selftest_wait_timeout": (_i32, [_vp, _u32]),
     "ws_lane_release": (_i32, [_vp]),
     "ws_lane_destroy": (_i32, [_vp]),
     "ws_lane_state": (_i32, [_vp]),
@@ -185,6 +193,16 @@ def ws_device_error(clear: bool = False) -> tuple[int, int]:
 
 def ws_selftest_wait_timeout(limit_us: int, stream: int = 0) -> int:
     return lib.ws_selftest_wait_timeout(limit_us, stream)
+
+
+def ws_debug_inject_failure(nth: int, count: int = 1) -> int:
+    return lib.ws_debug_inject_failure(nth, count)
+
+
+def ws_debug_get_counters() -> tuple[int, ws_debug_counters]:
+    c = ws_debug_counters()
+    st = lib.ws_debug_get_counters(ctypes.byref(c))
+    return st, c
 
 
 def ws_preprocess_validate(desc: ws_preprocess_desc, batch: int) -> int:
@@ -303,6 +321,10 @@ def ws_lane_wait(lane: int, timeout_us: int = -1) -> tuple[int, ws_lane_timing]:
     t = ws_lane_timing()
     st = lib.ws_lane_wait(lane, timeout_us, ctypes.byref(t))
     return st, t
+
+
+def ws_lane_selftest_wait_timeout(lane: int, limit_us: int) -> int:
+    return lib.ws_lane_selftest_wait_timeout(lane, limit_us)
 
 
 def ws_lane_release(lane: int) -> int:

@@ -68,6 +68,12 @@ struct ws_lane {
     cudaGraph_t graph[kMaxBuckets] = {};
     cudaGraphExec_t exec[kMaxBuckets] = {};
     std::chrono::steady_clock::time_point t_submit;
+    // this lane's error word (mapped pinned): its kernels set bits in it when
+    // a bounded wait gives up; wait reads and clears it
+    uint32_t* err_host = nullptr;
+    uint32_t* err_dev = nullptr;
+    // a failed rebind could not restore the previous graphs: only destroy
+    bool broken = false;
 };
 
 namespace ws {
@@ -107,48 +113,108 @@ int64_t bucket_rows(const ws_lane* L, int nb) {
     return nb == L->d.batch ? L->d.rows : L->d.rows / L->d.batch * nb;
 }
 
-void release_all(ws_lane* L) {
-    if (L->fake) return;
-    for (int i = 0; i < kMaxBuckets; ++i) {
-        if (L->exec[i]) cudaGraphExecDestroy(L->exec[i]);
-        if (L->graph[i]) cudaGraphDestroy(L->graph[i]);
-        if (L->ws[i]) cudaFree(L->ws[i]);
-    }
-    for (cudaEvent_t e : {L->ev_start, L->ev_end, L->ev_pre0, L->ev_pre1, L->ev_post1})
-        if (e) cudaEventDestroy(e);
-    if (L->own_r_dev) {
-        cudaFree(L->rv_dev);
-        cudaFree(L->ri_dev);
-    }
-    if (L->own_r_host) {
-        cudaFreeHost(L->rv_host);
-        cudaFreeHost(L->ri_host);
-    }
-    if (L->owned_logits) cudaFree(L->owned_logits);
-    if (L->own_tensor) cudaFree(L->tensor);
-    if (L->owned_in_dev) cudaFree(L->owned_in_dev);
-    if (L->owned_in_host) cudaFreeHost(L->owned_in_host);
-    if (L->own_stream) cudaStreamDestroy(L->stream);
-}
-
+// Every CUDA resource a lane makes or frees goes through these helpers: each
+// creation first passes a fault point (host-side fault injection, see
+// ws_debug_inject_failure) and the live resources are counted.
 ws_status alloc_dev(void** p, size_t bytes, const char* what) {
+    *p = nullptr;
+    if (fault_point()) return fail(WS_ERR_OUT_OF_MEMORY, "injected failure: cudaMalloc of %zu bytes for %s", bytes, what);
     cudaError_t e = cudaMalloc(p, bytes);
     if (e == cudaErrorMemoryAllocation) {
         cudaGetLastError();
         return fail(WS_ERR_OUT_OF_MEMORY, "cudaMalloc of %zu bytes for %s", bytes, what);
     }
     if (e != cudaSuccess) return cuda_fail(e, what);
+    count_resource(kResDevice, +1);
     return WS_OK;
 }
 
 ws_status alloc_host(void** p, size_t bytes, unsigned flags, const char* what) {
+    *p = nullptr;
+    if (fault_point()) return fail(WS_ERR_OUT_OF_MEMORY, "injected failure: cudaHostAlloc of %zu bytes for %s", bytes, what);
     cudaError_t e = cudaHostAlloc(p, bytes, flags);
     if (e == cudaErrorMemoryAllocation) {
         cudaGetLastError();
         return fail(WS_ERR_OUT_OF_MEMORY, "cudaHostAlloc of %zu bytes for %s", bytes, what);
     }
     if (e != cudaSuccess) return cuda_fail(e, what);
+    count_resource(kResHost, +1);
     return WS_OK;
+}
+
+void free_dev(void* p) {
+    if (!p) return;
+    cudaFree(p);
+    count_resource(kResDevice, -1);
+}
+
+void free_host(void* p) {
+    if (!p) return;
+    cudaFreeHost(p);
+    count_resource(kResHost, -1);
+}
+
+ws_status make_event(cudaEvent_t* ev, unsigned flags) {
+    *ev = nullptr;
+    if (fault_point()) return fail(WS_ERR_CUDA, "injected failure: cudaEventCreateWithFlags");
+    WS_TRY_CUDA(cudaEventCreateWithFlags(ev, flags));
+    count_resource(kResEvent, +1);
+    return WS_OK;
+}
+
+void destroy_event(cudaEvent_t ev) {
+    if (!ev) return;
+    cudaEventDestroy(ev);
+    count_resource(kResEvent, -1);
+}
+
+ws_status memset_async(void* p, size_t bytes, cudaStream_t s, const char* what) {
+    if (fault_point()) return fail(WS_ERR_CUDA, "injected failure: cudaMemsetAsync of %s", what);
+    cudaError_t e = cudaMemsetAsync(p, 0, bytes, s);
+    if (e != cudaSuccess) return cuda_fail(e, what);
+    return WS_OK;
+}
+
+void destroy_graph(cudaGraph_t g) {
+    if (!g) return;
+    cudaGraphDestroy(g);
+    count_resource(kResGraph, -1);
+}
+
+void destroy_exec(cudaGraphExec_t x) {
+    if (!x) return;
+    cudaGraphExecDestroy(x);
+    count_resource(kResExec, -1);
+}
+
+void release_all(ws_lane* L) {
+    if (L->fake) return;
+    for (int i = 0; i < kMaxBuckets; ++i) {
+        destroy_exec(L->exec[i]);
+        destroy_graph(L->graph[i]);
+        free_dev(L->ws[i]);
+        L->exec[i] = nullptr;
+        L->graph[i] = nullptr;
+        L->ws[i] = nullptr;
+    }
+    for (cudaEvent_t e : {L->ev_start, L->ev_end, L->ev_pre0, L->ev_pre1, L->ev_post1}) destroy_event(e);
+    if (L->own_r_dev) {
+        free_dev(L->rv_dev);
+        free_dev(L->ri_dev);
+    }
+    if (L->own_r_host) {
+        free_host(L->rv_host);
+        free_host(L->ri_host);
+    }
+    free_dev(L->owned_logits);
+    if (L->own_tensor) free_dev(L->tensor);
+    free_dev(L->owned_in_dev);
+    free_host(L->owned_in_host);
+    free_host(L->err_host);
+    if (L->own_stream) {
+        cudaStreamDestroy(L->stream);
+        count_resource(kResStream, -1);
+    }
 }
 
 ws_status device_view(void* host, void** dev, const char* what) {
@@ -169,6 +235,7 @@ ws_status record(cudaEvent_t ev, cudaStream_t s, bool capturing) {
 ws_status enqueue_path(ws_lane* L, bool capturing, int bi) {
     ws_status st;
     const NoPdlScope no_pdl((L->d.flags & WS_LANE_FLAG_NO_PDL) != 0);
+    const ErrWordScope err_word(L->err_dev);   // the lane's kernels report into its own word
     const int nb = L->bucket_batch[bi];
     const int64_t rows = bucket_rows(L, nb);
     if (L->d.input_mode == WS_INPUT_COPY)
@@ -203,38 +270,77 @@ ws_status enqueue_path(ws_lane* L, bool capturing, int bi) {
 // Capture bucket bi's path into a new graph (its buffers as bound now).
 ws_status capture_bucket(ws_lane* L, int bi, cudaGraph_t* out) {
     *out = nullptr;
+    if (fault_point()) return fail(WS_ERR_CAPTURE, "injected failure: begin capture");
     cudaError_t e = cudaStreamBeginCapture(L->stream, cudaStreamCaptureModeThreadLocal);
     if (e != cudaSuccess) return fail(WS_ERR_CAPTURE, "begin capture: %s", cudaGetErrorName(e));
     ws_status st = enqueue_path(L, true, bi);
     cudaGraph_t g = nullptr;
+    // the real end of capture always runs, so the stream leaves capture mode
+    const bool injected = fault_point();
     e = cudaStreamEndCapture(L->stream, &g);
-    if (st != WS_OK) {
-        if (g) cudaGraphDestroy(g);
-        return st;
+    if (g) count_resource(kResGraph, +1);
+    if (st != WS_OK || e != cudaSuccess || injected) {
+        destroy_graph(g);
+        cudaGetLastError();
+        if (st != WS_OK) return st;
+        if (injected) return fail(WS_ERR_CAPTURE, "injected failure: end capture");
+        return fail(WS_ERR_CAPTURE, "end capture: %s", cudaGetErrorName(e));
     }
-    if (e != cudaSuccess) return fail(WS_ERR_CAPTURE, "end capture: %s", cudaGetErrorName(e));
     *out = g;
     return WS_OK;
 }
 
-ws_status instantiate_bucket(ws_lane* L, int bi) {
-    cudaError_t e = cudaGraphInstantiateWithFlags(&L->exec[bi], L->graph[bi], 0);
-    if (e != cudaSuccess) return fail(WS_ERR_CAPTURE, "instantiate: %s", cudaGetErrorName(e));
-    // Upload once so the first submit pays no first-launch set-up.
-    e = cudaGraphUpload(L->exec[bi], L->stream);
-    if (e != cudaSuccess) return fail(WS_ERR_CAPTURE, "upload: %s", cudaGetErrorName(e));
+// An executable graph of g, uploaded once so the first submit pays no
+// first-launch set-up.  *out is NULL on failure.
+ws_status instantiate_graph(cudaGraph_t g, cudaGraphExec_t* out, cudaStream_t stream) {
+    *out = nullptr;
+    if (fault_point()) return fail(WS_ERR_CAPTURE, "injected failure: instantiate");
+    cudaGraphExec_t x = nullptr;
+    cudaError_t e = cudaGraphInstantiateWithFlags(&x, g, 0);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return fail(WS_ERR_CAPTURE, "instantiate: %s", cudaGetErrorName(e));
+    }
+    count_resource(kResExec, +1);
+    if (fault_point()) {
+        destroy_exec(x);
+        return fail(WS_ERR_CAPTURE, "injected failure: upload");
+    }
+    e = cudaGraphUpload(x, stream);
+    if (e != cudaSuccess) {
+        destroy_exec(x);
+        cudaGetLastError();
+        return fail(WS_ERR_CAPTURE, "upload: %s", cudaGetErrorName(e));
+    }
+    *out = x;
     return WS_OK;
+}
+
+// In-place update of executable graph x to graph g's parameters; false when
+// refused (the executable graph is then unchanged).
+bool exec_update(cudaGraphExec_t x, cudaGraph_t g) {
+    if (fault_point()) return false;
+    cudaGraphExecUpdateResultInfo info;
+    if (cudaGraphExecUpdate(x, g, &info) == cudaSuccess) return true;
+    cudaGetLastError();
+    return false;
 }
 
 ws_status build(ws_lane* L) {
     const ws_lane_desc& d = L->d;
+    ws_status st;
     if (d.stream) {
         L->stream = d.stream;
     } else {
+        if (fault_point()) return fail(WS_ERR_CUDA, "injected failure: cudaStreamCreateWithFlags");
         WS_TRY_CUDA(cudaStreamCreateWithFlags(&L->stream, cudaStreamNonBlocking));
         L->own_stream = true;
+        count_resource(kResStream, +1);
     }
-    ws_status st;
+    // the lane's error word: zero, read by the host after each submit
+    if ((st = alloc_host((void**)&L->err_host, 64, cudaHostAllocMapped, "error word")) != WS_OK) return st;
+    *(volatile uint32_t*)L->err_host = 0u;
+    WS_TRY_CUDA(cudaHostGetDevicePointer((void**)&L->err_dev, L->err_host, 0));
     L->input_bytes = (size_t)d.batch * (size_t)d.pre.src_frame_stride;
     const size_t elem = d.pre.dst_type == WS_DTYPE_F32 ? 4 : 2;
     L->tensor_bytes = (size_t)d.batch * 3 * d.pre.dst_h * d.pre.dst_w * elem;
@@ -300,7 +406,7 @@ ws_status build(ws_lane* L) {
     } else {
         if ((st = alloc_dev((void**)&L->logits, L->logits_bytes, "logits")) != WS_OK) return st;
         L->owned_logits = L->logits;
-        WS_TRY_CUDA(cudaMemsetAsync(L->logits, 0, L->logits_bytes, L->stream));
+        if ((st = memset_async(L->logits, L->logits_bytes, L->stream, "logits")) != WS_OK) return st;
     }
 
     // result slot
@@ -312,7 +418,7 @@ ws_status build(ws_lane* L) {
             } else {
                 if ((st = alloc_dev(&L->rv_dev, L->rv_bytes, "result")) != WS_OK) return st;
                 if ((st = alloc_dev(&L->ri_dev, L->ri_bytes, "result")) != WS_OK) {
-                    cudaFree(L->rv_dev);
+                    free_dev(L->rv_dev);
                     L->rv_dev = nullptr;
                     return st;
                 }
@@ -328,7 +434,7 @@ ws_status build(ws_lane* L) {
             } else {
                 if ((st = alloc_host(&L->rv_host, L->rv_bytes, flags, "result")) != WS_OK) return st;
                 if ((st = alloc_host(&L->ri_host, L->ri_bytes, flags, "result")) != WS_OK) {
-                    cudaFreeHost(L->rv_host);
+                    free_host(L->rv_host);
                     L->rv_host = nullptr;
                     return st;
                 }
@@ -340,7 +446,7 @@ ws_status build(ws_lane* L) {
             } else {
                 if ((st = alloc_dev(&L->rv_dev, L->rv_bytes, "result")) != WS_OK) return st;
                 if ((st = alloc_dev(&L->ri_dev, L->ri_bytes, "result")) != WS_OK) {
-                    cudaFree(L->rv_dev);
+                    free_dev(L->rv_dev);
                     L->rv_dev = nullptr;
                     return st;
                 }
@@ -366,21 +472,22 @@ ws_status build(ws_lane* L) {
         }
         if (L->ws_bytes[bi]) {   // cudaMalloc's alignment covers both workspaces' 256-byte rule
             if ((st = alloc_dev(&L->ws[bi], L->ws_bytes[bi], "post-processing workspace")) != WS_OK) return st;
-            WS_TRY_CUDA(cudaMemsetAsync(L->ws[bi], 0, L->ws_bytes[bi], L->stream));
+            if ((st = memset_async(L->ws[bi], L->ws_bytes[bi], L->stream, "post-processing workspace")) != WS_OK)
+                return st;
         }
     }
 
     if (submit_timing(L)) {
-        WS_TRY_CUDA(cudaEventCreate(&L->ev_start));
-        WS_TRY_CUDA(cudaEventCreate(&L->ev_end));
+        if ((st = make_event(&L->ev_start, cudaEventDefault)) != WS_OK) return st;
+        if ((st = make_event(&L->ev_end, cudaEventDefault)) != WS_OK) return st;
     } else {
         // completion only: a timing-disabled event is the lightest marker
-        WS_TRY_CUDA(cudaEventCreateWithFlags(&L->ev_end, cudaEventDisableTiming));
+        if ((st = make_event(&L->ev_end, cudaEventDisableTiming)) != WS_OK) return st;
     }
     if (stage_timing(L)) {
-        WS_TRY_CUDA(cudaEventCreate(&L->ev_pre0));
-        WS_TRY_CUDA(cudaEventCreate(&L->ev_pre1));
-        WS_TRY_CUDA(cudaEventCreate(&L->ev_post1));
+        if ((st = make_event(&L->ev_pre0, cudaEventDefault)) != WS_OK) return st;
+        if ((st = make_event(&L->ev_pre1, cudaEventDefault)) != WS_OK) return st;
+        if ((st = make_event(&L->ev_post1, cudaEventDefault)) != WS_OK) return st;
     }
 
     // Warm direct runs: settle lazy module loading and kernel attributes
@@ -392,7 +499,7 @@ ws_status build(ws_lane* L) {
     if (use_graph(L)) {
         for (int bi = 0; bi < L->nbuckets; ++bi) {
             if ((st = capture_bucket(L, bi, &L->graph[bi])) != WS_OK) return st;
-            if ((st = instantiate_bucket(L, bi)) != WS_OK) return st;
+            if ((st = instantiate_graph(L->graph[bi], &L->exec[bi], L->stream)) != WS_OK) return st;
         }
         WS_TRY_CUDA(cudaStreamSynchronize(L->stream));
     }
@@ -509,6 +616,7 @@ ws_status ws_lane_submit_n(ws_lane* L, int32_t n) {
     if (L->state != WS_LANE_ACQUIRED)
         return fail(WS_ERR_LANE_STATE, "submit needs an acquired lane (state %d)", L->state);
     if (n < 1 || n > L->d.batch) return fail(WS_ERR_INVALID_ARGUMENT, "%d frames for a lane of %d", n, L->d.batch);
+    if (L->broken) return fail(WS_ERR_CAPTURE, "the lane's graphs could not be restored after a failed rebind; destroy it");
     L->t_submit = std::chrono::steady_clock::now();
     if (L->fake) {
         L->fake_left = L->d.fake_polls;
@@ -548,13 +656,14 @@ ws_status ws_lane_rebind(ws_lane* L, void* input, float* logits, int32_t* reinst
     if (!L) return fail(WS_ERR_INVALID_ARGUMENT, "lane is NULL");
     NvtxRange r(L, "ws_lane_rebind");
     if (L->state == WS_LANE_IN_FLIGHT) return fail(WS_ERR_LANE_BUSY, "lane is in flight; wait first");
+    if (L->broken) return fail(WS_ERR_CAPTURE, "the lane's graphs could not be restored after a failed rebind; destroy it");
     if (!input && !logits) return WS_OK;
     if (L->fake) {
         if (input) L->d.input = input;
         if (logits) L->d.logits = logits;
         return WS_OK;
     }
-    // the new slot addresses; the old ones stay valid if anything fails
+    // the new slot addresses
     void* in_host = L->in_host;
     void* in_dev = L->in_dev;
     if (input) {
@@ -569,6 +678,9 @@ ws_status ws_lane_rebind(ws_lane* L, void* input, float* logits, int32_t* reinst
             default: in_host = input; break;   // COPY: the graph's copy source
         }
     }
+    void* const old_in_host = L->in_host;
+    void* const old_in_dev = L->in_dev;
+    float* const old_logits = L->logits;
     L->in_host = in_host;
     L->in_dev = in_dev;
     if (logits) L->logits = logits;
@@ -576,22 +688,49 @@ ws_status ws_lane_rebind(ws_lane* L, void* input, float* logits, int32_t* reinst
     // Re-capture each bucket with the new addresses and update its executable
     // graph in place ("Streams, concurrency and CUDA Graphs", CUDA Graphs:
     // cudaGraphExecUpdate instead of re-instantiation); re-instantiate only if
-    // the update is refused.
+    // the update is refused.  All or nothing: every bucket is captured before
+    // any executable graph changes, and on a later failure the graphs already
+    // updated are put back to their previous parameters.
+    cudaGraph_t ng[kMaxBuckets] = {};
+    cudaGraphExec_t nx[kMaxBuckets] = {};
+    bool updated[kMaxBuckets] = {};
+    auto undo = [&](ws_status st) {
+        for (int bi = 0; bi < L->nbuckets; ++bi) {
+            if (updated[bi]) {
+                cudaGraphExecUpdateResultInfo info;
+                if (cudaGraphExecUpdate(L->exec[bi], L->graph[bi], &info) != cudaSuccess) {
+                    cudaGetLastError();
+                    L->broken = true;
+                }
+            }
+            destroy_exec(nx[bi]);
+            destroy_graph(ng[bi]);
+        }
+        L->in_host = old_in_host;
+        L->in_dev = old_in_dev;
+        L->logits = old_logits;
+        return st;
+    };
     for (int bi = 0; bi < L->nbuckets; ++bi) {
-        cudaGraph_t g = nullptr;
-        ws_status st = capture_bucket(L, bi, &g);
-        if (st != WS_OK) return st;
-        cudaGraphExecUpdateResultInfo info;
-        cudaError_t e = cudaGraphExecUpdate(L->exec[bi], g, &info);
-        cudaGraphDestroy(L->graph[bi]);
-        L->graph[bi] = g;
-        if (e != cudaSuccess) {
-            cudaGetLastError();
-            cudaGraphExecDestroy(L->exec[bi]);
-            L->exec[bi] = nullptr;
-            if ((st = instantiate_bucket(L, bi)) != WS_OK) return st;
+        ws_status st = capture_bucket(L, bi, &ng[bi]);
+        if (st != WS_OK) return undo(st);
+    }
+    for (int bi = 0; bi < L->nbuckets; ++bi) {
+        if (exec_update(L->exec[bi], ng[bi])) {
+            updated[bi] = true;
+            continue;
+        }
+        ws_status st = instantiate_graph(ng[bi], &nx[bi], L->stream);
+        if (st != WS_OK) return undo(st);
+    }
+    for (int bi = 0; bi < L->nbuckets; ++bi) {
+        if (nx[bi]) {
+            destroy_exec(L->exec[bi]);
+            L->exec[bi] = nx[bi];
             if (reinstantiated) *reinstantiated = 1;
         }
+        destroy_graph(L->graph[bi]);
+        L->graph[bi] = ng[bi];
     }
     return WS_OK;
 }
@@ -632,6 +771,9 @@ ws_status ws_lane_wait(ws_lane* L, int64_t timeout_us, ws_lane_timing* timing) {
         }
     }
     const auto t1 = std::chrono::steady_clock::now();
+    // The work has completed, so whatever its kernels wrote into the mapped
+    // error word is visible here.
+    const uint32_t dev_err = L->fake ? 0u : *(volatile uint32_t*)L->err_host;
     if (timing) {
         timing->host_us = std::chrono::duration<double, std::micro>(t1 - L->t_submit).count();
         timing->gpu_us = timing->preprocess_us = timing->post_us = -1.f;
@@ -649,7 +791,23 @@ ws_status ws_lane_wait(ws_lane* L, int64_t timeout_us, ws_lane_timing* timing) {
         }
     }
     L->state = WS_LANE_FREE;
+    if (dev_err) {
+        *(volatile uint32_t*)L->err_host = 0u;   // the next submit starts clean
+        return fail(WS_ERR_DEVICE,
+                    "a kernel of this lane gave up a bounded wait (error bits 0x%x%s); this submit's results are "
+                    "undefined",
+                    dev_err, (dev_err & kDevErrBulkCopyTimeout) ? ": a bulk copy did not complete in time" : "");
+    }
     return WS_OK;
+}
+
+ws_status ws_lane_selftest_wait_timeout(ws_lane* L, uint32_t limit_us) {
+    using namespace ws;
+    clear_error();
+    if (!L) return fail(WS_ERR_INVALID_ARGUMENT, "lane is NULL");
+    if (L->fake) return fail(WS_ERR_UNSUPPORTED, "a host-only lane has no GPU error word");
+    if (L->state == WS_LANE_IN_FLIGHT) return fail(WS_ERR_LANE_BUSY, "lane is in flight; wait first");
+    return launch_selftest_wait(L->err_dev, limit_us, L->stream);
 }
 
 ws_status ws_lane_release(ws_lane* L) {

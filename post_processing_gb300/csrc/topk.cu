@@ -221,6 +221,146 @@ __device__ __forceinline__ void rank_and_emit(const unsigned long long* keys, ui
     }
 }
 
+// Takes the row's ticket once this block's list is written: true for the
+// row's last block, which then merges.  One thread makes the block's writes
+// visible at GPU scope (the block barrier orders the other threads' writes
+// before its release fence) and counts the block in.
+__device__ __forceinline__ bool take_ticket(const TopkParams& p, long long row, Shared& s) {
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        __threadfence();
+        const unsigned prev = atomicAdd(&p.tickets[row], 1u);
+        s.last = (prev == (unsigned)p.nchunks - 1u);
+    }
+    __syncthreads();
+    if (!s.last) return false;
+    __threadfence();
+    return true;
+}
+
+// The row's last block: merges the chunks' sorted lists into the row's Top-K
+// and resets the row's ticket for the next call or graph replay.
+__device__ __forceinline__ void merge_chunk_lists(const TopkParams& p, long long row, const float* xr, Shared& s) {
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int k = p.k;
+    uint32_t cnt;
+    const unsigned long long* all = p.keys + row * p.nchunks * k;
+    const int total = p.nchunks * k;
+    if (p.nchunks <= kBitonicChunks || p.nchunks > kMergeChunks) {
+        // Warp w folds the lists of chunks w, w + 8, ... (lane i holding the
+        // i-th key of each; 0 past a list's K keys, and every real key is
+        // larger than 0) with bitonic merges in registers, a batch of
+        // kLists lists at a time with the next batch's loads in flight; warp
+        // 0 then folds the eight warps' lists.  The result is the row's
+        // Top-K in rank order: no threshold, no ranking, one block barrier.
+        constexpr int kLists = kBitonicChunks / kWarps;   // per warp and batch
+        auto load_batch = [&](int c0, unsigned long long (&kb)[kLists]) {
+#pragma unroll
+            for (int r = 0; r < kLists; ++r) {
+                const int c = c0 + r * kWarps;
+                kb[r] = (c < p.nchunks && lane < k) ? __ldcg(all + (long long)c * k + lane) : 0ull;
+            }
+        };
+        unsigned long long cur[kLists], nxt[kLists];
+        load_batch(warp, cur);
+        unsigned long long acc = 0ull;
+        for (int c0 = warp; c0 < p.nchunks; c0 += kWarps * kLists) {
+            const int cn = c0 + kWarps * kLists;
+            if (cn < p.nchunks) load_batch(cn, nxt);
+#pragma unroll
+            for (int step = 1; step < kLists; step *= 2)
+#pragma unroll
+                for (int r = 0; r + step < kLists; r += 2 * step)
+                    if (c0 + (r + step) * kWarps < p.nchunks) cur[r] = merge_top32(cur[r], cur[r + step]);
+            acc = c0 == warp ? cur[0] : merge_top32(acc, cur[0]);
+#pragma unroll
+            for (int r = 0; r < kLists; ++r) cur[r] = nxt[r];
+        }
+        s.wlist[warp][lane] = acc;
+        __syncthreads();
+        if (warp != 0) return;
+        unsigned long long w8[kWarps];
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w) w8[w] = s.wlist[w][lane];
+#pragma unroll
+        for (int step = 1; step < kWarps; step *= 2)
+#pragma unroll
+            for (int r = 0; r + step < kWarps; r += 2 * step)
+                if (r + step < p.nchunks) w8[r] = merge_top32(w8[r], w8[r + step]);
+        if (lane < k) {
+            p.out_val[row * k + lane] = key_value(w8[0], xr);
+            p.out_idx[row * k + lane] = (int)key_index(w8[0]);
+        }
+        if (lane == 0) p.tickets[row] = 0u;   // ready for the next call / replay
+        return;
+    }
+    // Threshold from the sorted chunk lists: the first m = ceil(K / chunks)
+    // keys of every chunk hold at least K keys, so the K-th largest of that
+    // union has at least K keys at or above it, and every key of the row's
+    // Top-K is at or above it.  It is found by counting, like the ranks.
+    const int m = (k + p.nchunks - 1) / p.nchunks;
+    const int U = m * p.nchunks;
+    {   // 48 < chunks <= 96: U <= 96
+        // One round trip: warp w holds the lists of chunks w, w + 8, ... in
+        // registers, lane i the i-th key of each.  As the lists are sorted,
+        // the keys at or above the threshold are a prefix of each list.
+        unsigned long long key[kMergeRegs];
+#pragma unroll
+        for (int r = 0; r < kMergeRegs; ++r)
+            key[r] = __ldcg(all + (long long)min(warp + r * kWarps, p.nchunks - 1) * k + min(lane, k - 1));
+#pragma unroll
+        for (int r = 0; r < kMergeRegs; ++r) {
+            const int c = warp + r * kWarps;
+            if (c >= p.nchunks || lane >= k) key[r] = 0ull;
+            else if (lane < m) s.cand[c * m + lane] = key[r];
+        }
+        __syncthreads();
+        // The U first keys are real keys, hence unique: exactly one of them
+        // has rank K - 1, and it is the K-th largest.
+        rank_and_emit(s.cand, (uint32_t)U, k, [&](int rank, unsigned long long kv) {
+            if (rank == k - 1) s.red[0] = kv;
+        });
+        __syncthreads();
+        unsigned long long t64 = s.red[0];
+        if (t64 == 0) t64 = 1;   // padding keys (0) never pass
+        int warp_total = 0;
+#pragma unroll
+        for (int r = 0; r < kMergeRegs; ++r) warp_total += __popc(__ballot_sync(kFull, key[r] >= t64));
+        int all_total;
+        int off = block_offsets(lane == 0 ? warp_total : 0, all_total, s);
+        off = __shfl_sync(kFull, off, 0);   // the warp's first slot
+        if (all_total <= kCap) {
+            const unsigned below = (1u << lane) - 1u;
+#pragma unroll
+            for (int r = 0; r < kMergeRegs; ++r) {
+                const unsigned mask = __ballot_sync(kFull, key[r] >= t64);
+                if ((mask >> lane) & 1u) s.cand[off + __popc(mask & below)] = key[r];
+                off += __popc(mask);
+            }
+        }
+        if (tid == 0) s.cnt = (uint32_t)all_total;
+    }
+    __syncthreads();
+    cnt = s.cnt;
+    if (cnt > kCap) {
+        auto key_at = [&](int i) { return __ldcg(all + i); };
+        const unsigned long long kth = block_kth_largest(key_at, total, k, s);
+        if (tid == 0) s.cnt = 0;
+        __syncthreads();
+        for (int i = tid; i < total; i += kThreads) {
+            const unsigned long long key = __ldcg(all + i);
+            if (key >= kth) s.cand[atomicAdd(&s.cnt, 1u)] = key;
+        }
+        __syncthreads();
+        cnt = s.cnt;
+    }
+    rank_and_emit(s.cand, cnt, k, [&](int rank, unsigned long long key) {
+        p.out_val[row * k + rank] = key_value(key, xr);
+        p.out_idx[row * k + rank] = (int)key_index(key);
+    });
+    if (tid == 0) p.tickets[row] = 0u;   // ready for the next call / replay
+}
+
 template <bool kVec>
 __global__ void __launch_bounds__(kThreads, 4) topk_kernel(const __grid_constant__ TopkParams p) {
     extern __shared__ __align__(128) unsigned char dsmem[];
@@ -256,6 +396,16 @@ __global__ void __launch_bounds__(kThreads, 4) topk_kernel(const __grid_constant
                 atomicOr(p.err, kDevErrBulkCopyTimeout);
                 mbar_wait_bounded(&bar, 0, kWaitLimitNs);   // let the copy land before leaving
             }
+            if (p.nchunks == 1) return;
+            // A row split over several blocks: this chunk contributes an
+            // empty list (padding keys) but still takes the row's ticket, so
+            // that the row's last block merges and resets the ticket, and the
+            // workspace is ready for the next call.  The error bit says the
+            // row's result is not to be used.
+            unsigned long long* kr = p.keys + (row * p.nchunks + chunk) * k;
+            for (int r = tid; r < k; r += kThreads) kr[r] = 0ull;
+            if (!take_ticket(p, row, s)) return;
+            merge_chunk_lists(p, row, xr, s);
             return;
         }
         // The phase is complete: each thread's own (immediately satisfied)
@@ -393,131 +543,8 @@ __global__ void __launch_bounds__(kThreads, 4) topk_kernel(const __grid_constant
     for (int r = kk + tid; r < k; r += kThreads) kr[r] = 0ull;   // chunk shorter than K
 
     // Last block of the row merges.
-    __threadfence();
-    __syncthreads();
-    if (tid == 0) {
-        const unsigned prev = atomicAdd(&p.tickets[row], 1u);
-        s.last = (prev == (unsigned)p.nchunks - 1u);
-    }
-    __syncthreads();
-    if (!s.last) return;
-    __threadfence();
-
-    const unsigned long long* all = p.keys + row * p.nchunks * k;
-    const int total = p.nchunks * k;
-    if (p.nchunks <= kBitonicChunks || p.nchunks > kMergeChunks) {
-        // Warp w folds the lists of chunks w, w + 8, ... (lane i holding the
-        // i-th key of each; 0 past a list's K keys, and every real key is
-        // larger than 0) with bitonic merges in registers, a batch of
-        // kLists lists at a time with the next batch's loads in flight; warp
-        // 0 then folds the eight warps' lists.  The result is the row's
-        // Top-K in rank order: no threshold, no ranking, one block barrier.
-        constexpr int kLists = kBitonicChunks / kWarps;   // per warp and batch
-        auto load_batch = [&](int c0, unsigned long long (&kb)[kLists]) {
-#pragma unroll
-            for (int r = 0; r < kLists; ++r) {
-                const int c = c0 + r * kWarps;
-                kb[r] = (c < p.nchunks && lane < k) ? __ldcg(all + (long long)c * k + lane) : 0ull;
-            }
-        };
-        unsigned long long cur[kLists], nxt[kLists];
-        load_batch(warp, cur);
-        unsigned long long acc = 0ull;
-        for (int c0 = warp; c0 < p.nchunks; c0 += kWarps * kLists) {
-            const int cn = c0 + kWarps * kLists;
-            if (cn < p.nchunks) load_batch(cn, nxt);
-#pragma unroll
-            for (int step = 1; step < kLists; step *= 2)
-#pragma unroll
-                for (int r = 0; r + step < kLists; r += 2 * step)
-                    if (c0 + (r + step) * kWarps < p.nchunks) cur[r] = merge_top32(cur[r], cur[r + step]);
-            acc = c0 == warp ? cur[0] : merge_top32(acc, cur[0]);
-#pragma unroll
-            for (int r = 0; r < kLists; ++r) cur[r] = nxt[r];
-        }
-        s.wlist[warp][lane] = acc;
-        __syncthreads();
-        if (warp != 0) return;
-        unsigned long long w8[kWarps];
-#pragma unroll
-        for (int w = 0; w < kWarps; ++w) w8[w] = s.wlist[w][lane];
-#pragma unroll
-        for (int step = 1; step < kWarps; step *= 2)
-#pragma unroll
-            for (int r = 0; r + step < kWarps; r += 2 * step)
-                if (r + step < p.nchunks) w8[r] = merge_top32(w8[r], w8[r + step]);
-        if (lane < k) {
-            p.out_val[row * k + lane] = key_value(w8[0], xr);
-            p.out_idx[row * k + lane] = (int)key_index(w8[0]);
-        }
-        if (lane == 0) p.tickets[row] = 0u;   // ready for the next call / replay
-        return;
-    }
-    // Threshold from the sorted chunk lists: the first m = ceil(K / chunks)
-    // keys of every chunk hold at least K keys, so the K-th largest of that
-    // union has at least K keys at or above it, and every key of the row's
-    // Top-K is at or above it.  It is found by counting, like the ranks.
-    const int m = (k + p.nchunks - 1) / p.nchunks;
-    const int U = m * p.nchunks;
-    {   // 48 < chunks <= 96: U <= 96
-        // One round trip: warp w holds the lists of chunks w, w + 8, ... in
-        // registers, lane i the i-th key of each.  As the lists are sorted,
-        // the keys at or above the threshold are a prefix of each list.
-        unsigned long long key[kMergeRegs];
-#pragma unroll
-        for (int r = 0; r < kMergeRegs; ++r)
-            key[r] = __ldcg(all + (long long)min(warp + r * kWarps, p.nchunks - 1) * k + min(lane, k - 1));
-#pragma unroll
-        for (int r = 0; r < kMergeRegs; ++r) {
-            const int c = warp + r * kWarps;
-            if (c >= p.nchunks || lane >= k) key[r] = 0ull;
-            else if (lane < m) s.cand[c * m + lane] = key[r];
-        }
-        __syncthreads();
-        // The U first keys are real keys, hence unique: exactly one of them
-        // has rank K - 1, and it is the K-th largest.
-        rank_and_emit(s.cand, (uint32_t)U, k, [&](int rank, unsigned long long kv) {
-            if (rank == k - 1) s.red[0] = kv;
-        });
-        __syncthreads();
-        unsigned long long t64 = s.red[0];
-        if (t64 == 0) t64 = 1;   // padding keys (0) never pass
-        int warp_total = 0;
-#pragma unroll
-        for (int r = 0; r < kMergeRegs; ++r) warp_total += __popc(__ballot_sync(kFull, key[r] >= t64));
-        int all_total;
-        int off = block_offsets(lane == 0 ? warp_total : 0, all_total, s);
-        off = __shfl_sync(kFull, off, 0);   // the warp's first slot
-        if (all_total <= kCap) {
-            const unsigned below = (1u << lane) - 1u;
-#pragma unroll
-            for (int r = 0; r < kMergeRegs; ++r) {
-                const unsigned mask = __ballot_sync(kFull, key[r] >= t64);
-                if ((mask >> lane) & 1u) s.cand[off + __popc(mask & below)] = key[r];
-                off += __popc(mask);
-            }
-        }
-        if (tid == 0) s.cnt = (uint32_t)all_total;
-    }
-    __syncthreads();
-    cnt = s.cnt;
-    if (cnt > kCap) {
-        auto key_at = [&](int i) { return __ldcg(all + i); };
-        const unsigned long long kth = block_kth_largest(key_at, total, k, s);
-        if (tid == 0) s.cnt = 0;
-        __syncthreads();
-        for (int i = tid; i < total; i += kThreads) {
-            const unsigned long long key = __ldcg(all + i);
-            if (key >= kth) s.cand[atomicAdd(&s.cnt, 1u)] = key;
-        }
-        __syncthreads();
-        cnt = s.cnt;
-    }
-    rank_and_emit(s.cand, cnt, k, [&](int rank, unsigned long long key) {
-        p.out_val[row * k + rank] = key_value(key, xr);
-        p.out_idx[row * k + rank] = (int)key_index(key);
-    });
-    if (tid == 0) p.tickets[row] = 0u;   // ready for the next call / replay
+    if (!take_ticket(p, row, s)) return;
+    merge_chunk_lists(p, row, xr, s);
 }
 
 // ---------------------------------------------------------------------------
@@ -952,6 +979,9 @@ extern "C" ws_status ws_topk_noalloc(const float* x, int64_t rows, int64_t cols,
     ws::clear_error();
     ws_status st = ws::validate_topk(rows, cols, k);
     if (st != WS_OK) return st;
+    // Refuse bad pointers before anything is enqueued (the ticket clearing
+    // below is stream work).
+    if (!x || !out_val || !out_idx) return ws::fail(WS_ERR_INVALID_ARGUMENT, "x, out_val or out_idx is NULL");
     const size_t need = ws::topk_workspace_size(rows, cols, k);
     if (need > kNoAllocScratchBytes)
         return ws::fail(WS_ERR_UNSUPPORTED,

@@ -1,5 +1,6 @@
 // ws_core.cu -- status strings, per-thread error text, version, the device
 // property cache and the device error word.
+#include <atomic>
 #include <cstring>
 #include <mutex>
 #include <string>
@@ -73,12 +74,39 @@ NoPdlScope::NoPdlScope(bool active) : prev(t_no_pdl) {
 
 NoPdlScope::~NoPdlScope() { t_no_pdl = prev; }
 
+namespace {
+thread_local uint32_t* t_err_word = nullptr;
+}
+
+ErrWordScope::ErrWordScope(uint32_t* word) : prev(t_err_word) {
+    if (word) t_err_word = word;
+}
+
+ErrWordScope::~ErrWordScope() { t_err_word = prev; }
+
 uint32_t* device_error_word() {
+    if (t_err_word) return t_err_word;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
     std::lock_guard<std::mutex> lock(g_mu);
     return g_err_word[dev];
 }
+
+// ---- host-side fault injection and resource counters -----------------------
+namespace {
+std::atomic<long long> g_fault_reached{0};   // fault points reached since the last arming
+std::atomic<long long> g_fault_first{0};     // first failing point (1-based), 0 = off
+std::atomic<long long> g_fault_count{0};     // consecutive points that fail
+std::atomic<long long> g_live[kResCount];
+}  // namespace
+
+bool fault_point() {
+    const long long first = g_fault_first.load(std::memory_order_relaxed);
+    const long long n = g_fault_reached.fetch_add(1, std::memory_order_relaxed) + 1;
+    return first > 0 && n >= first && n < first + g_fault_count.load(std::memory_order_relaxed);
+}
+
+void count_resource(Resource r, int delta) { g_live[r].fetch_add(delta, std::memory_order_relaxed); }
 
 }  // namespace ws
 
@@ -116,6 +144,14 @@ __global__ void selftest_wait_kernel(uint32_t* err, unsigned long long limit_ns)
     if (!mbar_wait_bounded(&bar, 0, limit_ns)) atomicOr(err, kDevErrBulkCopyTimeout);
 }
 
+ws_status launch_selftest_wait(uint32_t* word, uint32_t limit_us, cudaStream_t stream) {
+    if (limit_us < 1 || limit_us > 1000000) return fail(WS_ERR_INVALID_ARGUMENT, "limit %u us outside 1..1e6", limit_us);
+    if (!word) return fail(WS_ERR_INVALID_ARGUMENT, "no error word");
+    selftest_wait_kernel<<<1, 32, 0, stream>>>(word, 1000ull * limit_us);
+    WS_TRY_CUDA(cudaGetLastError());
+    return WS_OK;
+}
+
 }  // namespace ws
 
 extern "C" {
@@ -126,13 +162,33 @@ int32_t ws_version(void) { return 100; }  // 0.1.0
 
 ws_status ws_selftest_wait_timeout(uint32_t limit_us, cudaStream_t stream) {
     ws::clear_error();
-    if (limit_us < 1 || limit_us > 1000000) return ws::fail(WS_ERR_INVALID_ARGUMENT, "limit %u us outside 1..1e6", limit_us);
     int dev;
     const ws::DeviceInfo* info;
     ws_status st = ws::current_device_info(&dev, &info);
     if (st != WS_OK) return st;
-    ws::selftest_wait_kernel<<<1, 32, 0, stream>>>(ws::device_error_word(), 1000ull * limit_us);
-    WS_TRY_CUDA(cudaGetLastError());
+    return ws::launch_selftest_wait(ws::device_error_word(), limit_us, stream);
+}
+
+ws_status ws_debug_inject_failure(int32_t nth, int32_t count) {
+    ws::clear_error();
+    if (count < 0) return ws::fail(WS_ERR_INVALID_ARGUMENT, "count %d < 0", count);
+    ws::g_fault_first.store(0, std::memory_order_relaxed);
+    ws::g_fault_count.store(count, std::memory_order_relaxed);
+    ws::g_fault_reached.store(0, std::memory_order_relaxed);
+    ws::g_fault_first.store(nth > 0 && count > 0 ? nth : 0, std::memory_order_relaxed);
+    return WS_OK;
+}
+
+ws_status ws_debug_get_counters(ws_debug_counters* c) {
+    ws::clear_error();
+    if (!c) return ws::fail(WS_ERR_INVALID_ARGUMENT, "counters is NULL");
+    c->device_allocs = ws::g_live[ws::kResDevice].load();
+    c->host_allocs = ws::g_live[ws::kResHost].load();
+    c->graphs = ws::g_live[ws::kResGraph].load();
+    c->graph_execs = ws::g_live[ws::kResExec].load();
+    c->events = ws::g_live[ws::kResEvent].load();
+    c->streams = ws::g_live[ws::kResStream].load();
+    c->fault_points = ws::g_fault_reached.load();
     return WS_OK;
 }
 

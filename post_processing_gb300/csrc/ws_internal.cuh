@@ -42,9 +42,30 @@ size_t topk_workspace_size(int64_t rows, int64_t cols, int32_t k);
 enum : uint32_t {
     kDevErrBulkCopyTimeout = 1u,
 };
-// Device address of the current device's error word; kernels receive it as a
+// Device address of the error word the calling thread's kernels report
+// into: a lane's own word while that lane enqueues or captures its path (see
+// ErrWordScope), else the current device's word.  Kernels receive it as a
 // parameter (no relocatable device code, so they cannot name it directly).
 uint32_t* device_error_word();
+// While alive, kernels enqueued by this thread report into `word` (NULL keeps
+// the current choice).
+struct ErrWordScope {
+    uint32_t* prev;
+    explicit ErrWordScope(uint32_t* word);
+    ~ErrWordScope();
+};
+// Enqueues the bounded-wait self-test kernel (see ws_selftest_wait_timeout)
+// reporting into `word`.
+ws_status launch_selftest_wait(uint32_t* word, uint32_t limit_us, cudaStream_t stream);
+
+// Host-side fault injection for the lanes' and the pool's cleanup paths (see
+// ws_debug_inject_failure): true when the fault point reached now is to fail.
+// Every internal call that can fail during lane creation or re-binding passes
+// through one before the CUDA call it guards.
+bool fault_point();
+// Live CUDA resources the library made (see ws_debug_get_counters).
+enum Resource { kResDevice = 0, kResHost, kResGraph, kResExec, kResEvent, kResStream, kResCount };
+void count_resource(Resource r, int delta);
 
 // Programmatic dependent launch of the stream-ordered kernels (preprocess,
 // Top-K, class scan, DFL, NMS): on unless the calling thread is inside a

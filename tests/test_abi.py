@@ -39,7 +39,7 @@ def test_struct_layout_matches_c(B, tmp_path):
     structs = {"ws_preprocess_desc": B.ws_preprocess_desc, "ws_lane_desc": B.ws_lane_desc,
                "ws_lane_buffers": B.ws_lane_buffers, "ws_lane_timing": B.ws_lane_timing,
                "ws_detect_desc": B.ws_detect_desc, "ws_candidate": B.ws_candidate,
-               "ws_detection": B.ws_detection}
+               "ws_detection": B.ws_detection, "ws_debug_counters": B.ws_debug_counters}
     lines = ['#include <stdio.h>', '#include <stddef.h>', '#include "ws.h"', "int main(void) {"]
     for name, cls in structs.items():
         lines.append(f'printf("{name} size %zu\\n", sizeof({name}));')
@@ -204,3 +204,22 @@ def test_detect_validation(B):
     assert B.ws_detect_validate(d, 0)[0] == B.WS_ERR_INVALID_ARGUMENT
     # a workspace that is too small is refused before any launch
     assert B.ws_detect(d, 16, 4, 16, 16, 256, n - 32, 0) == B.WS_ERR_INVALID_ARGUMENT
+
+
+def test_fault_injection_hook_host_only(B):
+    """The fault-injection hook arms and disarms without a GPU; host-only
+    lanes make no CUDA call, so they reach no fault point and hold nothing."""
+    assert B.ws_debug_inject_failure(1, -1) == B.WS_ERR_INVALID_ARGUMENT
+    B.check(B.ws_debug_inject_failure(1, 1))
+    st, before = B.ws_debug_get_counters()
+    assert st == B.WS_OK and before.fault_points == 0
+    d = B.lane_desc(B.preprocess_desc(64, 48, 32, 32), 1, 1, 100, 5, flags=B.WS_LANE_FLAG_NO_DEVICE)
+    st, h = B.ws_lane_create(d)
+    assert st == B.WS_OK
+    st, after = B.ws_debug_get_counters()
+    assert after.fault_points == 0
+    for f in ("device_allocs", "host_allocs", "graphs", "graph_execs", "events", "streams"):
+        assert getattr(after, f) == getattr(before, f), f
+    assert B.ws_lane_selftest_wait_timeout(h, 1000) == B.WS_ERR_UNSUPPORTED
+    assert B.ws_lane_destroy(h) == B.WS_OK
+    B.check(B.ws_debug_inject_failure(0, 0))

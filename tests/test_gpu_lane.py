@@ -8,7 +8,7 @@ import pytest
 import torch
 
 import synth
-from cudart import memcpy
+from cudart import _cudart, memcpy
 
 pytestmark = pytest.mark.gpu
 
@@ -62,8 +62,6 @@ MODES = [(0, 0, 0), (0, 0, 1), (1, 1, 0), (2, 2, 0), (2, 1, 2), (1, 2, 1), (0, 2
 def test_lane_parity(B, oracle, name, mode):
     from post_processing_gb300 import Lane
     w = synth.WORKLOADS[name]
-    if name == "b8_4k_to_512" and mode[0] == 1:
-        pytest.skip("mapped 4K input is covered by the smaller workloads")
     frames = synth.make_frames(name)
     logits = synth.make_logits(name)
     pre = B.preprocess_desc(w["src_w"], w["src_h"], w["dst_w"], w["dst_h"],
@@ -199,3 +197,116 @@ def test_bf16_bgr_lane(B, oracle):
         got = torch.from_numpy(raw.view(np.int16)).view(torch.bfloat16).float().reshape(4, 3, 96, 128)
         want = torch.from_numpy(oracle.preprocess(rgb, 320, 240, 128, 96)).to(torch.bfloat16).float()
         assert float((got - want).abs().max()) <= 2.0 ** -6 * 4    # at most one bf16 ulp at |x| < 4
+
+
+def staged_kernel_taken(B, w, batch):
+    """ws_preprocess takes the staged bulk-copy kernel above 460,000 output
+    pixels (destinations up to 8192 wide)."""
+    return batch * w["dst_w"] * w["dst_h"] > 460_000 and w["dst_w"] <= 8192
+
+
+@pytest.mark.parametrize("name,batch", [("b64_1080p_to_224", 10), ("b64_1080p_to_224", 64), ("b8_4k_to_512", 2),
+                                        ("b8_4k_to_512", 8)])
+def test_mapped_input_staged_kernel(B, oracle, name, batch):
+    """Mapped pinned input read in place by the staged kernel: its bulk copies
+    pull the needed source rows straight from host memory across the host
+    link (the end-to-end path: "Inside WarpStream TRT", mapped pinned memory).
+    The tensor is within 1e-5 of the oracle and the Top-K bit-exact, for two
+    replays."""
+    from post_processing_gb300 import Lane
+    w = synth.WORKLOADS[name]
+    assert staged_kernel_taken(B, w, batch)
+    frames = synth.make_frames(name, batch=batch)
+    rows = w["rows"] * batch // w["batch"] if w["rows"] >= w["batch"] else w["rows"]
+    logits = synth.make_logits(name, rows=rows)
+    pre = B.preprocess_desc(w["src_w"], w["src_h"], w["dst_w"], w["dst_h"], norm=w["norm"])
+    d = B.lane_desc(pre, batch, rows, w["cols"], w["k"], input_mode=B.WS_INPUT_MAPPED,
+                    result_mode=B.WS_RESULT_MAPPED)
+    with Lane(d) as lane:
+        fill_lane(B, lane, frames, logits)
+        want = oracle.preprocess(frames, w["src_w"], w["src_h"], w["dst_w"], w["dst_h"], norm=w["norm"])
+        wv, wi = oracle.topk(logits, w["k"])
+        for _ in range(2):
+            lane.acquire()
+            lane.submit()
+            lane.wait()
+            tensor, v, i = read_lane(B, lane, batch, w["dst_h"], w["dst_w"], rows, w["k"])
+            assert np.max(np.abs(tensor - want)) <= 1e-5
+            assert np.array_equal(i, wi) and np.array_equal(v.view(np.uint32), wv.view(np.uint32))
+
+
+def test_mapped_input_unaligned_borrowed(B, oracle):
+    """A borrowed mapped slot whose base, row stride and frame stride are not
+    multiples of 16 (a producer's own pinned buffer need not be aligned): the
+    staged kernel copies each row's 16-byte window from host memory."""
+    from post_processing_gb300 import Lane
+    batch, sw, sh, dw, dh = 10, 1920, 1080, 224, 224
+    stride, fstride, base_off = 3 * sw + 1, (3 * sw + 1) * sh + 3, 5
+    frames = synth.frames_uniform(0x5EED, batch, sh, sw)
+    logits = synth.logits_normal(0x5EEE, batch, 1000)
+    lib = _cudart()
+    lib.cudaHostAlloc.argtypes = [ctypes.POINTER(ctypes.c_void_p), ctypes.c_size_t, ctypes.c_uint]
+    lib.cudaFreeHost.argtypes = [ctypes.c_void_p]
+    nbytes = base_off + batch * fstride
+    ptr = ctypes.c_void_p()
+    assert lib.cudaHostAlloc(ctypes.byref(ptr), nbytes, 2) == 0      # cudaHostAllocMapped
+    try:
+        host = np.frombuffer((ctypes.c_char * nbytes).from_address(ptr.value), dtype=np.uint8)
+        host[:] = 0x5A
+        fr = frames.reshape(batch, sh, 3 * sw)
+        for b in range(batch):
+            rows = host[base_off + b * fstride: base_off + b * fstride + sh * stride].reshape(sh, stride)
+            rows[:, :3 * sw] = fr[b]
+        pre = B.preprocess_desc(sw, sh, dw, dh, row_stride=stride, frame_stride=fstride)
+        d = B.lane_desc(pre, batch, batch, 1000, 32, input_mode=B.WS_INPUT_MAPPED, input=ptr.value + base_off)
+        with Lane(d) as lane:
+            lg = np.ascontiguousarray(logits)
+            memcpy(lane.buffers.logits, lg.ctypes.data, lg.nbytes)
+            lane.acquire()
+            lane.submit()
+            lane.wait()
+            tensor, v, i = read_lane(B, lane, batch, dh, dw, batch, 32)
+            assert np.max(np.abs(tensor - oracle.preprocess(frames, sw, sh, dw, dh))) <= 1e-5
+            wv, wi = oracle.topk(logits, 32)
+            assert np.array_equal(i, wi) and np.array_equal(v.view(np.uint32), wv.view(np.uint32))
+    finally:
+        lib.cudaFreeHost(ptr)
+
+
+@pytest.mark.parametrize("name", ["b64_1080p_to_224", "b8_4k_to_512"])
+def test_bench_throughput_lanes_on_own_streams(B, oracle, name):
+    """The benchmark's headline configuration: four lanes without timing
+    events, each on its own stream, replayed in rotation so that one lane's
+    preprocess overlaps the previous lane's Top-K.  Each lane holds different
+    frames and logits; after three rotations every lane's tensor and Top-K
+    equal the oracle's for its own inputs."""
+    from post_processing_gb300 import Lane
+    w = synth.WORKLOADS[name]
+    pre = B.preprocess_desc(w["src_w"], w["src_h"], w["dst_w"], w["dst_h"], norm=w["norm"])
+    lanes, wants = [], []
+    try:
+        for j in range(4):
+            frames = synth.frames_uniform(0x4A00 + j, w["batch"], w["src_h"], w["src_w"])
+            logits = synth.logits_with_ties(0x4B00 + j, w["rows"], w["cols"])
+            ln = Lane(B.lane_desc(pre, w["batch"], w["rows"], w["cols"], w["k"], flags=B.WS_LANE_FLAG_NO_TIMING))
+            lanes.append(ln)
+            fill_lane(B, ln, frames, logits)
+            wants.append((oracle.preprocess(frames, w["src_w"], w["src_h"], w["dst_w"], w["dst_h"], norm=w["norm"]),
+                          oracle.topk(logits, w["k"])))
+        streams = {ln.buffers.stream for ln in lanes}
+        assert len(streams) == 4
+        for step in range(12):
+            ln = lanes[step % 4]
+            if ln.state == B.WS_LANE_IN_FLIGHT:
+                ln.wait()
+            ln.acquire()
+            ln.submit()
+        for ln, (want_t, (want_v, want_i)) in zip(lanes, wants):
+            if ln.state == B.WS_LANE_IN_FLIGHT:
+                ln.wait()
+            tensor, v, i = read_lane(B, ln, w["batch"], w["dst_h"], w["dst_w"], w["rows"], w["k"])
+            assert np.max(np.abs(tensor - want_t)) <= 1e-5
+            assert np.array_equal(i, want_i) and np.array_equal(v.view(np.uint32), want_v.view(np.uint32))
+    finally:
+        for ln in lanes:
+            ln.close()
