@@ -644,13 +644,21 @@ def run_steps(B, ls, n):
     return inflight
 
 
+HOLD_CYCLES = 400_000   # about 0.2 ms of SM clock cycles
+
+
 def timed_steps(B, torch, stream, ls, n):
     """Device time (s) of n steps: a start event on `stream`, which every lane
     stream waits on, and an end event after `stream` has waited on every lane
-    stream's last work."""
+    stream's last work.  A short spin kernel on `stream` ahead of the start
+    event holds the GPU while the host makes its first submissions, so that
+    the interval is the GPU running the n steps rather than the host's
+    latency to its first launch (every step's work is inside the interval)."""
     lane_streams = [torch.cuda.ExternalStream(lane.buffers.stream) for lane in ls]
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        torch.cuda._sleep(HOLD_CYCLES)
     ev0.record(stream)
     for ls_ in lane_streams:
         ls_.wait_event(ev0)

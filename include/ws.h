@@ -215,9 +215,12 @@ ws_status ws_topk_workspace_init(void* workspace, size_t bytes, cudaStream_t str
  * values (+0 equals -0) go to the lower index; NaN ranks as -inf.  out_val
  * holds the input's own bits (-0.0 stays -0.0) except that NaN is written as
  * -inf.  The result is unique, so it is bit-exact.
- * workspace: device, at least ws_topk_workspace_bytes(), zeroed once by
- * ws_topk_workspace_init() (or cudaMemset) before first use; calls that share
- * a workspace must not overlap on the GPU.  May be NULL when the size is 0.
+ * workspace: device, 256-byte aligned, at least ws_topk_workspace_bytes()
+ * bytes, zeroed once by ws_topk_workspace_init() (or cudaMemset) before first
+ * use; it holds a ticket per row and each chunk's K keys of rows longer than
+ * 8192 entries, and every completed call leaves the tickets at zero again.
+ * Calls that share a workspace must not overlap on the GPU.  May be NULL when
+ * the size is 0.
  * One kernel launch on `stream`.
  * Errors: WS_ERR_INVALID_ARGUMENT (shape, K, NULL pointer, workspace too
  * small), WS_ERR_CUDA (launch failed). */

@@ -13,6 +13,7 @@
 #include <deque>
 #include <mutex>
 #include <new>
+#include <string>
 #include <vector>
 
 #include "ws_internal.cuh"
@@ -77,9 +78,12 @@ ws_status ws_pool_create(const ws_lane_desc* desc, int32_t nlanes, ws_pool** out
         ws_lane* L = nullptr;
         ws_status st = ws_lane_create(desc, &L);
         if (st != WS_OK) {
+            // destroying the lanes already made clears the thread's message:
+            // keep the failing lane's
+            const std::string msg = ws_last_error();
             destroy_lanes(P);
             delete P;
-            return st;   // the lane's own message stays in ws_last_error
+            return fail(st, "lane %d of %d: %s", i, nlanes, msg.c_str());
         }
         P->lanes.push_back(L);
         P->where.push_back(kFree);

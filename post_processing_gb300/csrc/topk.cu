@@ -12,7 +12,8 @@
 // larger value or, for equal values, a lower index.  Keys are unique, the
 // order is total and the Top-K set is unique: results are bit-exact.
 //
-// One block per (row, chunk of up to 8192 elements):
+// One block per (row, chunk of up to 8192 elements; 16384 in rows cut into
+// more than 16 chunks):
 //  1. The chunk is staged in shared memory (one bulk copy when the row is
 //     16-byte aligned, else coalesced loads); each thread keeps the maxima of
 //     its 4-element groups in registers, and their maximum (a "delegate").
@@ -29,11 +30,10 @@
 // Rows longer than one chunk: every chunk writes its K keys, sorted, to a
 // workspace; the last block of the row to finish (an atomic ticket, reset by
 // that block so the workspace is ready for the next call or graph replay)
-// merges the sorted lists: with bitonic merges in registers, except between
-// 49 and 96 chunks, where the threshold / rank steps are faster (the
-// threshold is the K-th largest of the lists' first keys).
-// Many short rows take a second kernel with one warp per row and no block
-// barrier (topk_warp_kernel, further down); use_warp_kernel() picks it.
+// merges the sorted lists: its warps fold them into at most eight sorted
+// lists with bitonic merges in registers, and every key of those is ranked by
+// binary searches in all eight at once (its rank is the number of larger
+// keys); ranks below K are the row's result, in rank order.
 #include <algorithm>
 #include <atomic>
 #include <cmath>
@@ -51,9 +51,8 @@ constexpr int kVpt = 32;                       // values per thread
 constexpr int kChunk = kThreads * kVpt;        // 8192 elements per block
 constexpr int kCap = 2048;                     // shared candidate capacity
 constexpr int kMaxK = 32;
-constexpr int kMergeRegs = 12;                 // chunk lists per warp held in registers (<= 96 chunks)
-constexpr int kMergeChunks = kWarps * kMergeRegs;   // blocks per row the one-round-trip merge handles
-constexpr int kBitonicChunks = 48;             // up to here the lists are merged bitonically
+constexpr int kBigChunk = 2 * kChunk;          // 16384: the chunk of rows cut into many chunks
+constexpr int kFoldBatch = 6;                  // chunk lists a warp loads per round of the merge
 constexpr int kMinChunk = 2048;                // shortest chunk a long row is cut into
 constexpr int kCutChunks = 16;                 // most blocks per row when a row is cut finer than 8192
 constexpr unsigned kFull = 0xffffffffu;
@@ -63,7 +62,7 @@ struct TopkParams {
     long long cols;
     int k;
     int nchunks;
-    int chunk;                    // elements per block (a multiple of 4, <= kChunk)
+    int chunk;                    // elements per block (a multiple of 4, <= kBigChunk)
     float* out_val;
     int* out_idx;
     unsigned int* tickets;        // [rows]
@@ -125,6 +124,7 @@ struct __align__(16) Shared {
 
 constexpr int kSharedBytes = (int)((sizeof(Shared) + 127) / 128 * 128);
 constexpr int kDynSmem = kSharedBytes + kChunk * 4;
+constexpr int kDynSmemBig = kSharedBytes + kBigChunk * 4;
 
 // Exact kth-largest (1-based) of n unique 64-bit keys by radix select.
 template <class KeyAt>
@@ -222,150 +222,89 @@ __device__ __forceinline__ void rank_and_emit(const unsigned long long* keys, ui
 }
 
 // Takes the row's ticket once this block's list is written: true for the
-// row's last block, which then merges.  One thread makes the block's writes
+// row's last block, which then merges.  Thread 0 makes the block's writes
 // visible at GPU scope (the block barrier orders the other threads' writes
-// before its release fence) and counts the block in.
+// before its fence) and counts the block in; in the last block it then
+// orders its reads of the other lists after the count, and the second block
+// barrier carries that order to the other threads.
 __device__ __forceinline__ bool take_ticket(const TopkParams& p, long long row, Shared& s) {
     __syncthreads();
     if (threadIdx.x == 0) {
         __threadfence();
         const unsigned prev = atomicAdd(&p.tickets[row], 1u);
         s.last = (prev == (unsigned)p.nchunks - 1u);
+        if (s.last) __threadfence();
     }
     __syncthreads();
-    if (!s.last) return false;
-    __threadfence();
-    return true;
+    return s.last != 0;
 }
 
-// The row's last block: merges the chunks' sorted lists into the row's Top-K
-// and resets the row's ticket for the next call or graph replay.
+// The row's last block: the row's Top-K from the chunks' sorted lists, and
+// the row's ticket reset for the next call or graph replay.  Warp w folds the
+// lists w, w + 8, ... into one sorted list with bitonic merges in registers
+// (lane i holding the i-th key; 0 past a list's K keys, and every real key is
+// larger than 0), a batch of lists at a time with the next batch's loads in
+// flight.  Then every key of the (at most eight) folded lists is ranked: the
+// lists are sorted, so the number of larger keys in each is found by a
+// branch-free binary search in shared memory, all eight searches in lockstep
+// so that their loads overlap (the key's own list holds exactly `lane`
+// larger keys).  Keys are unique, so the K keys of rank below K are written
+// once each, in rank order.
 __device__ __forceinline__ void merge_chunk_lists(const TopkParams& p, long long row, const float* xr, Shared& s) {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int k = p.k;
-    uint32_t cnt;
-    const unsigned long long* all = p.keys + row * p.nchunks * k;
-    const int total = p.nchunks * k;
-    if (p.nchunks <= kBitonicChunks || p.nchunks > kMergeChunks) {
-        // Warp w folds the lists of chunks w, w + 8, ... (lane i holding the
-        // i-th key of each; 0 past a list's K keys, and every real key is
-        // larger than 0) with bitonic merges in registers, a batch of
-        // kLists lists at a time with the next batch's loads in flight; warp
-        // 0 then folds the eight warps' lists.  The result is the row's
-        // Top-K in rank order: no threshold, no ranking, one block barrier.
-        constexpr int kLists = kBitonicChunks / kWarps;   // per warp and batch
-        auto load_batch = [&](int c0, unsigned long long (&kb)[kLists]) {
+    const int k = p.k, nch = p.nchunks;
+    const unsigned long long* all = p.keys + row * nch * k;
+    unsigned long long acc = 0ull;
+    if (warp < nch) {
+        auto load_batch = [&](int c0, unsigned long long (&kb)[kFoldBatch]) {
 #pragma unroll
-            for (int r = 0; r < kLists; ++r) {
+            for (int r = 0; r < kFoldBatch; ++r) {
                 const int c = c0 + r * kWarps;
-                kb[r] = (c < p.nchunks && lane < k) ? __ldcg(all + (long long)c * k + lane) : 0ull;
+                kb[r] = (c < nch && lane < k) ? __ldcg(all + (long long)c * k + lane) : 0ull;
             }
         };
-        unsigned long long cur[kLists], nxt[kLists];
+        unsigned long long cur[kFoldBatch], nxt[kFoldBatch];
         load_batch(warp, cur);
-        unsigned long long acc = 0ull;
-        for (int c0 = warp; c0 < p.nchunks; c0 += kWarps * kLists) {
-            const int cn = c0 + kWarps * kLists;
-            if (cn < p.nchunks) load_batch(cn, nxt);
+        for (int c0 = warp; c0 < nch; c0 += kWarps * kFoldBatch) {
+            const int cn = c0 + kWarps * kFoldBatch;
+            if (cn < nch) load_batch(cn, nxt);
 #pragma unroll
-            for (int step = 1; step < kLists; step *= 2)
+            for (int step = 1; step < kFoldBatch; step *= 2)
 #pragma unroll
-                for (int r = 0; r + step < kLists; r += 2 * step)
-                    if (c0 + (r + step) * kWarps < p.nchunks) cur[r] = merge_top32(cur[r], cur[r + step]);
+                for (int r = 0; r + step < kFoldBatch; r += 2 * step)
+                    if (c0 + (r + step) * kWarps < nch) cur[r] = merge_top32(cur[r], cur[r + step]);
             acc = c0 == warp ? cur[0] : merge_top32(acc, cur[0]);
 #pragma unroll
-            for (int r = 0; r < kLists; ++r) cur[r] = nxt[r];
+            for (int r = 0; r < kFoldBatch; ++r) cur[r] = nxt[r];
         }
-        s.wlist[warp][lane] = acc;
-        __syncthreads();
-        if (warp != 0) return;
-        unsigned long long w8[kWarps];
-#pragma unroll
-        for (int w = 0; w < kWarps; ++w) w8[w] = s.wlist[w][lane];
-#pragma unroll
-        for (int step = 1; step < kWarps; step *= 2)
-#pragma unroll
-            for (int r = 0; r + step < kWarps; r += 2 * step)
-                if (r + step < p.nchunks) w8[r] = merge_top32(w8[r], w8[r + step]);
-        if (lane < k) {
-            p.out_val[row * k + lane] = key_value(w8[0], xr);
-            p.out_idx[row * k + lane] = (int)key_index(w8[0]);
-        }
-        if (lane == 0) p.tickets[row] = 0u;   // ready for the next call / replay
-        return;
     }
-    // Threshold from the sorted chunk lists: the first m = ceil(K / chunks)
-    // keys of every chunk hold at least K keys, so the K-th largest of that
-    // union has at least K keys at or above it, and every key of the row's
-    // Top-K is at or above it.  It is found by counting, like the ranks.
-    const int m = (k + p.nchunks - 1) / p.nchunks;
-    const int U = m * p.nchunks;
-    {   // 48 < chunks <= 96: U <= 96
-        // One round trip: warp w holds the lists of chunks w, w + 8, ... in
-        // registers, lane i the i-th key of each.  As the lists are sorted,
-        // the keys at or above the threshold are a prefix of each list.
-        unsigned long long key[kMergeRegs];
-#pragma unroll
-        for (int r = 0; r < kMergeRegs; ++r)
-            key[r] = __ldcg(all + (long long)min(warp + r * kWarps, p.nchunks - 1) * k + min(lane, k - 1));
-#pragma unroll
-        for (int r = 0; r < kMergeRegs; ++r) {
-            const int c = warp + r * kWarps;
-            if (c >= p.nchunks || lane >= k) key[r] = 0ull;
-            else if (lane < m) s.cand[c * m + lane] = key[r];
-        }
-        __syncthreads();
-        // The U first keys are real keys, hence unique: exactly one of them
-        // has rank K - 1, and it is the K-th largest.
-        rank_and_emit(s.cand, (uint32_t)U, k, [&](int rank, unsigned long long kv) {
-            if (rank == k - 1) s.red[0] = kv;
-        });
-        __syncthreads();
-        unsigned long long t64 = s.red[0];
-        if (t64 == 0) t64 = 1;   // padding keys (0) never pass
-        int warp_total = 0;
-#pragma unroll
-        for (int r = 0; r < kMergeRegs; ++r) warp_total += __popc(__ballot_sync(kFull, key[r] >= t64));
-        int all_total;
-        int off = block_offsets(lane == 0 ? warp_total : 0, all_total, s);
-        off = __shfl_sync(kFull, off, 0);   // the warp's first slot
-        if (all_total <= kCap) {
-            const unsigned below = (1u << lane) - 1u;
-#pragma unroll
-            for (int r = 0; r < kMergeRegs; ++r) {
-                const unsigned mask = __ballot_sync(kFull, key[r] >= t64);
-                if ((mask >> lane) & 1u) s.cand[off + __popc(mask & below)] = key[r];
-                off += __popc(mask);
-            }
-        }
-        if (tid == 0) s.cnt = (uint32_t)all_total;
-    }
+    s.wlist[warp][lane] = acc;   // zero keys for warps without a list
     __syncthreads();
-    cnt = s.cnt;
-    if (cnt > kCap) {
-        auto key_at = [&](int i) { return __ldcg(all + i); };
-        const unsigned long long kth = block_kth_largest(key_at, total, k, s);
-        if (tid == 0) s.cnt = 0;
-        __syncthreads();
-        for (int i = tid; i < total; i += kThreads) {
-            const unsigned long long key = __ldcg(all + i);
-            if (key >= kth) s.cand[atomicAdd(&s.cnt, 1u)] = key;
-        }
-        __syncthreads();
-        cnt = s.cnt;
-    }
-    rank_and_emit(s.cand, cnt, k, [&](int rank, unsigned long long key) {
-        p.out_val[row * k + rank] = key_value(key, xr);
-        p.out_idx[row * k + rank] = (int)key_index(key);
-    });
     if (tid == 0) p.tickets[row] = 0u;   // ready for the next call / replay
+    if (acc == 0ull) return;             // padding
+    int lo[kWarps];
+#pragma unroll
+    for (int c = 0; c < kWarps; ++c) lo[c] = 0;
+#pragma unroll
+    for (int step = 16; step >= 1; step >>= 1)
+#pragma unroll
+        for (int c = 0; c < kWarps; ++c) lo[c] += s.wlist[c][lo[c] + step - 1] > acc ? step : 0;
+    int rank = 0;
+#pragma unroll
+    for (int c = 0; c < kWarps; ++c) rank += lo[c] + (s.wlist[c][lo[c]] > acc ? 1 : 0);
+    if (rank < k) {
+        p.out_val[row * k + rank] = key_value(acc, xr);
+        p.out_idx[row * k + rank] = (int)key_index(acc);
+    }
 }
 
-template <bool kVec>
-__global__ void __launch_bounds__(kThreads, 4) topk_kernel(const __grid_constant__ TopkParams p) {
+// kG: 4-element groups a thread (8 for chunks of up to 8192 elements, 16 for
+// up to 16384).
+template <bool kVec, int kG>
+__global__ void __launch_bounds__(kThreads, kG == 8 ? 4 : 2) topk_kernel(const __grid_constant__ TopkParams p) {
     extern __shared__ __align__(128) unsigned char dsmem[];
     Shared& s = *reinterpret_cast<Shared*>(dsmem);
-    float* sx = reinterpret_cast<float*>(dsmem + kSharedBytes);   // [kChunk] the staged chunk
+    float* sx = reinterpret_cast<float*>(dsmem + kSharedBytes);   // [chunk] the staged chunk
     __shared__ uint64_t bar;
     // Launched as a programmatic dependent of the previous kernel on the
     // stream: wait here until that grid has finished and its writes (the
@@ -428,7 +367,6 @@ __global__ void __launch_bounds__(kThreads, 4) topk_kernel(const __grid_constant
         return make_float4(e < n ? sx[e] : qnan, e + 1 < n ? sx[e + 1] : qnan, e + 2 < n ? sx[e + 2] : qnan,
                            e + 3 < n ? sx[e + 3] : qnan);
     };
-    constexpr int kG = kChunk / 4 / kThreads;   // groups per thread
     float gmax[kG];
     float dm = -INFINITY;   // the delegate: fmaxf skips NaN, so a NaN counts as -inf
 #pragma unroll
@@ -837,9 +775,35 @@ int blocks_per_row(int64_t rows, int64_t cols, int sm_count) {
 }
 
 // Chunk length for a number of blocks per row: a multiple of 4 elements.
-int chunk_len(int64_t cols, int nchunks) {
+int chunk_len(int64_t cols, int nchunks, int max_chunk) {
     const long long c = (cols + nchunks - 1) / nchunks;
-    return (int)std::min<long long>(kChunk, (c + 3) / 4 * 4);
+    return (int)std::min<long long>(max_chunk, (c + 3) / 4 * 4);
+}
+
+// How a row longer than one block is cut: blocks_per_row() chunks of at most
+// 8192 elements, except rows that would take more than kCutChunks of them,
+// which take chunks of up to 16384 (half the lists for the last block to
+// merge).  Measured on GB300, back-to-back launches, K = 32: [1,1000000] 123
+// chunks 9.9 us against 62 chunks 7.9 us (register-held chunks); [1,672000]
+// 83 against 42 chunks 7.6 against 7.3 us.
+struct ChunkPlan {
+    int nchunks, chunk, groups;   // groups: 4-element groups a thread (8 or 16)
+};
+
+ChunkPlan plan_chunks(int64_t rows, int64_t cols, int sm_count) {
+    ChunkPlan c{};
+    const long long base = (cols + kChunk - 1) / kChunk;
+    if (base > kCutChunks) {
+        c.groups = 16;
+        c.nchunks = (int)((cols + kBigChunk - 1) / kBigChunk);
+        c.chunk = chunk_len(cols, c.nchunks, kBigChunk);
+    } else {
+        c.groups = 8;
+        c.nchunks = blocks_per_row(rows, cols, sm_count);
+        c.chunk = chunk_len(cols, c.nchunks, kChunk);
+    }
+    c.nchunks = (int)((cols + c.chunk - 1) / c.chunk);
+    return c;
 }
 
 size_t topk_workspace_size(int64_t rows, int64_t cols, int32_t k) {
@@ -907,9 +871,9 @@ ws_status ws_topk(const float* x, int64_t rows, int64_t cols, int32_t k, float* 
     p.x = x;
     p.cols = cols;
     p.k = k;
-    p.nchunks = blocks_per_row(rows, cols, info->sm_count);
-    p.chunk = chunk_len(cols, p.nchunks);
-    p.nchunks = (int)((cols + p.chunk - 1) / p.chunk);
+    const ChunkPlan plan = plan_chunks(rows, cols, info->sm_count);
+    p.nchunks = plan.nchunks;
+    p.chunk = plan.chunk;
     p.out_val = out_val;
     p.out_idx = out_idx;
     if (need > 0) {
@@ -924,15 +888,24 @@ ws_status ws_topk(const float* x, int64_t rows, int64_t cols, int32_t k, float* 
     // stream is still running and waits in griddepcontrol.wait, which hides
     // the launch gap between the preprocess and the Top-K.
     if (!g_topk_attr_set[dev].load(std::memory_order_acquire)) {
-        WS_TRY_CUDA(cudaFuncSetAttribute(topk_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kDynSmem));
-        WS_TRY_CUDA(cudaFuncSetAttribute(topk_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kDynSmem));
+        WS_TRY_CUDA(cudaFuncSetAttribute(topk_kernel<true, 8>, cudaFuncAttributeMaxDynamicSharedMemorySize, kDynSmem));
+        WS_TRY_CUDA(cudaFuncSetAttribute(topk_kernel<false, 8>, cudaFuncAttributeMaxDynamicSharedMemorySize, kDynSmem));
+        WS_TRY_CUDA(
+            cudaFuncSetAttribute(topk_kernel<true, 16>, cudaFuncAttributeMaxDynamicSharedMemorySize, kDynSmemBig));
+        WS_TRY_CUDA(
+            cudaFuncSetAttribute(topk_kernel<false, 16>, cudaFuncAttributeMaxDynamicSharedMemorySize, kDynSmemBig));
         g_topk_attr_set[dev].store(true, std::memory_order_release);
     }
     p.err = device_error_word();
-    // the staged chunk only needs the row's length when the row is short
+    // the staged chunk only needs the chunk's length when the chunk is short
     const size_t smem = (size_t)kSharedBytes + (size_t)(p.chunk + 3) / 4 * 16;
-    const cudaError_t e = vec ? launch_pdl(topk_kernel<true>, dim3((unsigned)blocks), dim3(kThreads), smem, stream, p)
-                              : launch_pdl(topk_kernel<false>, dim3((unsigned)blocks), dim3(kThreads), smem, stream, p);
+    cudaError_t e;
+    if (plan.groups == 16)
+        e = vec ? launch_pdl(topk_kernel<true, 16>, dim3((unsigned)blocks), dim3(kThreads), smem, stream, p)
+                : launch_pdl(topk_kernel<false, 16>, dim3((unsigned)blocks), dim3(kThreads), smem, stream, p);
+    else
+        e = vec ? launch_pdl(topk_kernel<true, 8>, dim3((unsigned)blocks), dim3(kThreads), smem, stream, p)
+                : launch_pdl(topk_kernel<false, 8>, dim3((unsigned)blocks), dim3(kThreads), smem, stream, p);
     if (e != cudaSuccess) return cuda_fail(e, "top-k launch");
     return WS_OK;
 }

@@ -103,11 +103,10 @@ def test_special_rows(B, oracle, cols, k):
     check_topk_invariants(x, got[0], got[1], k)
 
 
-# The same adversarial rows at the lengths of the long-row merge paths (19
-# chunk lists: bitonic; 49 and 83: threshold from the lists' first keys; 97:
-# bitonic in batches).  In a constant or all-NaN row that threshold keeps the
-# whole lists of the K - 1 lowest chunks and the first key of the next one:
-# 993 survivors at K = 32, ranked in the merging block.
+# The same adversarial rows on long rows cut into 16384-element chunks (10,
+# 25, 42 and 49 chunk lists: the merging block's warps fold up to six lists
+# each per round, so 49 lists take two rounds).  A constant or all-NaN row
+# sends every chunk to the exact radix-select fallback.
 @pytest.mark.parametrize("cols", [150000, 393217, 672000, 786433])
 @pytest.mark.parametrize("k", [1, 32])
 def test_special_long_rows(B, oracle, cols, k):
@@ -237,14 +236,18 @@ def test_warp_rows_fallback(B, oracle, cols, k, offset):
     check_topk_invariants(x, got[0], got[1], k)
 
 
-# Long rows: the last block of a row merges the chunks' sorted lists with
-# bitonic merges up to 48 chunks, with a threshold from the lists' first keys
-# from 49 to 96, and with bitonic merges in batches beyond.  Chunk counts on
-# a 152-SM GB300: [64,131072] 16, [4,65536] 16, [2,100000] 16, [1,150000] 19,
-# [1,393217] 49, [1,672000] 83, [1,786432] 96, [1,786433] 97, [1,1000000]
-# 123, [2,2000000] 245.
-@pytest.mark.parametrize("rows,cols", [(64, 131072), (4, 65536), (2, 100000), (1, 150000), (1, 393217),
-                                       (1, 672000), (1, 786432), (1, 786433), (1, 1_000_000), (2, 2_000_000)])
+# Long rows: one block per chunk writes the chunk's K keys, and the row's
+# last block merges the lists (its warps fold them into at most eight, then
+# every key is ranked by binary searches).  Rows are cut into chunks of up to
+# 8192 (cut finer down to 2048 while SMs would idle), or of up to 16384 when
+# that would give more than 16 chunks.  On a 152-SM GB300: [8,131072] 16
+# lists of 8192, [4,65536] 16 of 4096, [2,100000] 16 of 6252, [32,131072] 16
+# of 8192, [64,131072] 16, [200,16384] 2, [320,9000] 2, [1,150000] 10 of
+# 15000, [1,393217] 25, [1,672000] 42, [1,786433] 49 (two fold rounds),
+# [1,1000000] 62, [2,2000000] 123.
+@pytest.mark.parametrize("rows,cols", [(8, 131072), (4, 65536), (2, 100000), (32, 131072), (64, 131072),
+                                       (200, 16384), (320, 9000), (1, 150000), (1, 393217), (1, 672000),
+                                       (1, 786433), (1, 1_000_000), (2, 2_000_000)])
 @pytest.mark.parametrize("k", [1, 5, 32])
 def test_long_row_merge_paths(B, oracle, rows, cols, k):
     x = synth.logits_with_ties(rows * 7 + cols + k, rows, cols, frac=0.05)
@@ -258,3 +261,25 @@ def test_long_row_merge_paths(B, oracle, rows, cols, k):
     got = gpu_topk(B, x, k)
     assert_exact(got, oracle.topk(x, k))
     check_topk_invariants(x, got[0], got[1], k)
+
+
+@pytest.mark.parametrize("rows,cols", [(3, 150001), (33, 131071), (5, 20003)])
+@pytest.mark.parametrize("offset", [1, 2])
+def test_long_rows_misaligned(B, oracle, rows, cols, offset):
+    """Long rows whose start is not 16-byte aligned (coalesced loads instead of
+    the bulk copy), in both chunk sizes, with a ragged last chunk."""
+    x = synth.logits_with_ties(rows + cols + offset, rows, cols, frac=0.05)
+    got = gpu_topk(B, x, 32, offset=offset)
+    assert_exact(got, oracle.topk(x, 32))
+
+
+def test_long_rows_all_top_in_one_chunk(B, oracle):
+    """The whole Top-K inside one chunk (the other lists' keys all rank
+    below): the ranks come from one list alone."""
+    rows, cols = 4, 200000
+    x = synth.logits_normal(91, rows, cols)
+    for r in range(rows):
+        at = 16384 * (r + 3) + 100
+        x[r, at:at + 40] = 50.0 + np.arange(40, dtype=np.float32)
+    for k in (1, 32):
+        assert_exact(gpu_topk(B, x, k), oracle.topk(x, k))
