@@ -32,6 +32,7 @@
 // neighbours clamped to [0, S-1]; three FP32 lerps; out = (v - M_c) * R_c.
 #include <algorithm>
 #include <atomic>
+#include <climits>
 #include <cmath>
 
 #include <cuda_bf16.h>
@@ -91,28 +92,39 @@ struct PreParams {
     uint32_t* err;            // device error word
 };
 
-// Taps of destination coordinate x of a D-pixel box sampled from S pixels.
+// Taps of destination coordinate x of a D-pixel box sampled from S pixels:
+// the source coordinate is num / den with num = (2x + 1) S - D and den = 2D;
+// lo = floor(num / den), rem = num - lo den in [0, den), w = rem / den in one
+// correctly rounded division; both taps clamped to [0, S - 1].  32-bit
+// arithmetic whenever num fits (every size up to about 23,000 pixels; 64-bit
+// conversions and compares are slow), 64-bit otherwise.
 __device__ __forceinline__ void axis_taps(int x, int S, int D, int& lo, int& hi, float& w) {
     const long long num = (2LL * x + 1) * S - D;
-    const long long den = 2LL * D;
-    long long q, rem;
-    if (num >= -0x3fffffffLL && num <= 0x3fffffffLL && den <= 0x3fffffffLL) {
-        // same integer arithmetic in 32 bits (every size up to ~23k pixels)
-        const int n32 = (int)num, d32 = (int)den;
-        int q32 = n32 / d32;                  // truncates toward zero
-        if (n32 < 0 && q32 * d32 != n32) --q32;
-        q = q32;
-        rem = n32 - q32 * d32;
+    const int den = 2 * D;   // at most 131,070
+    int q, rem;
+    if (num >= (long long)INT_MIN && num <= (long long)INT_MAX) {
+        const int n = (int)num;
+        q = n / den;               // truncates toward zero
+        rem = n - q * den;
+        if (rem < 0) {             // floor for negative num
+            --q;
+            rem += den;
+        }
     } else {
-        q = num / den;
-        if (num < 0 && q * den != num) --q;   // floor
-        rem = num - q * den;
+        long long q64 = num / den;
+        long long r64 = num - q64 * den;
+        if (r64 < 0) {
+            --q64;
+            r64 += den;
+        }
+        // only the clamped taps are needed: [-1, S] keeps them
+        q = (int)(q64 < -1 ? -1 : (q64 > S ? S : q64));
+        rem = (int)r64;
     }
     // 0 <= rem < den
     w = __fdiv_rn((float)rem, (float)den);
-    lo = (int)(q < 0 ? 0 : (q > S - 1 ? S - 1 : q));
-    const long long q1 = q + 1;
-    hi = (int)(q1 < 0 ? 0 : (q1 > S - 1 ? S - 1 : q1));
+    lo = min(max(q, 0), S - 1);
+    hi = min(max(q + 1, 0), S - 1);
 }
 
 // Output element conversion (round to nearest even for the half types).
@@ -327,34 +339,46 @@ __global__ void __launch_bounds__(kMaxThreads) pre_ring_kernel(const __grid_cons
     }
 }
 
-// One thread per destination pixel, plain byte loads; any alignment.
+// One thread per destination pixel, plain byte loads; any alignment.  A 3-D
+// grid: x from the block column and thread, output row blockIdx.y (its taps
+// are the same for the whole block), frame blockIdx.z (frames beyond the
+// grid's z extent loop).  No index divisions: the loads are issued after a
+// few dozen instructions.
 template <typename OutT>
-__global__ void __launch_bounds__(256) pre_direct_kernel(const __grid_constant__ PreParams p, long long total) {
+__global__ void __launch_bounds__(256) pre_direct_kernel(const __grid_constant__ PreParams p, int batch) {
     asm volatile("griddepcontrol.launch_dependents;");
     asm volatile("griddepcontrol.wait;" ::: "memory");
+    const int x = blockIdx.x * blockDim.x + threadIdx.x;
+    const int y = blockIdx.y;
+    if (x >= p.dw) return;
     const size_t plane = (size_t)p.dh * p.dw;
-    for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < total;
-         i += (long long)gridDim.x * blockDim.x) {
-        const int x = (int)(i % p.dw);
-        const long long t = i / p.dw;
-        const int y = (int)(t % p.dh);
-        const long long b = t / p.dh;
+    const bool in_x = x >= p.left && x < p.left + p.nw;
+    const bool in_y = y >= p.top && y < p.top + p.nh;
+    int i0 = 0, i1 = 0, j0 = 0, j1 = 0;
+    float wx = 0.f, wy = 0.f;
+    if (in_x && in_y) {
+        axis_taps(x - p.left, p.sw, p.nw, i0, i1, wx);
+        axis_taps(y - p.top, p.sh, p.nh, j0, j1, wy);
+    }
+    for (int b = blockIdx.z; b < batch; b += gridDim.z) {
         float v[3];
-        if (x >= p.left && x < p.left + p.nw && y >= p.top && y < p.top + p.nh) {
-            int i0, i1, j0, j1;
-            float wx, wy;
-            axis_taps(x - p.left, p.sw, p.nw, i0, i1, wx);
-            axis_taps(y - p.top, p.sh, p.nh, j0, j1, wy);
-            const uint8_t* f = p.src + b * p.frame_stride;
+        if (in_x && in_y) {
+            const uint8_t* f = p.src + (long long)b * p.frame_stride;
             const uint8_t* A = f + (long long)j0 * p.row_stride;
-            const uint8_t* B = f + (long long)j1 * p.row_stride;
+            const uint8_t* Bq = f + (long long)j1 * p.row_stride;
+            float q[3][4];
 #pragma unroll
             for (int c = 0; c < 3; ++c) {
                 const int sc = p.cmap[c];
-                const float p00 = __ldg(A + 3 * i0 + sc), p01 = __ldg(A + 3 * i1 + sc);
-                const float p10 = __ldg(B + 3 * i0 + sc), p11 = __ldg(B + 3 * i1 + sc);
-                const float tt = p00 + wx * (p01 - p00);
-                const float u = p10 + wx * (p11 - p10);
+                q[c][0] = __ldg(A + 3 * i0 + sc);
+                q[c][1] = __ldg(A + 3 * i1 + sc);
+                q[c][2] = __ldg(Bq + 3 * i0 + sc);
+                q[c][3] = __ldg(Bq + 3 * i1 + sc);
+            }
+#pragma unroll
+            for (int c = 0; c < 3; ++c) {
+                const float tt = q[c][0] + wx * (q[c][1] - q[c][0]);
+                const float u = q[c][2] + wx * (q[c][3] - q[c][2]);
                 v[c] = tt + wy * (u - tt);
             }
         } else {
@@ -506,7 +530,11 @@ ws_status launch_any(const PreParams& p, bool ring, bool vec, int dev, const Dev
                                          (int)cudaSharedmemCarveoutMaxShared));
         g_direct_attr_set[dev][type_slot].store(true, std::memory_order_release);
     }
-    return pdl_launch(pre_direct_kernel<OutT>, dim3(blocks), dim3(256), 0, stream, p, total);
+    // x across blocks of up to 256 threads, one output row per blockIdx.y,
+    // frames across blockIdx.z (the kernel loops over frames beyond it)
+    const int tx = std::min(256, (p.dw + 31) / 32 * 32);
+    const dim3 grid((unsigned)((p.dw + tx - 1) / tx), (unsigned)p.dh, (unsigned)std::min<long long>(total, 65535));
+    return pdl_launch(pre_direct_kernel<OutT>, grid, dim3(tx), 0, stream, p, (int)total);
 }
 
 }  // namespace
@@ -606,8 +634,8 @@ ws_status preprocess_launch(const ws_preprocess_desc* d, const uint8_t* src, int
         vec = (d->dst_w % 4 == 0) && ((uintptr_t)dst % 16 == 0);
         blocks = (unsigned)std::min<long long>(p.units, (long long)info->sm_count * t.blocks_per_sm);
     } else {
-        total = (long long)batch * d->dst_h * d->dst_w;
-        blocks = (unsigned)std::min<long long>((total + 255) / 256, (long long)info->sm_count * 16);
+        total = batch;   // the per-pixel kernel's grid is set up in launch_any
+        blocks = 0;
     }
     switch (d->dst_type) {
         case WS_DTYPE_F16:
