@@ -781,11 +781,15 @@ int chunk_len(int64_t cols, int nchunks, int max_chunk) {
 }
 
 // How a row longer than one block is cut: blocks_per_row() chunks of at most
-// 8192 elements, except rows that would take more than kCutChunks of them,
-// which take chunks of up to 16384 (half the lists for the last block to
-// merge).  Measured on GB300, back-to-back launches, K = 32: [1,1000000] 123
-// chunks 9.9 us against 62 chunks 7.9 us (register-held chunks); [1,672000]
-// 83 against 42 chunks 7.6 against 7.3 us.
+// 8192 elements, except where that would give more than kCutChunks chunks in
+// a row or more than two blocks per SM; those take chunks of up to 16384 (half
+// the blocks, half the lists for the last block to merge, and each thread's
+// fixed per-block steps spread over twice the elements).  Measured on GB300,
+// K = 32, back-to-back launches: [32,131072] 9.3 -> 8.0 us, [64,131072] 14.7
+// -> 13.3 us, [1,1000000] 9.9 -> 8.0 us; inside the 8 x 4K -> 512 lanes the
+// step went 21.6 -> 20.9 us with lanes on their own streams and 34.5 -> 33.7
+// us on one stream.  Chunks of 32768 (one block per SM) were faster alone
+// ([32,131072] 7.6 us) but slowed the own-stream step to 21.4 us.
 struct ChunkPlan {
     int nchunks, chunk, groups;   // groups: 4-element groups a thread (8 or 16)
 };
@@ -793,7 +797,7 @@ struct ChunkPlan {
 ChunkPlan plan_chunks(int64_t rows, int64_t cols, int sm_count) {
     ChunkPlan c{};
     const long long base = (cols + kChunk - 1) / kChunk;
-    if (base > kCutChunks) {
+    if (base > kCutChunks || rows * base > 2LL * sm_count) {
         c.groups = 16;
         c.nchunks = (int)((cols + kBigChunk - 1) / kBigChunk);
         c.chunk = chunk_len(cols, c.nchunks, kBigChunk);

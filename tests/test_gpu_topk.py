@@ -240,10 +240,11 @@ def test_warp_rows_fallback(B, oracle, cols, k, offset):
 # last block merges the lists (its warps fold them into at most eight, then
 # every key is ranked by binary searches).  Rows are cut into chunks of up to
 # 8192 (cut finer down to 2048 while SMs would idle), or of up to 16384 when
-# that would give more than 16 chunks.  On a 152-SM GB300: [8,131072] 16
-# lists of 8192, [4,65536] 16 of 4096, [2,100000] 16 of 6252, [32,131072] 16
-# of 8192, [64,131072] 16, [200,16384] 2, [320,9000] 2, [1,150000] 10 of
-# 15000, [1,393217] 25, [1,672000] 42, [1,786433] 49 (two fold rounds),
+# that would give more than 16 chunks a row or more than two blocks per SM.
+# On a 152-SM GB300: [8,131072] 16 lists of 8192, [4,65536] 16 of 4096,
+# [2,100000] 16 of 6252, [32,131072] and [64,131072] 8 of 16384 (no fold),
+# [200,16384] and [320,9000] one chunk in the 16384-element kernel, [1,150000]
+# 10 of 15000, [1,393217] 25, [1,672000] 42, [1,786433] 49 (two fold rounds),
 # [1,1000000] 62, [2,2000000] 123.
 @pytest.mark.parametrize("rows,cols", [(8, 131072), (4, 65536), (2, 100000), (32, 131072), (64, 131072),
                                        (200, 16384), (320, 9000), (1, 150000), (1, 393217), (1, 672000),
