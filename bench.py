@@ -65,12 +65,12 @@ MAX_LANES = 64
 # Filled from the committed ncu summary under profiles/.
 NCU_TRAFFIC = {
     "b64_1080p_to_224": {
-        "bytes": 186_106_368,
-        "source_sha": "9cca8d83a1b65414634c257685b1256b9dbf66086563187ddacec092e849a3dd",
+        "bytes": 185_236_992,
+        "source_sha": "a4330c898ecea40b12c4caef5c38cad52f8e70a6a199a9d321e1daf16bdadb57",
     },
     "b8_4k_to_512": {
-        "bytes": 99_771_904,
-        "source_sha": "9cca8d83a1b65414634c257685b1256b9dbf66086563187ddacec092e849a3dd",
+        "bytes": 99_776_256,
+        "source_sha": "a4330c898ecea40b12c4caef5c38cad52f8e70a6a199a9d321e1daf16bdadb57",
     },
 }
 
