@@ -440,6 +440,24 @@ def detect_measurements(B, Lane, device, stream, samples: int) -> dict:
     # sectors they sit in (A-strided rows: one sector each), its 32-byte record
     alg_decode = DETECT_BATCH * C * A * 4 + n_cand * (4 * R * 32 + 32) + DETECT_BATCH * 4
 
+    # Worst case: every anchor a candidate.  The same heads with the class
+    # logits moved up by 13 (N(5, 2)): 8400 candidates an image, capped at
+    # max_cand 1024 by the NMS's selection, 300 kept.
+    shifted = head.copy()
+    shifted[:, 4 * desc.reg_max:] += 13.0
+    worst = {}
+    for nb in (1, DETECT_BATCH):
+        hw = torch.from_numpy(shifted[:nb].copy()).to(device)
+        B.check(B.ws_detect_workspace_init(wp, nws, s))
+
+        def worst_call(i, hw=hw, nb=nb):
+            B.check(B.ws_detect(desc, hw.data_ptr(), nb, out.data_ptr(), oc.data_ptr(), wp, nws, s))
+
+        worst[f"batch{nb}_us"] = timed(worst_call, 200)
+        torch.cuda.synchronize()
+        worst[f"batch{nb}_kept_per_image"] = int(oc[:nb].sum()) / nb
+    del shifted
+
     # batch-1 latency through a detection lane
     pre = B.preprocess_desc(1280, 720, 640, 640, letterbox=True, norm="scale")
     frame = torch.from_numpy(synth.frames_uniform(DETECT_SEED, 1, 720, 1280)).to(device)
@@ -470,6 +488,8 @@ def detect_measurements(B, Lane, device, stream, samples: int) -> dict:
         "nms_us_by_difference": detect_us - decode_us,
         "candidates_per_image": n_cand / DETECT_BATCH,
         "kept_per_image": kept / DETECT_BATCH,
+        "all_candidates": dict(workload="the same heads with class logits + 13 (N(5,2)): every anchor a candidate, "
+                                        "8400 -> max_cand 1024 -> 300 kept; ws_detect back to back", **worst),
         "decode_roofline": {"bound": "hbm", "kernels": "class scan + DFL boxes in one kernel (ws_detect_decode)",
                             "algorithmic_bytes_per_launch": alg_decode,
                             "bytes_rule": "class plane + 32-byte sector per DFL logit of each candidate + "

@@ -1,6 +1,7 @@
 // ws_ptx.cuh -- inline-PTX helpers shared by the kernels: 1-D bulk copies
 // (cp.async.bulk) into a block's shared memory with completion counted on an
-// mbarrier, and bounded mbarrier waits.
+// mbarrier, bounded mbarrier waits, and thread-block cluster barriers and
+// distributed shared-memory loads and stores.
 #pragma once
 
 #include <cstdint>
@@ -65,5 +66,62 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
 }
 
 constexpr unsigned long long kWaitLimitNs = 1ull << 30;   // ~1.07 s
+
+// Thread-block clusters.  A CTA's place in its cluster and the cluster's
+// size (1 and 1 without a cluster launch).
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+__device__ __forceinline__ uint32_t cluster_nctarank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
+    return r;
+}
+
+// The cluster barrier, split: every thread of every CTA arrives once, then
+// waits.  Release / acquire order shared-memory writes (local and remote)
+// before the arrival against reads after the wait.
+__device__ __forceinline__ void cluster_arrive() { asm volatile("barrier.cluster.arrive.release;" ::: "memory"); }
+__device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.acquire;" ::: "memory"); }
+__device__ __forceinline__ void cluster_sync() {
+    cluster_arrive();
+    cluster_wait();
+}
+
+// The shared::cluster address of `p` (this CTA's shared memory) in the CTA
+// of rank `rank` of the cluster: the same variable in that CTA.
+__device__ __forceinline__ uint32_t cluster_map(const void* p, uint32_t rank) {
+    uint32_t a;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(a) : "r"(smem_u32(p)), "r"(rank));
+    return a;
+}
+
+__device__ __forceinline__ uint32_t ld_cluster_u32(uint32_t a) {
+    uint32_t v;
+    asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(a) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ unsigned long long ld_cluster_u64(uint32_t a) {
+    unsigned long long v;
+    asm volatile("ld.shared::cluster.u64 %0, [%1];" : "=l"(v) : "r"(a) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void st_cluster_u32(uint32_t a, uint32_t v) {
+    asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(a), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ void st_cluster_u64(uint32_t a, unsigned long long v) {
+    asm volatile("st.shared::cluster.u64 [%0], %1;" ::"r"(a), "l"(v) : "memory");
+}
+
+__device__ __forceinline__ void st_cluster_v4(uint32_t a, float4 v) {
+    asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(a), "f"(v.x), "f"(v.y), "f"(v.z), "f"(v.w)
+                 : "memory");
+}
 
 }  // namespace ws

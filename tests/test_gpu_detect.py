@@ -140,6 +140,22 @@ def test_decode_whole_tile_kernel_scalar(B, oracle):
     assert sum(len(g["anchor"]) for g in got) > 1000
 
 
+@pytest.mark.parametrize("batch", [2, 1101])
+@pytest.mark.parametrize("geom", ["64x64", "40x24"])
+def test_decode_reg_max_above_16(B, oracle, batch, geom):
+    """reg_max 17 .. 32 takes the 32-bin DFL kernels: the split form (2
+    images) and the whole-tile form (1101 one-tile images), with 16-byte loads
+    (84 anchors) and scalar loads (15 anchors)."""
+    if geom == "64x64":
+        desc = B.detect_desc(in_w=64, in_h=64, reg_max=20, num_classes=6, conf=0.3)
+        head = synth.yolo_head(93, batch, 64, 64, reg_max=20, num_classes=6, cls_mu=-1.0)
+    else:
+        desc = B.detect_desc(in_w=40, in_h=24, strides=(8,), reg_max=20, num_classes=6, conf=0.3)
+        head = synth.yolo_head(94, batch, 40, 24, reg_max=20, num_classes=6, cls_mu=-1.0, strides=(8,))
+    got = check_decode(B, oracle, desc, head)
+    assert sum(len(g["anchor"]) for g in got) > batch
+
+
 def test_decode_small_geometry(B, oracle):
     desc = B.detect_desc(in_w=320, in_h=192, reg_max=8, num_classes=3, conf=0.3)
     head = synth.yolo_head(22, 2, 320, 192, reg_max=8, num_classes=3, cls_mu=-2.0)
@@ -166,9 +182,11 @@ def test_decode_nan_and_signed_zero(B, oracle):
         assert 9 in g["anchor"] and not any(a < 5 for a in g["anchor"])
 
 
-def test_nms_nan_and_signed_zero(B, oracle):
+@pytest.mark.parametrize("objects,per_object", [(30, 8), (60, 10), (100, 12)])
+def test_nms_nan_and_signed_zero(B, oracle, objects, per_object):
+    # 240 candidates (one CTA), 600 (cluster, no cap) and 1200 (cluster, cap selection)
     desc = B.detect_desc(iou_thr=0.5)
-    c = synth.clustered_candidates(70, 30, 8)
+    c = synth.clustered_candidates(70, objects, per_object)
     lg = np.round(c["logits"])                              # many ties
     lg[::7] = np.nan
     lg[1::5] = np.where(lg[1::5] == 0, -0.0, lg[1::5])
@@ -234,6 +252,51 @@ def test_nms_caps_and_ties(B, oracle):
     assert all(len(c["anchors"]) > 1000 for c in cands)
     check_nms(B, oracle, desc, cands)
     desc.max_cand, desc.max_det = 1024, 1024
+    check_nms(B, oracle, desc, cands)
+
+
+def first_n(c, n):
+    return {k: np.asarray(v)[:n] for k, v in c.items()}
+
+
+# Candidate counts across the NMS's paths: none, the one-CTA fast path (at
+# most 256), and above it the cluster path (or one CTA when the batch leaves
+# no room for clusters), with and without the cap selection.
+NMS_COUNTS = [0, 100, 256, 257, 600, 1024, 1025, 3000, 8400]
+
+
+@pytest.mark.parametrize("batch", [1, 3, 9, 24, 48, 80])
+def test_nms_cluster_sizes_and_mixed_counts(B, oracle, batch):
+    # the batch sets the CTAs per image (8, 4, 2 or 1 on a 152-SM GPU); images
+    # of one launch mix every path
+    desc = B.detect_desc(max_cand=1024, max_det=300)
+    cands = []
+    for b in range(batch):
+        n = NMS_COUNTS[(b + batch) % len(NMS_COUNTS)]
+        cands.append(first_n(synth.clustered_candidates(400 + b, 280, 30), n))
+    check_nms(B, oracle, desc, cands)
+
+
+@pytest.mark.parametrize("max_cand,max_det", [(1, 1), (5, 5), (9, 3), (200, 40), (257, 257), (1000, 1000)])
+def test_nms_cluster_small_caps(B, oracle, max_cand, max_det):
+    # caps below the cluster size and around the fast-path limit, on images
+    # with more than 256 candidates
+    desc = B.detect_desc(max_cand=max_cand, max_det=max_det)
+    cands = [first_n(synth.clustered_candidates(500 + b, 280, 30), n) for b, n in enumerate((300, 1500, 8400))]
+    check_nms(B, oracle, desc, cands)
+
+
+@pytest.mark.parametrize("batch", [1, 2])
+def test_nms_keys_beyond_registers(B, oracle, batch):
+    # a 2560 x 2560 input: 134,400 anchors, every one a candidate, more keys
+    # per CTA than its registers hold, so the selection re-reads them
+    desc = B.detect_desc(in_w=2560, in_h=2560, max_cand=1024, max_det=300)
+    st, A = B.ws_detect_validate(desc, batch)
+    B.check(st)
+    assert A == 134400
+    cands = [synth.clustered_candidates(600 + b, 1344, 100, in_w=2560, in_h=2560, anchors=A) for b in range(batch)]
+    for c in cands:
+        c["logits"] = np.round(c["logits"] * 8) / 8          # ties resolved by anchor
     check_nms(B, oracle, desc, cands)
 
 
