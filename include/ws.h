@@ -78,9 +78,11 @@ const char* ws_last_error(void);
 /* Library version: major * 10000 + minor * 100 + patch. */
 int32_t ws_version(void);
 
-/* Error bits that kernels set on the current device when a bounded wait
- * (an mbarrier wait on a bulk copy) runs out, instead of hanging.  Reads the
- * flags synchronously; clears them when clear != 0.  *flags == 0 means none. */
+/* Error bits that kernels set on the current device instead of hanging or
+ * faulting: 0x1 when a bounded wait (an mbarrier wait on a bulk copy) runs
+ * out, 0x2 when a kernel finds its launch inconsistent with its parameters
+ * (a cluster shape it was not built for) and does nothing.  Reads the flags
+ * synchronously; clears them when clear != 0.  *flags == 0 means none. */
 ws_status ws_device_error(uint32_t* flags, int32_t clear);
 
 /* Diagnostic of that path: launches one thread that arms an mbarrier for 16

@@ -252,8 +252,9 @@ ws_status enqueue_path(ws_lane* L, bool capturing, int bi) {
         rv = rv / L->d.batch * nb;
         ri = ri / L->d.batch * nb;
     } else {
-        st = ws_topk(L->logits, rows, L->d.cols, L->d.k, static_cast<float*>(L->rv_dev),
-                     static_cast<int32_t*>(L->ri_dev), L->ws[bi], L->ws_bytes[bi], L->stream);
+        // the row ticket, not a cluster merge: lanes share the GPU with other lanes' kernels
+        st = topk_enqueue(L->logits, rows, L->d.cols, L->d.k, static_cast<float*>(L->rv_dev),
+                          static_cast<int32_t*>(L->ri_dev), L->ws[bi], L->ws_bytes[bi], L->stream, false);
         rv = ri = (size_t)rows * L->d.k * sizeof(float);
     }
     if (st != WS_OK) return st;
@@ -794,9 +795,9 @@ ws_status ws_lane_wait(ws_lane* L, int64_t timeout_us, ws_lane_timing* timing) {
     if (dev_err) {
         *(volatile uint32_t*)L->err_host = 0u;   // the next submit starts clean
         return fail(WS_ERR_DEVICE,
-                    "a kernel of this lane gave up a bounded wait (error bits 0x%x%s); this submit's results are "
-                    "undefined",
-                    dev_err, (dev_err & kDevErrBulkCopyTimeout) ? ": a bulk copy did not complete in time" : "");
+                    "a kernel of this lane reported an error (bits 0x%x%s%s); this submit's results are undefined",
+                    dev_err, (dev_err & kDevErrBulkCopyTimeout) ? ": a bulk copy did not complete in time" : "",
+                    (dev_err & kDevErrBadLaunch) ? ": a launch did not match its parameters" : "");
     }
     return WS_OK;
 }

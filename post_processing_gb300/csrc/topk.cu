@@ -37,7 +37,9 @@
 #include <algorithm>
 #include <atomic>
 #include <cmath>
+#include <map>
 #include <mutex>
+#include <tuple>
 
 #include "ws_internal.cuh"
 #include "ws_ptx.cuh"
@@ -68,6 +70,7 @@ struct TopkParams {
     unsigned int* tickets;        // [rows]
     unsigned long long* keys;     // [rows][nchunks][k]
     uint32_t* err;                // device error word
+    int cluster;                  // 1: a row's blocks form a thread-block cluster and merge through it
 };
 
 __device__ __forceinline__ uint32_t order_bits(float f) {
@@ -113,6 +116,7 @@ __device__ __forceinline__ unsigned long long merge_top32(unsigned long long a, 
 struct __align__(16) Shared {
     unsigned long long cand[kCap + kThreads];   // candidates, then one spare slot per thread
     unsigned long long wlist[kWarps][32];       // merge: each warp's top-K list
+    unsigned long long list[kMaxK];             // cluster merge: this chunk's sorted list
     unsigned long long red[kWarps];
     uint32_t hist[256];
     uint32_t warp_t[kWarps];
@@ -298,6 +302,46 @@ __device__ __forceinline__ void merge_chunk_lists(const TopkParams& p, long long
     }
 }
 
+// The row's blocks as one thread-block cluster (at most 8 chunks): each
+// chunk's sorted list stays in its block's shared memory (s.list), and one
+// cluster barrier replaces the ticket.  Rank 0 reads the lists through
+// distributed shared memory (warp c takes chunk c's list), lets the other
+// blocks leave, and ranks every key as merge_chunk_lists does.
+__device__ __forceinline__ void cluster_merge(const TopkParams& p, long long row, const float* xr, Shared& s) {
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int k = p.k;
+    cluster_sync();   // every chunk's list is written
+    const bool lead = cluster_ctarank() == 0;
+    unsigned long long acc = 0ull;
+    if (lead) {
+        if (warp < p.nchunks && lane < k) acc = ld_cluster_u64(cluster_map(&s.list[lane], (uint32_t)warp));
+        s.wlist[warp][lane] = acc;   // zero keys for warps without a list
+    }
+    cluster_arrive();   // rank 0 has its copies: the other blocks' shared memory may go
+    if (!lead) {
+        cluster_wait();
+        return;
+    }
+    __syncthreads();
+    if (acc != 0ull) {
+        int lo[kWarps];
+#pragma unroll
+        for (int c = 0; c < kWarps; ++c) lo[c] = 0;
+#pragma unroll
+        for (int step = 16; step >= 1; step >>= 1)
+#pragma unroll
+            for (int c = 0; c < kWarps; ++c) lo[c] += s.wlist[c][lo[c] + step - 1] > acc ? step : 0;
+        int rank = 0;
+#pragma unroll
+        for (int c = 0; c < kWarps; ++c) rank += lo[c] + (s.wlist[c][lo[c]] > acc ? 1 : 0);
+        if (rank < k) {
+            p.out_val[row * k + rank] = key_value(acc, xr);
+            p.out_idx[row * k + rank] = (int)key_index(acc);
+        }
+    }
+    cluster_wait();
+}
+
 // kG: 4-element groups a thread (8 for chunks of up to 8192 elements, 16 for
 // up to 16384).
 template <bool kVec, int kG>
@@ -311,6 +355,11 @@ __global__ void __launch_bounds__(kThreads, kG == 8 ? 4 : 2) topk_kernel(const _
     // logits) are visible.  A no-op for an ordinary launch.
     asm volatile("griddepcontrol.wait;" ::: "memory");
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    // a cluster merge needs the launch's clusters to be the rows
+    if (p.cluster && (int)cluster_nctarank() != p.nchunks) {
+        if (tid == 0) atomicOr(p.err, kDevErrBadLaunch);
+        return;
+    }
     const long long row = blockIdx.x / p.nchunks;
     const int chunk = (int)(blockIdx.x - row * p.nchunks);
     const long long c0 = (long long)chunk * p.chunk;
@@ -337,10 +386,16 @@ __global__ void __launch_bounds__(kThreads, kG == 8 ? 4 : 2) topk_kernel(const _
             }
             if (p.nchunks == 1) return;
             // A row split over several blocks: this chunk contributes an
-            // empty list (padding keys) but still takes the row's ticket, so
-            // that the row's last block merges and resets the ticket, and the
-            // workspace is ready for the next call.  The error bit says the
-            // row's result is not to be used.
+            // empty list (padding keys) but still takes part in the merge
+            // (the cluster's barriers, or the row's ticket, so that the row's
+            // last block merges and resets the ticket and the workspace is
+            // ready for the next call).  The error bit says the row's result
+            // is not to be used.
+            if (p.cluster) {
+                for (int r = tid; r < k; r += kThreads) s.list[r] = 0ull;
+                cluster_merge(p, row, xr, s);
+                return;
+            }
             unsigned long long* kr = p.keys + (row * p.nchunks + chunk) * k;
             for (int r = tid; r < k; r += kThreads) kr[r] = 0ull;
             if (!take_ticket(p, row, s)) return;
@@ -474,6 +529,12 @@ __global__ void __launch_bounds__(kThreads, kG == 8 ? 4 : 2) topk_kernel(const _
             p.out_val[row * k + rank] = key_value(key, xr);
             p.out_idx[row * k + rank] = (int)key_index(key);
         });
+        return;
+    }
+    if (p.cluster) {
+        rank_and_emit(s.cand, cnt, kk, [&](int rank, unsigned long long key) { s.list[rank] = key; });
+        for (int r = kk + tid; r < k; r += kThreads) s.list[r] = 0ull;   // chunk shorter than K
+        cluster_merge(p, row, xr, s);
         return;
     }
     unsigned long long* kr = p.keys + (row * p.nchunks + chunk) * k;
@@ -710,6 +771,59 @@ __global__ void __launch_bounds__(128) topk_warp_kernel(const __grid_constant__ 
 // 5.1 us; 4096 x 1000: 8.8 against 24.0 us) and on rows of at most 512
 // entries (304 x 256: 3.2 against 5.5 us); with fewer, longer rows the block
 // kernel's wider fan-out is faster (64 x 1000: 3.3 against 4.0 us).
+// A row cut into 2 .. 8 chunks merges through a thread-block cluster of its
+// blocks (cluster_merge) when the runtime can place clusters of that many of
+// these blocks; asked once per device, kernel variant, shared-memory size and
+// cluster size.
+template <bool kVec, int kG>
+bool topk_cluster_fits(int dev, int nch, size_t smem) {
+    static std::mutex mu;
+    static std::map<std::tuple<int, size_t, int>, bool> fits;
+    std::lock_guard<std::mutex> lock(mu);
+    const auto key = std::make_tuple(dev, smem, nch);
+    auto it = fits.find(key);
+    if (it != fits.end()) return it->second;
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3((unsigned)nch);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)nch;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, topk_kernel<kVec, kG>, &cfg) != cudaSuccess) {
+        (void)cudaGetLastError();   // not kept: asked again next time
+        return false;
+    }
+    fits.emplace(key, n > 0);
+    return n > 0;
+}
+
+template <bool kVec, int kG>
+cudaError_t launch_topk_block(const TopkParams& p, long long blocks, size_t smem, cudaStream_t stream) {
+    if (!p.cluster) return launch_pdl(topk_kernel<kVec, kG>, dim3((unsigned)blocks), dim3(kThreads), smem, stream, p);
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3((unsigned)blocks);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)p.nchunks;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl_enabled() ? 2 : 1;
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, topk_kernel<kVec, kG>, p);
+    return e == cudaSuccess ? cudaGetLastError() : e;
+}
+
 bool use_warp_kernel(int64_t rows, int64_t cols, int sm_count) {
     return cols <= kWarpMaxCols && (cols <= 512 || rows >= 2LL * sm_count);
 }
@@ -847,8 +961,16 @@ ws_status ws_topk_workspace_init(void* workspace, size_t bytes, cudaStream_t str
 
 ws_status ws_topk(const float* x, int64_t rows, int64_t cols, int32_t k, float* out_val, int32_t* out_idx,
                   void* workspace, size_t workspace_bytes, cudaStream_t stream) {
-    using namespace ws;
-    clear_error();
+    ws::clear_error();
+    return ws::topk_enqueue(x, rows, cols, k, out_val, out_idx, workspace, workspace_bytes, stream, true);
+}
+
+}  // extern "C"
+
+namespace ws {
+
+ws_status topk_enqueue(const float* x, int64_t rows, int64_t cols, int32_t k, float* out_val, int32_t* out_idx,
+                       void* workspace, size_t workspace_bytes, cudaStream_t stream, bool cluster_merge_ok) {
     ws_status st = validate_topk(rows, cols, k);
     if (st != WS_OK) return st;
     if (!x || !out_val || !out_idx) return fail(WS_ERR_INVALID_ARGUMENT, "x, out_val or out_idx is NULL");
@@ -903,18 +1025,23 @@ ws_status ws_topk(const float* x, int64_t rows, int64_t cols, int32_t k, float* 
     p.err = device_error_word();
     // the staged chunk only needs the chunk's length when the chunk is short
     const size_t smem = (size_t)kSharedBytes + (size_t)(p.chunk + 3) / 4 * 16;
+    if (cluster_merge_ok && p.nchunks >= 2 && p.nchunks <= 8)
+        p.cluster = (plan.groups == 16 ? (vec ? topk_cluster_fits<true, 16>(dev, p.nchunks, smem)
+                                              : topk_cluster_fits<false, 16>(dev, p.nchunks, smem))
+                                       : (vec ? topk_cluster_fits<true, 8>(dev, p.nchunks, smem)
+                                              : topk_cluster_fits<false, 8>(dev, p.nchunks, smem)))
+                        ? 1
+                        : 0;
     cudaError_t e;
     if (plan.groups == 16)
-        e = vec ? launch_pdl(topk_kernel<true, 16>, dim3((unsigned)blocks), dim3(kThreads), smem, stream, p)
-                : launch_pdl(topk_kernel<false, 16>, dim3((unsigned)blocks), dim3(kThreads), smem, stream, p);
+        e = vec ? launch_topk_block<true, 16>(p, blocks, smem, stream) : launch_topk_block<false, 16>(p, blocks, smem, stream);
     else
-        e = vec ? launch_pdl(topk_kernel<true, 8>, dim3((unsigned)blocks), dim3(kThreads), smem, stream, p)
-                : launch_pdl(topk_kernel<false, 8>, dim3((unsigned)blocks), dim3(kThreads), smem, stream, p);
+        e = vec ? launch_topk_block<true, 8>(p, blocks, smem, stream) : launch_topk_block<false, 8>(p, blocks, smem, stream);
     if (e != cudaSuccess) return cuda_fail(e, "top-k launch");
     return WS_OK;
 }
 
-}  // extern "C"
+}  // namespace ws
 
 // ---------------------------------------------------------------------------
 // ws_topk_noalloc: the same Top-K for callers that cannot allocate device

@@ -37,10 +37,18 @@ ws_status current_device_info(int* device, const DeviceInfo** info);
 ws_status validate_preprocess(const ws_preprocess_desc* d, int32_t batch);
 ws_status validate_topk(int64_t rows, int64_t cols, int32_t k);
 size_t topk_workspace_size(int64_t rows, int64_t cols, int32_t k);
+// The Top-K launch behind ws_topk (same arguments and checks).  With
+// cluster_merge_ok a row cut into 2 .. 8 chunks merges through a thread-block
+// cluster of its blocks instead of the row ticket, which is faster when the
+// Top-K has the GPU to itself; the lanes pass false, because beside other
+// lanes' kernels a cluster waits for all its block slots in one GPC at once.
+ws_status topk_enqueue(const float* x, int64_t rows, int64_t cols, int32_t k, float* out_val, int32_t* out_idx,
+                       void* workspace, size_t workspace_bytes, cudaStream_t stream, bool cluster_merge_ok);
 
 // Error bits kernels raise instead of waiting forever (see ws_device_error).
 enum : uint32_t {
     kDevErrBulkCopyTimeout = 1u,
+    kDevErrBadLaunch = 2u,   // a kernel's launch did not match its parameters: it did nothing
 };
 // Device address of the error word the calling thread's kernels report
 // into: a lane's own word while that lane enqueues or captures its path (see

@@ -12,6 +12,7 @@ import pytest
 import torch
 
 import synth
+from cudart import memcpy
 from pins import check_topk_invariants
 
 pytestmark = pytest.mark.gpu
@@ -262,6 +263,35 @@ def test_long_row_merge_paths(B, oracle, rows, cols, k):
     got = gpu_topk(B, x, k)
     assert_exact(got, oracle.topk(x, k))
     check_topk_invariants(x, got[0], got[1], k)
+
+
+
+# A row cut into 2 .. 8 chunks merges through a thread-block cluster of its
+# blocks when ws_topk is called directly, and through the row ticket inside
+# a lane (lanes share the GPU with other lanes' kernels).  Both paths against
+# the oracle on the same rows: 8 chunks of 16384, 5 of 8000, 8 of 7500, 2 of
+# 8192, and 2 chunks in the 16384-element kernel.
+@pytest.mark.parametrize("rows,cols", [(32, 131072), (40, 40000), (20, 60000), (64, 16384), (300, 20000)])
+@pytest.mark.parametrize("k", [1, 7, 32])
+def test_cluster_and_ticket_merges(B, oracle, rows, cols, k):
+    from post_processing_gb300 import Lane
+    x = synth.logits_with_ties(rows * 3 + cols + k, rows, cols, frac=0.05)
+    want = oracle.topk(x, k)
+    assert_exact(gpu_topk(B, x, k), want)
+    pre = B.preprocess_desc(16, 16, 16, 16)
+    with Lane(B.lane_desc(pre, 1, rows, cols, k)) as lane:
+        b = lane.buffers
+        torch.cuda.synchronize()
+        memcpy(b.logits, np.ascontiguousarray(x).ctypes.data, x.nbytes)
+        for _ in range(2):   # a replay reuses the row tickets
+            lane.acquire()
+            lane.submit()
+            lane.wait()
+            v = np.empty((rows, k), np.float32)
+            i = np.empty((rows, k), np.int32)
+            memcpy(v.ctypes.data, b.result_val_device, v.nbytes)
+            memcpy(i.ctypes.data, b.result_idx_device, i.nbytes)
+            assert_exact((v, i), want)
 
 
 @pytest.mark.parametrize("rows,cols", [(3, 150001), (33, 131071), (5, 20003)])
