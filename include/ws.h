@@ -78,11 +78,23 @@ const char* ws_last_error(void);
 /* Library version: major * 10000 + minor * 100 + patch. */
 int32_t ws_version(void);
 
+/* Features of the loaded build, a bit mask.  WS_FEATURE_BOUNDS_CHECK: the
+ * checked build (libws_bounds.so, the same sources compiled with
+ * WS_BOUNDS_CHECK), whose preprocess kernels test every index into their
+ * shared stage slots and column-tap table and every source tap; an index out
+ * of range sets device error bit 0x4 (ws_device_error) and is clamped into
+ * its buffer, so the kernel neither traps nor touches memory outside it.  The
+ * checks cost time; the default build has none. */
+#define WS_FEATURE_BOUNDS_CHECK 1
+int32_t ws_build_features(void);
+
 /* Error bits that kernels set on the current device instead of hanging or
  * faulting: 0x1 when a bounded wait (an mbarrier wait on a bulk copy) runs
  * out, 0x2 when a kernel finds its launch inconsistent with its parameters
- * (a cluster shape it was not built for) and does nothing.  Reads the flags
- * synchronously; clears them when clear != 0.  *flags == 0 means none. */
+ * (a cluster shape it was not built for) and does nothing, 0x4 in the checked
+ * build when an index was out of range and was clamped (ws_build_features).
+ * Reads the flags synchronously; clears them when clear != 0.  *flags == 0
+ * means none. */
 ws_status ws_device_error(uint32_t* flags, int32_t clear);
 
 /* Diagnostic of that path: launches one thread that arms an mbarrier for 16

@@ -102,6 +102,7 @@ SIGNATURES = {
     "ws_status_string": (ctypes.c_char_p, [_i32]),
     "ws_last_error": (ctypes.c_char_p, []),
     "ws_version": (_i32, []),
+    "ws_build_features": (_i32, []),
     "ws_device_error": (_i32, [ctypes.POINTER(_u32), _i32]),
     "ws_selftest_wait_timeout": (_i32, [_u32, _vp]),
     "ws_debug_inject_failure": (_i32, [_i32, _i32]),
@@ -141,8 +142,13 @@ SIGNATURES = {
 }
 
 
+def _library_path() -> str:
+    """libws.so, or the checked build libws_bounds.so when WS_BOUNDS_CHECK=1."""
+    return _build.BOUNDS_LIBRARY if os.environ.get("WS_BOUNDS_CHECK") == "1" else _build.LIBRARY
+
+
 def _load():
-    path = _build.LIBRARY
+    path = _library_path()
     if not os.path.exists(path):
         raise ImportError(
             f"{path} is missing: build it first (python -m post_processing_gb300.build or "
@@ -156,7 +162,7 @@ def _load():
 
 
 lib = _load()
-LIBRARY_PATH = _build.LIBRARY
+LIBRARY_PATH = _library_path()
 
 
 class WsError(RuntimeError):
@@ -183,6 +189,13 @@ def ws_last_error() -> str:
 
 def ws_version() -> int:
     return lib.ws_version()
+
+
+WS_FEATURE_BOUNDS_CHECK = 1
+
+
+def ws_build_features() -> int:
+    return lib.ws_build_features()
 
 
 def ws_device_error(clear: bool = False) -> tuple[int, int]:

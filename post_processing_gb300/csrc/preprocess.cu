@@ -169,11 +169,14 @@ __device__ void issue_unit(const PreParams& p, long long u, uint64_t* bar, Stage
     uint32_t na = 0, nb = 0;
     if (lane < nrows) {
         const int y = y0 + lane;
+        const int pl = WS_CHECKED(lane, 0, kMaxBand, p.err);   // the plan's row slot
         int a = -1, b = -1;
         float wy = 0.f;
         if (y >= p.top && y < p.top + p.nh) {
             int j0, j1;
             axis_taps(y - p.top, p.sh, p.nh, j0, j1, wy);
+            j0 = WS_CHECKED(j0, 0, p.sh, p.err);
+            j1 = WS_CHECKED(j1, 0, p.sh, p.err);
             const uint8_t* ra = fr + (long long)j0 * p.row_stride;
             const int oa = (int)((uintptr_t)ra & 15u);
             wa = ra - oa;
@@ -188,10 +191,21 @@ __device__ void issue_unit(const PreParams& p, long long u, uint64_t* bar, Stage
             } else {
                 b = a;
             }
+#ifdef WS_BOUNDS_CHECK
+            // each row's window fits its slot, and the slots fit the stage
+            if (na > (uint32_t)p.slot_bytes || nb > (uint32_t)p.slot_bytes ||
+                (2 * lane + 2) * p.slot_bytes > p.stage_bytes) {
+                atomicOr(p.err, (uint32_t)kDevErrBounds);
+                na = nb = 0;   // nothing copied; the row reads the slot as it is
+                a = b = 2 * (lane % max(1, p.stage_bytes / (2 * p.slot_bytes))) * p.slot_bytes;
+            }
+            a = WS_CHECKED(a, 0, p.stage_bytes - p.row_bytes + 1, p.err);
+            b = WS_CHECKED(b, 0, p.stage_bytes - p.row_bytes + 1, p.err);
+#endif
         }
-        plan->a[lane] = a;
-        plan->b[lane] = b;
-        plan->wy[lane] = wy;
+        plan->a[pl] = a;
+        plan->b[pl] = b;
+        plan->wy[pl] = wy;
     }
     if (lane == 0) {
         plan->frame = frame;
@@ -223,7 +237,7 @@ __device__ __forceinline__ void compute_unit(const PreParams& p, const StagePlan
     const size_t plane = (size_t)p.dh * p.dw;
     OutT* out_b = static_cast<OutT*>(p.dst) + (size_t)plan.frame * 3 * plane;
     for (int it = threadIdx.x; it < items; it += blockDim.x) {
-        const int r = it / groups;
+        const int r = WS_CHECKED(it / groups, 0, kMaxBand, p.err);
         const int x0 = (it - r * groups) * 4;
         const int y = plan.y0 + r;
         float o[3][4];
@@ -234,18 +248,18 @@ __device__ __forceinline__ void compute_unit(const PreParams& p, const StagePlan
 #pragma unroll
                 for (int c = 0; c < 3; ++c) o[c][q] = padn[c];
         } else {
-            const unsigned char* A = stage + sa;
-            const unsigned char* B = stage + plan.b[r];
+            const unsigned char* A = stage + WS_CHECKED(sa, 0, p.stage_bytes - p.row_bytes + 1, p.err);
+            const unsigned char* B = stage + WS_CHECKED(plan.b[r], 0, p.stage_bytes - p.row_bytes + 1, p.err);
             const float wy = plan.wy[r];
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
                 const int x = x0 + q;
                 if (x < p.dw && x >= p.left && x < p.left + p.nw) {
-                    const int2 tap = s_tap[x];
+                    const int2 tap = s_tap[WS_CHECKED(x, 0, p.dw, p.err)];
                     const bool same = (tap.x & kTapSame) != 0;
-                    const int o0 = tap.x & ~kTapSame;
+                    const int o0 = WS_CHECKED(tap.x & ~kTapSame, 0, p.row_bytes - 2, p.err);
                     const float wx = __int_as_float(tap.y);
-                    const int o1 = same ? o0 : o0 + 3;
+                    const int o1 = WS_CHECKED(same ? o0 : o0 + 3, 0, p.row_bytes - 2, p.err);
 #pragma unroll
                     for (int c = 0; c < 3; ++c) {
                         const int sc = p.cmap[c];
@@ -310,7 +324,9 @@ __global__ void __launch_bounds__(kMaxThreads) pre_ring_kernel(const __grid_cons
         int i0 = 0, i1 = 0;
         float wx = 0.f;
         if (x >= p.left && x < p.left + p.nw) axis_taps(x - p.left, p.sw, p.nw, i0, i1, wx);
-        s_tap[x] = make_int2(3 * i0 | (i1 == i0 ? kTapSame : 0), __float_as_int(wx));
+        i0 = WS_CHECKED(i0, 0, p.sw, p.err);
+        i1 = WS_CHECKED(i1, 0, p.sw, p.err);
+        s_tap[WS_CHECKED(x, 0, p.dw, p.err)] = make_int2(3 * i0 | (i1 == i0 ? kTapSame : 0), __float_as_int(wx));
     }
     float padn[3];
 #pragma unroll
@@ -359,6 +375,10 @@ __global__ void __launch_bounds__(256) pre_direct_kernel(const __grid_constant__
     if (in_x && in_y) {
         axis_taps(x - p.left, p.sw, p.nw, i0, i1, wx);
         axis_taps(y - p.top, p.sh, p.nh, j0, j1, wy);
+        i0 = WS_CHECKED(i0, 0, p.sw, p.err);
+        i1 = WS_CHECKED(i1, 0, p.sw, p.err);
+        j0 = WS_CHECKED(j0, 0, p.sh, p.err);
+        j1 = WS_CHECKED(j1, 0, p.sh, p.err);
     }
     for (int b = blockIdx.z; b < batch; b += gridDim.z) {
         float v[3];

@@ -160,6 +160,14 @@ const char* ws_last_error(void) { return ws::t_error.c_str(); }
 
 int32_t ws_version(void) { return 100; }  // 0.1.0
 
+int32_t ws_build_features(void) {
+#ifdef WS_BOUNDS_CHECK
+    return WS_FEATURE_BOUNDS_CHECK;
+#else
+    return 0;
+#endif
+}
+
 ws_status ws_selftest_wait_timeout(uint32_t limit_us, cudaStream_t stream) {
     ws::clear_error();
     int dev;

@@ -49,7 +49,25 @@ ws_status topk_enqueue(const float* x, int64_t rows, int64_t cols, int32_t k, fl
 enum : uint32_t {
     kDevErrBulkCopyTimeout = 1u,
     kDevErrBadLaunch = 2u,   // a kernel's launch did not match its parameters: it did nothing
+    kDevErrBounds = 4u,      // checked build: an index was out of range and was clamped
 };
+
+// Checked build (compiled with WS_BOUNDS_CHECK): an index tested against its
+// buffer; out of range it sets kDevErrBounds in `err` and is clamped into
+// [lo, hi), so nothing outside the buffer is read or written.  Without the
+// macro the check is the index itself.
+#ifdef WS_BOUNDS_CHECK
+__device__ __forceinline__ int checked_index(int i, int lo, int hi, uint32_t* err) {
+    if (i < lo || i >= hi) {
+        atomicOr(err, (uint32_t)kDevErrBounds);
+        i = i < lo ? lo : hi - 1;
+    }
+    return i;
+}
+#define WS_CHECKED(i, lo, hi, err) checked_index((i), (lo), (hi), (err))
+#else
+#define WS_CHECKED(i, lo, hi, err) (i)
+#endif
 // Device address of the error word the calling thread's kernels report
 // into: a lane's own word while that lane enqueues or captures its path (see
 // ErrWordScope), else the current device's word.  Kernels receive it as a

@@ -35,6 +35,19 @@ def test_every_declared_symbol_is_exported(B):
     assert sorted(B.SIGNATURES) == names, "binding and header disagree"
 
 
+def test_checked_build_exports_the_same_symbols(B):
+    # the checked build (libws_bounds.so, compiled with WS_BOUNDS_CHECK) is a
+    # drop-in replacement: same symbols, and it says what it is
+    from post_processing_gb300 import build
+    lib = ctypes.CDLL(build.BOUNDS_LIBRARY)
+    for n in header_functions():
+        assert hasattr(lib, n), f"{n} missing from the checked build"
+    lib.ws_build_features.restype = ctypes.c_int32
+    assert lib.ws_build_features() & B.WS_FEATURE_BOUNDS_CHECK
+    expected = B.WS_FEATURE_BOUNDS_CHECK if os.environ.get("WS_BOUNDS_CHECK") == "1" else 0
+    assert B.ws_build_features() & B.WS_FEATURE_BOUNDS_CHECK == expected
+
+
 def test_struct_layout_matches_c(B, tmp_path):
     structs = {"ws_preprocess_desc": B.ws_preprocess_desc, "ws_lane_desc": B.ws_lane_desc,
                "ws_lane_buffers": B.ws_lane_buffers, "ws_lane_timing": B.ws_lane_timing,

@@ -25,6 +25,19 @@ def B():
     return binding
 
 
+@pytest.fixture(autouse=True)
+def no_index_out_of_range(B):
+    """Under the checked build (WS_BOUNDS_CHECK=1 loads libws_bounds.so)
+    every test must leave the device error word without the bounds bit: no
+    index into a stage slot or the column-tap table, and no source tap, was
+    out of range."""
+    yield
+    if B.ws_build_features() & B.WS_FEATURE_BOUNDS_CHECK:
+        torch.cuda.synchronize()
+        st, flags = B.ws_device_error(True)
+        assert st == B.WS_OK and flags & 0x4 == 0, f"a bounds check failed (device error bits {flags:#x})"
+
+
 def run_gpu(B, frames, sw, sh, dw, dh, *, letterbox=False, norm="mean_std", row_stride=None,
             frame_stride=None, offset=0, pad_value=114, path=0):
     """frames: uint8 [B, H, stride] laid out with the given strides."""
