@@ -405,6 +405,41 @@ def test_detection_lane(B, oracle, result_mode, flags):
                 assert np.array_equal(got["boxes"].view(np.uint32), c["boxes"][keep].view(np.uint32))
 
 
+@pytest.mark.parametrize("batch", [1, 3])
+def test_detection_lane_all_candidates(B, oracle, batch):
+    """The cluster NMS inside a lane's captured graph: every anchor of every
+    image a candidate (8400 -> cap 1024 -> 300 kept), alternating with a
+    typical head (one CTA), over several replays; each against the oracle's NMS
+    of the candidates the GPU decoded."""
+    from post_processing_gb300.api import Lane
+    desc = B.detect_desc()
+    pre = B.preprocess_desc(1280, 720, 640, 640, letterbox=True, norm="scale")
+    d = B.lane_desc(pre, batch, 0, 0, 0, detect=desc)
+    with Lane(d) as lane:
+        buf = lane.buffers
+        for rep in range(4):
+            head = synth.yolo_head(90 + rep, batch, cls_mu=5.0 if rep % 2 == 0 else -8.0)
+            hdev = torch.from_numpy(head).cuda()
+            memcpy(buf.logits, hdev.data_ptr(), head.nbytes)
+            lane.acquire()
+            lane.submit()
+            lane.wait()
+            dets = torch.empty((batch, desc.max_det, 8), dtype=torch.int32, device="cuda")
+            cnts = torch.empty(batch, dtype=torch.int32, device="cuda")
+            memcpy(dets.data_ptr(), buf.detections_device, dets.numel() * 4)
+            memcpy(cnts.data_ptr(), buf.det_count_device, batch * 4)
+            o, k = dets.cpu().numpy(), cnts.cpu().numpy()
+            dec = gpu_decode(B, desc, head)
+            for b in range(batch):
+                c = dec[b]
+                if rep % 2 == 0:
+                    assert len(c["anchor"]) == 8400
+                keep = oracle.nms(c["boxes"], c["f4"], c["cls"], c["anchor"], desc.iou_thr, desc.max_det,
+                                  desc.max_cand)
+                got = unpack(o[b, :k[b]])
+                assert list(got["anchor"]) == [int(c["anchor"][j]) for j in keep], (rep, b)
+
+
 @pytest.mark.parametrize("geom", [
     dict(in_w=40, in_h=24, strides=(8,), reg_max=4, num_classes=3),          # A = 15: scalar scan
     dict(in_w=64, in_h=64, strides=(8, 16, 32, 64), reg_max=1, num_classes=1),  # one bin, one class, 4 levels

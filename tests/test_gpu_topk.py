@@ -124,8 +124,11 @@ def test_misaligned_pointer_scalar_path(B, oracle):
     assert_exact(gpu_topk(B, x, 5, offset=3), oracle.topk(x, 5))
 
 
-def test_workspace_reuse_and_graph_replay(B, oracle):
-    rows, cols, k = 8, 50000, 32
+@pytest.mark.parametrize("rows,cols", [(8, 50000), (32, 40000)], ids=["ticket", "cluster"])
+def test_workspace_reuse_and_graph_replay(B, oracle, rows, cols):
+    # [8,50000]: 16 chunks a row, the ticket merge; [32,40000]: 5 chunks, the
+    # cluster merge, captured as a cluster launch
+    k = 32
     xs = [synth.logits_with_ties(40 + i, rows, cols) for i in range(3)]
     st, n = B.ws_topk_workspace_bytes(rows, cols, k)
     ws = torch.empty(n, dtype=torch.uint8, device="cuda")
