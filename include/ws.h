@@ -235,7 +235,11 @@ ws_status ws_topk_workspace_init(void* workspace, size_t bytes, cudaStream_t str
  * 8192 entries, and every completed call leaves the tickets at zero again.
  * Calls that share a workspace must not overlap on the GPU.  May be NULL when
  * the size is 0.
- * One kernel launch on `stream`.
+ * One kernel launch on `stream`.  A row cut into 2 to 8 chunks is launched
+ * as one thread-block cluster per row when the GPU can place such clusters:
+ * the chunks' lists then meet in shared memory and the workspace is not
+ * touched (lanes use the workspace form, which shares SMs better with other
+ * lanes' kernels).
  * Errors: WS_ERR_INVALID_ARGUMENT (shape, K, NULL pointer, workspace too
  * small), WS_ERR_CUDA (launch failed). */
 ws_status ws_topk(const float* x, int64_t rows, int64_t cols, int32_t k,
@@ -342,7 +346,7 @@ ws_status ws_detect_workspace_init(void* workspace, size_t bytes, cudaStream_t s
  * Deployment note: each DFL logit is an isolated 4-byte read.  With the
  * context limit cudaLimitMaxL2FetchGranularity at 32 bytes, such a read
  * fetches one 32-byte sector instead of two (batch-64 640x640 head on GB300:
- * 194 instead of 241 MB read, 39.5 instead of 42.0 us).  The library does not
+ * 194 instead of 241 MB read, 37.2 instead of 40.4 us).  The library does not
  * change the limit: it is context-wide and also affects other kernels. */
 ws_status ws_detect_decode(const ws_detect_desc* desc, const float* head, int32_t batch,
                            ws_candidate* cand, int32_t* count, cudaStream_t stream);
@@ -352,13 +356,17 @@ ws_status ws_detect_decode(const ws_detect_desc* desc, const float* head, int32_
  * ws_detection [batch][max_det] in keep order; out_count: device int32
  * [batch].  count[b] is reset to zero.  One kernel launch, programmatically
  * dependent on the previous kernel in the stream (it waits for that
- * kernel's results before reading cand / count). */
+ * kernel's results before reading cand / count).  When the GPU can hold the
+ * whole batch that way, each image gets a thread-block cluster of 2, 4 or 8
+ * CTAs of about 210 KB of shared memory each (max_cand 1024): an image with
+ * more than 256 candidates is selected, sorted and compared across the
+ * cluster, the others run on one CTA while the rest leave at once. */
 ws_status ws_detect_nms(const ws_detect_desc* desc, ws_candidate* cand, int32_t* count, int32_t batch,
                         ws_detection* out, int32_t* out_count, cudaStream_t stream);
 
-/* Decode + NMS with the candidates in `workspace`.  Three kernel launches
- * (class scan, DFL boxes, NMS), each after the first a programmatic dependent
- * launch of the one before.
+/* Decode + NMS with the candidates in `workspace`.  Two kernel launches (the
+ * decode, then the NMS as its programmatic dependent), as in
+ * ws_detect_decode and ws_detect_nms.
  * Errors: WS_ERR_INVALID_ARGUMENT (descriptor, pointers, workspace too
  * small), WS_ERR_CUDA (launch failed). */
 ws_status ws_detect(const ws_detect_desc* desc, const float* head, int32_t batch,
