@@ -65,12 +65,12 @@ MAX_LANES = 64
 # Filled from the committed ncu summary under profiles/.
 NCU_TRAFFIC = {
     "b64_1080p_to_224": {
-        "bytes": 185_236_992,
-        "source_sha": "a4330c898ecea40b12c4caef5c38cad52f8e70a6a199a9d321e1daf16bdadb57",
+        "bytes": 185_237_760,
+        "source_sha": "084f6c76b3b2aa2ff2e2df4063500e9f55313b39b9971ca2bf0d538841ae7c27",
     },
     "b8_4k_to_512": {
-        "bytes": 99_776_256,
-        "source_sha": "a4330c898ecea40b12c4caef5c38cad52f8e70a6a199a9d321e1daf16bdadb57",
+        "bytes": 99_373_312,
+        "source_sha": "084f6c76b3b2aa2ff2e2df4063500e9f55313b39b9971ca2bf0d538841ae7c27",
     },
 }
 
