@@ -13,25 +13,29 @@
 //    segments (16 bytes a lane, 8 rows in flight), so the arg-max needs no
 //    merge across warps and no block barrier.  One atomic reserves slots for
 //    the anchors whose best logit clears the threshold (about 2 % of them),
-//    and the same warp then takes their DFL: four lanes per candidate, one
-//    per side, load that side's reg_max logits and take the softmax
-//    expectation.  All tiles stream at once; a warp's scattered DFL loads
-//    overlap the other warps' class rows.
-//  * NMS: one block per image, launched as a programmatic dependent of the
-//    decode kernel so its launch overlaps the decode's tail.  If the image has more
-//    than max_cand candidates, their 64-bit keys (logit order bits, then the
-//    complemented anchor) are held in registers and a radix select
-//    (warp-aggregated histogram counts, early exit once a digit bin closes
-//    the count) keeps the best max_cand.  The survivors are ranked by counting
-//    when there are few, else bitonic-sorted at the next power of two of the
-//    live count (shuffles within a warp's 64 elements, shared memory above).  Every pair's suppression test (same class, IoU > threshold)
-//    is evaluated in parallel into a bit matrix, a thread per (row, 64-bit
+//    numbered in anchor order, and the same warp then takes their DFL: four
+//    lanes per candidate, one per side, load that side's reg_max logits and
+//    take the softmax expectation.  All tiles stream at once; a warp's
+//    scattered DFL loads overlap the other warps' class rows.  With few tiles
+//    a block of four warps splits a tile's classes and then its DFL work.
+//  * NMS: launched as a programmatic dependent of the decode kernel so its
+//    launch overlaps the decode's tail; a thread-block cluster of up to 8
+//    CTAs per image when the batch leaves room.  An image with at most 256
+//    candidates runs on one CTA: each thread ranks its candidate by counting.
+//    Above that, one CTA alone (large batches) takes a radix select of the
+//    best max_cand keys (64-bit: logit order bits, then the complemented
+//    anchor) and a bitonic sort; a cluster shares the work: the radix select
+//    sums its histograms over distributed shared memory, each CTA sorts its
+//    run of the kept keys, a key's rank is its position summed over the
+//    sorted runs, and the suppression matrix is split between the CTAs.
+//    Every pair's suppression test (same class, IoU > threshold) is evaluated
+//    in parallel into a word-major bit matrix, a thread per (row, 64-bit
 //    word), the IoU only where a class-bucket table shows a match, and one
-//    warp walks the sorted list a 64-candidate word at a time,
-//    deciding at each step every candidate that nothing live can still
-//    suppress.  The IoU test is FP32 with every operation rounded
-//    separately (no fused multiply-add), so given the same boxes the
-//    decisions are exactly those of the definition.
+//    warp walks the sorted list a 64-candidate word at a time, deciding at
+//    each step every candidate that nothing live can still suppress.  The IoU
+//    test is FP32 with every operation rounded separately (no fused
+//    multiply-add), so given the same boxes the decisions are exactly those of
+//    the definition.
 #include <algorithm>
 #include <atomic>
 #include <cmath>
