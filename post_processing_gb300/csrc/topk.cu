@@ -12,8 +12,8 @@
 // larger value or, for equal values, a lower index.  Keys are unique, the
 // order is total and the Top-K set is unique: results are bit-exact.
 //
-// One block per (row, chunk of up to 8192 elements; 16384 in rows cut into
-// more than 16 chunks):
+// One block per (row, chunk of up to 8192 elements; 16384 where the 8192 cut
+// would give more than 16 chunks a row or more than two blocks per SM):
 //  1. The chunk is staged in shared memory (one bulk copy when the row is
 //     16-byte aligned, else coalesced loads); each thread keeps the maxima of
 //     its 4-element groups in registers, and their maximum (a "delegate").
@@ -33,7 +33,11 @@
 // merges the sorted lists: its warps fold them into at most eight sorted
 // lists with bitonic merges in registers, and every key of those is ranked by
 // binary searches in all eight at once (its rank is the number of larger
-// keys); ranks below K are the row's result, in rank order.
+// keys); ranks below K are the row's result, in rank order.  On a direct call
+// a row of 2 to 8 chunks is instead one thread-block cluster: the lists stay
+// in the blocks' shared memory and rank 0 reads them through distributed
+// shared memory after one cluster barrier (no ticket, fence or global round
+// trip); lanes keep the ticket, which shares SMs better with other lanes.
 #include <algorithm>
 #include <atomic>
 #include <cmath>
