@@ -504,12 +504,12 @@ __device__ __forceinline__ void nms_cluster_build(const DetParams& p, const NmsS
         unsigned long long prefix = 0, mask = 0;
         uint32_t remaining = (uint32_t)m;
         int pass = 0;
+        // pass 0's histogram is cleared here; each later pass's in the pass
+        // before it (below)
+        for (int d = tid; d < 256; d += kNmsThreads) hbuf[d] = 0;
+        __syncthreads();
         for (int shift = 56; shift >= 0; shift -= 8, ++pass) {
-            // the other CTAs last read this buffer two passes ago, before
-            // the cluster barrier of the previous pass
             uint32_t* h = hbuf + (pass & 1) * 256;
-            for (int d = tid; d < 256; d += kNmsThreads) h[d] = 0;
-            __syncthreads();
             if (in_regs) {
 #pragma unroll
                 for (int r = 0; r < kKeysPerThread; ++r)
@@ -521,6 +521,12 @@ __device__ __forceinline__ void nms_cluster_build(const DetParams& p, const NmsS
                 }
             }
             cluster_sync();
+            // Every CTA has read the other buffer (the previous pass's sums
+            // came before this barrier): clear it for the next pass.  The
+            // barriers below order the clear before the next pass's counts,
+            // and this pass's reads of s.misc before the next pass's
+            // find_digit (after its cluster barrier).
+            for (int d = tid; d < 256; d += kNmsThreads) hbuf[((pass + 1) & 1) * 256 + d] = 0;
             if (tid < 256) s.hist[tid] = sum_over_cluster(h + tid, G);
             __syncthreads();
             if (warp == 0) find_digit(s.hist, remaining, s.misc, lane);
@@ -528,9 +534,7 @@ __device__ __forceinline__ void nms_cluster_build(const DetParams& p, const NmsS
             prefix |= (unsigned long long)s.misc[1] << shift;
             mask |= 0xffull << shift;
             remaining = s.misc[2];
-            const bool done = s.misc[4] != 0;
-            __syncthreads();
-            if (done) break;
+            if (s.misc[4] != 0) break;
         }
         // this CTA's kept keys per warp (s.hist is free after the last pass)
         int wcount = 0;
