@@ -21,7 +21,7 @@
 //  * NMS: launched as a programmatic dependent of the decode kernel so its
 //    launch overlaps the decode's tail; a thread-block cluster of up to 8
 //    CTAs per image when the batch leaves room.  An image with at most 256
-//    candidates runs on one CTA: each thread ranks its candidate by counting.
+//    candidates runs on one CTA: two threads rank each candidate by counting.
 //    Above that, one CTA alone (large batches) takes a radix select of the
 //    best max_cand keys (64-bit: logit order bits, then the complemented
 //    anchor) and a bitonic sort; a cluster shares the work: the radix select
@@ -774,28 +774,41 @@ __global__ void __launch_bounds__(kNmsThreads) detect_nms_kernel(const __grid_co
     unsigned long long* s_m = reinterpret_cast<unsigned long long*>(s_u);
     unsigned long long* s_tab = reinterpret_cast<unsigned long long*>(s_u + p.off_tab);   // [Wl][kBuckets]
     if (!coop) {
-        // Few candidates (the usual case): each thread reads its candidate's
-        // 32-byte record once and keeps it in registers; its rank by counting
-        // then places the record and sets its class-table bit directly.
+        // Few candidates (the usual case): two threads per candidate read its
+        // 32-byte record once and keep it in registers, each counts the larger
+        // keys in half of the list (16-byte loads, summed by a shuffle), and
+        // the rank then places the record and sets its class-table bit
+        // directly.  Two threads per candidate instead of one: batch-1
+        // ws_detect 11.1 -> 10.1 us, batch 64 46.2 -> 45.1 us.
         const bool fast = n <= p.max_cand && n <= kCountSortMax;
         if (fast) {
             float4 box = make_float4(0.f, 0.f, 0.f, 0.f), rest = box;
             unsigned long long key = 0ull;
-            if (tid < n) {
-                const float4* c = reinterpret_cast<const float4*>(cb + tid);
+            const int ci = tid >> 1, part = tid & 1;   // two threads per candidate
+            if (ci < n) {
+                const float4* c = reinterpret_cast<const float4*>(cb + ci);
                 box = __ldcg(c);
                 rest = __ldcg(c + 1);
                 key = ((unsigned long long)order_bits(rest.x) << 32) | (uint32_t)(~(uint32_t)__float_as_int(rest.z));
-                s_key[tid] = key;
+                if (part == 0) s_key[ci] = key;
             }
+            if (tid == 0 && (n & 1)) s_key[n] = 0ull;   // pads the list to pairs (below every key)
             // the histograms of the cap selection are not used on this path, so
             // the match table can be cleared now
             for (int q = tid; q < Wl * kBuckets; q += kNmsThreads) s_tab[q] = 0ull;
             __syncthreads();
-            if (tid < n) {
-                int r = 0;
+            int r = 0;
+            if (ci < n) {
+                const ulonglong2* key2 = reinterpret_cast<const ulonglong2*>(s_key);
+                const int pairs = (n + 1) >> 1;
 #pragma unroll 4
-                for (int j = 0; j < n; ++j) r += s_key[j] > key;
+                for (int q = part; q < pairs; q += 2) {
+                    const ulonglong2 kk = key2[q];
+                    r += (kk.x > key) + (kk.y > key);
+                }
+            }
+            r += __shfl_xor_sync(kFull, r, 1);
+            if (ci < n && part == 0) {
                 s_box[r] = box;
                 s_logit[r] = rest.x;
                 s_cls[r] = __float_as_int(rest.y);
