@@ -422,6 +422,16 @@ struct NmsSmem {
 // The sum of a shared word over the cluster's CTAs 0 .. ranks - 1 (at most
 // kMaxCluster): every remote load is issued before the first is used.
 constexpr int kMaxCluster = 8;
+// Cluster NMS: runs of at least kSplitRun keys on average (2 CTAs an image,
+// up to 1024 keys) are sorted in sub-runs of kSubRun keys; shorter runs are
+// sorted whole, so a key is ranked against G sorted runs.  Measured on GB300
+// (every anchor a candidate, ws_detect): sub-runs of 256 at 2 CTAs an image
+// 130.9 -> 125.5 us at batch 64; sub-runs at 4 or 8 CTAs an image (runs of
+// about 256 and 128 keys, often split one key past the length) cost more
+// ranking lanes than the sort saves (batch 1: 36.6 -> 38.0 us with sub-runs
+// of 128).
+constexpr int kSubRun = 256;
+constexpr int kSplitRun = 384;
 __device__ __forceinline__ uint32_t sum_over_cluster(const uint32_t* p, int ranks) {
     uint32_t v[kMaxCluster];
 #pragma unroll
@@ -456,11 +466,13 @@ __device__ __forceinline__ int count_above(const unsigned long long* run, int le
 //     (exactly m over the cluster), at list positions after the lower ranks'
 //     runs.  With n <= max_cand every CTA reads all n keys, and CTA r's run is
 //     list positions [r m / G, (r + 1) m / G).
-//  2. Order.  Each CTA sorts its run by counting (1 .. 32 threads per key) and
-//     writes it back in place; every CTA then copies the other runs (coalesced
-//     remote loads), so all hold the same list of G sorted runs.  A key's rank
-//     is the number of keys above it summed over the runs (a binary search in
-//     each, G lanes per key); each CTA ranks its own run's keys, then reads the
+//  2. Order.  Each CTA sorts its run, whole or (long runs) in sub-runs of
+//     kSubRun keys, by counting within each (1 .. 32 threads per key), and
+//     writes it back in place;
+//     every CTA then copies the other runs (coalesced remote loads), so all
+//     hold the same list of sorted sub-runs.  A key's rank is the number of
+//     keys above it summed over the sub-runs (a binary search in each, one
+//     lane per sub-run); each CTA ranks its own run's keys, then reads the
 //     other CTAs' ranks, so it knows the candidate slot at every sorted
 //     position, and loads the sorted records from global memory itself.
 //  3. Suppression matrix: each CTA builds the class-bucket table and computes
@@ -598,8 +610,10 @@ __device__ __forceinline__ void nms_cluster_build(const DetParams& p, const NmsS
     }
     __syncthreads();
 
-    // 2. this CTA's run sorted (by counting) into list positions
-    //    bound[rank] .. bound[rank + 1] - 1
+    // 2. this CTA's run, list positions bound[rank] .. bound[rank + 1] - 1,
+    //    sorted whole or in sub-runs of kSubRun keys (by counting within each)
+    const bool split = m / G >= kSplitRun;   // the same in every CTA
+    const int sub = split ? kSubRun : kMaxCand;   // a power of two at least L when the runs are whole
     int off = 0, L = 0;
 #pragma unroll
     for (int d = 0; d < kMaxCluster; ++d)
@@ -619,15 +633,17 @@ __device__ __forceinline__ void nms_cluster_build(const DetParams& p, const NmsS
             const int e = it * per + tid / tpk;
             const bool act = e < L;
             const unsigned long long k = act ? run_key[e] : 0ull;
+            const int sb = e & ~(sub - 1);   // this key's sub-run: sb .. sb + sub - 1
             int r = 0;
             if (act) {
+                const int se = min(L, sb + sub);
 #pragma unroll 4
-                for (int q = part; q < L; q += tpk) r += run_key[q] > k;
+                for (int q = sb + part; q < se; q += tpk) r += run_key[q] > k;
             }
             for (int o = 1; o < tpk; o <<= 1) r += __shfl_xor_sync(kFull, r, o);
             hk[it] = k;
             hx[it] = act ? run_idx[e] : 0;
-            hr[it] = act && part == 0 ? r : -1;
+            hr[it] = act && part == 0 ? sb + r : -1;
         }
         __syncthreads();   // the run is read; the direct case writes it back in place
 #pragma unroll
@@ -652,25 +668,61 @@ __device__ __forceinline__ void nms_cluster_build(const DetParams& p, const NmsS
     unsigned long long* s_tab = reinterpret_cast<unsigned long long*>(s.u + p.off_tab);   // [Wl][kBuckets]
     for (int q = tid; q < Wl * kBuckets; q += kNmsThreads) s_tab[q] = 0ull;   // the staging area is done with
     __syncthreads();
-    // ranks of this run's keys: G consecutive lanes per key, lane c searching run c
+    // Ranks of this run's keys: a key's rank is the number of larger keys summed
+    // over the sorted runs (whole runs: G lanes per key, lane c searching run
+    // c) or over every sorted sub-run of every CTA's run (at most 12: m <= 1024
+    // keys in sub-runs of 256 plus one partial sub-run per CTA; lpk lanes per
+    // key, lane q searching sub-run q).
     int* rank_of = s.keep;         // [m] ranks of this CTA's list positions (read by the other CTAs)
     int* sorted_slot = s.anchor;   // [m] the candidate slot at each sorted position
-    for (int t0 = 0; t0 < L * G; t0 += kNmsThreads) {   // the same trip count in every thread
-        const int t = t0 + tid, e = t / G, c = t - e * G;
-        const bool act = e < L;
-        int r = 0;
-        if (act) {
-            int b0 = 0, b1 = 0;
+    if (!split) {
+        for (int t0 = 0; t0 < L * G; t0 += kNmsThreads) {   // the same trip count in every thread
+            const int t = t0 + tid, e = t / G, c = t - e * G;
+            const bool act = e < L;
+            int r = 0;
+            if (act) {
+                int b0 = 0, b1 = 0;
 #pragma unroll
-            for (int d = 0; d < kMaxCluster; ++d)
-                if (d == c) {
-                    b0 = bound[d];
-                    b1 = bound[d + 1];
-                }
-            r = count_above(s.key + b0, b1 - b0, s.key[off + e]);
+                for (int d = 0; d < kMaxCluster; ++d)
+                    if (d == c) {
+                        b0 = bound[d];
+                        b1 = bound[d + 1];
+                    }
+                r = count_above(s.key + b0, b1 - b0, s.key[off + e]);
+            }
+            for (int o = 1; o < G; o <<= 1) r += __shfl_xor_sync(kFull, r, o);
+            if (act && c == 0) rank_of[off + e] = r;
         }
-        for (int o = 1; o < G; o <<= 1) r += __shfl_xor_sync(kFull, r, o);
-        if (act && c == 0) rank_of[off + e] = r;
+    } else {
+        constexpr int kSubShift = 8;   // log2(kSubRun)
+        static_assert((1 << kSubShift) == kSubRun, "sub-run shift");
+        int nsub[kMaxCluster];
+        int nr = 0;
+#pragma unroll
+        for (int c = 0; c < kMaxCluster; ++c) {
+            nsub[c] = (bound[c + 1] - bound[c] + kSubRun - 1) >> kSubShift;
+            nr += nsub[c];
+        }
+        int lpk = 1;   // lanes per key
+        while (lpk < nr) lpk <<= 1;
+        for (int t0 = 0; t0 < L * lpk; t0 += kNmsThreads) {   // the same trip count in every thread
+            const int t = t0 + tid, e = t / lpk, q = t - e * lpk;
+            int r = 0;
+            if (e < L && q < nr) {
+                int b0 = 0, b1 = 0, j = q;   // sub-run q: of run c, its sub-run j
+#pragma unroll
+                for (int c = 0; c < kMaxCluster; ++c) {
+                    if (j >= 0 && j < nsub[c]) {
+                        b0 = bound[c] + (j << kSubShift);
+                        b1 = min(bound[c + 1], b0 + kSubRun);
+                    }
+                    j -= nsub[c];
+                }
+                r = count_above(s.key + b0, b1 - b0, s.key[off + e]);
+            }
+            for (int o = 1; o < lpk; o <<= 1) r += __shfl_xor_sync(kFull, r, o);
+            if (e < L && q == 0) rank_of[off + e] = r;
+        }
     }
     cluster_sync();
     for (int j = tid; j < m; j += kNmsThreads) {
