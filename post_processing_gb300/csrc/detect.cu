@@ -54,6 +54,7 @@ constexpr int kDecodeAnchors = 128;                    // anchors per decode til
 constexpr int kLaneAnchors = 4;
 constexpr int kWarpScanWarps = 4;                      // warps (tiles) per decode block
 constexpr int kWarpScanLoads = 8;                      // class rows in flight per lane
+constexpr int kWideLoads = 20;                         // ... in the one-block-per-SM split form
 constexpr int kDecodeSplit = 4;                        // warps per tile when tiles are few
 constexpr long long kDecodeSplitTiles = 1100;          // up to this many tiles in all (16 640x640 heads)
 constexpr int kNmsThreads = 512;
@@ -126,8 +127,11 @@ __device__ __forceinline__ void take4(float (&best)[kLaneAnchors], int (&bc)[kLa
 // the candidates' slots; then all kSplit warps share the DFL work.  A warp's
 // chain of dependent loads (class rows, then DFL rounds) is then kSplit times
 // shorter.
-template <bool kVec, int kSplit, int kR>
-__global__ void __launch_bounds__(32 * (kSplit == 1 ? kWarpScanWarps : kSplit), 8)
+// kWide (with kSplit > 1, when the launch has at most one block per SM, e.g.
+// one 640x640 image): each warp loads up to kWideLoads class rows at once, one
+// round trip for a quarter of 80 classes, at up to 128 registers.
+template <bool kVec, int kSplit, int kR, bool kWide = false>
+__global__ void __launch_bounds__(32 * (kSplit == 1 ? kWarpScanWarps : kSplit), kWide ? 4 : 8)
     detect_decode_warp_kernel(const __grid_constant__ DetParams p) {
     constexpr int kTilesPerBlock = kSplit == 1 ? kWarpScanWarps : 1;
     __shared__ int s_loc[kTilesPerBlock][kDecodeAnchors];   // tile offset of each local candidate
@@ -158,15 +162,27 @@ __global__ void __launch_bounds__(32 * (kSplit == 1 ? kWarpScanWarps : kSplit), 
             return live ? __ldg(reinterpret_cast<const float4*>(col + (size_t)c * p.A))
                         : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
         };
-        int c = cbeg;
-        for (; c + kWarpScanLoads <= cend; c += kWarpScanLoads) {
-            float4 v4[kWarpScanLoads];
+        if constexpr (kWide) {
+            for (int c = cbeg; c < cend; c += kWideLoads) {
+                float4 v4[kWideLoads];
 #pragma unroll
-            for (int u = 0; u < kWarpScanLoads; ++u) v4[u] = load(c + u);
+                for (int u = 0; u < kWideLoads; ++u)
+                    v4[u] = c + u < cend ? load(c + u) : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
 #pragma unroll
-            for (int u = 0; u < kWarpScanLoads; ++u) take4(best, bc, v4[u], c + u);
+                for (int u = 0; u < kWideLoads; ++u)
+                    if (c + u < cend) take4(best, bc, v4[u], c + u);
+            }
+        } else {
+            int c = cbeg;
+            for (; c + kWarpScanLoads <= cend; c += kWarpScanLoads) {
+                float4 v4[kWarpScanLoads];
+#pragma unroll
+                for (int u = 0; u < kWarpScanLoads; ++u) v4[u] = load(c + u);
+#pragma unroll
+                for (int u = 0; u < kWarpScanLoads; ++u) take4(best, bc, v4[u], c + u);
+            }
+            for (; c < cend; ++c) take4(best, bc, load(c), c);
         }
-        for (; c < cend; ++c) take4(best, bc, load(c), c);
     } else {
 #pragma unroll 2
         for (int c = cbeg; c < cend; ++c) {
@@ -1200,13 +1216,28 @@ std::atomic<bool> g_nms_attr_set[64];
 bool decode_split(int tiles, int32_t batch) { return (long long)tiles * batch <= kDecodeSplitTiles; }
 
 ws_status launch_decode(DetParams p, int32_t batch, cudaStream_t stream) {
+    int dev;
+    const DeviceInfo* info;
+    const ws_status st = current_device_info(&dev, &info);
+    if (st != WS_OK) return st;
     const int tiles = (int)((p.A + kDecodeAnchors - 1) / kDecodeAnchors);
     const bool vec = p.A % 4 == 0 && (uintptr_t)p.head % 16 == 0;
     // one kernel, a programmatic dependent of whatever wrote the head
     cudaError_t e;
     // the DFL bins of a side in registers: 16 (the usual reg_max) or up to 32
     const bool r16 = p.R <= 16;
-    if (decode_split(tiles, batch)) {
+    if ((long long)tiles * batch <= info->sm_count) {
+        // at most one block per SM: every warp loads its classes' rows at once.
+        // Measured on one 640x640 image (a detection lane, GPU p50): 20.8 ->
+        // 19.5 us; with more blocks the wider registers cost occupancy (batch
+        // 16: 15.7 -> 17.3 us) and back-to-back calls overlap less (batch 4:
+        // 11.5 -> 11.85 us), so those keep the narrower forms.
+        const dim3 grid((unsigned)tiles, (unsigned)batch), block(32 * kDecodeSplit);
+        e = vec ? (r16 ? launch_pdl(detect_decode_warp_kernel<true, kDecodeSplit, 16, true>, grid, block, 0, stream, p)
+                       : launch_pdl(detect_decode_warp_kernel<true, kDecodeSplit, kMaxRegMax, true>, grid, block, 0, stream, p))
+                : (r16 ? launch_pdl(detect_decode_warp_kernel<false, kDecodeSplit, 16, true>, grid, block, 0, stream, p)
+                       : launch_pdl(detect_decode_warp_kernel<false, kDecodeSplit, kMaxRegMax, true>, grid, block, 0, stream, p));
+    } else if (decode_split(tiles, batch)) {
         const dim3 grid((unsigned)tiles, (unsigned)batch), block(32 * kDecodeSplit);
         e = vec ? (r16 ? launch_pdl(detect_decode_warp_kernel<true, kDecodeSplit, 16>, grid, block, 0, stream, p)
                        : launch_pdl(detect_decode_warp_kernel<true, kDecodeSplit, kMaxRegMax>, grid, block, 0, stream, p))
