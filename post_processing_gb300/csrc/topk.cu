@@ -14,9 +14,11 @@
 //
 // One block per (row, chunk of up to 8192 elements; 16384 where the 8192 cut
 // would give more than 16 chunks a row or more than two blocks per SM):
-//  1. The chunk is staged in shared memory (one bulk copy when the row is
-//     16-byte aligned, else coalesced loads); each thread keeps the maxima of
-//     its 4-element groups in registers, and their maximum (a "delegate").
+//  1. The chunk is staged in shared memory (four bulk copies of consecutive
+//     quarters when the row is 16-byte aligned, each with its own barrier,
+//     else coalesced loads); each thread keeps the maxima of its 4-element
+//     groups in registers, and their maximum (a "delegate"), reading each
+//     quarter as soon as it has landed.
 //  2. Threshold without sorting: each warp finds the ceil(K/8)-th largest of
 //     its 32 delegates with warp max-reductions; t = the minimum over warps.
 //     Every warp then owns ceil(K/8) distinct elements >= t, so at least K
@@ -35,10 +37,11 @@
 // lists with bitonic merges in registers, and every key of those is ranked by
 // binary searches in all eight at once (its rank is the number of larger
 // keys); ranks below K are the row's result, in rank order.  On a direct call
-// a row of 2 to 8 chunks is instead one thread-block cluster: the lists stay
-// in the blocks' shared memory and rank 0 reads them through distributed
-// shared memory after one cluster barrier (no ticket, fence or global round
-// trip); lanes keep the ticket, which shares SMs better with other lanes.
+// a row of 2 to 8 chunks is instead one thread-block cluster: each block
+// stores its list into rank 0's shared memory (distributed shared memory),
+// and one cluster barrier hands rank 0 all of them (no ticket, fence or
+// global round trip); lanes keep the ticket, which shares SMs better with
+// other lanes.
 #include <algorithm>
 #include <atomic>
 #include <cmath>
@@ -121,7 +124,6 @@ __device__ __forceinline__ unsigned long long merge_top32(unsigned long long a, 
 struct __align__(16) Shared {
     unsigned long long cand[kCap + kThreads];   // candidates, then one spare slot per thread
     unsigned long long wlist[kWarps][32];       // merge: each warp's top-K list
-    unsigned long long list[kMaxK];             // cluster merge: this chunk's sorted list
     unsigned long long red[kWarps];
     uint32_t hist[256];
     uint32_t warp_t[kWarps];
@@ -282,44 +284,44 @@ __device__ __forceinline__ void merge_chunk_lists(const TopkParams& p, long long
     }
 }
 
-// The row's blocks as one thread-block cluster (at most 8 chunks): each
-// chunk's sorted list stays in its block's shared memory (s.list), and one
-// cluster barrier replaces the ticket.  Rank 0 reads the lists through
-// distributed shared memory (warp c takes chunk c's list), lets the other
-// blocks leave, and ranks every key as merge_chunk_lists does.
+// The row's blocks as one thread-block cluster (at most 8 chunks).  Every
+// block arrives once on the cluster barrier as it starts; once that phase is
+// complete (cluster_push_begin) all of the cluster's blocks exist, and each
+// block stores its chunk's sorted list straight into rank 0's shared memory
+// (s.wlist[chunk], zero keys past the list) with remote stores.  One cluster
+// barrier (release / acquire) then hands rank 0 every list, with no ticket,
+// fence, global round trip or remote load; the other blocks leave, and rank
+// 0 ranks every key as merge_chunk_lists does.
+__device__ __forceinline__ uint32_t cluster_push_begin(int chunk, Shared& s) {
+    cluster_wait();   // the phase every block arrived on at its start
+    return cluster_map(&s.wlist[chunk][0], 0u);
+}
+
 __device__ __forceinline__ void cluster_merge(const TopkParams& p, long long row, const float* xr, Shared& s) {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int k = p.k;
-    cluster_sync();   // every chunk's list is written
+    const int k = p.k, nch = p.nchunks;
     const bool lead = cluster_ctarank() == 0;
-    unsigned long long acc = 0ull;
-    if (lead) {
-        if (warp < p.nchunks && lane < k) acc = ld_cluster_u64(cluster_map(&s.list[lane], (uint32_t)warp));
-        s.wlist[warp][lane] = acc;   // zero keys for warps without a list
+    if (lead)   // zero keys for the rows of absent chunks
+        for (int i = nch * 32 + tid; i < kWarps * 32; i += kThreads) s.wlist[i >> 5][i & 31] = 0ull;
+    cluster_arrive();
+    cluster_wait();   // every list is in rank 0's shared memory
+    if (!lead) return;
+    const unsigned long long acc = s.wlist[warp][lane];
+    if (acc == 0ull) return;
+    int lo[kWarps];
+#pragma unroll
+    for (int c = 0; c < kWarps; ++c) lo[c] = 0;
+#pragma unroll
+    for (int step = 16; step >= 1; step >>= 1)
+#pragma unroll
+        for (int c = 0; c < kWarps; ++c) lo[c] += s.wlist[c][lo[c] + step - 1] > acc ? step : 0;
+    int rank = 0;
+#pragma unroll
+    for (int c = 0; c < kWarps; ++c) rank += lo[c] + (s.wlist[c][lo[c]] > acc ? 1 : 0);
+    if (rank < k) {
+        p.out_val[row * k + rank] = key_value(acc, xr);
+        p.out_idx[row * k + rank] = (int)key_index(acc);
     }
-    cluster_arrive();   // rank 0 has its copies: the other blocks' shared memory may go
-    if (!lead) {
-        cluster_wait();
-        return;
-    }
-    __syncthreads();
-    if (acc != 0ull) {
-        int lo[kWarps];
-#pragma unroll
-        for (int c = 0; c < kWarps; ++c) lo[c] = 0;
-#pragma unroll
-        for (int step = 16; step >= 1; step >>= 1)
-#pragma unroll
-            for (int c = 0; c < kWarps; ++c) lo[c] += s.wlist[c][lo[c] + step - 1] > acc ? step : 0;
-        int rank = 0;
-#pragma unroll
-        for (int c = 0; c < kWarps; ++c) rank += lo[c] + (s.wlist[c][lo[c]] > acc ? 1 : 0);
-        if (rank < k) {
-            p.out_val[row * k + rank] = key_value(acc, xr);
-            p.out_idx[row * k + rank] = (int)key_index(acc);
-        }
-    }
-    cluster_wait();
 }
 
 // kG: 4-element groups a thread (8 for chunks of up to 8192 elements, 16 for
@@ -329,17 +331,35 @@ __global__ void __launch_bounds__(kThreads, kG == 8 ? 4 : 2) topk_kernel(const _
     extern __shared__ __align__(128) unsigned char dsmem[];
     Shared& s = *reinterpret_cast<Shared*>(dsmem);
     float* sx = reinterpret_cast<float*>(dsmem + kSharedBytes);   // [chunk] the staged chunk
-    __shared__ uint64_t bar;
+    // 4 parts of the staged chunk, one bulk copy and one barrier each
+    constexpr int kParts = 4;
+    constexpr int kPartGroups = kG / kParts;                 // a thread's 4-element groups in one part
+    constexpr int kPartElems = kThreads * 4 * kPartGroups;   // elements of one part
+    __shared__ uint64_t bar[kParts];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    if (kVec) {
+        // The part barriers are initialised, and the block barrier makes
+        // that visible, before the wait below: on a programmatic launch this
+        // overlaps the previous grid's tail.
+        if (tid == 0) {
+#pragma unroll
+            for (int q = 0; q < kParts; ++q) mbar_init(&bar[q], 1);
+            fence_mbar_init();
+        }
+        __syncthreads();
+    }
     // Launched as a programmatic dependent of the previous kernel on the
     // stream: wait here until that grid has finished and its writes (the
     // logits) are visible.  A no-op for an ordinary launch.
     asm volatile("griddepcontrol.wait;" ::: "memory");
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     if (tid == 0) s.cnt = 0u;   // the candidate counter (read after the next barriers)
     // a cluster merge needs the launch's clusters to be the rows
-    if (p.cluster && (int)cluster_nctarank() != p.nchunks) {
-        if (tid == 0) atomicOr(p.err, kDevErrBadLaunch);
-        return;
+    if (p.cluster) {
+        if ((int)cluster_nctarank() != p.nchunks) {
+            if (tid == 0) atomicOr(p.err, kDevErrBadLaunch);
+            return;
+        }
+        cluster_arrive_relaxed();   // this block has started (see cluster_merge)
     }
     const long long row = blockIdx.x / p.nchunks;
     const int chunk = (int)(blockIdx.x - row * p.nchunks);
@@ -348,44 +368,23 @@ __global__ void __launch_bounds__(kThreads, kG == 8 ? 4 : 2) topk_kernel(const _
     const float* xr = p.x + row * p.cols;
     const int k = p.k;
 
-    // 1. stage the chunk in shared memory: one bulk copy (16-byte aligned
-    // rows), else coalesced loads.
+    // 1. stage the chunk in shared memory: four bulk copies of consecutive
+    // parts (16-byte aligned rows), each completing its own barrier, else
+    // coalesced loads.  The delegate pass below reads each part as soon as
+    // it has landed, so its shared-memory reads overlap the later parts'
+    // transfer.
     if (kVec) {
         if (tid == 0) {
-            mbar_init(&bar, 1);
-            fence_mbar_init();
-            mbar_arrive_expect_tx(&bar, (uint32_t)n * 4u);
-            bulk_g2s(sx, xr + c0, (uint32_t)n * 4u, &bar);
-        }
-        // One thread polls the barrier; the others sleep in the block barrier
-        // (which costs no issue slots) instead of spinning beside it.
-        const bool ok = tid == 0 ? mbar_wait_bounded(&bar, 0, kWaitLimitNs) : true;
-        if (__syncthreads_or(!ok)) {
-            if (tid == 0) {
-                atomicOr(p.err, kDevErrBulkCopyTimeout);
-                mbar_wait_bounded(&bar, 0, kWaitLimitNs);   // let the copy land before leaving
+#pragma unroll
+            for (int q = 0; q < kParts; ++q) {
+                const int e0 = q * kPartElems;
+                if (e0 < n) {
+                    const uint32_t bytes = (uint32_t)min(kPartElems, n - e0) * 4u;
+                    mbar_arrive_expect_tx(&bar[q], bytes);
+                    bulk_g2s(sx + e0, xr + c0 + e0, bytes, &bar[q]);
+                }
             }
-            if (p.nchunks == 1) return;
-            // A row split over several blocks: this chunk contributes an
-            // empty list (padding keys) but still takes part in the merge
-            // (the cluster's barriers, or the row's ticket, so that the row's
-            // last block merges and resets the ticket and the workspace is
-            // ready for the next call).  The error bit says the row's result
-            // is not to be used.
-            if (p.cluster) {
-                for (int r = tid; r < k; r += kThreads) s.list[r] = 0ull;
-                cluster_merge(p, row, xr, s);
-                return;
-            }
-            unsigned long long* kr = p.keys + (row * p.nchunks + chunk) * k;
-            for (int r = tid; r < k; r += kThreads) kr[r] = 0ull;
-            if (!take_ticket(p, row, s)) return;
-            merge_chunk_lists(p, row, xr, s);
-            return;
         }
-        // The phase is complete: each thread's own (immediately satisfied)
-        // wait is its acquire of the bytes the bulk copy wrote.
-        if (tid != 0) mbar_wait_bounded(&bar, 0, kWaitLimitNs);
     } else {
         for (int i = tid; i < n; i += kThreads) sx[i] = __ldcs(xr + c0 + i);
         __syncthreads();
@@ -393,7 +392,11 @@ __global__ void __launch_bounds__(kThreads, kG == 8 ? 4 : 2) topk_kernel(const _
     // Thread tid owns the 4-element groups tid, tid + 256, ... of the chunk
     // (the last group padded with NaN), and keeps each group's maximum in a
     // register: the candidate pass then re-reads only the rare groups whose
-    // maximum reaches the threshold.
+    // maximum reaches the threshold.  Group g * 256 + tid lies in part
+    // g / kPartGroups; a thread's successful wait on that part's barrier is
+    // its acquire of the bytes the part's copy wrote.  A wait that runs out
+    // leaves ok false; the block leaves through the error path at the
+    // threshold's barrier (the values read meanwhile are not used).
     const int ng = (n + 3) >> 2;
     const float qnan = __int_as_float(0x7fffffff);
     const float4* sx4 = reinterpret_cast<const float4*>(sx);
@@ -403,10 +406,15 @@ __global__ void __launch_bounds__(kThreads, kG == 8 ? 4 : 2) topk_kernel(const _
         return make_float4(e < n ? sx[e] : qnan, e + 1 < n ? sx[e + 1] : qnan, e + 2 < n ? sx[e + 2] : qnan,
                            e + 3 < n ? sx[e + 3] : qnan);
     };
+    bool ok = true;
     float gmax[kG];
     float dm = -INFINITY;   // the delegate: fmaxf skips NaN, so a NaN counts as -inf
 #pragma unroll
     for (int g = 0; g < kG; ++g) {
+        if (kVec && g % kPartGroups == 0) {
+            const int q = g / kPartGroups;
+            if (ok && q * kPartElems < n) ok = mbar_wait_bounded(&bar[q], 0, kWaitLimitNs);
+        }
         const int i = g * kThreads + tid;
         float mx = qnan;
         if (i < ng) {
@@ -429,7 +437,33 @@ __global__ void __launch_bounds__(kThreads, kG == 8 ? 4 : 2) topk_kernel(const _
         if (lane == __ffs(who) - 1) d = 0;
     }
     if (lane == 0) s.warp_t[warp] = tw;
-    __syncthreads();
+    if (__syncthreads_or(!ok)) {
+        // A part's copy did not land in time.
+        if (tid == 0) {
+            atomicOr(p.err, kDevErrBulkCopyTimeout);
+#pragma unroll
+            for (int q = 0; q < kParts; ++q)   // let the copies land before leaving
+                if (q * kPartElems < n) mbar_wait_bounded(&bar[q], 0, kWaitLimitNs);
+        }
+        if (p.nchunks == 1) return;
+        // A row split over several blocks: this chunk contributes an empty
+        // list (padding keys) but still takes part in the merge (the
+        // cluster's barriers, or the row's ticket, so that the row's last
+        // block merges and resets the ticket and the workspace is ready for
+        // the next call).  The error bit says the row's result is not to be
+        // used.
+        if (p.cluster) {
+            const uint32_t dst = cluster_push_begin(chunk, s);
+            if (tid < 32) st_cluster_u64(dst + 8u * tid, 0ull);
+            cluster_merge(p, row, xr, s);
+            return;
+        }
+        unsigned long long* kr = p.keys + (row * p.nchunks + chunk) * k;
+        for (int r = tid; r < k; r += kThreads) kr[r] = 0ull;
+        if (!take_ticket(p, row, s)) return;
+        merge_chunk_lists(p, row, xr, s);
+        return;
+    }
     // Warps that hold kw delegates each vouch for kw elements >= their own
     // threshold; the minimum over enough such warps is a valid threshold.
     uint32_t t = 0xffffffffu;
@@ -516,8 +550,9 @@ __global__ void __launch_bounds__(kThreads, kG == 8 ? 4 : 2) topk_kernel(const _
         return;
     }
     if (p.cluster) {
-        rank_and_emit(s.cand, cnt, kk, [&](int rank, unsigned long long key) { s.list[rank] = key; });
-        for (int r = kk + tid; r < k; r += kThreads) s.list[r] = 0ull;   // chunk shorter than K
+        const uint32_t dst = cluster_push_begin(chunk, s);
+        rank_and_emit(s.cand, cnt, kk, [&](int rank, unsigned long long key) { st_cluster_u64(dst + 8u * rank, key); });
+        for (int r = kk + tid; r < 32; r += kThreads) st_cluster_u64(dst + 8u * r, 0ull);   // past the list
         cluster_merge(p, row, xr, s);
         return;
     }

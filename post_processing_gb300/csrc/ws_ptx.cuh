@@ -86,6 +86,8 @@ __device__ __forceinline__ uint32_t cluster_nctarank() {
 // before the arrival against reads after the wait.
 __device__ __forceinline__ void cluster_arrive() { asm volatile("barrier.cluster.arrive.release;" ::: "memory"); }
 __device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.acquire;" ::: "memory"); }
+// An arrival that orders no memory (e.g. "this CTA has started").
+__device__ __forceinline__ void cluster_arrive_relaxed() { asm volatile("barrier.cluster.arrive.relaxed;" ::: "memory"); }
 __device__ __forceinline__ void cluster_sync() {
     cluster_arrive();
     cluster_wait();

@@ -273,8 +273,11 @@ def test_long_row_merge_paths(B, oracle, rows, cols, k):
 # blocks when ws_topk is called directly, and through the row ticket inside
 # a lane (lanes share the GPU with other lanes' kernels).  Both paths against
 # the oracle on the same rows: 8 chunks of 16384, 5 of 8000, 8 of 7500, 2 of
-# 8192, and 2 chunks in the 16384-element kernel.
-@pytest.mark.parametrize("rows,cols", [(32, 131072), (40, 40000), (20, 60000), (64, 16384), (300, 20000)])
+# 8192, and 2 chunks in the 16384-element kernel.  Longer rows take the
+# ticket on both paths, checked here inside lanes and replayed: 16 chunks of
+# 8192, 16 of 6252, 42 of 16000 and 49 of 16052 (two fold rounds).
+@pytest.mark.parametrize("rows,cols", [(32, 131072), (40, 40000), (20, 60000), (64, 16384), (300, 20000),
+                                       (8, 131072), (2, 100000), (1, 672000), (1, 786433)])
 @pytest.mark.parametrize("k", [1, 7, 32])
 def test_cluster_and_ticket_merges(B, oracle, rows, cols, k):
     from post_processing_gb300 import Lane
