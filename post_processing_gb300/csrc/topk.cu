@@ -19,10 +19,11 @@
 //     else coalesced loads); each thread keeps the maxima of its 4-element
 //     groups in registers, and their maximum (a "delegate"), reading each
 //     quarter as soon as it has landed.
-//  2. Threshold without sorting: each warp finds the ceil(K/8)-th largest of
-//     its 32 delegates with warp max-reductions; t = the minimum over warps.
-//     Every warp then owns ceil(K/8) distinct elements >= t, so at least K
-//     elements of the chunk are >= t and the chunk's Top-K are all among them.
+//  2. Threshold without sorting: each warp finds the kw-th largest of its
+//     delegates with warp max-reductions (kw = ceil(K/8) when all 256
+//     threads hold one, more on short chunks); t = the minimum over the warps
+//     that hold kw.  Those warps own kw distinct elements >= t each, at least
+//     K in all, so the chunk's Top-K are all among the elements >= t.
 //  3. Elements >= t (typically a few dozen) are appended to shared memory
 //     (slots from one shared counter).
 //  4. Each candidate's rank is the number of candidates with a larger key
@@ -79,6 +80,7 @@ struct TopkParams {
     unsigned long long* keys;     // [rows][nchunks][k]
     uint32_t* err;                // device error word
     int cluster;                  // 1: a row's blocks form a thread-block cluster and merge through it
+    int kw, kw_last;              // delegates each warp vouches for: full chunks, the row's last chunk
 };
 
 __device__ __forceinline__ uint32_t order_bits(float f) {
@@ -428,8 +430,9 @@ __global__ void __launch_bounds__(kThreads, kG == 8 ? 4 : 2) topk_kernel(const _
     }
     uint32_t d = tid < ng ? order_bits(dm) : 0u;   // threads without elements have no delegate
 
-    // 2. threshold: min over warps of each warp's ceil(K/warps)-th largest delegate
-    const int kw = (k + kWarps - 1) / kWarps;
+    // 2. threshold: min over warps of each warp's kw-th largest delegate
+    // (kw from delegate_rounds() on the host, by the chunk's length).
+    const int kw = chunk + 1 == p.nchunks ? p.kw_last : p.kw;
     uint32_t tw = 0;
     for (int r = 0; r < kw; ++r) {
         const uint32_t m = __reduce_max_sync(kFull, d);
@@ -909,6 +912,28 @@ int blocks_per_row(int64_t rows, int64_t cols, int sm_count) {
     return (int)std::min<long long>(cap, std::max<long long>(base, want));
 }
 
+// Delegates each warp of a block vouches for in the threshold step, for a
+// chunk of n elements: the least kw for which the warps holding at least kw
+// delegates (a thread holds one if it has an element) own K elements between
+// them.  ceil(K/8) when all 256 threads hold a delegate (n >= 1024); more on
+// shorter chunks, where fewer warps hold delegates: a 576-element chunk has
+// four full warps and one of 16, so kw = 7 for K = 32, where ceil(K/8) = 4
+// would leave too few vouching warps and make every element a candidate
+// (ranked against every other: [1,576] took 14.5 us instead of 2.9).
+// Chunks too short for any kw fall back to every element being a candidate.
+int delegate_rounds(long long n, int k) {
+    const long long ng = (n + 3) / 4;
+    const int full = (int)std::min<long long>(kWarps, ng / 32);   // warps whose 32 threads hold one
+    const int part = ng < kThreads ? (int)(ng % 32) : 0;           // delegates of the one partial warp
+    int kw = (k + kWarps - 1) / kWarps;
+    if ((full + (part >= kw ? 1 : 0)) * kw < k) {
+        const int w = full + (part > 0 ? 1 : 0);
+        kw = (k + w - 1) / w;
+        if (part > 0 && part < kw && full > 0) kw = (k + full - 1) / full;
+    }
+    return std::min(kw, 32);
+}
+
 // Chunk length for a number of blocks per row: a multiple of 4 elements.
 int chunk_len(int64_t cols, int nchunks, int max_chunk) {
     const long long c = (cols + nchunks - 1) / nchunks;
@@ -1021,6 +1046,8 @@ ws_status topk_enqueue(const float* x, int64_t rows, int64_t cols, int32_t k, fl
     const ChunkPlan plan = plan_chunks(rows, cols, info->sm_count);
     p.nchunks = plan.nchunks;
     p.chunk = plan.chunk;
+    p.kw = delegate_rounds(std::min<long long>(plan.chunk, cols), k);
+    p.kw_last = delegate_rounds(cols - (long long)(plan.nchunks - 1) * plan.chunk, k);
     p.out_val = out_val;
     p.out_idx = out_idx;
     if (need > 0) {

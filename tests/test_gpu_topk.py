@@ -61,8 +61,8 @@ def test_workload_parity(B, oracle, name):
     assert_exact(gpu_topk(B, x, w["k"]), oracle.topk(x, w["k"]))
 
 
-@pytest.mark.parametrize("cols", [1, 2, 3, 31, 32, 33, 100, 1000, 4097, 8191, 8192, 8193, 16384, 20001,
-                                  65536 + 3])
+@pytest.mark.parametrize("cols", [1, 2, 3, 31, 32, 33, 100, 576, 700, 911, 913, 1000, 4097, 8191, 8192, 8193,
+                                  16384, 20001, 65536 + 3])
 @pytest.mark.parametrize("k", [1, 5, 32])
 def test_lengths(B, oracle, cols, k):
     if k > cols:
