@@ -30,7 +30,9 @@
 //     (keys are unique, so ranks are distinct): rank < K is written in place.
 //  If more than 2048 elements pass the threshold (adversarial inputs, e.g. a
 //  constant row), an exact radix select on the 64-bit keys (8 passes of 8
-//  bits, warp-aggregated shared histograms) finds the K-th key instead.
+//  bits, warp-aggregated shared histograms) finds the K-th key instead; with
+//  385 to 2048 candidates (many ties at the top) the same select runs over
+//  the candidates, and only the K keys at or above the K-th are ranked.
 // Rows longer than one chunk: every chunk writes its K keys, sorted, to a
 // workspace; the last block of the row to finish (an atomic ticket, reset by
 // that block so the workspace is ready for the next call or graph replay)
@@ -61,6 +63,7 @@ constexpr int kWarps = kThreads / 32;
 constexpr int kVpt = 32;                       // values per thread
 constexpr int kChunk = kThreads * kVpt;        // 8192 elements per block
 constexpr int kCap = 2048;                     // shared candidate capacity
+constexpr int kRankMax = 384;                  // candidates ranked by counting; more take a radix select first
 constexpr int kMaxK = 32;
 constexpr int kBigChunk = 2 * kChunk;          // 16384: the chunk of rows cut into many chunks
 constexpr int kFoldBatch = 6;                  // chunk lists a warp loads per round of the merge
@@ -532,6 +535,7 @@ __global__ void __launch_bounds__(kThreads, kG == 8 ? 4 : 2) topk_kernel(const _
     __syncthreads();
     uint32_t cnt = s.cnt;
     const int kk = min(k, n);
+    const unsigned long long* ck = s.cand;   // the keys step 4 ranks
     if (cnt > kCap) {
         // exact fallback: radix select over the chunk's keys
         auto key_at = [&](int i) { return make_key(order_bits(sx[i]), (uint32_t)(c0 + i)); };
@@ -544,11 +548,26 @@ __global__ void __launch_bounds__(kThreads, kG == 8 ? 4 : 2) topk_kernel(const _
         }
         __syncthreads();
         cnt = s.cnt;
+    } else if (cnt > (uint32_t)kRankMax) {
+        // Many candidates (ties at the top of the chunk): ranking each against
+        // all is quadratic (1500 candidates of an 8000-entry row took 68 us).
+        // The kk-th largest candidate by radix select instead, and the kk keys
+        // at or above it, copied past the candidates, are ranked.
+        const unsigned long long kth = block_kth_largest([&](int i) { return s.cand[i]; }, (int)cnt, kk, s);
+        if (tid == 0) s.cnt = 0;
+        __syncthreads();
+        for (uint32_t i = tid; i < cnt; i += kThreads) {
+            const unsigned long long key = s.cand[i];
+            if (key >= kth) s.cand[kCap + atomicAdd(&s.cnt, 1u)] = key;   // exactly kk keys
+        }
+        __syncthreads();
+        cnt = s.cnt;
+        ck = s.cand + kCap;
     }
 
     // 4. rank and emit
     if (p.nchunks == 1) {
-        rank_and_emit(s.cand, cnt, kk, [&](int rank, unsigned long long key) {
+        rank_and_emit(ck, cnt, kk, [&](int rank, unsigned long long key) {
             p.out_val[row * k + rank] = key_value(key, xr);
             p.out_idx[row * k + rank] = (int)key_index(key);
         });
@@ -556,13 +575,13 @@ __global__ void __launch_bounds__(kThreads, kG == 8 ? 4 : 2) topk_kernel(const _
     }
     if (p.cluster) {
         const uint32_t dst = cluster_push_begin(chunk, s);
-        rank_and_emit(s.cand, cnt, kk, [&](int rank, unsigned long long key) { st_cluster_u64(dst + 8u * rank, key); });
+        rank_and_emit(ck, cnt, kk, [&](int rank, unsigned long long key) { st_cluster_u64(dst + 8u * rank, key); });
         for (int r = kk + tid; r < 32; r += kThreads) st_cluster_u64(dst + 8u * r, 0ull);   // past the list
         cluster_merge(p, row, xr, s);
         return;
     }
     unsigned long long* kr = p.keys + (row * p.nchunks + chunk) * k;
-    rank_and_emit(s.cand, cnt, kk, [&](int rank, unsigned long long key) { kr[rank] = key; });
+    rank_and_emit(ck, cnt, kk, [&](int rank, unsigned long long key) { kr[rank] = key; });
     for (int r = kk + tid; r < k; r += kThreads) kr[r] = 0ull;   // chunk shorter than K
 
     // Last block of the row merges.

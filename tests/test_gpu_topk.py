@@ -300,6 +300,24 @@ def test_cluster_and_ticket_merges(B, oracle, rows, cols, k):
             assert_exact((v, i), want)
 
 
+# Many ties at the top of a row, or at its cut (the K-th value): a chunk
+# then has 385 to 2048 candidates, which take a radix select over the
+# candidates before the rank (and above 2048, the select over the chunk).
+@pytest.mark.parametrize("rows,cols,ties", [(64, 1000, 600), (4, 1000, 390), (1, 8000, 1500), (3, 16384, 1900),
+                                            (2, 50000, 3000), (1, 8000, 2100)])
+@pytest.mark.parametrize("k", [1, 5, 32])
+@pytest.mark.parametrize("where", ["top", "cut"])
+def test_many_tied_candidates(B, oracle, rows, cols, ties, k, where):
+    x = synth.logits_normal(rows * 13 + cols + ties + k, rows, cols)
+    rng = np.random.default_rng(cols + ties + k)
+    for r in range(rows):
+        v = x[r].max() + 1.0 if where == "top" else np.sort(x[r])[-k]
+        x[r, rng.choice(cols, ties, replace=False)] = v
+    got = gpu_topk(B, x, k)
+    assert_exact(got, oracle.topk(x, k))
+    check_topk_invariants(x, got[0], got[1], k)
+
+
 @pytest.mark.parametrize("rows,cols", [(3, 150001), (33, 131071), (5, 20003)])
 @pytest.mark.parametrize("offset", [1, 2])
 def test_long_rows_misaligned(B, oracle, rows, cols, offset):
