@@ -318,6 +318,19 @@ def test_many_tied_candidates(B, oracle, rows, cols, ties, k, where):
     check_topk_invariants(x, got[0], got[1], k)
 
 
+# Rows whose chunks all hold the same values (a period of 8192 entries), so
+# that every chunk's list holds the same values and only the indices decide
+# the ties across lists: 16 chunks of 8192, and 24 of 16384.
+@pytest.mark.parametrize("rows,cols", [(2, 16 * 8192), (1, 48 * 8192)])
+@pytest.mark.parametrize("k", [1, 5, 32])
+def test_merge_of_identical_chunks(B, oracle, rows, cols, k):
+    base = synth.logits_normal(cols + k, 1, 8192)[0]
+    x = np.ascontiguousarray(np.tile(base, (rows, cols // 8192)))
+    got = gpu_topk(B, x, k)
+    assert_exact(got, oracle.topk(x, k))
+    check_topk_invariants(x, got[0], got[1], k)
+
+
 @pytest.mark.parametrize("rows,cols", [(3, 150001), (33, 131071), (5, 20003)])
 @pytest.mark.parametrize("offset", [1, 2])
 def test_long_rows_misaligned(B, oracle, rows, cols, offset):
